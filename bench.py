@@ -1,0 +1,364 @@
+#!/usr/bin/env python
+"""Decode throughput of the KV-cached Llama decoder step on GB300.
+
+A step is one pass of the whole hot path for a batch: embedding, every layer (norm, Q/K/V,
+RoPE, KV write, attention, o_proj, norm, SwiGLU MLP), final norm, LM head and the sampler,
+run as `llm_step_dev` on device-resident inputs.  The default workload is the Llama-3.1-8B
+shape (hidden 4096, 32 layers, 32/8 heads of 128, MLP 14336, vocabulary 128256, untied head,
+llama3 RoPE) at batch 1 with a 2048-position cache prefilled from synthetic tokens, greedy.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the plain f32
+decoder under oracle/) on the same workload instead, on a bounded sample per step.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+from synth import WORKLOADS  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+GATEUP = 3  # kernel id of the norm + gate/up + SwiGLU GEMV (llm_profile_kernel)
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama8b_b1", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-steps", type=int, default=2, help="oracle decode steps for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-layers", type=int, default=2,
+                    help="reference arm: layers of the model run per timed step")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, under_load_from=0):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines[under_load_from:]:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_from_profile(kernel_file, profile_name):
+    """dram bytes per launch from the committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    src = os.path.join(ROOT, "llama_architecture_kv_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+        m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        if m_sha and m_tr and m_sha.group(1) == sha:
+            return float(m_tr.group(1))
+    except OSError:
+        pass
+    return None
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------------------------
+# the CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------------------
+
+def oracle_for(w, blob, cap):
+    import oracle
+    m = oracle.Model(oracle.cfg_of(w.shape, 1, cap), blob)
+    s = w.shape
+    if w.prompt:  # a synthetic cache of the prompt's length (values do not change the cost)
+        for layer in range(s.layers):
+            k, v = synth.kv_values(w.seed_kv, layer, 0, 1, s.kv, w.prompt, s.hd, bf16=s.bf16)
+            m.kv_write(layer, 0, 0, k, v)
+    return m
+
+
+def time_oracle_layers(m, w, pos, nl, steps, warmup):
+    """Per timed step: one token's embedding plus `nl` consecutive layers (rotating through the
+    model), and the final norm + LM head on every (L / nl)-th step, so that L / nl steps do
+    exactly one token's work.  Returns seconds per token (the mean step time x L / nl)."""
+    L = w.shape.layers
+    per_token = max(1, L // nl)
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        m.embed(1)
+        l0 = (i * nl) % L
+        for l in range(l0, min(L, l0 + nl)):
+            m.layer(l, 0, pos)
+        if i % per_token == per_token - 1:
+            m.head()
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    return float(np.mean(times)) * per_token, len(times)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    blob = synth.model_blob(w.shape, w.seed_weights)
+    cap = w.prompt + 2
+    m = oracle_for(w, blob, cap)
+    nl = max(1, min(args.ref_layers, w.shape.layers))
+    t0 = time.perf_counter()
+    sec_per_tok, n = time_oracle_layers(m, w, w.prompt, nl, args.steps, args.warmup)
+    wall = time.perf_counter() - t0
+    value = w.batch / (sec_per_tok * w.batch)  # one row at a time: tokens per second of one row
+    sample = (f"row 0 of batch {w.batch} at position {w.prompt} over a synthetic {w.prompt}-position "
+              f"cache; each step runs {nl} of {w.shape.layers} layers (the LM head every "
+              f"{max(1, w.shape.layers // nl)} steps), step time scaled by {w.shape.layers // nl}")
+    line = {
+        "impl": "reference", "metric": "decode tok/s", "value": value, "unit": "tok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec_per_tok * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "prompt": w.prompt},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    m.close()
+
+
+# ---------------------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import llama_architecture_kv_gb300 as pkg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = WORKLOADS[args.workload]
+    s, B, P = w.shape, w.batch, w.prompt
+    K, W = args.steps, args.warmup
+    cap = max(w.cap, P + W + K + 1)
+    stream = torch.cuda.Stream()
+
+    t0 = time.perf_counter()
+    blob = synth.model_blob(s, w.seed_weights)
+    log(f"[bench] weights generated: {blob.nbytes / 1e9:.2f} GB in {time.perf_counter() - t0:.1f} s")
+    t0 = time.perf_counter()
+    model = pkg.Model(s, blob, max_batch=B, max_seq=cap, stream=stream.cuda_stream)
+    h = model.h
+    log(f"[bench] model created in {time.perf_counter() - t0:.1f} s")
+    t0 = time.perf_counter()
+    if P:
+        prompt = synth.tokens(w.seed_tokens, 0, B * P, s.vocab).reshape(B, P)
+        model.prefill(prompt, 0, logits=False)
+    else:
+        for layer in range(s.layers):
+            for b in range(B):
+                k, v = synth.kv_values(w.seed_kv, layer, b, B, s.kv, w.fill, s.hd, bf16=s.bf16)
+                model.kv_import(layer, b, 0, k, v)
+    pos0 = P if P else w.fill
+    log(f"[bench] cache filled to {pos0} positions in {time.perf_counter() - t0:.1f} s")
+
+    dev = torch.device("cuda", local)
+    first = synth.tokens(w.seed_tokens, B * P, B, s.vocab)
+    tok = [torch.from_numpy(first).to(dev), torch.empty(B, dtype=torch.int32, device=dev)]
+    u_all = synth.uniforms(w.seed_uniform, 0, B * (W + K)).reshape(W + K, B)
+    u_dev = torch.from_numpy(u_all).to(dev)
+    temp, k_, p_ = w.temp, (w.top_k or s.vocab), w.top_p
+    with torch.cuda.stream(stream):
+        for i in range(W):  # warm-up: rewind to the prompt end every time
+            pkg.llm_step_dev(h, tok[0], B, pos0, temp, k_, p_, u_dev[i], tok[1])
+        pkg.llm_synchronize(h)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clocks:
+            e0.record(stream)
+            for i in range(K):
+                pkg.llm_step_dev(h, tok[i % 2], B, pos0 + i, temp, k_, p_, u_dev[W + i], tok[(i + 1) % 2])
+            e1.record(stream)
+            e1.synchronize()
+        pkg.llm_synchronize(h)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    elapsed = ms / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+        torch.distributed.barrier()
+    value = world * B * K / elapsed
+    clk = clocks.summary()
+
+    # end to end through the public host API: tokens in from pinned host memory, ids out
+    tok_h = torch.from_numpy(first.copy()).pin_memory()
+    ids_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    u_h = torch.from_numpy(u_all[:1].reshape(-1).copy()).pin_memory()
+    E = min(K, 100)
+    torch.cuda.synchronize()
+    te = time.perf_counter()
+    for i in range(E):
+        pkg.llm_step(h, tok_h if i == 0 else ids_h, B, pos0 + i, temp, k_, p_,
+                     u_h if temp > 0 else None, ids_h)
+    e2e_s = time.perf_counter() - te
+    e2e = {"value": B * E / e2e_s, "unit": "tok/s",
+           "h2d_bytes_per_step": 4 * B + (4 * B if temp > 0 else 0), "d2h_bytes_per_step": 4 * B}
+
+    # the dominant kernel, timed alone (consecutive launches walk the layers: weights from HBM)
+    reps = 4 * s.layers
+    kms = pkg.llm_profile_kernel(h, GATEUP, B, pos0, reps)
+    bytes_gu = 2 * s.ffn * s.d * (2 if s.bf16 else 4)  # algorithmic: the gate and up weights
+    achieved = bytes_gu / (kms / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    traffic = traffic_from_profile("gemv.cu", "gate_up_gemv_llama8b_b1.md") if w.name == "llama8b_b1" else None
+    roofline = {"bound": "hbm", "kernel": "gemv_kernel<bf16, EPI_SWIGLU> (norm + gate/up + SwiGLU)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": peak_kind, "traffic": traffic, "ms_per_launch": kms,
+                "algorithmic_bytes_per_launch": bytes_gu}
+    # whole-step byte roofline: weights (all but the embedding table) + the KV read
+    es = 2 if s.bf16 else 4
+    wbytes = (pkg.llm_weight_count(model.cfg) - s.vocab * s.d) * es  # all but the embedding table
+    if s.tied:
+        wbytes += s.vocab * s.d * es  # the tied LM head is that table, read in full every step
+    mean_pos = pos0 + (K - 1) / 2
+    kv_bytes = B * 2 * s.layers * s.kv * s.hd * es * (mean_pos + 1)
+    step_bytes = wbytes + kv_bytes
+    step_roof = {"bytes_per_step": step_bytes, "roofline_tok_s": B * peak * 1e9 / step_bytes,
+                 "frac_of_roofline": (value / world) / (B * peak * 1e9 / step_bytes),
+                 "hbm_gbs_achieved": step_bytes * K / elapsed / 1e9}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        t0 = time.perf_counter()
+        m = oracle_for(w, blob, pos0 + 2)
+        n = max(1, args.cpu_steps)
+        ts = []
+        for i in range(n):
+            t1 = time.perf_counter()
+            m.forward(0, int(first[0]), pos0 + (i % 2), logits=True)
+            ts.append(time.perf_counter() - t1)
+        m.close()
+        cpu = {"value": 1.0 / float(np.mean(ts)), "unit": "tok/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} full decode steps of row 0 at position {pos0} over a synthetic "
+                         f"{pos0}-position cache, single-threaded f32 C"}
+        log(f"[bench] cpu baseline in {time.perf_counter() - t0:.1f} s")
+
+    line = {
+        "metric": "decode tok/s", "value": value, "unit": "tok/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "prompt": P, "cache_positions": pos0,
+                   "weights": "bf16" if s.bf16 else "f32", "kv_cache": "bf16" if s.bf16 else "f32",
+                   "sampling": "greedy" if temp == 0 else f"temp {temp} top-k {k_} top-p {p_}",
+                   "l2": "inputs larger than L2 (weights %.1f GB per step)" % (wbytes / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clk, "gpu_launches": K * (5 * s.layers + 4),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    model.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * llm.h — C ABI of the GB300 KV-cached Llama decoder library (libllm.so).
+ *
+ * The library runs the KV-cached forward step of a Llama-architecture decoder and its
+ * sampler on one GPU, in hand-written sm_103a kernels:
+ *   embedding -> per layer { RMSNorm -> Q/K/V projections -> half-split RoPE (optionally
+ *   with llama3 three-band frequency rescaling) -> KV-cache write -> grouped-query attention
+ *   over cache positions 0..t -> o_proj + residual -> RMSNorm -> SwiGLU MLP + residual }
+ *   -> final RMSNorm -> tied or untied LM head -> greedy or temperature/top-k/top-p sampling.
+ *
+ * Sources, by page title and section:
+ *   "bend-ml-llama 0.2.1.0, main.bend" (P1): "The configuration" (Cfg), "A layer" (block),
+ *     "The model" (forward, forward_pre, argmax), "Sampling" (sample), "Loading" (tensor order).
+ *   "Llama 3.1 8B Instruct" model card (P3): README "Entries" (decode, prefill, next_token),
+ *     rope.linnet (llama3 tables), attention.linnet (decode/prefill; cache [Batch, KvHeads,
+ *     MaxSeq, hd]; the where-clauses on head counts).
+ *   "needle-core v2 model.rs" (P5): the preallocated per-sequence state and the error results
+ *     of forward (position beyond the cache, token beyond the vocabulary).
+ *
+ * Conventions for every function:
+ *   - The return value is an llm_status; LLM_OK (0) on success.  On failure nothing on the
+ *     device has been changed unless stated, and llm_last_error(h) holds a message.
+ *   - Pointers named *_host are host memory; *_dev are device memory of the handle's GPU.
+ *     Functions without a _dev suffix take host pointers and return after the result is in
+ *     host memory.  _dev functions are ordered on the handle's CUDA stream and do not wait
+ *     for the GPU; call llm_synchronize() to wait and to collect errors found on the device.
+ *   - The library never frees or keeps caller memory after a call returns.
+ *   - One handle is used by one host thread at a time.  Results are deterministic: the same
+ *     inputs on the same GPU give bit-identical outputs.
+ */
+#ifndef LLM_GB300_H
+#define LLM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t llm_status;
+enum {
+  LLM_OK = 0,
+  LLM_ERR_CONFIG = 1,         /* invalid llm_config (P3 attention.linnet where-clauses)      */
+  LLM_ERR_WEIGHTS_SIZE = 2,   /* nbytes differs from the layout count (P1 layout laws)        */
+  LLM_ERR_OOM = 3,            /* device allocation failed in llm_create                      */
+  LLM_ERR_POS_RANGE = 4,      /* position outside the cache or past the filled length (P5)    */
+  LLM_ERR_TOKEN_RANGE = 5,    /* token id < 0 or >= vocab (P5 forward)                        */
+  LLM_ERR_BATCH = 6,          /* batch < 1 or > max_batch                                    */
+  LLM_ERR_ARG = 7,            /* another argument out of its documented range, or NULL       */
+  LLM_ERR_CUDA = 8,           /* a CUDA runtime call failed (message in llm_last_error)      */
+  LLM_ERR_DEVICE_TIMEOUT = 9  /* a bounded device-side wait gave up                          */
+};
+
+enum { LLM_DTYPE_F32 = 0, LLM_DTYPE_BF16 = 1 };
+
+/*
+ * Model shape and capacity (P1 Cfg; P3 nest.toml generics and rope.linnet constants).
+ * Derived: head size hd = 2*half, query heads H = kv_heads*group, hidden d = H*hd,
+ * key width kvw = kv_heads*hd.
+ */
+typedef struct llm_config {
+  int32_t kv_heads;     /* key/value heads                                    */
+  int32_t group;        /* query heads per key/value head (g)                 */
+  int32_t half;         /* half a head; a head has 2*half numbers             */
+  int32_t ffn;          /* MLP inner width                                    */
+  int32_t layers;
+  int32_t vocab;
+  float eps;            /* RMSNorm epsilon                                    */
+  float theta;          /* RoPE base                                          */
+  int32_t tied;         /* 1: LM head = embedding; 0: untied lm_head at the end of the blob */
+  int32_t rope_llama3;  /* 1: llama3 rescaling of the [half] frequency table  */
+  float rope_factor, rope_low_freq, rope_high_freq, rope_orig_max_pos;
+  int32_t max_batch;    /* cache rows                                         */
+  int32_t max_seq;      /* cache positions per row                            */
+  int32_t dtype;        /* LLM_DTYPE_BF16: bf16 weights and bf16 cache; LLM_DTYPE_F32: both f32 */
+  int32_t debug_trace;  /* 1: keep per-layer intermediates (slow path, for llm_debug_trace) */
+} llm_config;
+
+typedef struct llm_handle llm_handle;
+
+/* Number of weight values the blob of cfg must hold:
+ *   V*d + L*(2d + 2d^2 + 2*kvw*d + 3*f*d) + d (+ V*d if untied)   (P1 "The configuration",
+ *   Cfg.layer_size and Cfg.size). */
+uint64_t llm_weight_count(const llm_config* cfg);
+
+/*
+ * Create a model on the current CUDA device.
+ * weights: the blob in the tensor order of P1 "Loading" (t_layer): emb[V][d]; for each layer
+ *   ln1[d] q[d][d] k[kvw][d] v[kvw][d] o[d][d] ln2[d] gate[f][d] up[f][d] down[d][f]; lnf[d];
+ *   then lm_head[V][d] when untied.  Matrices are row-major [out][in].  Elements are bf16 bit
+ *   patterns (uint16) for LLM_DTYPE_BF16, f32 otherwise.  weights_on_device selects whether
+ *   `weights` is a device pointer (1) or host pointer (0).  The library copies and repacks the
+ *   weights into its own device memory; the caller keeps ownership of `weights`.
+ * nbytes must equal llm_weight_count(cfg) * element size, else LLM_ERR_WEIGHTS_SIZE.
+ * cuda_stream: the cudaStream_t every call is ordered on (NULL: the library creates one).
+ * All device memory (weights, KV cache [layers][max_batch][kv][max_seq][hd], activations,
+ * scratch) is allocated here; no later call allocates.
+ */
+llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbytes,
+                      int32_t weights_on_device, void* cuda_stream, llm_handle** out);
+llm_status llm_destroy(llm_handle* h);
+
+/* Mark every cache row empty (filled length 0); the cache memory is not cleared (P5 reset). */
+llm_status llm_reset(llm_handle* h);
+
+/*
+ * Prefill (P3 "prefill<S>(tokens, pos)"; P1 forward_pre for every position but the last):
+ * rows 0..B-1 take tokens[b*S + i] at positions pos+i, i < S; their keys and values are written
+ * to the cache.  logits_host [B][V] (may be NULL: no final norm / head) receives the logits after
+ * the last token.  Requires 1 <= B <= max_batch (else LLM_ERR_BATCH), S >= 1 (else LLM_ERR_ARG),
+ * 0 <= pos <= filled length of every row b < B and pos + S <= max_seq (else LLM_ERR_POS_RANGE),
+ * tokens in [0, vocab) (else LLM_ERR_TOKEN_RANGE).  On success the filled length of rows
+ * b < B becomes pos + S (positions after it are dead and never read).
+ */
+llm_status llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t B, int32_t S,
+                       int32_t pos, float* logits_host);
+
+/*
+ * One decode step (P3 "decode(token, pos)"; P1 forward): row b takes tokens[b] at position
+ * pos, writes its key and value at pos and attends over cache positions 0..pos inclusive;
+ * logits_host [B][V] receives the logits.  Same checks as llm_prefill with S = 1.  A pos
+ * below the filled length rewinds the row.  After success the filled length is pos + 1.
+ */
+llm_status llm_decode(llm_handle* h, const int32_t* tokens_host, int32_t B, int32_t pos,
+                      float* logits_host);
+
+/*
+ * Sampling (P1 "Sampling": sample(xs, temp, k, p, u); argmax).  For each row b of logits [B][V]:
+ *   temp == 0: ids[b] = the first index of the largest logit (greedy; k, p and u unused);
+ *   temp > 0: the k largest logits (k > V clamps to V; ties: lower id first) weigh
+ *     exp(v/temp - top/temp); top-p keeps each candidate whose cumulative weight before it is
+ *     below p * Z (the first is always kept); the draw u[b] in [0, 1) returns the first kept
+ *     candidate whose cumulative weight is above u[b] * Zp, else the last kept.
+ * Arguments: temp >= 0, k >= 1, 0 < p <= 1, 0 <= u[b] < 1, else LLM_ERR_ARG.  The exp of the
+ * weights is a fixed sequence of IEEE operations, so ids can be reproduced bit for bit on a CPU.
+ */
+llm_status llm_sample(llm_handle* h, const float* logits_host, int32_t B, float temp, int32_t k,
+                      float p, const float* u_host, int32_t* ids_host);
+
+/*
+ * A generation step: llm_decode then llm_sample on the device, without moving the logits.
+ * ids_host [B] receives the drawn tokens; logits_host (may be NULL) the logits; u_host may be
+ * NULL when temp == 0.  Same checks as the two calls.
+ */
+llm_status llm_step(llm_handle* h, const int32_t* tokens_host, int32_t B, int32_t pos, float temp,
+                    int32_t k, float p, const float* u_host, int32_t* ids_host, float* logits_host);
+
+/* Device-pointer variants: the same operations on device buffers, ordered on the handle's
+ * stream, returning without waiting.  Position, batch and argument checks happen on the host
+ * before launch; token ids are checked on the device (an out-of-range id is replaced by 0 and
+ * LLM_ERR_TOKEN_RANGE is reported by the next llm_synchronize). */
+llm_status llm_prefill_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t S,
+                           int32_t pos, float* logits_dev);
+llm_status llm_decode_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t pos,
+                          float* logits_dev);
+llm_status llm_sample_dev(llm_handle* h, const float* logits_dev, int32_t B, float temp, int32_t k,
+                          float p, const float* u_dev, int32_t* ids_dev);
+llm_status llm_step_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t pos, float temp,
+                        int32_t k, float p, const float* u_dev, int32_t* ids_dev, float* logits_dev);
+
+/* Wait for the handle's stream; return the first error recorded on the device since the last
+ * call (LLM_ERR_TOKEN_RANGE, LLM_ERR_DEVICE_TIMEOUT) and clear it. */
+llm_status llm_synchronize(llm_handle* h);
+
+/* The handle's stream (cudaStream_t) and its internal logits buffer [max_batch][V] (f32, device),
+ * which decode writes; passing it back as logits_dev avoids a copy. */
+void* llm_stream(llm_handle* h);
+float* llm_logits_buffer(llm_handle* h);
+
+/* Filled length of cache row b (-1 if b is out of range). */
+int32_t llm_filled(const llm_handle* h, int32_t b);
+
+/* A message for the last failure on h (owned by h; valid until the next call), and a name for
+ * a status code. */
+const char* llm_last_error(const llm_handle* h);
+const char* llm_status_string(llm_status s);
+
+/*
+ * Test hooks.  kv_import / kv_export copy n positions starting at pos0 of one layer and cache
+ * row, for every key/value head, from / to host memory laid out [kv][n][hd] in the cache element
+ * type (bf16 bits or f32).  kv_import raises the row's filled length to at least pos0 + n.
+ * Positions must satisfy 0 <= pos0, pos0 + n <= max_seq (else LLM_ERR_POS_RANGE).
+ */
+llm_status llm_kv_import(llm_handle* h, int32_t layer, int32_t row, int32_t pos0, int32_t n,
+                         const void* k_host, const void* v_host);
+llm_status llm_kv_export(llm_handle* h, int32_t layer, int32_t row, int32_t pos0, int32_t n,
+                         void* k_host, void* v_host);
+
+/*
+ * Intermediates of the last decode step, kept only when created with debug_trace = 1
+ * (the step then runs kernel by kernel, not as a graph).  name: "q" (rotated queries [B][d]),
+ * "attn" (attention output [B][d]), "x1" (after o_proj + residual [B][d]), "m" (SwiGLU
+ * [B][f]), "y" (layer output [B][d]).  dst_host receives [B][width] f32.
+ */
+llm_status llm_debug_trace(llm_handle* h, int32_t layer, const char* name, float* dst_host);
+
+/*
+ * Measurement hook: the mean duration of `reps` back-to-back launches of one kernel of the
+ * decode step, timed alone with CUDA events on the handle's stream.  which: 0 Q/K/V projection
+ * (with norm, RoPE and cache write), 1 attention, 2 o_proj + residual, 3 norm + gate/up +
+ * SwiGLU, 4 down + residual, 5 final norm + LM head, 6 sampler.  Launch r uses layer r % layers,
+ * so consecutive launches stream different weights from HBM.  B rows at position pos (pos <=
+ * filled length; the cache entry at pos is rewritten).  *ms_per_launch receives the mean.
+ */
+llm_status llm_profile_kernel(llm_handle* h, int32_t which, int32_t B, int32_t pos, int32_t reps,
+                              float* ms_per_launch);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,329 @@
+// Weight-streaming matrix-vector products of the decode step.
+//
+// y[b][r] = sum_c W[r][c] * x'[b][c] for a batch of B activation rows, W bf16 (or f32)
+// row-major [out][in] ("row = output", bend-ml-llama "A layer", LW), accumulated in f32.
+// The input x' is either x itself or RMSNorm(x) (bend-ml-llama "The numeric pieces",
+// rmsnorm: g * (x * (1 / sqrt(mean(x^2) + eps)))), computed in the prologue of every CTA.
+// Epilogues fuse what follows each projection in the layer (bend-ml-llama "A layer", block):
+//   EPI_QKV    rows come in RoPE pairs (element i and i + half of one head): rotate q and k
+//              (rot_lo = lo*cos - hi*sin, rot_hi = hi*cos + lo*sin), store the rotated q, and
+//              write the rotated k and the plain v into the KV cache at position pos
+//              (KV.push), rounding to the cache element type;
+//   EPI_RESID  x1 = x + W_o attn, y = x1 + W_down m;
+//   EPI_SWIGLU rows come in (gate, up) pairs: m = silu(gate) * up, silu(v) = v / (1 + exp(-v));
+//   EPI_STORE  logits = W_head nf.
+//
+// Design: the decode step is bound by HBM bandwidth (each weight byte is read once per step),
+// so the kernel is a streaming engine.  Each CTA owns a contiguous, balanced range of rows
+// (whole work units, so RoPE and SwiGLU pairs stay in one CTA) and reads them with 16-byte
+// non-allocating loads, 8 rows in flight per thread.  The threads of a row split its columns;
+// the (normalized) input lives in shared memory as f32.  Partial dot products are reduced
+// with warp shuffles and a fixed-order sum across warps, so results are deterministic.
+#include "gemv.cuh"
+
+namespace llm {
+
+template <int BT> struct GemvTile {
+  static constexpr int RB = BT >= 8 ? 1 : 8 / BT;  // rows per thread per batch
+};
+
+template <int WT, int BT, int EPI, bool NORM>
+__global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a) {
+  constexpr int E = Elem<WT>::per16;
+  constexpr int RB = GemvTile<BT>::RB;
+  constexpr int NW = kGemvThreads / 32;
+  extern __shared__ __align__(16) float sm[];
+  const int seg_cols = a.seg_ch * E;
+  float* xs = sm;                            // [BT][seg_cols]
+  float* acc = xs + BT * seg_cols;           // [rows_cap][BT]
+  float* wpart = acc + a.rows_cap * BT;      // [2][NW][RB][BT]
+  float* inv = wpart + 2 * NW * RB * BT;     // [BT]
+
+  const int tid = threadIdx.x;
+  const int units = a.rows / a.rg;
+  const int u0 = (int)(((long long)units * blockIdx.x) / gridDim.x);
+  const int u1 = (int)(((long long)units * (blockIdx.x + 1)) / gridDim.x);
+  const int r0 = u0 * a.rg;
+  const int nrows = (u1 - u0) * a.rg;
+  const size_t row_bytes = (size_t)a.cols * Elem<WT>::bytes;
+  const char* Wb = (const char*)a.W + (size_t)r0 * row_bytes;
+
+  // the weights do not depend on the previous kernel: start pulling them into L2
+  if (tid == 0 && nrows > 0) {
+    size_t bytes = (size_t)nrows * row_bytes;
+    if (bytes > 65536) bytes = 65536;
+    prefetch_l2(Wb, (uint32_t)bytes);
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+
+  const int lpr = a.lpr;
+  const int RP = kGemvThreads / lpr;  // rows processed side by side
+  const int rs = tid / lpr, li = tid - (tid / lpr) * lpr;
+  const int nch = a.seg_ch / lpr;     // chunks per thread per row per segment
+  const int warp = tid >> 5, lane = tid & 31;
+
+  for (int b0 = 0; b0 < a.B; b0 += BT) {
+    const int nb = min(BT, a.B - b0);
+    if constexpr (NORM) {
+      if (warp < nb) {
+        const float* xr = a.x + (size_t)(b0 + warp) * a.x_stride;
+        float s = 0.f;
+        for (int c = lane; c < a.cols; c += 32) {
+          const float v = xr[c];
+          s = fmaf(v, v, s);
+        }
+        s = warp_sum(s);
+        if (lane == 0)
+          inv[warp] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)a.cols), a.eps)));
+      }
+    }
+    for (int i = tid; i < nrows * BT; i += kGemvThreads) acc[i] = 0.f;
+    int buf = 0;
+    for (int seg = 0; seg < a.nseg; ++seg) {
+      __syncthreads();
+      const int c0 = seg * seg_cols;
+      for (int i = tid; i < BT * seg_cols; i += kGemvThreads) {
+        const int b = i / seg_cols, c = i - b * seg_cols;
+        float v = 0.f;
+        if (b < nb) {
+          v = a.x[(size_t)(b0 + b) * a.x_stride + c0 + c];
+          if constexpr (NORM) v = __fmul_rn(a.gain[c0 + c], __fmul_rn(inv[b], v));
+        }
+        xs[i] = v;
+      }
+      __syncthreads();
+      const char* Wseg = Wb + (size_t)seg * a.seg_ch * 16;
+      for (int rbase = 0; rbase < nrows; rbase += RP * RB) {
+        float av[RB][BT];
+#pragma unroll
+        for (int k = 0; k < RB; ++k)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) av[k][b] = 0.f;
+        for (int m = 0; m < nch; ++m) {
+          const int ch = li + m * lpr;
+          uint4 w[RB];
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            const int rl = rbase + rs + k * RP;
+            w[k] = rl < nrows ? ld_stream(Wseg + (size_t)rl * row_bytes + (size_t)ch * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
+          }
+          float xv[BT][E];
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            const float4* xp = reinterpret_cast<const float4*>(xs + b * seg_cols + ch * E);
+#pragma unroll
+            for (int e4 = 0; e4 < E / 4; ++e4) {
+              const float4 t = xp[e4];
+              xv[b][4 * e4 + 0] = t.x;
+              xv[b][4 * e4 + 1] = t.y;
+              xv[b][4 * e4 + 2] = t.z;
+              xv[b][4 * e4 + 3] = t.w;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            float wf[E];
+            unpack16<WT>(w[k], wf);
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+#pragma unroll
+              for (int e = 0; e < E; ++e) av[k][b] = fmaf(wf[e], xv[b][e], av[k][b]);
+          }
+        }
+        if (lpr >= 32) {
+#pragma unroll
+          for (int k = 0; k < RB; ++k)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+              const float v = warp_sum(av[k][b]);
+              if (lane == 0) wpart[((buf * NW + warp) * RB + k) * BT + b] = v;
+            }
+          __syncthreads();
+          const int wpr = lpr >> 5;
+          for (int i = tid; i < RP * RB * BT; i += kGemvThreads) {
+            const int b = i % BT, k = (i / BT) % RB, r = i / (BT * RB);
+            const int rl = rbase + r + k * RP;
+            if (rl < nrows && b < nb) {
+              float s = 0.f;
+              for (int wi = 0; wi < wpr; ++wi) s += wpart[((buf * NW + r * wpr + wi) * RB + k) * BT + b];
+              acc[rl * BT + b] += s;
+            }
+          }
+          buf ^= 1;
+        } else {
+#pragma unroll
+          for (int k = 0; k < RB; ++k)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+              float v = av[k][b];
+              for (int o = lpr >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+              av[k][b] = v;
+            }
+          if (li == 0) {
+#pragma unroll
+            for (int k = 0; k < RB; ++k) {
+              const int rl = rbase + rs + k * RP;
+              if (rl < nrows)
+#pragma unroll
+                for (int b = 0; b < BT; ++b)
+                  if (b < nb) acc[rl * BT + b] += av[k][b];
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- epilogue ----
+    if constexpr (EPI == EPI_QKV) {
+      const int pos = a.step->pos, half = a.hd >> 1;
+      const int npairs = nrows >> 1;
+      for (int i = tid; i < npairs * nb; i += kGemvThreads) {
+        const int b = i / npairs, p = i - b * npairs;
+        const int R = r0 + 2 * p;
+        const int head = R / a.hd, e = (R - head * a.hd) >> 1;
+        const float x0 = acc[(2 * p) * BT + b], x1 = acc[(2 * p + 1) * BT + b];
+        const size_t row = (size_t)(b0 + b);
+        if (head < a.H + a.kv) {
+          const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];
+          const float lo = __fadd_rn(__fmul_rn(x0, c), __fmul_rn(-x1, s));
+          const float hi = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
+          if (head < a.H) {
+            float* q = a.q_out + row * a.q_stride + (size_t)head * a.hd;
+            q[e] = lo;
+            q[e + half] = hi;
+          } else {
+            const size_t ci = ((row * a.kv + (size_t)(head - a.H)) * a.cap + pos) * a.hd;
+            store_elem<WT>(a.kc, ci + e, lo);
+            store_elem<WT>(a.kc, ci + e + half, hi);
+          }
+        } else {
+          const size_t ci = ((row * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pos) * a.hd;
+          store_elem<WT>(a.vc, ci + e, x0);
+          store_elem<WT>(a.vc, ci + e + half, x1);
+        }
+      }
+    } else if constexpr (EPI == EPI_SWIGLU) {
+      const int npairs = nrows >> 1;
+      for (int i = tid; i < npairs * nb; i += kGemvThreads) {
+        const int b = i / npairs, p = i - b * npairs;
+        const float gt = acc[(2 * p) * BT + b], up = acc[(2 * p + 1) * BT + b];
+        const float si = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
+        a.out[(size_t)(b0 + b) * a.out_stride + (r0 >> 1) + p] = __fmul_rn(si, up);
+      }
+    } else if constexpr (EPI == EPI_RESID) {
+      for (int i = tid; i < nrows * nb; i += kGemvThreads) {
+        const int b = i / nrows, r = i - b * nrows;
+        const float rv = a.resid[(size_t)(b0 + b) * a.resid_stride + r0 + r];
+        a.out[(size_t)(b0 + b) * a.out_stride + r0 + r] = __fadd_rn(rv, acc[r * BT + b]);
+      }
+    } else {
+      for (int i = tid; i < nrows * nb; i += kGemvThreads) {
+        const int b = i / nrows, r = i - b * nrows;
+        a.out[(size_t)(b0 + b) * a.out_stride + r0 + r] = acc[r * BT + b];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------
+
+GemvPlan plan_gemv(int rows, int cols, int rg, int wt, int B, int num_sms, int ctas_per_sm) {
+  GemvPlan p{};
+  const int E = wt ? 8 : 4;
+  const int CH = cols / E;
+  p.bt = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;
+  int lpr = 1;
+  while (lpr < kGemvThreads && CH % (lpr * 2) == 0) lpr *= 2;
+  const size_t budget = 64 * 1024;
+  for (;;) {
+    const int q = CH / lpr;
+    int best = -1;
+    for (int k = 1; k <= q; ++k)
+      if (q % k == 0 && (size_t)(CH / k) * E * p.bt * 4 <= budget) {
+        best = k;
+        break;
+      }
+    if (best > 0) {
+      p.seg_ch = CH / best;
+      p.nseg = best;
+      break;
+    }
+    lpr /= 2;
+  }
+  p.lpr = lpr;
+  const int units = rows / rg;
+  const int RP = kGemvThreads / lpr;
+  int grid = num_sms * ctas_per_sm;
+  const int by_rows = (rows + RP - 1) / RP;  // at least one row per row slot
+  if (grid > by_rows) grid = by_rows;
+  if (grid > units) grid = units;
+  if (grid < 1) grid = 1;
+  p.grid = grid;
+  p.rows_cap = ((units + grid - 1) / grid) * rg;
+  const int RB = p.bt >= 8 ? 1 : 8 / p.bt;
+  p.smem = ((size_t)p.bt * p.seg_ch * E + (size_t)p.rows_cap * p.bt + 2 * 8 * RB * p.bt + 8) * 4;
+  return p;
+}
+
+using GemvFn = void (*)(const GemvArgs);
+
+template <int WT, int BT>
+static GemvFn pick_epi(int epi, bool norm) {
+  switch (epi) {
+    case EPI_QKV: return gemv_kernel<WT, BT, EPI_QKV, true>;
+    case EPI_SWIGLU: return gemv_kernel<WT, BT, EPI_SWIGLU, true>;
+    case EPI_RESID: return gemv_kernel<WT, BT, EPI_RESID, false>;
+    default: return norm ? gemv_kernel<WT, BT, EPI_STORE, true> : gemv_kernel<WT, BT, EPI_STORE, false>;
+  }
+}
+
+template <int WT>
+static GemvFn pick_bt(int bt, int epi, bool norm) {
+  switch (bt) {
+    case 1: return pick_epi<WT, 1>(epi, norm);
+    case 2: return pick_epi<WT, 2>(epi, norm);
+    case 4: return pick_epi<WT, 4>(epi, norm);
+    default: return pick_epi<WT, 8>(epi, norm);
+  }
+}
+
+static GemvFn pick(int wt, int bt, int epi, bool norm) {
+  return wt ? pick_bt<1>(bt, epi, norm) : pick_bt<0>(bt, epi, norm);
+}
+
+cudaError_t gemv_prepare(int max_smem_optin) {
+  for (int wt = 0; wt < 2; ++wt)
+    for (int bt : {1, 2, 4, 8})
+      for (int epi = 0; epi < 4; ++epi)
+        for (int norm = 0; norm < 2; ++norm) {
+          cudaError_t e = cudaFuncSetAttribute(pick(wt, bt, epi, norm != 0),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               max_smem_optin);
+          if (e != cudaSuccess) return e;
+        }
+  return cudaSuccess;
+}
+
+cudaError_t launch_gemv(const GemvArgs& a, const GemvPlan& p, int wt, int epi, bool norm,
+                        cudaStream_t s, bool pdl) {
+  GemvFn fn = pick(wt, p.bt, epi, norm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
+}  // namespace llm

@@ -1,0 +1,889 @@
+// libllm: the C ABI (include/llm.h) over the decode-step kernels.
+//
+// One handle = one model on one GPU: weights repacked once into the layouts the kernels
+// stream, the KV cache [layers][max_batch][kv][max_seq][hd], activations and scratch, all
+// allocated in llm_create (needle-core v2 model.rs, V2State: the per-sequence state is
+// preallocated so that a step does no allocation).  A decode step is captured once per
+// (batch, mode) as a CUDA graph of programmatic-dependent launches:
+//   step prologue (position, tokens, sampling parameters into device memory)
+//   -> embedding -> per layer {QKV+norm+RoPE+KV write, attention, o_proj+residual,
+//      norm+gate/up+SwiGLU, down+residual} -> final norm + LM head -> sampler.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "attention.cuh"
+#include "common.cuh"
+#include "gemv.cuh"
+#include "llm.h"
+#include "sampler.cuh"
+
+using namespace llm;
+
+namespace {
+
+constexpr int kInline = 64;  // rows whose token / draw travel inside the prologue's arguments
+
+struct BeginArgs {
+  StepState* st;
+  int32_t pos, B;
+  float temp;
+  int32_t k;
+  float p;
+  int32_t vocab;
+  const int32_t* tok_dev;  // [B] with stride tok_stride, or NULL: tok_inline
+  int32_t tok_stride, tok_col;
+  const float* u_dev;      // or NULL: u_inline
+  int32_t* tok_buf;        // [max_batch]
+  float* u_buf;            // [max_batch]
+  int32_t* status;
+  int32_t tok_inline[kInline];
+  float u_inline[kInline];
+};
+
+__global__ void step_begin_kernel(const BeginArgs a) {
+  const int t = threadIdx.x;
+  if (t == 0) {
+    a.st->pos = a.pos;
+    a.st->B = a.B;
+    a.st->temp = a.temp;
+    a.st->k = a.k;
+    a.st->p = a.p;
+  }
+  for (int b = t; b < a.B; b += blockDim.x) {
+    int tok = a.tok_dev ? a.tok_dev[(size_t)b * a.tok_stride + a.tok_col] : a.tok_inline[b];
+    if (tok < 0 || tok >= a.vocab) {
+      atomicCAS(a.status, 0, kErrTokenRange);
+      tok = 0;
+    }
+    a.tok_buf[b] = tok;
+    a.u_buf[b] = a.u_dev ? a.u_dev[b] : a.u_inline[b];
+  }
+}
+
+template <int WT>
+__global__ void embed_kernel(const void* emb, const int32_t* tok, float* x, int d, int x_stride) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.y;
+  const size_t row = (size_t)tok[b] * d;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x)
+    x[(size_t)b * x_stride + i] = load_elem<WT>(emb, row + i);
+}
+
+// row gather used by the repacking: dst row r = src row map[r], rows of `row_bytes` bytes
+__global__ void gather_rows_kernel(char* dst, const char* src, const int64_t* map, int64_t nrows,
+                                   int64_t row_bytes) {
+  for (int64_t r = blockIdx.x; r < nrows; r += gridDim.x) {
+    const uint4* s = reinterpret_cast<const uint4*>(src + map[r] * row_bytes);
+    uint4* o = reinterpret_cast<uint4*>(dst + r * row_bytes);
+    for (int64_t c = threadIdx.x; c < row_bytes / 16; c += blockDim.x) o[c] = s[c];
+  }
+}
+
+template <int WT>
+__global__ void widen_kernel(float* dst, const void* src, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = load_elem<WT>(src, (uint64_t)i);
+}
+
+// P1 inv_freq (1 / theta^(2i/hd)) and the llama3 band rescaling of the Llama 3.1 8B card
+// (rope.linnet tables), every step an IEEE f32 operation; theta^e is the f32 rounding of the
+// double power.  Then cos/sin of t * inv[i] (f32 product), rounded from double.
+struct RopeArgs {
+  float theta;
+  int hd, half, cap, llama3;
+  float factor, low, high, orig;
+  float* cs;
+  float* sn;
+};
+
+__device__ float rope_inv(const RopeArgs& a, int i) {
+  const float PI = 3.14159265f;
+  const float e = __fdiv_rn((float)(2 * i), (float)a.hd);
+  const float pw = (float)pow((double)a.theta, (double)e);
+  const float base = __fdiv_rn(1.0f, pw);
+  if (!a.llama3) return base;
+  const float wavelen = __fdiv_rn(__fmul_rn(2.0f, PI), base);
+  const float low_wl = __fdiv_rn(a.orig, a.low), high_wl = __fdiv_rn(a.orig, a.high);
+  const float smooth = __fdiv_rn(__fsub_rn(__fdiv_rn(a.orig, wavelen), a.low), __fsub_rn(a.high, a.low));
+  const float smoothed = __fadd_rn(__fmul_rn(__fsub_rn(1.0f, smooth), __fdiv_rn(base, a.factor)),
+                                   __fmul_rn(smooth, base));
+  if (wavelen > low_wl) return __fdiv_rn(base, a.factor);
+  if (wavelen < high_wl) return base;
+  return smoothed;
+}
+
+__global__ void rope_table_kernel(const RopeArgs a) {
+  const int64_t n = (int64_t)a.cap * a.half;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / a.half), i = (int)(idx % a.half);
+    const float ang = __fmul_rn((float)t, rope_inv(a, i));
+    a.cs[idx] = (float)cos((double)ang);
+    a.sn[idx] = (float)sin((double)ang);
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------
+// the handle
+// ---------------------------------------------------------------------------------------
+
+struct LayerW {
+  void* qkv;   // packed [(H + 2kv) * hd][d], rows in RoPE pairs
+  float* ln1;  // [d]
+  void* o;     // [d][d]
+  float* ln2;
+  void* gu;    // packed [2f][d], rows (gate i, up i)
+  void* down;  // [d][f]
+};
+
+struct GraphKey {
+  int B, mode;
+  bool operator<(const GraphKey& o) const { return B != o.B ? B < o.B : mode < o.mode; }
+};
+
+enum { MODE_NOHEAD = 0, MODE_HEAD = 1, MODE_SAMPLE = 2 };
+
+struct llm_handle {
+  llm_config cfg;
+  int hd, H, d, kvw, f, V, L, wt, es;
+  int dev, num_sms, smem_optin;
+  cudaStream_t stream = nullptr, cap_stream = nullptr;
+  bool own_stream = false;
+  std::vector<void*> allocs;
+  void* emb = nullptr;
+  void* head = nullptr;
+  float* lnf = nullptr;
+  std::vector<LayerW> lw;
+  void* kc = nullptr;  // [L][max_batch][kv][cap][hd]
+  void* vc = nullptr;
+  size_t layer_cache_elems = 0;
+  float *rope_cos = nullptr, *rope_sin = nullptr;
+  float *xa = nullptr, *xb = nullptr, *q = nullptr, *attn = nullptr, *m = nullptr, *logits = nullptr;
+  float* part = nullptr;
+  uint32_t* ticket = nullptr;
+  int part_ns = 0;
+  StepState* st = nullptr;
+  int32_t* status = nullptr;
+  int32_t* tok_buf = nullptr;
+  float* u_buf = nullptr;
+  int32_t* ids_buf = nullptr;
+  uint32_t* s_keys = nullptr;
+  int32_t* s_idx = nullptr;
+  float* s_pre = nullptr;
+  int V_pad = 0;
+  float* trace = nullptr;  // [L][5][max_batch][max(d, f)]
+  std::vector<int32_t> filled;
+  std::map<GraphKey, cudaGraphExec_t> graphs;
+  std::string err;
+};
+
+namespace {
+
+llm_status fail(llm_handle* h, llm_status s, const char* fmt, ...) {
+  if (h) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    h->err = buf;
+  }
+  return s;
+}
+
+#define CUDA_TRY(h, call)                                                                     \
+  do {                                                                                        \
+    cudaError_t e_ = (call);                                                                  \
+    if (e_ != cudaSuccess) return fail((h), LLM_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+uint64_t count_of(const llm_config* c) {
+  const uint64_t hd = 2 * (uint64_t)c->half, H = (uint64_t)c->kv_heads * (uint64_t)c->group;
+  const uint64_t d = H * hd, kvw = (uint64_t)c->kv_heads * hd, f = (uint64_t)c->ffn, V = (uint64_t)c->vocab;
+  const uint64_t layer = 2 * d + 2 * d * d + 2 * kvw * d + 3 * f * d;
+  return V * d + (uint64_t)c->layers * layer + d + (c->tied ? 0 : V * d);
+}
+
+const char* check_config(const llm_config* c) {
+  if (c->kv_heads <= 0 || c->group <= 0 || c->half <= 0 || c->ffn <= 0 || c->layers <= 0 || c->vocab <= 0)
+    return "kv_heads, group, half, ffn, layers and vocab must be positive";
+  if (c->max_batch <= 0 || c->max_seq <= 0) return "max_batch and max_seq must be positive";
+  if (c->dtype != LLM_DTYPE_F32 && c->dtype != LLM_DTYPE_BF16) return "dtype must be LLM_DTYPE_F32 or LLM_DTYPE_BF16";
+  if (!(c->eps >= 0.0f) || !(c->theta > 0.0f)) return "eps must be >= 0 and theta > 0";
+  if (c->rope_llama3 && !(c->rope_factor > 0.0f && c->rope_low_freq > 0.0f && c->rope_high_freq > c->rope_low_freq &&
+                          c->rope_orig_max_pos > 0.0f))
+    return "llama3 rope scaling needs factor > 0, 0 < low_freq < high_freq, orig_max_pos > 0";
+  const int hd = 2 * c->half;
+  if (!attn_supported(hd, c->group)) return "head size must be 16, 32, 64, 128 or 256 and group at most 16";
+  const int per16 = c->dtype == LLM_DTYPE_BF16 ? 8 : 4;
+  const int64_t d = (int64_t)c->kv_heads * c->group * hd;
+  if (d % per16 || c->ffn % per16) return "hidden and ffn widths must fill whole 16-byte chunks";
+  if ((int64_t)c->max_seq * c->max_batch > (int64_t)1 << 40) return "cache too large";
+  return nullptr;
+}
+
+template <class T>
+llm_status dalloc(llm_handle* h, T** p, size_t bytes) {
+  void* v = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(&v, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(h, LLM_ERR_OOM, "cudaMalloc(%zu bytes): %s", bytes, cudaGetErrorString(e));
+  }
+  h->allocs.push_back(v);
+  *p = static_cast<T*>(v);
+  return LLM_OK;
+}
+
+#define TRY(x)                  \
+  do {                          \
+    llm_status s_ = (x);        \
+    if (s_ != LLM_OK) return s_; \
+  } while (0)
+
+// ---- repacking of one layer's tensors from the blob (device copy) ----
+llm_status gather(llm_handle* h, void* dst, const char* src, const std::vector<int64_t>& map, int64_t row_bytes,
+                  int64_t* dmap) {
+  CUDA_TRY(h, cudaMemcpyAsync(dmap, map.data(), map.size() * 8, cudaMemcpyHostToDevice, h->stream));
+  gather_rows_kernel<<<1024, 256, 0, h->stream>>>((char*)dst, src, dmap, (int64_t)map.size(), row_bytes);
+  CUDA_TRY(h, cudaGetLastError());
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  return LLM_OK;
+}
+
+llm_status widen(llm_handle* h, float* dst, const char* src, int64_t n) {
+  if (h->wt) widen_kernel<1><<<64, 256, 0, h->stream>>>(dst, src, n);
+  else widen_kernel<0><<<64, 256, 0, h->stream>>>(dst, src, n);
+  CUDA_TRY(h, cudaGetLastError());
+  return LLM_OK;
+}
+
+llm_status load_weights(llm_handle* h, const char* blob /* device */) {
+  const int64_t d = h->d, kvw = h->kvw, f = h->f, V = h->V, hd = h->hd, half = hd / 2;
+  const int64_t es = h->es, H = h->H, kv = h->cfg.kv_heads;
+  const int64_t rowd = d * es;
+  int64_t* dmap = nullptr;
+  TRY(dalloc(h, &dmap, (size_t)std::max<int64_t>(std::max<int64_t>(V, 2 * f), (H + 2 * kv) * hd) * 8));
+  // embedding and head: as given
+  TRY(dalloc(h, &h->emb, (size_t)(V * d * es)));
+  CUDA_TRY(h, cudaMemcpyAsync(h->emb, blob, (size_t)(V * d * es), cudaMemcpyDeviceToDevice, h->stream));
+  int64_t off = V * d;  // elements
+  h->lw.resize(h->L);
+  for (int l = 0; l < h->L; ++l) {
+    LayerW& w = h->lw[l];
+    const int64_t o_ln1 = off, o_q = o_ln1 + d, o_k = o_q + d * d, o_v = o_k + kvw * d, o_o = o_v + kvw * d;
+    const int64_t o_ln2 = o_o + d * d, o_g = o_ln2 + d, o_u = o_g + f * d, o_dn = o_u + f * d;
+    off = o_dn + d * f;
+    TRY(dalloc(h, &w.ln1, (size_t)d * 4));
+    TRY(dalloc(h, &w.ln2, (size_t)d * 4));
+    TRY(widen(h, w.ln1, blob + o_ln1 * es, d));
+    TRY(widen(h, w.ln2, blob + o_ln2 * es, d));
+    // QKV: q heads, then k heads, then v heads; inside a head the rows (i, i + half) side by side.
+    // The source rows are addressed relative to o_q (q, k and v are adjacent in the blob).
+    std::vector<int64_t> map;
+    map.reserve((size_t)((H + 2 * kv) * hd));
+    for (int64_t head = 0; head < H + 2 * kv; ++head) {
+      int64_t base;  // first source row of this head, counted from o_q
+      if (head < H) base = head * hd;
+      else if (head < H + kv) base = d + (head - H) * hd;
+      else base = d + kvw + (head - H - kv) * hd;
+      for (int64_t i = 0; i < half; ++i) {
+        map.push_back(base + i);
+        map.push_back(base + i + half);
+      }
+    }
+    TRY(dalloc(h, &w.qkv, (size_t)((H + 2 * kv) * hd * rowd)));
+    TRY(gather(h, w.qkv, blob + o_q * es, map, rowd, dmap));
+    TRY(dalloc(h, &w.o, (size_t)(d * d * es)));
+    CUDA_TRY(h, cudaMemcpyAsync(w.o, blob + o_o * es, (size_t)(d * d * es), cudaMemcpyDeviceToDevice, h->stream));
+    map.clear();
+    for (int64_t i = 0; i < f; ++i) {
+      map.push_back(i);      // gate row i (relative to o_g)
+      map.push_back(f + i);  // up row i
+    }
+    TRY(dalloc(h, &w.gu, (size_t)(2 * f * rowd)));
+    TRY(gather(h, w.gu, blob + o_g * es, map, rowd, dmap));
+    TRY(dalloc(h, &w.down, (size_t)(d * f * es)));
+    CUDA_TRY(h, cudaMemcpyAsync(w.down, blob + o_dn * es, (size_t)(d * f * es), cudaMemcpyDeviceToDevice, h->stream));
+  }
+  TRY(dalloc(h, &h->lnf, (size_t)d * 4));
+  TRY(widen(h, h->lnf, blob + off * es, d));
+  off += d;
+  if (h->cfg.tied) {
+    h->head = h->emb;
+  } else {
+    TRY(dalloc(h, &h->head, (size_t)(V * d * es)));
+    CUDA_TRY(h, cudaMemcpyAsync(h->head, blob + off * es, (size_t)(V * d * es), cudaMemcpyDeviceToDevice, h->stream));
+  }
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  return LLM_OK;
+}
+
+// ---- the decode step ----
+
+enum { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GATEUP = 3, K_DOWN = 4, K_HEAD = 5, K_SAMPLE = 6, K_EMBED = 7 };
+
+// launch one kernel of the decode step (layer l where it applies)
+llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
+  const int wt = h->wt;
+  const int cps = 2;
+  const llm_config& c = h->cfg;
+  if (which == K_EMBED) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((h->d + 255) / 256, B);
+    lc.blockDim = dim3(256);
+    lc.stream = h->stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 0;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (wt) CUDA_TRY(h, cudaLaunchKernelEx(&lc, embed_kernel<1>, (const void*)h->emb, (const int32_t*)h->tok_buf, h->xa, h->d, h->d));
+    else CUDA_TRY(h, cudaLaunchKernelEx(&lc, embed_kernel<0>, (const void*)h->emb, (const int32_t*)h->tok_buf, h->xa, h->d, h->d));
+    return LLM_OK;
+  }
+  if (which == K_HEAD) {
+    const GemvPlan p_h = plan_gemv(h->V, h->d, 1, wt, B, h->num_sms, cps);
+    GemvArgs hd = {};
+    hd.step = h->st; hd.B = B; hd.eps = c.eps; hd.W = h->head; hd.rows = h->V; hd.cols = h->d; hd.rg = 1;
+    hd.x = h->xa; hd.x_stride = h->d; hd.gain = h->lnf;
+    hd.lpr = p_h.lpr; hd.seg_ch = p_h.seg_ch; hd.nseg = p_h.nseg; hd.rows_cap = p_h.rows_cap;
+    hd.out = h->logits; hd.out_stride = h->V;
+    CUDA_TRY(h, launch_gemv(hd, p_h, wt, EPI_STORE, true, h->stream, pdl));
+    return LLM_OK;
+  }
+  if (which == K_SAMPLE) {
+    SampleArgs s = {};
+    s.logits = h->logits; s.logits_stride = h->V; s.V = h->V; s.V_pad = h->V_pad;
+    s.keys = h->s_keys; s.idx = h->s_idx; s.pre = h->s_pre; s.u = h->u_buf; s.ids = h->ids_buf; s.step = h->st;
+    CUDA_TRY(h, launch_sample(s, B, h->stream, pdl));
+    return LLM_OK;
+  }
+  const LayerW& w = h->lw[l];
+  char* kcl = (char*)h->kc + (size_t)l * h->layer_cache_elems * h->es;
+  char* vcl = (char*)h->vc + (size_t)l * h->layer_cache_elems * h->es;
+  if (which == K_QKV) {
+    const int qkv_rows = (h->H + 2 * c.kv_heads) * h->hd;
+    const GemvPlan p = plan_gemv(qkv_rows, h->d, 2, wt, B, h->num_sms, cps);
+    GemvArgs a = {};
+    a.step = h->st; a.B = B; a.eps = c.eps;
+    a.W = w.qkv; a.rows = qkv_rows; a.cols = h->d; a.rg = 2;
+    a.x = h->xa; a.x_stride = h->d; a.gain = w.ln1;
+    a.lpr = p.lpr; a.seg_ch = p.seg_ch; a.nseg = p.nseg; a.rows_cap = p.rows_cap;
+    a.q_out = h->q; a.q_stride = h->d; a.kc = kcl; a.vc = vcl;
+    a.H = h->H; a.kv = c.kv_heads; a.hd = h->hd; a.cap = c.max_seq;
+    a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin;
+    CUDA_TRY(h, launch_gemv(a, p, wt, EPI_QKV, true, h->stream, pdl));
+  } else if (which == K_ATTN) {
+    const int ns = attn_splits(B, c.kv_heads, c.max_seq, h->num_sms);
+    if (ns > h->part_ns) return fail(h, LLM_ERR_ARG, "internal: attention splits %d > %d", ns, h->part_ns);
+    AttnArgs at = {};
+    at.q = h->q; at.q_stride = h->d; at.kc = kcl; at.vc = vcl; at.out = h->attn; at.out_stride = h->d;
+    at.part = h->part; at.ticket = h->ticket; at.B = B; at.kv = c.kv_heads; at.g = c.group; at.hd = h->hd;
+    at.cap = c.max_seq; at.ns = ns; at.scale = 1.0f / sqrtf((float)h->hd); at.step = h->st;
+    CUDA_TRY(h, launch_attn(at, wt, h->stream, pdl));
+  } else if (which == K_O) {
+    // o_proj + residual: x1 (xb) = x (xa) + W_o attn
+    const GemvPlan p = plan_gemv(h->d, h->d, 1, wt, B, h->num_sms, cps);
+    GemvArgs o = {};
+    o.step = h->st; o.B = B; o.W = w.o; o.rows = h->d; o.cols = h->d; o.rg = 1;
+    o.x = h->attn; o.x_stride = h->d;
+    o.lpr = p.lpr; o.seg_ch = p.seg_ch; o.nseg = p.nseg; o.rows_cap = p.rows_cap;
+    o.out = h->xb; o.out_stride = h->d; o.resid = h->xa; o.resid_stride = h->d;
+    CUDA_TRY(h, launch_gemv(o, p, wt, EPI_RESID, false, h->stream, pdl));
+  } else if (which == K_GATEUP) {
+    // RMSNorm + gate/up + SwiGLU: m = silu(W_g n2) * (W_u n2)
+    const GemvPlan p = plan_gemv(2 * h->f, h->d, 2, wt, B, h->num_sms, cps);
+    GemvArgs g = {};
+    g.step = h->st; g.B = B; g.eps = c.eps; g.W = w.gu; g.rows = 2 * h->f; g.cols = h->d; g.rg = 2;
+    g.x = h->xb; g.x_stride = h->d; g.gain = w.ln2;
+    g.lpr = p.lpr; g.seg_ch = p.seg_ch; g.nseg = p.nseg; g.rows_cap = p.rows_cap;
+    g.out = h->m; g.out_stride = h->f;
+    CUDA_TRY(h, launch_gemv(g, p, wt, EPI_SWIGLU, true, h->stream, pdl));
+  } else if (which == K_DOWN) {
+    // down + residual: y (xa) = x1 (xb) + W_down m
+    const GemvPlan p = plan_gemv(h->d, h->f, 1, wt, B, h->num_sms, cps);
+    GemvArgs dn = {};
+    dn.step = h->st; dn.B = B; dn.W = w.down; dn.rows = h->d; dn.cols = h->f; dn.rg = 1;
+    dn.x = h->m; dn.x_stride = h->f;
+    dn.lpr = p.lpr; dn.seg_ch = p.seg_ch; dn.nseg = p.nseg; dn.rows_cap = p.rows_cap;
+    dn.out = h->xa; dn.out_stride = h->d; dn.resid = h->xb; dn.resid_stride = h->d;
+    CUDA_TRY(h, launch_gemv(dn, p, wt, EPI_RESID, false, h->stream, pdl));
+  } else {
+    return fail(h, LLM_ERR_ARG, "unknown kernel %d", which);
+  }
+  return LLM_OK;
+}
+
+llm_status launch_layer_kernels(llm_handle* h, int B, int mode, bool pdl, bool trace) {
+  const llm_config& c = h->cfg;
+  TRY(launch_one(h, K_EMBED, 0, B, false));
+  const size_t maxw = (size_t)std::max(h->d, h->f);
+  for (int l = 0; l < h->L; ++l) {
+    for (int k = K_QKV; k <= K_DOWN; ++k) TRY(launch_one(h, k, l, B, pdl));
+    if (trace) {
+      float* t = h->trace + (size_t)l * 5 * c.max_batch * maxw;
+      const size_t row = (size_t)c.max_batch * maxw;
+      CUDA_TRY(h, cudaMemcpy2DAsync(t + 0 * row, maxw * 4, h->q, (size_t)h->d * 4, (size_t)h->d * 4, B, cudaMemcpyDeviceToDevice, h->stream));
+      CUDA_TRY(h, cudaMemcpy2DAsync(t + 1 * row, maxw * 4, h->attn, (size_t)h->d * 4, (size_t)h->d * 4, B, cudaMemcpyDeviceToDevice, h->stream));
+      CUDA_TRY(h, cudaMemcpy2DAsync(t + 2 * row, maxw * 4, h->xb, (size_t)h->d * 4, (size_t)h->d * 4, B, cudaMemcpyDeviceToDevice, h->stream));
+      CUDA_TRY(h, cudaMemcpy2DAsync(t + 3 * row, maxw * 4, h->m, (size_t)h->f * 4, (size_t)h->f * 4, B, cudaMemcpyDeviceToDevice, h->stream));
+      CUDA_TRY(h, cudaMemcpy2DAsync(t + 4 * row, maxw * 4, h->xa, (size_t)h->d * 4, (size_t)h->d * 4, B, cudaMemcpyDeviceToDevice, h->stream));
+    }
+  }
+  if (mode >= MODE_HEAD) TRY(launch_one(h, K_HEAD, 0, B, pdl));
+  if (mode == MODE_SAMPLE) TRY(launch_one(h, K_SAMPLE, 0, B, pdl));
+  return LLM_OK;
+}
+
+llm_status run_step(llm_handle* h, int B, int mode) {
+  if (h->cfg.debug_trace) return launch_layer_kernels(h, B, mode, false, true);
+  GraphKey key{B, mode};
+  auto it = h->graphs.find(key);
+  if (it == h->graphs.end()) {
+    // capture on a private stream, then replay on the handle's stream
+    cudaStream_t saved = h->stream;
+    h->stream = h->cap_stream;
+    CUDA_TRY(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+    llm_status s = launch_layer_kernels(h, B, mode, true, false);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(h->stream, &graph);
+    h->stream = saved;
+    if (s != LLM_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return s;
+    }
+    if (e != cudaSuccess) return fail(h, LLM_ERR_CUDA, "stream capture: %s", cudaGetErrorString(e));
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail(h, LLM_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    it = h->graphs.emplace(key, exec).first;
+  }
+  CUDA_TRY(h, cudaGraphLaunch(it->second, h->stream));
+  return LLM_OK;
+}
+
+llm_status begin(llm_handle* h, int pos, int B, const int32_t* tok_host, const int32_t* tok_dev, int tok_stride,
+                 int tok_col, float temp, int k, float p, const float* u_host, const float* u_dev) {
+  BeginArgs a = {};
+  a.st = h->st; a.pos = pos; a.B = B; a.temp = temp; a.k = k; a.p = p; a.vocab = h->V;
+  a.tok_buf = h->tok_buf; a.u_buf = h->u_buf; a.status = h->status;
+  a.tok_stride = tok_stride; a.tok_col = tok_col;
+  if (tok_dev) {
+    a.tok_dev = tok_dev;
+  } else if (B <= kInline) {
+    for (int b = 0; b < B; ++b) a.tok_inline[b] = tok_host[(size_t)b * tok_stride + tok_col];
+  } else {
+    std::vector<int32_t> col(B);
+    for (int b = 0; b < B; ++b) col[b] = tok_host[(size_t)b * tok_stride + tok_col];
+    CUDA_TRY(h, cudaMemcpyAsync(h->tok_buf, col.data(), (size_t)B * 4, cudaMemcpyHostToDevice, h->stream));
+    a.tok_dev = h->tok_buf;
+    a.tok_stride = 1;
+    a.tok_col = 0;
+  }
+  if (u_dev) {
+    a.u_dev = u_dev;
+  } else if (u_host && B > kInline) {
+    CUDA_TRY(h, cudaMemcpyAsync(h->u_buf, u_host, (size_t)B * 4, cudaMemcpyHostToDevice, h->stream));
+    a.u_dev = h->u_buf;
+  } else {
+    for (int b = 0; b < B && b < kInline; ++b) a.u_inline[b] = u_host ? u_host[b] : 0.0f;
+  }
+  step_begin_kernel<<<1, 128, 0, h->stream>>>(a);
+  CUDA_TRY(h, cudaGetLastError());
+  return LLM_OK;
+}
+
+llm_status check_rows(llm_handle* h, int B, int pos, int S) {
+  if (B < 1 || B > h->cfg.max_batch) return fail(h, LLM_ERR_BATCH, "batch %d outside 1..%d", B, h->cfg.max_batch);
+  if (S < 1) return fail(h, LLM_ERR_ARG, "prompt length %d < 1", S);
+  if (pos < 0 || (int64_t)pos + S > h->cfg.max_seq)
+    return fail(h, LLM_ERR_POS_RANGE, "positions %d..%lld outside the cache of %d", pos, (long long)pos + S - 1, h->cfg.max_seq);
+  for (int b = 0; b < B; ++b)
+    if (pos > h->filled[b])
+      return fail(h, LLM_ERR_POS_RANGE, "row %d: position %d after its filled length %d", b, pos, h->filled[b]);
+  return LLM_OK;
+}
+
+llm_status check_tokens(llm_handle* h, const int32_t* toks, size_t n) {
+  for (size_t i = 0; i < n; ++i)
+    if (toks[i] < 0 || toks[i] >= h->V) return fail(h, LLM_ERR_TOKEN_RANGE, "token %d at %zu outside 0..%d", toks[i], i, h->V - 1);
+  return LLM_OK;
+}
+
+llm_status check_sample_args(llm_handle* h, float temp, int k, float p) {
+  if (!(temp >= 0.0f) || temp == INFINITY) return fail(h, LLM_ERR_ARG, "temperature must be finite and >= 0");
+  if (temp > 0.0f) {
+    if (k < 1) return fail(h, LLM_ERR_ARG, "top-k must be >= 1");
+    if (!(p > 0.0f && p <= 1.0f)) return fail(h, LLM_ERR_ARG, "top-p must be in (0, 1]");
+  }
+  return LLM_OK;
+}
+
+void set_filled(llm_handle* h, int B, int v) {
+  for (int b = 0; b < B; ++b) h->filled[b] = v;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------------------
+
+extern "C" {
+
+uint64_t llm_weight_count(const llm_config* cfg) { return cfg ? count_of(cfg) : 0; }
+
+const char* llm_status_string(llm_status s) {
+  switch (s) {
+    case LLM_OK: return "ok";
+    case LLM_ERR_CONFIG: return "invalid config";
+    case LLM_ERR_WEIGHTS_SIZE: return "weight blob size mismatch";
+    case LLM_ERR_OOM: return "out of device memory";
+    case LLM_ERR_POS_RANGE: return "position out of range";
+    case LLM_ERR_TOKEN_RANGE: return "token out of range";
+    case LLM_ERR_BATCH: return "batch out of range";
+    case LLM_ERR_ARG: return "invalid argument";
+    case LLM_ERR_CUDA: return "CUDA error";
+    case LLM_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* llm_last_error(const llm_handle* h) { return h ? h->err.c_str() : "no handle"; }
+
+llm_status llm_destroy(llm_handle* h) {
+  if (!h) return LLM_ERR_ARG;
+  if (h->stream) cudaStreamSynchronize(h->stream);
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  for (void* p : h->allocs) cudaFree(p);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  if (h->own_stream && h->stream) cudaStreamDestroy(h->stream);
+  delete h;
+  return LLM_OK;
+}
+
+llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbytes, int32_t weights_on_device,
+                      void* cuda_stream, llm_handle** out) {
+  if (!cfg || !weights || !out) return LLM_ERR_ARG;
+  *out = nullptr;
+  if (check_config(cfg)) return LLM_ERR_CONFIG;
+  const uint64_t es = cfg->dtype == LLM_DTYPE_BF16 ? 2 : 4;
+  if (nbytes != count_of(cfg) * es) return LLM_ERR_WEIGHTS_SIZE;
+  llm_handle* h = new llm_handle();
+  h->cfg = *cfg;
+  const llm_config& c = h->cfg;
+  h->hd = 2 * c.half;
+  h->H = c.kv_heads * c.group;
+  h->d = h->H * h->hd;
+  h->kvw = c.kv_heads * h->hd;
+  h->f = c.ffn;
+  h->V = c.vocab;
+  h->L = c.layers;
+  h->wt = c.dtype == LLM_DTYPE_BF16 ? 1 : 0;
+  h->es = (int)es;
+  h->filled.assign(c.max_batch, 0);
+  llm_status st = LLM_OK;
+  auto bail = [&](llm_status s) {
+    h->err.clear();
+    llm_destroy(h);
+    return s;
+  };
+  if (cudaGetDevice(&h->dev) != cudaSuccess) return bail(LLM_ERR_CUDA);
+  cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->dev);
+  cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev);
+  if (cuda_stream) {
+    h->stream = (cudaStream_t)cuda_stream;
+  } else {
+    if (cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking) != cudaSuccess) return bail(LLM_ERR_CUDA);
+    h->own_stream = true;
+  }
+  if (cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) return bail(LLM_ERR_CUDA);
+  if (gemv_prepare(h->smem_optin) != cudaSuccess || attn_prepare(h->smem_optin) != cudaSuccess ||
+      sample_prepare() != cudaSuccess)
+    return bail(LLM_ERR_CUDA);
+  // weights: a device copy of the blob when it is on the host, then repacked
+  const char* blob = (const char*)weights;
+  char* staging = nullptr;
+  if (!weights_on_device) {
+    if (cudaMalloc(&staging, nbytes) != cudaSuccess) {
+      cudaGetLastError();
+      return bail(LLM_ERR_OOM);
+    }
+    if (cudaMemcpy(staging, weights, nbytes, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaFree(staging);
+      return bail(LLM_ERR_CUDA);
+    }
+    blob = staging;
+  }
+  st = load_weights(h, blob);
+  if (staging) cudaFree(staging);
+  if (st != LLM_OK) return bail(st);
+  // KV cache, RoPE table, activations, scratch
+  h->layer_cache_elems = (size_t)c.max_batch * c.kv_heads * c.max_seq * h->hd;
+  const size_t cache_bytes = (size_t)h->L * h->layer_cache_elems * es;
+  if ((st = dalloc(h, &h->kc, cache_bytes)) || (st = dalloc(h, &h->vc, cache_bytes))) return bail(st);
+  if ((st = dalloc(h, &h->rope_cos, (size_t)c.max_seq * c.half * 4)) ||
+      (st = dalloc(h, &h->rope_sin, (size_t)c.max_seq * c.half * 4)))
+    return bail(st);
+  const size_t B = c.max_batch;
+  if ((st = dalloc(h, &h->xa, B * h->d * 4)) || (st = dalloc(h, &h->xb, B * h->d * 4)) ||
+      (st = dalloc(h, &h->q, B * h->d * 4)) || (st = dalloc(h, &h->attn, B * h->d * 4)) ||
+      (st = dalloc(h, &h->m, B * h->f * 4)) || (st = dalloc(h, &h->logits, B * h->V * 4)))
+    return bail(st);
+  int maxns = 1;
+  for (int b = 1; b <= c.max_batch; ++b) maxns = std::max(maxns, attn_splits(b, c.kv_heads, c.max_seq, h->num_sms));
+  h->part_ns = maxns;
+  if ((st = dalloc(h, &h->part, B * h->H * maxns * (h->hd + 2) * 4)) ||
+      (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, sizeof(StepState))) ||
+      (st = dalloc(h, &h->status, 16)) || (st = dalloc(h, &h->tok_buf, B * 4)) || (st = dalloc(h, &h->u_buf, B * 4)) ||
+      (st = dalloc(h, &h->ids_buf, B * 4)))
+    return bail(st);
+  h->V_pad = (h->V + 31) & ~31;
+  if ((st = dalloc(h, &h->s_keys, B * 2 * h->V_pad * 4)) || (st = dalloc(h, &h->s_idx, B * 2 * h->V_pad * 4)) ||
+      (st = dalloc(h, &h->s_pre, B * h->V_pad * 4)))
+    return bail(st);
+  if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * 5 * B * std::max(h->d, h->f) * 4))) return bail(st);
+  if (cudaMemsetAsync(h->ticket, 0, B * c.kv_heads * 4, h->stream) != cudaSuccess ||
+      cudaMemsetAsync(h->status, 0, 16, h->stream) != cudaSuccess ||
+      cudaMemsetAsync(h->kc, 0, cache_bytes, h->stream) != cudaSuccess ||
+      cudaMemsetAsync(h->vc, 0, cache_bytes, h->stream) != cudaSuccess)
+    return bail(LLM_ERR_CUDA);
+  RopeArgs ra = {c.theta, h->hd, c.half, c.max_seq, c.rope_llama3, c.rope_factor, c.rope_low_freq, c.rope_high_freq,
+                 c.rope_orig_max_pos, h->rope_cos, h->rope_sin};
+  rope_table_kernel<<<1024, 256, 0, h->stream>>>(ra);
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(h->stream) != cudaSuccess) return bail(LLM_ERR_CUDA);
+  *out = h;
+  return LLM_OK;
+}
+
+llm_status llm_reset(llm_handle* h) {
+  if (!h) return LLM_ERR_ARG;
+  std::fill(h->filled.begin(), h->filled.end(), 0);
+  return LLM_OK;
+}
+
+void* llm_stream(llm_handle* h) { return h ? (void*)h->stream : nullptr; }
+float* llm_logits_buffer(llm_handle* h) { return h ? h->logits : nullptr; }
+int32_t llm_filled(const llm_handle* h, int32_t b) {
+  return (h && b >= 0 && b < h->cfg.max_batch) ? h->filled[b] : -1;
+}
+
+llm_status llm_synchronize(llm_handle* h) {
+  if (!h) return LLM_ERR_ARG;
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  int32_t s = 0;
+  CUDA_TRY(h, cudaMemcpy(&s, h->status, 4, cudaMemcpyDeviceToHost));
+  if (s != 0) {
+    CUDA_TRY(h, cudaMemset(h->status, 0, 4));
+    return fail(h, s, "device reported: %s", llm_status_string(s));
+  }
+  return LLM_OK;
+}
+
+static llm_status prefill_impl(llm_handle* h, const int32_t* tok_host, const int32_t* tok_dev, int32_t B, int32_t S,
+                               int32_t pos, float* logits, bool logits_on_host) {
+  TRY(check_rows(h, B, pos, S));
+  if (tok_host) TRY(check_tokens(h, tok_host, (size_t)B * S));
+  for (int i = 0; i < S; ++i) {
+    TRY(begin(h, pos + i, B, tok_host, tok_dev, S, i, 0.0f, 1, 1.0f, nullptr, nullptr));
+    TRY(run_step(h, B, (i == S - 1 && logits) ? MODE_HEAD : MODE_NOHEAD));
+  }
+  if (logits) {
+    if (logits_on_host) {
+      CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
+      CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+    } else if (logits != h->logits) {
+      CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToDevice, h->stream));
+    }
+  } else if (logits_on_host) {
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  }
+  set_filled(h, B, pos + S);
+  return LLM_OK;
+}
+
+llm_status llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t B, int32_t S, int32_t pos, float* logits_host) {
+  if (!h || !tokens_host) return LLM_ERR_ARG;
+  return prefill_impl(h, tokens_host, nullptr, B, S, pos, logits_host, true);
+}
+
+llm_status llm_prefill_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t S, int32_t pos, float* logits_dev) {
+  if (!h || !tokens_dev) return LLM_ERR_ARG;
+  return prefill_impl(h, nullptr, tokens_dev, B, S, pos, logits_dev, false);
+}
+
+llm_status llm_decode(llm_handle* h, const int32_t* tokens_host, int32_t B, int32_t pos, float* logits_host) {
+  if (!h || !tokens_host || !logits_host) return LLM_ERR_ARG;
+  return prefill_impl(h, tokens_host, nullptr, B, 1, pos, logits_host, true);
+}
+
+llm_status llm_decode_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t pos, float* logits_dev) {
+  if (!h || !tokens_dev || !logits_dev) return LLM_ERR_ARG;
+  return prefill_impl(h, nullptr, tokens_dev, B, 1, pos, logits_dev, false);
+}
+
+static llm_status sample_impl(llm_handle* h, const float* logits, bool logits_on_host, int32_t B, float temp, int32_t k,
+                              float p, const float* u, bool u_on_host, int32_t* ids, bool ids_on_host) {
+  if (B < 1 || B > h->cfg.max_batch) return fail(h, LLM_ERR_BATCH, "batch %d outside 1..%d", B, h->cfg.max_batch);
+  TRY(check_sample_args(h, temp, k, p));
+  if (temp > 0.0f && !u) return fail(h, LLM_ERR_ARG, "sampling needs uniform draws u");
+  if (u && u_on_host && temp > 0.0f)
+    for (int b = 0; b < B; ++b)
+      if (!(u[b] >= 0.0f && u[b] < 1.0f)) return fail(h, LLM_ERR_ARG, "u[%d] outside [0, 1)", b);
+  if (logits != h->logits)
+    CUDA_TRY(h, cudaMemcpyAsync(h->logits, logits, (size_t)B * h->V * 4,
+                                logits_on_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice, h->stream));
+  // the prologue also carries temp, k, p and u; its tokens are unused here
+  std::vector<int32_t> toks(B, 0);
+  TRY(begin(h, 0, B, toks.data(), nullptr, 1, 0, temp, k, p, u_on_host ? u : nullptr, u_on_host ? nullptr : u));
+  SampleArgs s = {};
+  s.logits = h->logits; s.logits_stride = h->V; s.V = h->V; s.V_pad = h->V_pad;
+  s.keys = h->s_keys; s.idx = h->s_idx; s.pre = h->s_pre; s.u = h->u_buf; s.ids = h->ids_buf; s.step = h->st;
+  CUDA_TRY(h, launch_sample(s, B, h->stream, false));
+  if (ids_on_host) {
+    CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToHost, h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  } else if (ids != h->ids_buf) {
+    CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToDevice, h->stream));
+  }
+  return LLM_OK;
+}
+
+llm_status llm_sample(llm_handle* h, const float* logits_host, int32_t B, float temp, int32_t k, float p,
+                      const float* u_host, int32_t* ids_host) {
+  if (!h || !logits_host || !ids_host) return LLM_ERR_ARG;
+  return sample_impl(h, logits_host, true, B, temp, k, p, u_host, true, ids_host, true);
+}
+
+llm_status llm_sample_dev(llm_handle* h, const float* logits_dev, int32_t B, float temp, int32_t k, float p,
+                          const float* u_dev, int32_t* ids_dev) {
+  if (!h || !logits_dev || !ids_dev) return LLM_ERR_ARG;
+  return sample_impl(h, logits_dev, false, B, temp, k, p, u_dev, false, ids_dev, false);
+}
+
+static llm_status step_impl(llm_handle* h, const int32_t* tok_host, const int32_t* tok_dev, int32_t B, int32_t pos,
+                            float temp, int32_t k, float p, const float* u_host, const float* u_dev, int32_t* ids,
+                            float* logits, bool host) {
+  TRY(check_rows(h, B, pos, 1));
+  TRY(check_sample_args(h, temp, k, p));
+  if (temp > 0.0f && !u_host && !u_dev) return fail(h, LLM_ERR_ARG, "sampling needs uniform draws u");
+  if (tok_host) TRY(check_tokens(h, tok_host, (size_t)B));
+  if (u_host && temp > 0.0f)
+    for (int b = 0; b < B; ++b)
+      if (!(u_host[b] >= 0.0f && u_host[b] < 1.0f)) return fail(h, LLM_ERR_ARG, "u[%d] outside [0, 1)", b);
+  TRY(begin(h, pos, B, tok_host, tok_dev, 1, 0, temp, k, p, u_host, u_dev));
+  TRY(run_step(h, B, MODE_SAMPLE));
+  if (host) {
+    if (logits) CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
+    CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToHost, h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  } else {
+    if (logits && logits != h->logits)
+      CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToDevice, h->stream));
+    if (ids != h->ids_buf) CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToDevice, h->stream));
+  }
+  set_filled(h, B, pos + 1);
+  return LLM_OK;
+}
+
+llm_status llm_step(llm_handle* h, const int32_t* tokens_host, int32_t B, int32_t pos, float temp, int32_t k, float p,
+                    const float* u_host, int32_t* ids_host, float* logits_host) {
+  if (!h || !tokens_host || !ids_host) return LLM_ERR_ARG;
+  return step_impl(h, tokens_host, nullptr, B, pos, temp, k, p, u_host, nullptr, ids_host, logits_host, true);
+}
+
+llm_status llm_step_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t pos, float temp, int32_t k,
+                        float p, const float* u_dev, int32_t* ids_dev, float* logits_dev) {
+  if (!h || !tokens_dev || !ids_dev) return LLM_ERR_ARG;
+  return step_impl(h, nullptr, tokens_dev, B, pos, temp, k, p, nullptr, u_dev, ids_dev, logits_dev, false);
+}
+
+static llm_status kv_copy(llm_handle* h, int32_t layer, int32_t row, int32_t pos0, int32_t n, void* k, void* v,
+                          bool import) {
+  if (!h || !k || !v) return LLM_ERR_ARG;
+  if (layer < 0 || layer >= h->L) return fail(h, LLM_ERR_ARG, "layer %d outside 0..%d", layer, h->L - 1);
+  if (row < 0 || row >= h->cfg.max_batch) return fail(h, LLM_ERR_BATCH, "row %d outside 0..%d", row, h->cfg.max_batch - 1);
+  if (pos0 < 0 || n < 0 || (int64_t)pos0 + n > h->cfg.max_seq)
+    return fail(h, LLM_ERR_POS_RANGE, "positions %d..+%d outside the cache of %d", pos0, n, h->cfg.max_seq);
+  const size_t es = h->es, hd = h->hd, kv = h->cfg.kv_heads, cap = h->cfg.max_seq;
+  const size_t bytes = (size_t)n * hd * es;
+  for (size_t j = 0; j < kv; ++j) {
+    const size_t elem = (size_t)layer * h->layer_cache_elems + (((size_t)row * kv + j) * cap + pos0) * hd;
+    char* dk = (char*)h->kc + elem * es;
+    char* dv = (char*)h->vc + elem * es;
+    char* hk = (char*)k + j * bytes;
+    char* hv = (char*)v + j * bytes;
+    if (import) {
+      CUDA_TRY(h, cudaMemcpyAsync(dk, hk, bytes, cudaMemcpyHostToDevice, h->stream));
+      CUDA_TRY(h, cudaMemcpyAsync(dv, hv, bytes, cudaMemcpyHostToDevice, h->stream));
+    } else {
+      CUDA_TRY(h, cudaMemcpyAsync(hk, dk, bytes, cudaMemcpyDeviceToHost, h->stream));
+      CUDA_TRY(h, cudaMemcpyAsync(hv, dv, bytes, cudaMemcpyDeviceToHost, h->stream));
+    }
+  }
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  if (import && h->filled[row] < pos0 + n) h->filled[row] = pos0 + n;
+  return LLM_OK;
+}
+
+llm_status llm_kv_import(llm_handle* h, int32_t layer, int32_t row, int32_t pos0, int32_t n, const void* k_host,
+                         const void* v_host) {
+  return kv_copy(h, layer, row, pos0, n, (void*)k_host, (void*)v_host, true);
+}
+
+llm_status llm_kv_export(llm_handle* h, int32_t layer, int32_t row, int32_t pos0, int32_t n, void* k_host, void* v_host) {
+  return kv_copy(h, layer, row, pos0, n, k_host, v_host, false);
+}
+
+llm_status llm_profile_kernel(llm_handle* h, int32_t which, int32_t B, int32_t pos, int32_t reps, float* ms_per_launch) {
+  if (!h || !ms_per_launch || reps < 1) return LLM_ERR_ARG;
+  if (which < K_QKV || which > K_SAMPLE) return fail(h, LLM_ERR_ARG, "kernel id %d outside 0..6", which);
+  TRY(check_rows(h, B, pos, 1));
+  std::vector<int32_t> toks(B, 0);
+  std::vector<float> u(B, 0.5f);
+  TRY(begin(h, pos, B, toks.data(), nullptr, 1, 0, 1.0f, h->V, 1.0f, u.data(), nullptr));
+  TRY(launch_one(h, K_EMBED, 0, B, false));
+  cudaEvent_t e0, e1;
+  CUDA_TRY(h, cudaEventCreate(&e0));
+  CUDA_TRY(h, cudaEventCreate(&e1));
+  CUDA_TRY(h, cudaEventRecord(e0, h->stream));
+  for (int r = 0; r < reps; ++r) TRY(launch_one(h, which, r % h->L, B, false));
+  CUDA_TRY(h, cudaEventRecord(e1, h->stream));
+  CUDA_TRY(h, cudaEventSynchronize(e1));
+  float ms = 0.f;
+  CUDA_TRY(h, cudaEventElapsedTime(&ms, e0, e1));
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  *ms_per_launch = ms / reps;
+  return LLM_OK;
+}
+
+llm_status llm_debug_trace(llm_handle* h, int32_t layer, const char* name, float* dst_host) {
+  if (!h || !name || !dst_host) return LLM_ERR_ARG;
+  if (!h->cfg.debug_trace) return fail(h, LLM_ERR_ARG, "the handle was created without debug_trace");
+  if (layer < 0 || layer >= h->L) return fail(h, LLM_ERR_ARG, "layer %d outside 0..%d", layer, h->L - 1);
+  static const char* names[5] = {"q", "attn", "x1", "m", "y"};
+  int which = -1;
+  for (int i = 0; i < 5; ++i)
+    if (!strcmp(name, names[i])) which = i;
+  if (which < 0) return fail(h, LLM_ERR_ARG, "unknown trace name %s", name);
+  const size_t maxw = (size_t)std::max(h->d, h->f);
+  const size_t width = which == 3 ? (size_t)h->f : (size_t)h->d;
+  const float* src = h->trace + ((size_t)layer * 5 + which) * h->cfg.max_batch * maxw;
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  CUDA_TRY(h, cudaMemcpy2D(dst_host, width * 4, src, maxw * 4, width * 4, h->cfg.max_batch, cudaMemcpyDeviceToHost));
+  return LLM_OK;
+}
+
+}  // extern "C"

@@ -57,6 +57,9 @@ def lib():
             "or_reset": ([vp], None),
             "or_forward": ([vp, i32, i32, i32, vp], i32),
             "or_prefill": ([vp, i32, vp, i32, i32, vp], i32),
+            "or_embed": ([vp, i32], i32),
+            "or_layer": ([vp, i32, i32, i32], i32),
+            "or_head": ([vp, vp], None),
             "or_forward_full": ([pc, vp, u64, vp, i32, vp], i32),
             "or_attend": ([vp, i32, i32, vp, i32, vp], i32),
             "or_kv_write": ([vp, i32, i32, i32, i32, vp, vp], i32),
@@ -227,6 +230,21 @@ class Model:
         r = lib().or_forward(self.h, b, int(tok), t, out.ctypes.data if logits else None)
         if r:
             raise ValueError(f"or_forward: {r}")
+        return out
+
+    def embed(self, tok):
+        r = lib().or_embed(self.h, int(tok))
+        if r:
+            raise ValueError(f"or_embed: {r}")
+
+    def layer(self, l, b, t):
+        r = lib().or_layer(self.h, l, b, t)
+        if r:
+            raise ValueError(f"or_layer: {r}")
+
+    def head(self):
+        out = np.empty(self.cfg.vocab, np.float32)
+        lib().or_head(self.h, out.ctypes.data)
         return out
 
     def prefill(self, b, toks, pos, logits=True):

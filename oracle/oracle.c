@@ -535,13 +535,21 @@ static void keep(or_model* M, int32_t l, int32_t which, const float* src, int32_
   if (M->trace) memcpy(M->act + ((size_t)l * A_COUNT + (size_t)which) * (size_t)M->act_w, src, sizeof(float) * (size_t)n);
 }
 
-/* [P1] forward (logits != NULL) / forward_pre (logits == NULL): token tok at position t of
- * row b, with that row's caches holding positions 0..t-1. */
-int32_t or_forward(or_model* M, int32_t b, int32_t tok, int32_t t, float* logits) {
+/* The pieces of one position, applied in P1 forward's order: or_embed (the embedding row of
+ * tok into the residual stream), or_layer for l = 0..L-1 (P1 block at position t of row b), and
+ * or_head (final norm and LM head).  or_forward runs them in that order. */
+int32_t or_embed(or_model* M, int32_t tok) {
+  if (tok < 0 || tok >= M->c.vocab) return OR_ERR_TOKEN_RANGE;
+  for (int32_t i = 0; i < M->d; ++i) M->x[i] = W(M, (uint64_t)tok * (uint64_t)M->d + (uint64_t)i);
+  return 0;
+}
+
+/* [P1] block: layer l at position t of row b on the residual stream x (in place), with the
+ * row's cache holding positions 0..t-1 of that layer */
+int32_t or_layer(or_model* M, int32_t l, int32_t b, int32_t t) {
   const or_cfg* c = &M->c;
-  if (b < 0 || b >= c->batch) return OR_ERR_ARG;
+  if (l < 0 || l >= M->L || b < 0 || b >= c->batch) return OR_ERR_ARG;
   if (t < 0 || t >= c->cap) return OR_ERR_POS_RANGE;
-  if (tok < 0 || tok >= c->vocab) return OR_ERR_TOKEN_RANGE;
   const int32_t d = M->d, hd = M->hd, half = c->half, kvw = M->kvw, f = M->f;
   float cs[256], sn[256];
   for (int32_t i = 0; i < half; ++i) {
@@ -549,57 +557,70 @@ int32_t or_forward(or_model* M, int32_t b, int32_t tok, int32_t t, float* logits
     cs[i] = (float)cos((double)a);
     sn[i] = (float)sin((double)a);
   }
-  /* embedding row (bf16 widened exactly) */
-  for (int32_t i = 0; i < d; ++i) M->x[i] = W(M, (uint64_t)tok * (uint64_t)d + (uint64_t)i);
   float* g = (float*)malloc(sizeof(float) * (size_t)d);
   uint64_t es = M->cache_bf16 ? 2 : 4;
-  for (int32_t l = 0; l < M->L; ++l) {
-    keep(M, l, A_X, M->x, d);
-    gains(M, toff(M, l, T_LN1), d, g);
-    or_rmsnorm(M->x, g, d, c->eps, M->n1);
-    matvec(M, toff(M, l, T_Q), d, d, M->n1, M->q);
-    matvec(M, toff(M, l, T_K), kvw, d, M->n1, M->k);
-    matvec(M, toff(M, l, T_V), kvw, d, M->n1, M->v);
-    for (int32_t h = 0; h < M->H; ++h) or_rope_head(M->q + (size_t)h * hd, half, cs, sn, M->qr + (size_t)h * hd);
-    for (int32_t j = 0; j < c->kv; ++j) or_rope_head(M->k + (size_t)j * hd, half, cs, sn, M->kr + (size_t)j * hd);
-    /* KV.push at t: the rotated keys and the values, one array pair per key/value head */
-    for (int32_t j = 0; j < c->kv; ++j)
-      for (int32_t e = 0; e < hd; ++e) {
-        uint64_t ci = cidx(M, l, b, j, t) + (uint64_t)e;
-        cput(M, M->kc, ci, M->kr[j * hd + e]);
-        cput(M, M->vc, ci, M->v[j * hd + e]);
-      }
-    uint64_t base = cidx(M, l, b, 0, 0);
-    attend(M, M->qr, (const char*)M->kc + base * es, (const char*)M->vc + base * es, t, M->att);
-    matvec(M, toff(M, l, T_O), d, d, M->att, M->a);
-    for (int32_t i = 0; i < d; ++i) M->x1[i] = M->x[i] + M->a[i];
-    gains(M, toff(M, l, T_LN2), d, g);
-    or_rmsnorm(M->x1, g, d, c->eps, M->n2);
-    matvec(M, toff(M, l, T_GATE), f, d, M->n2, M->gg);
-    matvec(M, toff(M, l, T_UP), f, d, M->n2, M->uu);
-    for (int32_t i = 0; i < f; ++i) M->uu[i] = silu(M->gg[i]) * M->uu[i];
-    matvec(M, toff(M, l, T_DOWN), d, f, M->uu, M->m);
-    for (int32_t i = 0; i < d; ++i) M->y[i] = M->x1[i] + M->m[i];
-    keep(M, l, A_N1, M->n1, d);
-    keep(M, l, A_Q, M->q, d);
-    keep(M, l, A_K, M->k, kvw);
-    keep(M, l, A_V, M->v, kvw);
-    keep(M, l, A_QR, M->qr, d);
-    keep(M, l, A_KR, M->kr, kvw);
-    keep(M, l, A_ATTN, M->att, d);
-    keep(M, l, A_A, M->a, d);
-    keep(M, l, A_X1, M->x1, d);
-    keep(M, l, A_N2, M->n2, d);
-    keep(M, l, A_M, M->m, d);
-    keep(M, l, A_Y, M->y, d);
-    memcpy(M->x, M->y, sizeof(float) * (size_t)d);
-  }
-  if (logits) {
-    gains(M, M->off_lnf, d, g);
-    or_rmsnorm(M->x, g, d, c->eps, M->nf);
-    matvec(M, M->off_head, M->V, d, M->nf, logits);
-  }
+  keep(M, l, A_X, M->x, d);
+  gains(M, toff(M, l, T_LN1), d, g);
+  or_rmsnorm(M->x, g, d, c->eps, M->n1);
+  matvec(M, toff(M, l, T_Q), d, d, M->n1, M->q);
+  matvec(M, toff(M, l, T_K), kvw, d, M->n1, M->k);
+  matvec(M, toff(M, l, T_V), kvw, d, M->n1, M->v);
+  for (int32_t h = 0; h < M->H; ++h) or_rope_head(M->q + (size_t)h * hd, half, cs, sn, M->qr + (size_t)h * hd);
+  for (int32_t j = 0; j < c->kv; ++j) or_rope_head(M->k + (size_t)j * hd, half, cs, sn, M->kr + (size_t)j * hd);
+  /* KV.push at t: the rotated keys and the values, one array pair per key/value head */
+  for (int32_t j = 0; j < c->kv; ++j)
+    for (int32_t e = 0; e < hd; ++e) {
+      uint64_t ci = cidx(M, l, b, j, t) + (uint64_t)e;
+      cput(M, M->kc, ci, M->kr[j * hd + e]);
+      cput(M, M->vc, ci, M->v[j * hd + e]);
+    }
+  uint64_t base = cidx(M, l, b, 0, 0);
+  attend(M, M->qr, (const char*)M->kc + base * es, (const char*)M->vc + base * es, t, M->att);
+  matvec(M, toff(M, l, T_O), d, d, M->att, M->a);
+  for (int32_t i = 0; i < d; ++i) M->x1[i] = M->x[i] + M->a[i];
+  gains(M, toff(M, l, T_LN2), d, g);
+  or_rmsnorm(M->x1, g, d, c->eps, M->n2);
+  matvec(M, toff(M, l, T_GATE), f, d, M->n2, M->gg);
+  matvec(M, toff(M, l, T_UP), f, d, M->n2, M->uu);
+  for (int32_t i = 0; i < f; ++i) M->uu[i] = silu(M->gg[i]) * M->uu[i];
+  matvec(M, toff(M, l, T_DOWN), d, f, M->uu, M->m);
+  for (int32_t i = 0; i < d; ++i) M->y[i] = M->x1[i] + M->m[i];
+  keep(M, l, A_N1, M->n1, d);
+  keep(M, l, A_Q, M->q, d);
+  keep(M, l, A_K, M->k, kvw);
+  keep(M, l, A_V, M->v, kvw);
+  keep(M, l, A_QR, M->qr, d);
+  keep(M, l, A_KR, M->kr, kvw);
+  keep(M, l, A_ATTN, M->att, d);
+  keep(M, l, A_A, M->a, d);
+  keep(M, l, A_X1, M->x1, d);
+  keep(M, l, A_N2, M->n2, d);
+  keep(M, l, A_M, M->m, d);
+  keep(M, l, A_Y, M->y, d);
+  memcpy(M->x, M->y, sizeof(float) * (size_t)d);
   free(g);
+  return 0;
+}
+
+/* [P1] head_of: the final norm, then logits = head . nf (head = the embedding when tied) */
+void or_head(or_model* M, float* logits) {
+  float* g = (float*)malloc(sizeof(float) * (size_t)M->d);
+  gains(M, M->off_lnf, M->d, g);
+  or_rmsnorm(M->x, g, M->d, M->c.eps, M->nf);
+  matvec(M, M->off_head, M->V, M->d, M->nf, logits);
+  free(g);
+}
+
+/* [P1] forward (logits != NULL) / forward_pre (logits == NULL): token tok at position t of
+ * row b, with that row's caches holding positions 0..t-1. */
+int32_t or_forward(or_model* M, int32_t b, int32_t tok, int32_t t, float* logits) {
+  const or_cfg* c = &M->c;
+  if (b < 0 || b >= c->batch) return OR_ERR_ARG;
+  if (t < 0 || t >= c->cap) return OR_ERR_POS_RANGE;
+  if (tok < 0 || tok >= c->vocab) return OR_ERR_TOKEN_RANGE;
+  or_embed(M, tok);
+  for (int32_t l = 0; l < M->L; ++l) or_layer(M, l, b, t);
+  if (logits) or_head(M, logits);
   return 0;
 }
 

@@ -35,6 +35,9 @@ or_model* or_create(const or_cfg* c, const void* weights, uint64_t nbytes, int32
 void or_destroy(or_model* m);
 void or_reset(or_model* m);
 int32_t or_forward(or_model* m, int32_t b, int32_t tok, int32_t t, float* logits);
+int32_t or_embed(or_model* m, int32_t tok);
+int32_t or_layer(or_model* m, int32_t l, int32_t b, int32_t t);
+void or_head(or_model* m, float* logits);
 int32_t or_prefill(or_model* m, int32_t b, const int32_t* toks, int32_t S, int32_t pos, float* logits);
 int32_t or_forward_full(const or_cfg* c, const void* weights, uint64_t nbytes, const int32_t* toks,
                         int32_t S, float* logits);

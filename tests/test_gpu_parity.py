@@ -1,0 +1,284 @@
+"""Parity of the GPU library with the oracle, through the C ABI (needs a GPU).
+
+Tolerances (fixed by the target): token ids and every integer decision bit-exact; the f32
+model's logits within 1e-4 of the oracle's logit range; bf16-weight models within an absolute
+3e-2 with greedy argmax agreement on at least 99% of decode steps.  Decoding is teacher-forced:
+the oracle replays the token stream the GPU produced, so one near-tie cannot make the two runs
+diverge (bend-ml-llama's blog notes free-running streams drift apart after a few hundred tokens).
+"""
+import multiprocessing as mp
+
+import numpy as np
+import pytest
+
+import llama_architecture_kv_gb300 as pkg
+import oracle
+import synth
+from synth import WORKLOADS, shrink
+from synth.configs import TINY
+from tests.blob import views
+
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 1e-4      # of the logit range, f32 model
+BF16_ABS = 3e-2     # absolute, bf16-weight models
+ARGMAX_AGREE = 0.99
+
+
+def rel_err(a, ref):
+    return float(np.max(np.abs(a - ref))) / float(ref.max() - ref.min())
+
+
+def make(shape, seed, B, cap, wstd=0.02, debug_trace=False):
+    blob = synth.model_blob(shape, seed, wstd=wstd)
+    g = pkg.Model(shape, blob, max_batch=B, max_seq=cap, debug_trace=debug_trace)
+    return blob, g
+
+
+def check_bf16(gl, ol, agree):
+    err = float(np.max(np.abs(gl - ol)))
+    assert err <= BF16_ABS, err
+    agree.append(int(np.argmax(gl)) == oracle.argmax(ol))
+
+
+# ---------------------------------------------------------------------------------------
+# f32 tiny model (the exact workload and shape variants)
+# ---------------------------------------------------------------------------------------
+
+def run_teacher_forced(shape, blob, gpu, prompts, steps, f32=True):
+    B, S = prompts.shape
+    cap = gpu.cfg.max_seq
+    refs = [oracle.Model(oracle.cfg_of(shape, 1, cap), blob) for _ in range(B)]
+    lg = gpu.prefill(prompts, 0)
+    agree = []
+    for b in range(B):
+        lo = refs[b].prefill(0, prompts[b], 0)
+        if f32:
+            assert rel_err(lg[b], lo) <= F32_TOL
+        else:
+            check_bf16(lg[b], lo, agree)
+    toks = np.array([np.argmax(lg[b]) for b in range(B)], np.int32)
+    for t in range(S, S + steps):
+        ids, lg = gpu.step(toks, t, logits=True)
+        for b in range(B):
+            lo = refs[b].forward(0, int(toks[b]), t)
+            if f32:
+                assert rel_err(lg[b], lo) <= F32_TOL, (t, b, rel_err(lg[b], lo))
+            else:
+                check_bf16(lg[b], lo, agree)
+            assert int(ids[b]) == oracle.argmax(lg[b])  # greedy id, bit-exact on the same logits
+        toks = ids
+    for r in refs:
+        r.close()
+    return agree
+
+
+def test_tiny_f32_workload():
+    w = WORKLOADS["tiny_f32"]
+    blob, g = make(w.shape, w.seed_weights, 1, w.cap)
+    prompt = synth.tokens(w.seed_tokens, 0, w.prompt, w.shape.vocab)[None]
+    run_teacher_forced(w.shape, blob, g, prompt, w.steps)
+    g.close()
+
+
+@pytest.mark.parametrize("name,shape", [
+    ("g1", shrink(TINY, kv=4, g=1)),
+    ("g4_odd_ffn", shrink(TINY, kv=1, g=4, ffn=92)),
+    ("untied_llama3", shrink(TINY, tied=False, llama3=True, orig_max=64.0)),
+    ("g3_hd64", shrink(TINY, kv=2, g=3, half=32, ffn=200, vocab=300)),
+    ("hd128_g4", shrink(TINY, kv=2, g=4, half=64, ffn=512, vocab=1000, layers=2)),
+], ids=lambda x: x if isinstance(x, str) else "")
+def test_tiny_f32_variants_batched(name, shape):
+    B, S, steps = 3, 7, 6
+    blob, g = make(shape, 77, B, 16, wstd=0.1)
+    prompts = synth.tokens(78, 0, B * S, shape.vocab).reshape(B, S)
+    run_teacher_forced(shape, blob, g, prompts, steps)
+    g.close()
+
+
+def test_long_cache_many_splits_f32():
+    # enough positions that attention uses many splits and a ragged last tile
+    shape = shrink(TINY, kv=2, g=2, half=32, ffn=256, vocab=512, layers=2)
+    cap = 700
+    blob, g = make(shape, 91, 2, cap, wstd=0.05)
+    prompts = synth.tokens(92, 0, 2 * 611, shape.vocab).reshape(2, 611)
+    run_teacher_forced(shape, blob, g, prompts, 3)
+    g.close()
+
+
+# ---------------------------------------------------------------------------------------
+# laws on the GPU
+# ---------------------------------------------------------------------------------------
+
+def test_causality_future_cache_entries_never_read():
+    w = WORKLOADS["tiny_f32"]
+    s = w.shape
+    blob, g = make(s, w.seed_weights, 1, 16)
+    toks = synth.tokens(w.seed_tokens, 0, 8, s.vocab)
+    g.prefill(toks[None, :6], 0, logits=False)
+    a = g.decode(toks[6:7], 6)
+    junk = np.full((s.kv, 16 - 7, s.hd), np.nan, np.float32)
+    for layer in range(s.layers):
+        g.kv_import(layer, 0, 7, junk, junk)
+    b = g.decode(toks[6:7], 6)  # rewind to 6: rewrites position 6, reads 0..6 only
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    g.close()
+
+
+def test_gqa_query_heads_read_their_group():
+    # one layer with W_q = W_k = 0 (every score 0: uniform weights) and W_v = 0 (the new value
+    # is 0); the cache holds marker(j) = (j+1) e_j at positions 0..t-1 of kv head j, so query
+    # head h's output is marker(h // g) * t / (t + 1)
+    s = shrink(TINY, kv=3, g=4, half=8, layers=1)
+    blob = synth.model_blob(s, 5)
+    v = views(s, blob)
+    for name in ("q", "k", "v"):
+        v[(0, name)][...] = 0
+    g = pkg.Model(s, blob, max_batch=1, max_seq=8, debug_trace=True)
+    t = 5
+    kk = np.zeros((s.kv, t, s.hd), np.float32)
+    vv = np.zeros((s.kv, t, s.hd), np.float32)
+    for j in range(s.kv):
+        vv[j, :, j] = j + 1
+    g.kv_import(0, 0, 0, kk, vv)
+    g.decode(np.array([3], np.int32), t)
+    att = g.trace(0, "attn")[0].reshape(s.heads, s.hd)
+    for h in range(s.heads):
+        want = np.zeros(s.hd, np.float32)
+        want[h // s.g] = (h // s.g + 1) * t / (t + 1)
+        np.testing.assert_allclose(att[h], want, rtol=1e-6, atol=1e-7)
+    g.close()
+
+
+def test_deterministic_bits():
+    w = WORKLOADS["tiny_f32"]
+    blob, g = make(w.shape, w.seed_weights, 2, 16)
+    toks = synth.tokens(w.seed_tokens, 0, 16, w.shape.vocab).reshape(2, 8)
+    a = g.prefill(toks, 0)
+    b = g.prefill(toks, 0)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    g.close()
+
+
+def test_kv_cache_holds_rotated_keys_rounded_like_the_oracle():
+    # bf16 model: the cache row written at position t equals the oracle's (same bf16 rounding of
+    # the same f32 values, up to the f32 differences of the projections)
+    s = shrink(WORKLOADS["smollm2_135m"].shape, layers=2, vocab=1000)
+    blob, g = make(s, 31, 1, 8)
+    ref = oracle.Model(oracle.cfg_of(s, 1, 8), blob)
+    toks = synth.tokens(32, 0, 5, s.vocab)
+    g.prefill(toks[None], 0, logits=False)
+    ref.prefill(0, toks, 0, logits=False)
+    for layer in range(2):
+        gk, gv = g.kv_export(layer, 0, 0, 5)
+        ok, ov = ref.kv_read(layer, 0, 0, 5)
+        for a, b in ((gk, ok), (gv, ov)):
+            fa, fb = synth.bf16_to_f32(a), synth.bf16_to_f32(b)
+            assert np.max(np.abs(fa - fb)) <= 2 ** -7 * np.max(np.abs(fb)) + 1e-6
+            assert np.mean(a == b) > 0.97
+    g.close()
+    ref.close()
+
+
+# ---------------------------------------------------------------------------------------
+# the sampler: bit-exact ids on identical logits and draws
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("V", [5, 256, 49152, 128256])
+def test_sampler_ids_bit_exact(V):
+    s = shrink(TINY, vocab=V)
+    blob, g = make(s, 3, 8, 4)
+    rng = np.random.default_rng(V)
+    for trial in range(12):
+        B = int(rng.integers(1, 9))
+        if trial % 4 == 0:
+            logits = rng.integers(-3, 4, (B, V)).astype(np.float32)  # many ties
+        else:
+            logits = (rng.standard_normal((B, V)) * rng.choice([0.5, 2, 8])).astype(np.float32)
+        temp = float(rng.choice([0.0, 0.3, 0.7, 0.8, 1.5]))
+        k = int(rng.choice([1, 2, 50, V, V + 10]))
+        p = float(rng.choice([1e-3, 0.5, 0.9, 0.95, 1.0]))
+        u = synth.uniforms(4000 + trial, 0, B)
+        ids = g.sample(logits, temp, k, p, u)
+        for b in range(B):
+            want = oracle.argmax(logits[b]) if temp == 0 else oracle.sample(logits[b], temp, k, p, float(u[b]))
+            assert int(ids[b]) == want, (trial, b, temp, k, p, float(u[b]))
+    g.close()
+
+
+# ---------------------------------------------------------------------------------------
+# errors at the boundary
+# ---------------------------------------------------------------------------------------
+
+def test_boundary_errors():
+    w = WORKLOADS["tiny_f32"]
+    blob, g = make(w.shape, w.seed_weights, 2, 8)
+    V = w.shape.vocab
+
+    def status(fn):
+        with pytest.raises(pkg.LlmError) as e:
+            fn()
+        return e.value.status
+
+    assert status(lambda: g.decode(np.array([1], np.int32), 1)) == pkg.LLM_ERR_POS_RANGE  # past filled
+    assert status(lambda: g.prefill(np.ones((1, 9), np.int32), 0)) == pkg.LLM_ERR_POS_RANGE  # > cap
+    assert status(lambda: g.decode(np.array([V], np.int32), 0)) == pkg.LLM_ERR_TOKEN_RANGE
+    assert status(lambda: g.decode(np.array([-1], np.int32), 0)) == pkg.LLM_ERR_TOKEN_RANGE
+    assert status(lambda: g.decode(np.ones(3, np.int32), 0)) == pkg.LLM_ERR_BATCH
+    lg = np.zeros((1, V), np.float32)
+    assert status(lambda: g.sample(lg, -1.0, 1, 1.0, [0.5])) == pkg.LLM_ERR_ARG
+    assert status(lambda: g.sample(lg, 1.0, 0, 1.0, [0.5])) == pkg.LLM_ERR_ARG
+    assert status(lambda: g.sample(lg, 1.0, 5, 0.0, [0.5])) == pkg.LLM_ERR_ARG
+    assert status(lambda: g.sample(lg, 1.0, 5, 1.0, [1.0])) == pkg.LLM_ERR_ARG
+    # a failed call leaves the handle usable
+    g.prefill(np.ones((2, 3), np.int32), 0)
+    assert g.filled(0) == 3 and g.filled(1) == 3
+    g.close()
+
+
+def test_device_token_check_reports_on_synchronize():
+    torch = pytest.importorskip("torch")
+    w = WORKLOADS["tiny_f32"]
+    blob, g = make(w.shape, w.seed_weights, 1, 8)
+    tok = torch.tensor([w.shape.vocab + 5], dtype=torch.int32, device="cuda")
+    out = torch.empty((1, w.shape.vocab), dtype=torch.float32, device="cuda")
+    pkg.llm_decode_dev(g.h, tok, 1, 0, out)
+    with pytest.raises(pkg.LlmError) as e:
+        g.synchronize()
+    assert e.value.status == pkg.LLM_ERR_TOKEN_RANGE
+    g.synchronize()  # cleared
+    g.close()
+
+
+def test_device_pointer_variants_match_host_variants():
+    torch = pytest.importorskip("torch")
+    w = WORKLOADS["tiny_f32"]
+    blob, g = make(w.shape, w.seed_weights, 2, 16)
+    toks = synth.tokens(w.seed_tokens, 0, 12, w.shape.vocab).reshape(2, 6)
+    host = g.prefill(toks, 0)
+    td = torch.from_numpy(toks).cuda()
+    out = torch.empty((2, w.shape.vocab), dtype=torch.float32, device="cuda")
+    pkg.llm_prefill_dev(g.h, td, 2, 6, 0, out)
+    g.synchronize()
+    assert np.array_equal(out.cpu().numpy(), host)
+    ids = torch.empty(2, dtype=torch.int32, device="cuda")
+    u = torch.tensor([0.25, 0.75], dtype=torch.float32, device="cuda")
+    pkg.llm_step_dev(g.h, td[:, 5].contiguous(), 2, 6, 0.8, 20, 0.9, u, ids, out)
+    g.synchronize()
+    lg = out.cpu().numpy()
+    for b in range(2):
+        assert int(ids[b]) == oracle.sample(lg[b], 0.8, 20, 0.9, [0.25, 0.75][b])
+    g.close()
+
+
+# ---------------------------------------------------------------------------------------
+# bf16 models
+# ---------------------------------------------------------------------------------------
+
+def test_smollm2_135m_short():
+    w = WORKLOADS["smollm2_135m"]
+    blob, g = make(w.shape, w.seed_weights, 1, 64)
+    prompt = synth.tokens(w.seed_tokens, 0, 24, w.shape.vocab)[None]
+    agree = run_teacher_forced(w.shape, blob, g, prompt, 12, f32=False)
+    assert np.mean(agree) >= ARGMAX_AGREE
+    g.close()
