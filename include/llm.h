@@ -171,8 +171,8 @@ float* llm_logits_buffer(llm_handle* h);
 /* Filled length of cache row b (-1 if b is out of range). */
 int32_t llm_filled(const llm_handle* h, int32_t b);
 
-/* A message for the last failure on h (owned by h; valid until the next call), and a name for
- * a status code. */
+/* A message for the last failure on h (owned by h; valid until the next call); with h == NULL,
+ * why the last llm_create on the calling thread failed.  And a name for a status code. */
 const char* llm_last_error(const llm_handle* h);
 const char* llm_status_string(llm_status s);
 

@@ -128,7 +128,9 @@ def llm_create(cfg: LlmConfig, weights, weights_on_device=False, stream=None):
     st = lib().llm_create(ctypes.byref(cfg), _ptr(weights), nbytes, int(weights_on_device),
                           stream, ctypes.byref(h))
     if st != LLM_OK:
-        raise LlmError(st, f"llm_create: {lib().llm_status_string(st).decode()}")
+        why = lib().llm_last_error(None)
+        raise LlmError(st, f"llm_create: {lib().llm_status_string(st).decode()}: "
+                           f"{why.decode() if why else ''}")
     return h.value
 
 

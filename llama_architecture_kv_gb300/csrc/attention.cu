@@ -269,7 +269,10 @@ cudaError_t attn_prepare(int max_smem_optin) {
     for (int hd : {16, 32, 64, 128, 256}) {
       size_t sm = 0;
       AttnFn fn = kt ? pick_hd<1>(hd, &sm, 1) : pick_hd<0>(hd, &sm, 1);
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin);
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin - (int)fa.sharedSizeBytes);
       if (e != cudaSuccess) return e;
     }
   return cudaSuccess;

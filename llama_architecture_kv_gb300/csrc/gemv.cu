@@ -302,9 +302,12 @@ cudaError_t gemv_prepare(int max_smem_optin) {
     for (int bt : {1, 2, 4, 8})
       for (int epi = 0; epi < 4; ++epi)
         for (int norm = 0; norm < 2; ++norm) {
-          cudaError_t e = cudaFuncSetAttribute(pick(wt, bt, epi, norm != 0),
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               max_smem_optin);
+          GemvFn fn = pick(wt, bt, epi, norm != 0);
+          cudaFuncAttributes fa;
+          cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+          if (e != cudaSuccess) return e;
+          e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   max_smem_optin - (int)fa.sharedSizeBytes);
           if (e != cudaSuccess) return e;
         }
   return cudaSuccess;

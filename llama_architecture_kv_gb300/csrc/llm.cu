@@ -187,6 +187,8 @@ struct llm_handle {
 
 namespace {
 
+thread_local std::string g_create_err;  // why the last llm_create on this thread failed
+
 llm_status fail(llm_handle* h, llm_status s, const char* fmt, ...) {
   if (h) {
     char buf[512];
@@ -560,7 +562,7 @@ const char* llm_status_string(llm_status s) {
   }
 }
 
-const char* llm_last_error(const llm_handle* h) { return h ? h->err.c_str() : "no handle"; }
+const char* llm_last_error(const llm_handle* h) { return h ? h->err.c_str() : g_create_err.c_str(); }
 
 llm_status llm_destroy(llm_handle* h) {
   if (!h) return LLM_ERR_ARG;
@@ -575,11 +577,24 @@ llm_status llm_destroy(llm_handle* h) {
 
 llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbytes, int32_t weights_on_device,
                       void* cuda_stream, llm_handle** out) {
-  if (!cfg || !weights || !out) return LLM_ERR_ARG;
+  if (!cfg || !weights || !out) {
+    g_create_err = "NULL argument";
+    return LLM_ERR_ARG;
+  }
   *out = nullptr;
-  if (check_config(cfg)) return LLM_ERR_CONFIG;
+  if (const char* why = check_config(cfg)) {
+    g_create_err = why;
+    return LLM_ERR_CONFIG;
+  }
   const uint64_t es = cfg->dtype == LLM_DTYPE_BF16 ? 2 : 4;
-  if (nbytes != count_of(cfg) * es) return LLM_ERR_WEIGHTS_SIZE;
+  if (nbytes != count_of(cfg) * es) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "weights hold %llu bytes, the layout needs %llu",
+             (unsigned long long)nbytes, (unsigned long long)(count_of(cfg) * es));
+    g_create_err = buf;
+    return LLM_ERR_WEIGHTS_SIZE;
+  }
+  g_create_err.clear();
   llm_handle* h = new llm_handle();
   h->cfg = *cfg;
   const llm_config& c = h->cfg;
@@ -595,34 +610,42 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   h->filled.assign(c.max_batch, 0);
   llm_status st = LLM_OK;
   auto bail = [&](llm_status s) {
-    h->err.clear();
+    cudaError_t ce = cudaGetLastError();
+    g_create_err = h->err.empty() ? std::string(llm_status_string(s)) : h->err;
+    if (ce != cudaSuccess) g_create_err += std::string(" (last CUDA error: ") + cudaGetErrorString(ce) + ")";
     llm_destroy(h);
     return s;
   };
-  if (cudaGetDevice(&h->dev) != cudaSuccess) return bail(LLM_ERR_CUDA);
+  auto cuda_bail = [&](const char* what, cudaError_t e) {
+    fail(h, LLM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return bail(LLM_ERR_CUDA);
+  };
+  cudaError_t ce;
+  if ((ce = cudaGetDevice(&h->dev)) != cudaSuccess) return cuda_bail("cudaGetDevice", ce);
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->dev);
   cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev);
   if (cuda_stream) {
     h->stream = (cudaStream_t)cuda_stream;
   } else {
-    if (cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking) != cudaSuccess) return bail(LLM_ERR_CUDA);
+    if ((ce = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking)) != cudaSuccess) return cuda_bail("stream", ce);
     h->own_stream = true;
   }
-  if (cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) return bail(LLM_ERR_CUDA);
-  if (gemv_prepare(h->smem_optin) != cudaSuccess || attn_prepare(h->smem_optin) != cudaSuccess ||
-      sample_prepare() != cudaSuccess)
-    return bail(LLM_ERR_CUDA);
+  if ((ce = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking)) != cudaSuccess) return cuda_bail("capture stream", ce);
+  if ((ce = gemv_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("gemv kernel attributes", ce);
+  if ((ce = attn_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("attention kernel attributes", ce);
+  if ((ce = sample_prepare()) != cudaSuccess) return cuda_bail("sampler kernel attributes", ce);
   // weights: a device copy of the blob when it is on the host, then repacked
   const char* blob = (const char*)weights;
   char* staging = nullptr;
   if (!weights_on_device) {
-    if (cudaMalloc(&staging, nbytes) != cudaSuccess) {
+    if ((ce = cudaMalloc(&staging, nbytes)) != cudaSuccess) {
       cudaGetLastError();
+      fail(h, LLM_ERR_OOM, "cudaMalloc(%llu bytes) for the weight staging copy: %s", (unsigned long long)nbytes, cudaGetErrorString(ce));
       return bail(LLM_ERR_OOM);
     }
-    if (cudaMemcpy(staging, weights, nbytes, cudaMemcpyHostToDevice) != cudaSuccess) {
+    if ((ce = cudaMemcpy(staging, weights, nbytes, cudaMemcpyHostToDevice)) != cudaSuccess) {
       cudaFree(staging);
-      return bail(LLM_ERR_CUDA);
+      return cuda_bail("weights upload", ce);
     }
     blob = staging;
   }
@@ -658,11 +681,12 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
       cudaMemsetAsync(h->status, 0, 16, h->stream) != cudaSuccess ||
       cudaMemsetAsync(h->kc, 0, cache_bytes, h->stream) != cudaSuccess ||
       cudaMemsetAsync(h->vc, 0, cache_bytes, h->stream) != cudaSuccess)
-    return bail(LLM_ERR_CUDA);
+    return cuda_bail("clearing the cache", cudaGetLastError());
   RopeArgs ra = {c.theta, h->hd, c.half, c.max_seq, c.rope_llama3, c.rope_factor, c.rope_low_freq, c.rope_high_freq,
                  c.rope_orig_max_pos, h->rope_cos, h->rope_sin};
   rope_table_kernel<<<1024, 256, 0, h->stream>>>(ra);
-  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(h->stream) != cudaSuccess) return bail(LLM_ERR_CUDA);
+  if ((ce = cudaGetLastError()) != cudaSuccess || (ce = cudaStreamSynchronize(h->stream)) != cudaSuccess)
+    return cuda_bail("RoPE tables", ce);
   *out = h;
   return LLM_OK;
 }
