@@ -13,6 +13,7 @@ Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the pla
 decoder under oracle/) on the same workload instead, on a bounded sample per step.
 """
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -50,6 +51,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-layers", type=int, default=2,
                     help="reference arm: layers of the model run per timed step")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
+    ap.add_argument("--prompt", type=int, default=-1, help="override the prompt length (profiling)")
+    ap.add_argument("--kernels", action="store_true",
+                    help="print each kernel's isolated launch time (CUDA events) and exit")
     return ap.parse_args()
 
 
@@ -213,6 +218,26 @@ def run_reference(args):
 # the GPU arm
 # ---------------------------------------------------------------------------------------
 
+def kernel_table(pkg, h, w, B, pos):
+    """Each kernel of the step timed alone (llm_profile_kernel), with its algorithmic bytes."""
+    s = w.shape
+    es = 2 if s.bf16 else 4
+    kvb = B * 2 * s.kv * s.hd * es * (pos + 1)
+    nbytes = {"qkv": (s.d + 2 * s.kvw) * s.d * es, "attention": kvb, "o_proj": s.d * s.d * es,
+              "gate_up": 2 * s.ffn * s.d * es, "down": s.d * s.ffn * es,
+              "lm_head": s.vocab * s.d * es, "sampler": B * s.vocab * 4}
+    peak, _ = peaks()
+    rows = {}
+    for name, kid in pkg.KERNELS.items():
+        ms = pkg.llm_profile_kernel(h, kid, B, pos, 2 * s.layers)
+        gbs = nbytes[name] / (ms / 1e3) / 1e9
+        rows[name] = {"us": ms * 1e3, "bytes": nbytes[name], "GB/s": gbs, "frac": gbs / peak}
+    per_step = sum(rows[k]["us"] * (s.layers if k in ("qkv", "attention", "o_proj", "gate_up", "down") else 1)
+                   for k in rows)
+    print(json.dumps({"workload": w.name, "layers": s.layers, "batch": B, "pos": pos,
+                      "kernels": rows, "sum_isolated_us_per_step": per_step}), flush=True)
+
+
 def run_ours(args):
     import torch
 
@@ -224,6 +249,10 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     w = WORKLOADS[args.workload]
+    if args.layers > 0:
+        w = dataclasses.replace(w, shape=dataclasses.replace(w.shape, layers=args.layers))
+    if args.prompt >= 0:
+        w = dataclasses.replace(w, prompt=args.prompt)
     s, B, P = w.shape, w.batch, w.prompt
     K, W = args.steps, args.warmup
     cap = max(w.cap, P + W + K + 1)
@@ -248,6 +277,10 @@ def run_ours(args):
     pos0 = P if P else w.fill
     log(f"[bench] cache filled to {pos0} positions in {time.perf_counter() - t0:.1f} s")
 
+    if args.kernels:
+        kernel_table(pkg, h, w, B, pos0)
+        model.close()
+        return
     dev = torch.device("cuda", local)
     first = synth.tokens(w.seed_tokens, B * P, B, s.vocab)
     tok = [torch.from_numpy(first).to(dev), torch.empty(B, dtype=torch.int32, device=dev)]

@@ -21,6 +21,7 @@ namespace llm {
 constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kMaxHeadsPerWarp = 4;
+constexpr int kMinChunk = 256;  // fewest positions a split takes
 
 LLM_D void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
@@ -66,10 +67,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   grid_dep_wait();
   grid_dep_launch();
 
+  // positions 0..t in contiguous slices of at least kMinChunk: the number of active splits
+  // follows t, so a short context is not cut into slivers whose merge would cost more than them
   const int t = a.step->pos;
   const int npos = t + 1;
   int chunk = (npos + a.ns - 1) / a.ns;
   chunk = (chunk + 31) & ~31;
+  if (chunk < kMinChunk) chunk = kMinChunk;
+  const int nact = (npos + chunk - 1) / chunk;
+  if (split >= nact) return;
   const int p0 = split * chunk;
   const int p1 = min(npos, p0 + chunk);
 
@@ -212,26 +218,47 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   __syncthreads();
   if (tid == 0) {
     const unsigned int prev = atomicAdd(a.ticket + (size_t)b * a.kv + j, 1u);
-    s_last = (prev == (unsigned int)(a.ns - 1));
+    s_last = (prev == (unsigned int)(nact - 1));
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   // ---- the last CTA of this (row, kv head): merge the splits in order ----
+  // weights f[i][s] = exp(m_s - M_i) / L_i per head and split (one warp per head, fixed order),
+  // then out[i][e] = sum_s f[i][s] o_s[e] with the o loads issued together
+  float* fw = reinterpret_cast<float*>(kbuf);  // [g][nact] (the tiles are no longer needed)
+  const float* pbase = a.part + (((size_t)b * H + (size_t)j * g) * a.ns) * (HD + 2);
+  for (int i = warp; i < g; i += kAttnWarps) {
+    const float* pb = pbase + (size_t)i * a.ns * (HD + 2);
+    float M = -INFINITY;
+    for (int s2 = lane; s2 < nact; s2 += 32) M = fmaxf(M, __ldcg(pb + (size_t)s2 * (HD + 2) + HD));
+    M = warp_max(M);
+    float L = 0.f;
+    for (int s2 = lane; s2 < nact; s2 += 32) {
+      const float ms = __ldcg(pb + (size_t)s2 * (HD + 2) + HD);
+      const float f = ms == -INFINITY ? 0.f : expf(ms - M);
+      fw[i * nact + s2] = f;
+      L += __ldcg(pb + (size_t)s2 * (HD + 2) + HD + 1) * f;
+    }
+    L = warp_sum(L);
+    const float rl = 1.0f / L;
+    for (int s2 = lane; s2 < nact; s2 += 32) fw[i * nact + s2] *= rl;
+  }
+  __syncthreads();
   for (int idx = tid; idx < g * HD; idx += kAttnThreads) {
     const int i = idx / HD, e = idx - i * HD;
-    const float* pb = a.part + (((size_t)b * H + (size_t)j * g + i) * a.ns) * (HD + 2);
-    float M = -INFINITY;
-    for (int s = 0; s < a.ns; ++s) M = fmaxf(M, __ldcg(pb + (size_t)s * (HD + 2) + HD));
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < a.ns; ++s) {
-      const float ms = __ldcg(pb + (size_t)s * (HD + 2) + HD);
-      if (ms == -INFINITY) continue;
-      const float f = expf(ms - M);
-      L += __ldcg(pb + (size_t)s * (HD + 2) + HD + 1) * f;
-      O += __ldcg(pb + (size_t)s * (HD + 2) + e) * f;
+    const float* pb = pbase + (size_t)i * a.ns * (HD + 2) + e;
+    float O = 0.f;
+    int s2 = 0;
+    for (; s2 + 8 <= nact; s2 += 8) {
+      float ov[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ov[q] = __ldcg(pb + (size_t)(s2 + q) * (HD + 2));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) O = fmaf(fw[i * nact + s2 + q], ov[q], O);
     }
-    a.out[(size_t)b * a.out_stride + ((size_t)j * g + i) * HD + e] = O / L;
+    for (; s2 < nact; ++s2) O = fmaf(fw[i * nact + s2], __ldcg(pb + (size_t)s2 * (HD + 2)), O);
+    a.out[(size_t)b * a.out_stride + ((size_t)j * g + i) * HD + e] = O;
   }
   if (tid == 0) a.ticket[(size_t)b * a.kv + j] = 0u;
 }
@@ -239,25 +266,26 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
 // ---------------------------------------------------------------------------------------
 
 template <int KT, int HD>
-static size_t smem_for(int g) {
+static size_t smem_for(int g, int ns) {
   const int HW = g < kAttnWarps ? g : kAttnWarps;
   const int PW = (kAttnWarps % HW == 0) ? kAttnWarps / HW : 1;
   const int TILE = 32 * PW;
   const int ROWB = HD * Elem<KT>::bytes;
-  return (size_t)g * HD * 4 + 2 * (size_t)TILE * (ROWB + 16) + 2 * (size_t)TILE * ROWB +
-         (size_t)kAttnWarps * kMaxHeadsPerWarp * (HD + 2) * 4;
+  size_t tiles = 2 * (size_t)TILE * (ROWB + 16) + 2 * (size_t)TILE * ROWB;
+  if (tiles < (size_t)g * ns * 4) tiles = (size_t)g * ns * 4;  // the merge reuses the tile space
+  return (size_t)g * HD * 4 + tiles + (size_t)kAttnWarps * kMaxHeadsPerWarp * (HD + 2) * 4;
 }
 
 using AttnFn = void (*)(const AttnArgs);
 
 template <int KT>
-static AttnFn pick_hd(int hd, size_t* smem, int g) {
+static AttnFn pick_hd(int hd, size_t* smem, int g, int ns) {
   switch (hd) {
-    case 16: *smem = smem_for<KT, 16>(g); return attn_decode_kernel<KT, 16>;
-    case 32: *smem = smem_for<KT, 32>(g); return attn_decode_kernel<KT, 32>;
-    case 64: *smem = smem_for<KT, 64>(g); return attn_decode_kernel<KT, 64>;
-    case 128: *smem = smem_for<KT, 128>(g); return attn_decode_kernel<KT, 128>;
-    case 256: *smem = smem_for<KT, 256>(g); return attn_decode_kernel<KT, 256>;
+    case 16: *smem = smem_for<KT, 16>(g, ns); return attn_decode_kernel<KT, 16>;
+    case 32: *smem = smem_for<KT, 32>(g, ns); return attn_decode_kernel<KT, 32>;
+    case 64: *smem = smem_for<KT, 64>(g, ns); return attn_decode_kernel<KT, 64>;
+    case 128: *smem = smem_for<KT, 128>(g, ns); return attn_decode_kernel<KT, 128>;
+    case 256: *smem = smem_for<KT, 256>(g, ns); return attn_decode_kernel<KT, 256>;
     default: return nullptr;
   }
 }
@@ -268,7 +296,7 @@ cudaError_t attn_prepare(int max_smem_optin) {
   for (int kt = 0; kt < 2; ++kt)
     for (int hd : {16, 32, 64, 128, 256}) {
       size_t sm = 0;
-      AttnFn fn = kt ? pick_hd<1>(hd, &sm, 1) : pick_hd<0>(hd, &sm, 1);
+      AttnFn fn = kt ? pick_hd<1>(hd, &sm, 1, 1) : pick_hd<0>(hd, &sm, 1, 1);
       cudaFuncAttributes fa;
       cudaError_t e = cudaFuncGetAttributes(&fa, fn);
       if (e != cudaSuccess) return e;
@@ -290,7 +318,7 @@ int attn_splits(int B, int kv, int cap, int num_sms) {
 
 cudaError_t launch_attn(const AttnArgs& a, int kt, cudaStream_t s, bool pdl) {
   size_t smem = 0;
-  AttnFn fn = kt ? pick_hd<1>(a.hd, &smem, a.g) : pick_hd<0>(a.hd, &smem, a.g);
+  AttnFn fn = kt ? pick_hd<1>(a.hd, &smem, a.g, a.ns) : pick_hd<0>(a.hd, &smem, a.g, a.ns);
   if (!fn) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ns, a.kv, a.B);

@@ -31,6 +31,7 @@ template <int WT, int BT, int EPI, bool NORM>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a) {
   constexpr int E = Elem<WT>::per16;
   constexpr int RB = GemvTile<BT>::RB;
+  constexpr int MU = BT == 1 ? 2 : 1;  // chunks of a row loaded together (loads in flight: RB*MU)
   constexpr int NW = kGemvThreads / 32;
   extern __shared__ __align__(16) float sm[];
   const int seg_cols = a.seg_ch * E;
@@ -38,6 +39,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
   float* acc = xs + BT * seg_cols;           // [rows_cap][BT]
   float* wpart = acc + a.rows_cap * BT;      // [2][NW][RB][BT]
   float* inv = wpart + 2 * NW * RB * BT;     // [BT]
+  float* red = inv + BT;                     // [NW][BT]
 
   const int tid = threadIdx.x;
   const int units = a.rows / a.rg;
@@ -51,7 +53,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
   // the weights do not depend on the previous kernel: start pulling them into L2
   if (tid == 0 && nrows > 0) {
     size_t bytes = (size_t)nrows * row_bytes;
-    if (bytes > 65536) bytes = 65536;
+    if (bytes > 131072) bytes = 131072;
     prefetch_l2(Wb, (uint32_t)bytes);
   }
   grid_dep_wait();
@@ -62,20 +64,40 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
   const int rs = tid / lpr, li = tid - (tid / lpr) * lpr;
   const int nch = a.seg_ch / lpr;     // chunks per thread per row per segment
   const int warp = tid >> 5, lane = tid & 31;
+  const int c4 = a.cols >> 2;          // float4 per input row
+  const int seg4 = seg_cols >> 2;
 
   for (int b0 = 0; b0 < a.B; b0 += BT) {
     const int nb = min(BT, a.B - b0);
     if constexpr (NORM) {
-      if (warp < nb) {
-        const float* xr = a.x + (size_t)(b0 + warp) * a.x_stride;
-        float s = 0.f;
-        for (int c = lane; c < a.cols; c += 32) {
-          const float v = xr[c];
-          s = fmaf(v, v, s);
+      // sum of squares of every input row, all threads, 16-byte loads issued together
+      float ss[BT];
+#pragma unroll
+      for (int b = 0; b < BT; ++b) ss[b] = 0.f;
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        if (b < nb) {
+          const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)(b0 + b) * a.x_stride);
+#pragma unroll 4
+          for (int i = tid; i < c4; i += kGemvThreads) {
+            const float4 v = __ldg(xr + i);
+            ss[b] = fmaf(v.x, v.x, ss[b]);
+            ss[b] = fmaf(v.y, v.y, ss[b]);
+            ss[b] = fmaf(v.z, v.z, ss[b]);
+            ss[b] = fmaf(v.w, v.w, ss[b]);
+          }
         }
-        s = warp_sum(s);
-        if (lane == 0)
-          inv[warp] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)a.cols), a.eps)));
+      }
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        const float v = warp_sum(ss[b]);
+        if (lane == 0) red[warp * BT + b] = v;
+      }
+      __syncthreads();
+      if (tid < nb) {
+        float s = 0.f;
+        for (int w = 0; w < NW; ++w) s += red[w * BT + tid];
+        inv[tid] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)a.cols), a.eps)));
       }
     }
     for (int i = tid; i < nrows * BT; i += kGemvThreads) acc[i] = 0.f;
@@ -83,14 +105,23 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
     for (int seg = 0; seg < a.nseg; ++seg) {
       __syncthreads();
       const int c0 = seg * seg_cols;
-      for (int i = tid; i < BT * seg_cols; i += kGemvThreads) {
-        const int b = i / seg_cols, c = i - b * seg_cols;
-        float v = 0.f;
+      // stage this segment of the (normalized) inputs, 16 bytes at a time
+#pragma unroll 4
+      for (int i = tid; i < BT * seg4; i += kGemvThreads) {
+        const int b = i / seg4, c = (i - b * seg4) * 4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (b < nb) {
-          v = a.x[(size_t)(b0 + b) * a.x_stride + c0 + c];
-          if constexpr (NORM) v = __fmul_rn(a.gain[c0 + c], __fmul_rn(inv[b], v));
+          v = __ldg(reinterpret_cast<const float4*>(a.x + (size_t)(b0 + b) * a.x_stride + c0 + c));
+          if constexpr (NORM) {
+            const float4 gv = __ldg(reinterpret_cast<const float4*>(a.gain + c0 + c));
+            const float iv = inv[b];
+            v.x = __fmul_rn(gv.x, __fmul_rn(iv, v.x));
+            v.y = __fmul_rn(gv.y, __fmul_rn(iv, v.y));
+            v.z = __fmul_rn(gv.z, __fmul_rn(iv, v.z));
+            v.w = __fmul_rn(gv.w, __fmul_rn(iv, v.w));
+          }
         }
-        xs[i] = v;
+        *reinterpret_cast<float4*>(xs + b * seg_cols + c) = v;
       }
       __syncthreads();
       const char* Wseg = Wb + (size_t)seg * a.seg_ch * 16;
@@ -100,36 +131,45 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
         for (int k = 0; k < RB; ++k)
 #pragma unroll
           for (int b = 0; b < BT; ++b) av[k][b] = 0.f;
-        for (int m = 0; m < nch; ++m) {
-          const int ch = li + m * lpr;
-          uint4 w[RB];
+        for (int m0 = 0; m0 < nch; m0 += MU) {
+          uint4 w[MU][RB];
 #pragma unroll
-          for (int k = 0; k < RB; ++k) {
-            const int rl = rbase + rs + k * RP;
-            w[k] = rl < nrows ? ld_stream(Wseg + (size_t)rl * row_bytes + (size_t)ch * 16)
-                              : make_uint4(0u, 0u, 0u, 0u);
-          }
-          float xv[BT][E];
+          for (int mu = 0; mu < MU; ++mu) {
+            const int ch = li + (m0 + mu) * lpr;
 #pragma unroll
-          for (int b = 0; b < BT; ++b) {
-            const float4* xp = reinterpret_cast<const float4*>(xs + b * seg_cols + ch * E);
-#pragma unroll
-            for (int e4 = 0; e4 < E / 4; ++e4) {
-              const float4 t = xp[e4];
-              xv[b][4 * e4 + 0] = t.x;
-              xv[b][4 * e4 + 1] = t.y;
-              xv[b][4 * e4 + 2] = t.z;
-              xv[b][4 * e4 + 3] = t.w;
+            for (int k = 0; k < RB; ++k) {
+              const int rl = rbase + rs + k * RP;
+              w[mu][k] = (rl < nrows && m0 + mu < nch)
+                             ? ld_stream(Wseg + (size_t)rl * row_bytes + (size_t)ch * 16)
+                             : make_uint4(0u, 0u, 0u, 0u);
             }
           }
 #pragma unroll
-          for (int k = 0; k < RB; ++k) {
-            float wf[E];
-            unpack16<WT>(w[k], wf);
+          for (int mu = 0; mu < MU; ++mu) {
+            if (m0 + mu >= nch) break;
+            const int ch = li + (m0 + mu) * lpr;
+            float xv[BT][E];
 #pragma unroll
-            for (int b = 0; b < BT; ++b)
+            for (int b = 0; b < BT; ++b) {
+              const float4* xp = reinterpret_cast<const float4*>(xs + b * seg_cols + ch * E);
 #pragma unroll
-              for (int e = 0; e < E; ++e) av[k][b] = fmaf(wf[e], xv[b][e], av[k][b]);
+              for (int e4 = 0; e4 < E / 4; ++e4) {
+                const float4 t = xp[e4];
+                xv[b][4 * e4 + 0] = t.x;
+                xv[b][4 * e4 + 1] = t.y;
+                xv[b][4 * e4 + 2] = t.z;
+                xv[b][4 * e4 + 3] = t.w;
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < RB; ++k) {
+              float wf[E];
+              unpack16<WT>(w[mu][k], wf);
+#pragma unroll
+              for (int b = 0; b < BT; ++b)
+#pragma unroll
+                for (int e = 0; e < E; ++e) av[k][b] = fmaf(wf[e], xv[b][e], av[k][b]);
+            }
           }
         }
         if (lpr >= 32) {
@@ -267,7 +307,7 @@ GemvPlan plan_gemv(int rows, int cols, int rg, int wt, int B, int num_sms, int c
   p.grid = grid;
   p.rows_cap = ((units + grid - 1) / grid) * rg;
   const int RB = p.bt >= 8 ? 1 : 8 / p.bt;
-  p.smem = ((size_t)p.bt * p.seg_ch * E + (size_t)p.rows_cap * p.bt + 2 * 8 * RB * p.bt + 8) * 4;
+  p.smem = ((size_t)p.bt * p.seg_ch * E + (size_t)p.rows_cap * p.bt + 2 * 8 * RB * p.bt + 8 + 8 * 8) * 4;
   return p;
 }
 

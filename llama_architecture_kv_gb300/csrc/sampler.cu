@@ -83,7 +83,22 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const SampleArgs a
     // ---- greedy ----
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int i = tid; i < V; i += kSampThreads) argmax_merge(bv, bi, lg[i], i);
+    if ((a.logits_stride & 3) == 0) {
+      // 16-byte loads, several in flight; each thread keeps the first index of its maximum
+      const float4* l4 = reinterpret_cast<const float4*>(lg);
+      const int n4 = V >> 2;
+#pragma unroll 8
+      for (int i = tid; i < n4; i += kSampThreads) {
+        const float4 v = l4[i];
+        argmax_merge(bv, bi, v.x, 4 * i);
+        argmax_merge(bv, bi, v.y, 4 * i + 1);
+        argmax_merge(bv, bi, v.z, 4 * i + 2);
+        argmax_merge(bv, bi, v.w, 4 * i + 3);
+      }
+      for (int i = 4 * n4 + tid; i < V; i += kSampThreads) argmax_merge(bv, bi, lg[i], i);
+    } else {
+      for (int i = tid; i < V; i += kSampThreads) argmax_merge(bv, bi, lg[i], i);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
