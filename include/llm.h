@@ -206,6 +206,25 @@ llm_status llm_debug_trace(llm_handle* h, int32_t layer, const char* name, float
 llm_status llm_profile_kernel(llm_handle* h, int32_t which, int32_t B, int32_t pos, int32_t reps,
                               float* ms_per_launch);
 
+/*
+ * Sampling without a handle and without allocating: the same draw as llm_sample_dev (greedy
+ * when temp == 0, else temperature / top-k / top-p with the draws u_dev), for callers that
+ * cannot call cudaMalloc -- code running inside an allocator or memory-pool callback, plugins
+ * whose host application owns all device memory, processes that reserved every byte up front.
+ * The pages have no counterpart; this is a convenience of this library.
+ * logits_dev [B][V] f32, u_dev [B] (may be NULL when temp == 0), ids_dev [B]: device memory of
+ * the current device; the work is ordered on cuda_stream and the call returns without waiting.
+ * The sort buffers live in one fixed device array inside the library, present on every GPU that
+ * loads it until the process exits: B * (V rounded up to 32) must not exceed
+ * LLM_SAMPLE_NOALLOC_MAX_ELEMS, else LLM_ERR_ARG (as for B < 1, V < 1, NULL pointers or the
+ * argument ranges of llm_sample).  Calls share that array, so calls that overlap on the GPU race.
+ * The first call on a device (with it current) looks up the array's device address and sets a
+ * kernel attribute; make it before any stream capture on that device.  Calls no allocator.
+ */
+#define LLM_SAMPLE_NOALLOC_MAX_ELEMS 262144
+llm_status llm_sample_noalloc(const float* logits_dev, int32_t B, int32_t V, float temp, int32_t k,
+                              float p, const float* u_dev, int32_t* ids_dev, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ EXPORTS = ("llm_weight_count", "llm_create", "llm_destroy", "llm_reset", "llm_pr
            "llm_sample", "llm_step", "llm_prefill_dev", "llm_decode_dev", "llm_sample_dev",
            "llm_step_dev", "llm_synchronize", "llm_stream", "llm_logits_buffer", "llm_filled",
            "llm_last_error", "llm_status_string", "llm_kv_import", "llm_kv_export",
-           "llm_debug_trace", "llm_profile_kernel")
+           "llm_debug_trace", "llm_profile_kernel", "llm_sample_noalloc")
 
 
 class LlmConfig(ctypes.Structure):
@@ -77,6 +77,7 @@ def lib():
             "llm_kv_export": ([vp, i32, i32, i32, i32, vp, vp], i32),
             "llm_debug_trace": ([vp, i32, ctypes.c_char_p, vp], i32),
             "llm_profile_kernel": ([vp, i32, i32, i32, i32, ctypes.POINTER(f32)], i32),
+            "llm_sample_noalloc": ([vp, i32, i32, f32, i32, f32, vp, vp, vp], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -211,6 +212,17 @@ def llm_profile_kernel(h, which, B, pos, reps) -> float:
     ms = ctypes.c_float()
     _check(h, lib().llm_profile_kernel(h, which, B, pos, reps, ctypes.byref(ms)))
     return float(ms.value)
+
+
+SAMPLE_NOALLOC_MAX_ELEMS = 262144
+
+
+def llm_sample_noalloc(logits, B, V, temp, k, p, u, ids, stream=None):
+    """Sampling on device buffers with no handle and no allocation (see include/llm.h): for
+    callers that cannot allocate device memory.  B * (V rounded up to 32) <= 262144."""
+    st = lib().llm_sample_noalloc(_ptr(logits), B, V, temp, k, p, _ptr(u), _ptr(ids), stream)
+    if st != LLM_OK:
+        raise LlmError(st, f"llm_sample_noalloc: {lib().llm_status_string(st).decode()}")
 
 
 # ---- a small convenience wrapper --------------------------------------------------------
