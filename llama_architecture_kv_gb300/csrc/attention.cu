@@ -21,7 +21,7 @@ namespace llm {
 constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kMaxHeadsPerWarp = 4;
-constexpr int kMinChunk = 256;  // fewest positions a split takes
+constexpr int kMinChunk = 64;  // fewest positions a split takes
 
 LLM_D void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
@@ -120,48 +120,72 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
       const int p = tb + pw * 32 + lane;  // this lane's position
       const bool valid = p < p1;
       const unsigned char* krow = kbuf + ((size_t)buf * TILE + pw * 32 + lane) * KPAD;
+      const int nh = (g - hw + HW - 1) / HW;  // heads this warp serves
+      // scores of every head of this warp: each key row is read from shared memory once
+      float s[kMaxHeadsPerWarp];
+#pragma unroll
+      for (int hh = 0; hh < kMaxHeadsPerWarp; ++hh) s[hh] = 0.f;
+      if (valid) {
+#pragma unroll 2
+        for (int c = 0; c < ROWB / 16; ++c) {
+          const uint4 kv4 = *reinterpret_cast<const uint4*>(krow + c * 16);
+          float kf[16 / ES];
+          unpack16<KT>(kv4, kf);
+#pragma unroll
+          for (int hh = 0; hh < kMaxHeadsPerWarp; ++hh) {
+            if (hh < nh) {
+              const float4* q4 = reinterpret_cast<const float4*>(qs + (hw + hh * HW) * HD + c * (16 / ES));
+#pragma unroll
+              for (int e4 = 0; e4 < 16 / ES / 4; ++e4) {
+                const float4 qv = q4[e4];
+                s[hh] = fmaf(qv.x, kf[4 * e4 + 0], s[hh]);
+                s[hh] = fmaf(qv.y, kf[4 * e4 + 1], s[hh]);
+                s[hh] = fmaf(qv.z, kf[4 * e4 + 2], s[hh]);
+                s[hh] = fmaf(qv.w, kf[4 * e4 + 3], s[hh]);
+              }
+            }
+          }
+        }
+      }
+      // online softmax per head (running max m, running sum l)
+      float w[kMaxHeadsPerWarp];
 #pragma unroll
       for (int hh = 0; hh < kMaxHeadsPerWarp; ++hh) {
-        const int i = hw + hh * HW;
-        if (i >= g) break;
-        const float* qh = qs + i * HD;
-        float s = 0.f;
-        if (valid) {
-#pragma unroll 4
-          for (int c = 0; c < ROWB / 16; ++c) {
-            const uint4 kv4 = *reinterpret_cast<const uint4*>(krow + c * 16);
-            float kf[16 / ES];
-            unpack16<KT>(kv4, kf);
+        w[hh] = 0.f;
+        if (hh < nh) {
+          const float sc = valid ? s[hh] * a.scale : -INFINITY;
+          const float mnew = fmaxf(m[hh], warp_max(sc));
+          if (mnew != -INFINITY) {  // uniform across the warp
+            const float corr = expf(m[hh] - mnew);
+            w[hh] = valid ? expf(sc - mnew) : 0.f;
+            l[hh] = l[hh] * corr + warp_sum(w[hh]);
+            m[hh] = mnew;
 #pragma unroll
-            for (int e = 0; e < 16 / ES; ++e) s = fmaf(qh[c * (16 / ES) + e], kf[e], s);
+            for (int n = 0; n < NE; ++n) {
+              o[hh][n][0] *= corr;
+              o[hh][n][1] *= corr;
+            }
           }
-          s *= a.scale;
-        } else {
-          s = -INFINITY;
         }
-        const float mt = warp_max(s);
-        const float mnew = fmaxf(m[hh], mt);
-        if (mnew == -INFINITY) continue;  // nothing valid yet (uniform across the warp)
-        const float corr = expf(m[hh] - mnew);
-        const float w = valid ? expf(s - mnew) : 0.f;
-        l[hh] = l[hh] * corr + warp_sum(w);
-        m[hh] = mnew;
+      }
+      // weighted values: each value row is read from shared memory once for all heads
+      const unsigned char* vt = vbuf + ((size_t)buf * TILE + pw * 32) * ROWB;
+      const int nv = min(32, p1 - (tb + pw * 32));
+      for (int pp = 0; pp < nv; ++pp) {
+        float2 v2[NE];
 #pragma unroll
         for (int n = 0; n < NE; ++n) {
-          o[hh][n][0] *= corr;
-          o[hh][n][1] *= corr;
+          const int e = 2 * lane + 64 * n;
+          v2[n] = e < HD ? load2<KT>(vt + (size_t)pp * ROWB, e) : make_float2(0.f, 0.f);
         }
-        const unsigned char* vt = vbuf + ((size_t)buf * TILE + pw * 32) * ROWB;
-        const int nv = min(32, p1 - (tb + pw * 32));
-        for (int pp = 0; pp < nv; ++pp) {
-          const float wp = __shfl_sync(0xffffffffu, w, pp);
 #pragma unroll
-          for (int n = 0; n < NE; ++n) {
-            const int e = 2 * lane + 64 * n;
-            if (e < HD) {
-              const float2 v2 = load2<KT>(vt + (size_t)pp * ROWB, e);
-              o[hh][n][0] = fmaf(wp, v2.x, o[hh][n][0]);
-              o[hh][n][1] = fmaf(wp, v2.y, o[hh][n][1]);
+        for (int hh = 0; hh < kMaxHeadsPerWarp; ++hh) {
+          if (hh < nh) {
+            const float wp = __shfl_sync(0xffffffffu, w[hh], pp);
+#pragma unroll
+            for (int n = 0; n < NE; ++n) {
+              o[hh][n][0] = fmaf(wp, v2[n].x, o[hh][n][0]);
+              o[hh][n][1] = fmaf(wp, v2[n].y, o[hh][n][1]);
             }
           }
         }

@@ -16,7 +16,8 @@
 // Design: the decode step is bound by HBM bandwidth (each weight byte is read once per step),
 // so the kernel is a streaming engine.  Each CTA owns a contiguous, balanced range of rows
 // (whole work units, so RoPE and SwiGLU pairs stay in one CTA) and reads them with 16-byte
-// non-allocating loads, 8 rows in flight per thread.  The threads of a row split its columns;
+// non-allocating loads in groups of 8 per thread, two groups in flight (double buffered).
+// The threads of a row split its columns;
 // the (normalized) input lives in shared memory as f32.  Partial dot products are reduced
 // with warp shuffles and a fixed-order sum across warps, so results are deterministic.
 #include "gemv.cuh"
@@ -31,7 +32,7 @@ template <int WT, int BT, int EPI, bool NORM>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a) {
   constexpr int E = Elem<WT>::per16;
   constexpr int RB = GemvTile<BT>::RB;
-  constexpr int MU = BT == 1 ? 2 : 1;  // chunks of a row loaded together (loads in flight: RB*MU)
+  constexpr int MU = 8 / RB;  // chunks of a row per load group (8 loads per group)
   constexpr int NW = kGemvThreads / 32;
   extern __shared__ __align__(16) float sm[];
   const int seg_cols = a.seg_ch * E;
@@ -40,6 +41,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
   float* wpart = acc + a.rows_cap * BT;      // [2][NW][RB][BT]
   float* inv = wpart + 2 * NW * RB * BT;     // [BT]
   float* red = inv + BT;                     // [NW][BT]
+  float* wsum = red + NW * BT;               // [lpr/32][rows_cap][BT] per-warp row partials (a.ws)
 
   const int tid = threadIdx.x;
   const int units = a.rows / a.rg;
@@ -101,7 +103,19 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
       }
     }
     for (int i = tid; i < nrows * BT; i += kGemvThreads) acc[i] = 0.f;
+    if (a.ws)
+      for (int i = tid; i < (lpr >> 5) * a.rows_cap * BT; i += kGemvThreads) wsum[i] = 0.f;
     int buf = 0;
+    // the loads of one "group": RB rows x MU chunks per thread; groups are double buffered, so
+    // the next group is in flight while this one is multiplied and its batch reduced
+    const int ngrp = (nch + MU - 1) / MU;                 // groups per batch of RP*RB rows
+    const int nbat = (nrows + RP * RB - 1) / (RP * RB);
+    const int G = nbat * ngrp;                            // groups per segment
+    float av[RB][BT];
+#pragma unroll
+    for (int k = 0; k < RB; ++k)
+#pragma unroll
+      for (int b = 0; b < BT; ++b) av[k][b] = 0.f;
     for (int seg = 0; seg < a.nseg; ++seg) {
       __syncthreads();
       const int c0 = seg * seg_cols;
@@ -125,54 +139,67 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
       }
       __syncthreads();
       const char* Wseg = Wb + (size_t)seg * a.seg_ch * 16;
-      for (int rbase = 0; rbase < nrows; rbase += RP * RB) {
-        float av[RB][BT];
+
+      auto load_group = [&](uint4 (&w)[MU][RB], int g) {
+        const int bi = g / ngrp, m0 = (g - bi * ngrp) * MU;
+        const int rbase = bi * RP * RB;
 #pragma unroll
-        for (int k = 0; k < RB; ++k)
+        for (int mu = 0; mu < MU; ++mu) {
+          const int ch = li + (m0 + mu) * lpr;
 #pragma unroll
-          for (int b = 0; b < BT; ++b) av[k][b] = 0.f;
-        for (int m0 = 0; m0 < nch; m0 += MU) {
-          uint4 w[MU][RB];
-#pragma unroll
-          for (int mu = 0; mu < MU; ++mu) {
-            const int ch = li + (m0 + mu) * lpr;
-#pragma unroll
-            for (int k = 0; k < RB; ++k) {
-              const int rl = rbase + rs + k * RP;
-              w[mu][k] = (rl < nrows && m0 + mu < nch)
-                             ? ld_stream(Wseg + (size_t)rl * row_bytes + (size_t)ch * 16)
-                             : make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-#pragma unroll
-          for (int mu = 0; mu < MU; ++mu) {
-            if (m0 + mu >= nch) break;
-            const int ch = li + (m0 + mu) * lpr;
-            float xv[BT][E];
-#pragma unroll
-            for (int b = 0; b < BT; ++b) {
-              const float4* xp = reinterpret_cast<const float4*>(xs + b * seg_cols + ch * E);
-#pragma unroll
-              for (int e4 = 0; e4 < E / 4; ++e4) {
-                const float4 t = xp[e4];
-                xv[b][4 * e4 + 0] = t.x;
-                xv[b][4 * e4 + 1] = t.y;
-                xv[b][4 * e4 + 2] = t.z;
-                xv[b][4 * e4 + 3] = t.w;
-              }
-            }
-#pragma unroll
-            for (int k = 0; k < RB; ++k) {
-              float wf[E];
-              unpack16<WT>(w[mu][k], wf);
-#pragma unroll
-              for (int b = 0; b < BT; ++b)
-#pragma unroll
-                for (int e = 0; e < E; ++e) av[k][b] = fmaf(wf[e], xv[b][e], av[k][b]);
-            }
+          for (int k = 0; k < RB; ++k) {
+            const int rl = rbase + rs + k * RP;
+            w[mu][k] = (rl < nrows && m0 + mu < nch)
+                           ? ld_stream(Wseg + (size_t)rl * row_bytes + (size_t)ch * 16)
+                           : make_uint4(0u, 0u, 0u, 0u);
           }
         }
-        if (lpr >= 32) {
+      };
+      auto fma_group = [&](const uint4 (&w)[MU][RB], int g) {
+        const int bi = g / ngrp, m0 = (g - bi * ngrp) * MU;
+#pragma unroll
+        for (int mu = 0; mu < MU; ++mu) {
+          if (m0 + mu >= nch) break;
+          const int ch = li + (m0 + mu) * lpr;
+          float xv[BT][E];
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            const float4* xp = reinterpret_cast<const float4*>(xs + b * seg_cols + ch * E);
+#pragma unroll
+            for (int e4 = 0; e4 < E / 4; ++e4) {
+              const float4 t = xp[e4];
+              xv[b][4 * e4 + 0] = t.x;
+              xv[b][4 * e4 + 1] = t.y;
+              xv[b][4 * e4 + 2] = t.z;
+              xv[b][4 * e4 + 3] = t.w;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            float wf[E];
+            unpack16<WT>(w[mu][k], wf);
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+#pragma unroll
+              for (int e = 0; e < E; ++e) av[k][b] = fmaf(wf[e], xv[b][e], av[k][b]);
+          }
+        }
+      };
+      auto reduce_batch = [&](int bi) {
+        const int rbase = bi * RP * RB;
+        if (lpr >= 32 && a.ws) {
+          // each warp keeps its own partial of each row; the warps are summed once at the end
+          const int wi = warp % (lpr >> 5);
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            const int rl = rbase + rs + k * RP;
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+              const float v = warp_sum(av[k][b]);
+              if (lane == 0 && rl < nrows) wsum[((size_t)wi * a.rows_cap + rl) * BT + b] += v;
+            }
+          }
+        } else if (lpr >= 32) {
 #pragma unroll
           for (int k = 0; k < RB; ++k)
 #pragma unroll
@@ -186,9 +213,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
             const int b = i % BT, k = (i / BT) % RB, r = i / (BT * RB);
             const int rl = rbase + r + k * RP;
             if (rl < nrows && b < nb) {
-              float s = 0.f;
-              for (int wi = 0; wi < wpr; ++wi) s += wpart[((buf * NW + r * wpr + wi) * RB + k) * BT + b];
-              acc[rl * BT + b] += s;
+              float sum = 0.f;
+              for (int wi = 0; wi < wpr; ++wi) sum += wpart[((buf * NW + r * wpr + wi) * RB + k) * BT + b];
+              acc[rl * BT + b] += sum;
             }
           }
           buf ^= 1;
@@ -212,9 +239,34 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
             }
           }
         }
+#pragma unroll
+        for (int k = 0; k < RB; ++k)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) av[k][b] = 0.f;
+      };
+
+      uint4 wa[MU][RB], wb[MU][RB];
+      if (G > 0) load_group(wa, 0);
+      for (int g = 0; g < G; g += 2) {
+        if (g + 1 < G) load_group(wb, g + 1);
+        fma_group(wa, g);
+        if (g % ngrp == ngrp - 1) reduce_batch(g / ngrp);
+        if (g + 1 >= G) break;
+        if (g + 2 < G) load_group(wa, g + 2);
+        fma_group(wb, g + 1);
+        if ((g + 1) % ngrp == ngrp - 1) reduce_batch((g + 1) / ngrp);
       }
     }
     __syncthreads();
+    if (a.ws) {
+      const int wpr = lpr >> 5;
+      for (int i = tid; i < nrows * BT; i += kGemvThreads) {
+        float sum = 0.f;
+        for (int wi = 0; wi < wpr; ++wi) sum += wsum[(size_t)wi * a.rows_cap * BT + i];
+        acc[i] = sum;
+      }
+      __syncthreads();
+    }
 
     // ---- epilogue ----
     if constexpr (EPI == EPI_QKV) {
@@ -307,7 +359,11 @@ GemvPlan plan_gemv(int rows, int cols, int rg, int wt, int B, int num_sms, int c
   p.grid = grid;
   p.rows_cap = ((units + grid - 1) / grid) * rg;
   const int RB = p.bt >= 8 ? 1 : 8 / p.bt;
-  p.smem = ((size_t)p.bt * p.seg_ch * E + (size_t)p.rows_cap * p.bt + 2 * 8 * RB * p.bt + 8 + 8 * 8) * 4;
+  // per-warp row partials (no CTA barrier per batch) when they fit
+  const size_t ws_floats = lpr >= 32 ? (size_t)(lpr / 32) * p.rows_cap * p.bt : 0;
+  p.ws = (lpr >= 32 && ws_floats * 4 <= 48 * 1024) ? 1 : 0;
+  p.smem = ((size_t)p.bt * p.seg_ch * E + (size_t)p.rows_cap * p.bt + 2 * 8 * RB * p.bt + 8 + 8 * 8 +
+            (p.ws ? ws_floats : 0)) * 4;
   return p;
 }
 

@@ -24,6 +24,7 @@ struct GemvArgs {
   int32_t seg_ch;       // 16-byte chunks per staged column segment
   int32_t nseg;         // segments per row (seg_ch * nseg = chunks per row)
   int32_t rows_cap;     // upper bound of rows per CTA (sizes the accumulator)
+  int32_t ws;           // 1: per-warp row partials in shared memory, summed once at the end
   const StepState* step;
   float* out;           // [B][out_stride]
   int32_t out_stride;
@@ -40,7 +41,7 @@ struct GemvArgs {
 };
 
 struct GemvPlan {
-  int bt, lpr, seg_ch, nseg, grid, rows_cap;
+  int bt, lpr, seg_ch, nseg, grid, rows_cap, ws;
   size_t smem;
 };
 

@@ -358,7 +358,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     GemvArgs hd = {};
     hd.step = h->st; hd.B = B; hd.eps = c.eps; hd.W = h->head; hd.rows = h->V; hd.cols = h->d; hd.rg = 1;
     hd.x = h->xa; hd.x_stride = h->d; hd.gain = h->lnf;
-    hd.lpr = p_h.lpr; hd.seg_ch = p_h.seg_ch; hd.nseg = p_h.nseg; hd.rows_cap = p_h.rows_cap;
+    hd.lpr = p_h.lpr; hd.seg_ch = p_h.seg_ch; hd.nseg = p_h.nseg; hd.rows_cap = p_h.rows_cap; hd.ws = p_h.ws;
     hd.out = h->logits; hd.out_stride = h->V;
     CUDA_TRY(h, launch_gemv(hd, p_h, wt, EPI_STORE, true, h->stream, pdl));
     return LLM_OK;
@@ -380,7 +380,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     a.step = h->st; a.B = B; a.eps = c.eps;
     a.W = w.qkv; a.rows = qkv_rows; a.cols = h->d; a.rg = 2;
     a.x = h->xa; a.x_stride = h->d; a.gain = w.ln1;
-    a.lpr = p.lpr; a.seg_ch = p.seg_ch; a.nseg = p.nseg; a.rows_cap = p.rows_cap;
+    a.lpr = p.lpr; a.seg_ch = p.seg_ch; a.nseg = p.nseg; a.rows_cap = p.rows_cap; a.ws = p.ws;
     a.q_out = h->q; a.q_stride = h->d; a.kc = kcl; a.vc = vcl;
     a.H = h->H; a.kv = c.kv_heads; a.hd = h->hd; a.cap = c.max_seq;
     a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin;
@@ -399,7 +399,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     GemvArgs o = {};
     o.step = h->st; o.B = B; o.W = w.o; o.rows = h->d; o.cols = h->d; o.rg = 1;
     o.x = h->attn; o.x_stride = h->d;
-    o.lpr = p.lpr; o.seg_ch = p.seg_ch; o.nseg = p.nseg; o.rows_cap = p.rows_cap;
+    o.lpr = p.lpr; o.seg_ch = p.seg_ch; o.nseg = p.nseg; o.rows_cap = p.rows_cap; o.ws = p.ws;
     o.out = h->xb; o.out_stride = h->d; o.resid = h->xa; o.resid_stride = h->d;
     CUDA_TRY(h, launch_gemv(o, p, wt, EPI_RESID, false, h->stream, pdl));
   } else if (which == K_GATEUP) {
@@ -408,7 +408,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     GemvArgs g = {};
     g.step = h->st; g.B = B; g.eps = c.eps; g.W = w.gu; g.rows = 2 * h->f; g.cols = h->d; g.rg = 2;
     g.x = h->xb; g.x_stride = h->d; g.gain = w.ln2;
-    g.lpr = p.lpr; g.seg_ch = p.seg_ch; g.nseg = p.nseg; g.rows_cap = p.rows_cap;
+    g.lpr = p.lpr; g.seg_ch = p.seg_ch; g.nseg = p.nseg; g.rows_cap = p.rows_cap; g.ws = p.ws;
     g.out = h->m; g.out_stride = h->f;
     CUDA_TRY(h, launch_gemv(g, p, wt, EPI_SWIGLU, true, h->stream, pdl));
   } else if (which == K_DOWN) {
@@ -417,7 +417,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     GemvArgs dn = {};
     dn.step = h->st; dn.B = B; dn.W = w.down; dn.rows = h->d; dn.cols = h->f; dn.rg = 1;
     dn.x = h->m; dn.x_stride = h->f;
-    dn.lpr = p.lpr; dn.seg_ch = p.seg_ch; dn.nseg = p.nseg; dn.rows_cap = p.rows_cap;
+    dn.lpr = p.lpr; dn.seg_ch = p.seg_ch; dn.nseg = p.nseg; dn.rows_cap = p.rows_cap; dn.ws = p.ws;
     dn.out = h->xa; dn.out_stride = h->d; dn.resid = h->xb; dn.resid_stride = h->d;
     CUDA_TRY(h, launch_gemv(dn, p, wt, EPI_RESID, false, h->stream, pdl));
   } else {
