@@ -18,7 +18,11 @@ struct AttnArgs {
   const StepState* step;
 };
 
+constexpr int kAttnMaxCluster = 16;  // most splits merged inside one thread-block cluster
+
 bool attn_supported(int hd, int g);
+// splits per (row, kv head); at most attn_max_cluster() means the splits form one cluster
+int attn_max_cluster();
 int attn_splits(int B, int kv, int cap, int num_sms);
 cudaError_t attn_prepare(int max_smem_optin);
 cudaError_t launch_attn(const AttnArgs& a, int kt, cudaStream_t s, bool pdl);
