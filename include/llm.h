@@ -218,8 +218,8 @@ llm_status llm_profile_kernel(llm_handle* h, int32_t which, int32_t B, int32_t p
  * loads it until the process exits: B * (V rounded up to 32) must not exceed
  * LLM_SAMPLE_NOALLOC_MAX_ELEMS, else LLM_ERR_ARG (as for B < 1, V < 1, NULL pointers or the
  * argument ranges of llm_sample).  Calls share that array, so calls that overlap on the GPU race.
- * The first call on a device (with it current) looks up the array's device address and sets a
- * kernel attribute; make it before any stream capture on that device.  Calls no allocator.
+ * The first call on a device (with it current) looks up the array's device address; make it
+ * before any stream capture on that device.  Calls no allocator.
  */
 #define LLM_SAMPLE_NOALLOC_MAX_ELEMS 262144
 llm_status llm_sample_noalloc(const float* logits_dev, int32_t B, int32_t V, float temp, int32_t k,

@@ -149,7 +149,8 @@ struct GraphKey {
   bool operator<(const GraphKey& o) const { return B != o.B ? B < o.B : mode < o.mode; }
 };
 
-enum { MODE_NOHEAD = 0, MODE_HEAD = 1, MODE_SAMPLE = 2 };
+// what follows the layers: nothing, the LM head, or the head and a greedy / top-k top-p draw
+enum { MODE_NOHEAD = 0, MODE_HEAD = 1, MODE_GREEDY = 2, MODE_TOPP = 3 };
 
 struct llm_handle {
   llm_config cfg;
@@ -178,6 +179,7 @@ struct llm_handle {
   uint32_t* s_keys = nullptr;
   int32_t* s_idx = nullptr;
   float* s_pre = nullptr;
+  uint32_t* s_hist = nullptr;
   int V_pad = 0;
   float* trace = nullptr;  // [L][5][max_batch][max(d, f)]
   std::vector<int32_t> filled;
@@ -332,7 +334,16 @@ llm_status load_weights(llm_handle* h, const char* blob /* device */) {
 
 // ---- the decode step ----
 
-enum { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GATEUP = 3, K_DOWN = 4, K_HEAD = 5, K_SAMPLE = 6, K_EMBED = 7 };
+// K_SAMPLE is the temperature / top-k / top-p chain, K_GREEDY the argmax
+enum { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GATEUP = 3, K_DOWN = 4, K_HEAD = 5, K_SAMPLE = 6, K_EMBED = 7, K_GREEDY = 8 };
+
+SampleArgs sample_args(const llm_handle* h) {
+  SampleArgs s = {};
+  s.logits = h->logits; s.logits_stride = h->V; s.V = h->V; s.V_pad = h->V_pad;
+  s.keys = h->s_keys; s.idx = h->s_idx; s.pre = h->s_pre; s.hist = h->s_hist;
+  s.u = h->u_buf; s.ids = h->ids_buf; s.step = h->st;
+  return s;
+}
 
 // launch one kernel of the decode step (layer l where it applies)
 llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
@@ -363,11 +374,8 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     CUDA_TRY(h, launch_gemv(hd, p_h, wt, EPI_STORE, true, h->stream, pdl));
     return LLM_OK;
   }
-  if (which == K_SAMPLE) {
-    SampleArgs s = {};
-    s.logits = h->logits; s.logits_stride = h->V; s.V = h->V; s.V_pad = h->V_pad;
-    s.keys = h->s_keys; s.idx = h->s_idx; s.pre = h->s_pre; s.u = h->u_buf; s.ids = h->ids_buf; s.step = h->st;
-    CUDA_TRY(h, launch_sample(s, B, h->stream, pdl));
+  if (which == K_SAMPLE || which == K_GREEDY) {
+    CUDA_TRY(h, launch_sample(sample_args(h), B, which == K_GREEDY, h->stream, pdl));
     return LLM_OK;
   }
   const LayerW& w = h->lw[l];
@@ -443,7 +451,8 @@ llm_status launch_layer_kernels(llm_handle* h, int B, int mode, bool pdl, bool t
     }
   }
   if (mode >= MODE_HEAD) TRY(launch_one(h, K_HEAD, 0, B, pdl));
-  if (mode == MODE_SAMPLE) TRY(launch_one(h, K_SAMPLE, 0, B, pdl));
+  if (mode == MODE_GREEDY) TRY(launch_one(h, K_GREEDY, 0, B, pdl));
+  if (mode == MODE_TOPP) TRY(launch_one(h, K_SAMPLE, 0, B, pdl));
   return LLM_OK;
 }
 
@@ -633,7 +642,6 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   if ((ce = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking)) != cudaSuccess) return cuda_bail("capture stream", ce);
   if ((ce = gemv_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("gemv kernel attributes", ce);
   if ((ce = attn_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("attention kernel attributes", ce);
-  if ((ce = sample_prepare()) != cudaSuccess) return cuda_bail("sampler kernel attributes", ce);
   // weights: a device copy of the blob when it is on the host, then repacked
   const char* blob = (const char*)weights;
   char* staging = nullptr;
@@ -674,7 +682,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     return bail(st);
   h->V_pad = (h->V + 31) & ~31;
   if ((st = dalloc(h, &h->s_keys, B * 2 * h->V_pad * 4)) || (st = dalloc(h, &h->s_idx, B * 2 * h->V_pad * 4)) ||
-      (st = dalloc(h, &h->s_pre, B * h->V_pad * 4)))
+      (st = dalloc(h, &h->s_pre, B * h->V_pad * 4)) || (st = dalloc(h, &h->s_hist, B * kSampleHistPerRow * 4)))
     return bail(st);
   if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * 5 * B * std::max(h->d, h->f) * 4))) return bail(st);
   if (cudaMemsetAsync(h->ticket, 0, B * c.kv_heads * 4, h->stream) != cudaSuccess ||
@@ -771,10 +779,7 @@ static llm_status sample_impl(llm_handle* h, const float* logits, bool logits_on
   // the prologue also carries temp, k, p and u; its tokens are unused here
   std::vector<int32_t> toks(B, 0);
   TRY(begin(h, 0, B, toks.data(), nullptr, 1, 0, temp, k, p, u_on_host ? u : nullptr, u_on_host ? nullptr : u));
-  SampleArgs s = {};
-  s.logits = h->logits; s.logits_stride = h->V; s.V = h->V; s.V_pad = h->V_pad;
-  s.keys = h->s_keys; s.idx = h->s_idx; s.pre = h->s_pre; s.u = h->u_buf; s.ids = h->ids_buf; s.step = h->st;
-  CUDA_TRY(h, launch_sample(s, B, h->stream, false));
+  CUDA_TRY(h, launch_sample(sample_args(h), B, !(temp > 0.0f), h->stream, false));
   if (ids_on_host) {
     CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToHost, h->stream));
     CUDA_TRY(h, cudaStreamSynchronize(h->stream));
@@ -807,7 +812,7 @@ static llm_status step_impl(llm_handle* h, const int32_t* tok_host, const int32_
     for (int b = 0; b < B; ++b)
       if (!(u_host[b] >= 0.0f && u_host[b] < 1.0f)) return fail(h, LLM_ERR_ARG, "u[%d] outside [0, 1)", b);
   TRY(begin(h, pos, B, tok_host, tok_dev, 1, 0, temp, k, p, u_host, u_dev));
-  TRY(run_step(h, B, MODE_SAMPLE));
+  TRY(run_step(h, B, temp > 0.0f ? MODE_TOPP : MODE_GREEDY));
   if (host) {
     if (logits) CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
     CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToHost, h->stream));

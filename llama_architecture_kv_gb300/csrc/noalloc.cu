@@ -8,8 +8,9 @@
 //
 // The scratch array: kScratchBytes of device memory in this library's image, present on every
 // GPU that loads the library until the process exits.  Layout: a 256-byte slot for the sampling
-// parameters, then keys [B][2][V_pad] (uint32), ids [B][2][V_pad] (int32) and running sums
-// [B][V_pad] (f32), V_pad = V rounded up to 32.  B * V_pad may be at most
+// parameters, then keys [B][2][V_pad] (uint32), ids [B][2][V_pad] (int32), running sums
+// [B][V_pad] (f32) and the sort's digit counts [B][16][slices] (uint32, slices = the CTAs that
+// share one row, at most V / 2048 + 1), V_pad = V rounded up to 32.  B * V_pad may be at most
 // LLM_SAMPLE_NOALLOC_MAX_ELEMS (262144, e.g. 2 rows of a 128256-token vocabulary or 5 rows of
 // 49152).  Every call writes every element it later reads, so nothing has to start at zero.
 // All calls share the array: two calls whose kernels overlap on the GPU (other streams, other
@@ -17,8 +18,8 @@
 //
 // Host code may not use the array's name as a device pointer (on the host it names a stand-in,
 // not device memory).  The first call on each device, with that device current, looks the real
-// address up with cudaGetSymbolAddress and records it (and sets the sampler kernel's shared-memory
-// limit); later calls reuse it.  Make that first call before any stream capture on the device.
+// address up with cudaGetSymbolAddress and records it; later calls reuse it.  Make that first
+// call before any stream capture on the device.
 #include <mutex>
 
 #include "llm.h"
@@ -29,7 +30,9 @@ using namespace llm;
 namespace {
 
 constexpr size_t kParamBytes = 256;
-constexpr size_t kScratchBytes = kParamBytes + (size_t)LLM_SAMPLE_NOALLOC_MAX_ELEMS * (8 + 8 + 4);
+constexpr size_t kMaxRows = LLM_SAMPLE_NOALLOC_MAX_ELEMS / 32;
+constexpr size_t kHistBytes = 16 * 4 * (LLM_SAMPLE_NOALLOC_MAX_ELEMS / 2048 + kMaxRows);
+constexpr size_t kScratchBytes = kParamBytes + (size_t)LLM_SAMPLE_NOALLOC_MAX_ELEMS * (8 + 8 + 4) + kHistBytes;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_sample_scratch[kScratchBytes];
@@ -53,7 +56,6 @@ llm_status scratch_for_current_device(unsigned char** out) {
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_sample_scratch) != cudaSuccess || !p) return LLM_ERR_CUDA;
-    if (sample_prepare() != cudaSuccess) return LLM_ERR_CUDA;
     g_scratch_ptr[dev] = static_cast<unsigned char*>(p);
   }
   *out = g_scratch_ptr[dev];
@@ -78,6 +80,9 @@ extern "C" llm_status llm_sample_noalloc(const float* logits_dev, int32_t B, int
   uint32_t* keys = reinterpret_cast<uint32_t*>(base + kParamBytes);
   int32_t* idx = reinterpret_cast<int32_t*>(base + kParamBytes + n * 8);
   float* pre = reinterpret_cast<float*>(base + kParamBytes + n * 16);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(base + kParamBytes + n * 20);
+  // B rows of sample_slices(V) CTAs each; sample_slices(V) <= V / 2048 + 1 and B * V <= the limit
+  if ((size_t)B * (size_t)sample_slices(V) * 16 * 4 > kHistBytes) return LLM_ERR_ARG;
   noalloc_params_kernel<<<1, 1, 0, stream>>>(st, temp, k, p);
   if (cudaGetLastError() != cudaSuccess) return LLM_ERR_CUDA;
   SampleArgs a = {};
@@ -88,9 +93,10 @@ extern "C" llm_status llm_sample_noalloc(const float* logits_dev, int32_t B, int
   a.keys = keys;
   a.idx = idx;
   a.pre = pre;
+  a.hist = hist;
   a.u = u_dev;
   a.ids = ids_dev;
   a.step = st;
-  if (launch_sample(a, B, stream, false) != cudaSuccess) return LLM_ERR_CUDA;
+  if (launch_sample(a, B, !(temp > 0.0f), stream, false) != cudaSuccess) return LLM_ERR_CUDA;
   return LLM_OK;
 }

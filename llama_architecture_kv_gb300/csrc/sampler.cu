@@ -12,7 +12,7 @@
 // same definition draws the same id bit for bit:
 //   - candidates: a stable least-significant-digit radix sort (4-bit digits, 8 passes) of all
 //     logits on an order-preserving 32-bit key (largest first); stability keeps equal values in
-//     id order.  One CTA per row; each thread owns a contiguous run, so the scatter is stable.
+//     id order.  Each pass runs over up to 64 CTAs per row (count, scan, stable scatter).
 //   - weights: exp_s, a fixed sequence of IEEE operations (Cody-Waite reduction, degree-8 Taylor
 //     polynomial with fused multiply-adds, scaling by 2^n), never the hardware exp.
 //   - the cumulative weights are one sequential f32 running sum; Z is its last value.  Adding
@@ -24,6 +24,7 @@ namespace llm {
 
 constexpr int kSampThreads = 1024;
 constexpr int kDigits = 16;
+constexpr int kSortMaxSlices = kSortMaxSlicesPerRow;
 
 LLM_D float exp_s(float x) {
   if (x != x) return x;
@@ -73,14 +74,12 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const SampleArgs a
   const float* lg = a.logits + (size_t)b * a.logits_stride;
   __shared__ float s_v[32];
   __shared__ int s_i[32];
-  __shared__ int s_id;
 
   grid_dep_wait();
   grid_dep_launch();
 
-  const float temp = a.step->temp;
-  if (!(temp > 0.0f)) {
-    // ---- greedy ----
+  // greedy: the first index of the largest logit
+  {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     if ((a.logits_stride & 3) == 0) {
@@ -121,143 +120,252 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const SampleArgs a
       }
       if (lane == 0) a.ids[b] = (bi == 0x7fffffff) ? 0 : bi;
     }
-    return;
   }
+}
 
-  // ---- top-k / top-p ----
-  extern __shared__ __align__(16) uint32_t cnt[];  // [kDigits][kSampThreads]
+// ---------------------------------------------------------------------------------------
+// temperature / top-k / top-p: a stable radix sort of each row, then the in-order sums
+// ---------------------------------------------------------------------------------------
+// Sort: least-significant-digit radix on the 32-bit order key, 4-bit digits, 8 passes; every
+// pass is count (per CTA slice) -> exclusive scan (per row, digit-major) -> stable scatter (each
+// CTA writes its slice in index order).  Stability keeps equal values in id order, so the sorted
+// row is exactly "largest value first, ties by lower id".
+
+constexpr int kSortThreads = 256;
+
+LLM_HD int sort_slice(int V) {  // elements per CTA: 2048, more when the row needs over 64 CTAs
+  int s = (V + kSortMaxSlices - 1) / kSortMaxSlices;
+  s = (s + kSortThreads - 1) / kSortThreads * kSortThreads;
+  return s < 2048 ? 2048 : s;
+}
+
+__global__ void __launch_bounds__(kSortThreads) sort_init_kernel(const SampleArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.y, S = sort_slice(a.V);
+  const int s0 = blockIdx.x * S, s1 = min(a.V, s0 + S);
+  const float* lg = a.logits + (size_t)b * a.logits_stride;
   uint32_t* k0 = a.keys + (size_t)b * 2 * a.V_pad;
-  uint32_t* k1 = k0 + a.V_pad;
   int32_t* i0 = a.idx + (size_t)b * 2 * a.V_pad;
-  int32_t* i1 = i0 + a.V_pad;
-  float* pre = a.pre + (size_t)b * a.V_pad;
-  const int run = (V + kSampThreads - 1) / kSampThreads;
-  const int lo = min(V, tid * run), hi = min(V, lo + run);
-  for (int i = lo; i < hi; ++i) {
+  for (int i = s0 + threadIdx.x; i < s1; i += kSortThreads) {
     k0[i] = desc_key(lg[i]);
     i0[i] = i;
   }
+}
+
+__global__ void __launch_bounds__(kSortThreads) sort_count_kernel(const SampleArgs a, int pass) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.y, c = blockIdx.x, NB = gridDim.x, S = sort_slice(a.V), sh = 4 * pass;
+  const int s0 = c * S, s1 = min(a.V, s0 + S);
+  const uint32_t* ks = a.keys + (size_t)b * 2 * a.V_pad + (pass & 1) * a.V_pad;
+  __shared__ uint32_t cnt[kDigits];
+  if (threadIdx.x < kDigits) cnt[threadIdx.x] = 0u;
   __syncthreads();
-  uint32_t *ks = k0, *kd = k1;
-  int32_t *is = i0, *id = i1;
-  for (int pass = 0; pass < 8; ++pass) {
-    const int sh = 4 * pass;
-#pragma unroll
-    for (int d = 0; d < kDigits; ++d) cnt[d * kSampThreads + tid] = 0u;
-    for (int i = lo; i < hi; ++i) cnt[((ks[i] >> sh) & 15u) * kSampThreads + tid] += 1u;
-    __syncthreads();
-    // exclusive scan over [digit][thread]: thread t owns entries 16t .. 16t+15
-    uint32_t loc[16], sum = 0u;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      loc[e] = cnt[tid * 16 + e];
-      sum += loc[e];
-    }
-    uint32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    __shared__ uint32_t wtot[32];
-    if (lane == 31) wtot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t w = wtot[lane], wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += v;
-      }
-      wtot[lane] = wi - w;
-    }
-    __syncthreads();
-    uint32_t run_off = wtot[warp] + incl - sum;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const uint32_t c = loc[e];
-      cnt[tid * 16 + e] = run_off;
-      run_off += c;
-    }
-    __syncthreads();
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t key = ks[i];
-      uint32_t& slot = cnt[((key >> sh) & 15u) * kSampThreads + tid];
-      const uint32_t dst = slot++;
-      kd[dst] = key;
-      id[dst] = is[i];
-    }
-    __syncthreads();
-    uint32_t* tk = ks; ks = kd; kd = tk;
-    int32_t* ti = is; is = id; id = ti;
+  const int lane = threadIdx.x & 31;
+  for (int i0 = s0; i0 < s1; i0 += kSortThreads) {
+    const int i = i0 + threadIdx.x;
+    const uint32_t d = i < s1 ? (ks[i] >> sh) & 15u : 16u;
+    const uint32_t peers = __match_any_sync(0xffffffffu, d);
+    if (d < 16u && lane == __ffs(peers) - 1) atomicAdd(&cnt[d], (uint32_t)__popc(peers));
   }
-  // ks / is: all ids, largest logit first, ties by id
+  __syncthreads();
+  if (threadIdx.x < kDigits) a.hist[((size_t)b * kDigits + threadIdx.x) * NB + c] = cnt[threadIdx.x];
+}
+
+__global__ void __launch_bounds__(kSortThreads) sort_scan_kernel(const SampleArgs a, int NB) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* h = a.hist + (size_t)b * kDigits * NB;
+  const int n = kDigits * NB;                    // at most 16 * 64 = 1024 entries
+  const int per = (n + kSortThreads - 1) / kSortThreads;
+  uint32_t loc[4], sum = 0u;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int i = tid * per + e;
+    loc[e] = (e < per && i < n) ? h[i] : 0u;
+    sum += loc[e];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  __shared__ uint32_t wt[kSortThreads / 32];
+  if (lane == 31) wt[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0u;
+  for (int w = 0; w < warp; ++w) before += wt[w];
+  uint32_t run = before + incl - sum;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int i = tid * per + e;
+    if (e < per && i < n) {
+      h[i] = run;
+      run += loc[e];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(const SampleArgs a, int pass) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.y, c = blockIdx.x, NB = gridDim.x, S = sort_slice(a.V), sh = 4 * pass;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kSortThreads / 32;
+  const int s0 = c * S, s1 = min(a.V, s0 + S);
+  const size_t rowk = (size_t)b * 2 * a.V_pad;
+  const uint32_t* ks = a.keys + rowk + (pass & 1) * a.V_pad;
+  uint32_t* kd = a.keys + rowk + ((pass + 1) & 1) * a.V_pad;
+  const int32_t* is = a.idx + rowk + (pass & 1) * a.V_pad;
+  int32_t* id = a.idx + rowk + ((pass + 1) & 1) * a.V_pad;
+  __shared__ uint32_t base[kDigits], tot[kDigits], wcnt[NW][kDigits], wpre[NW][kDigits];
+  if (tid < kDigits) base[tid] = a.hist[((size_t)b * kDigits + tid) * NB + c];
+  for (int i0 = s0; i0 < s1; i0 += kSortThreads) {
+    if (tid < NW * kDigits) wcnt[tid / kDigits][tid % kDigits] = 0u;
+    __syncthreads();
+    const int i = i0 + tid;
+    const bool valid = i < s1;
+    const uint32_t key = valid ? ks[i] : 0u;
+    const int32_t idv = valid ? is[i] : 0;
+    const uint32_t d = valid ? (key >> sh) & 15u : 16u;
+    const uint32_t peers = __match_any_sync(0xffffffffu, d);
+    const uint32_t rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] = __popc(peers);
+    __syncthreads();
+    if (tid < kDigits) {
+      uint32_t r = 0u;
+      for (int w = 0; w < NW; ++w) {
+        wpre[w][tid] = r;
+        r += wcnt[w][tid];
+      }
+      tot[tid] = r;
+    }
+    __syncthreads();
+    if (valid) {
+      const uint32_t dst = base[d] + wpre[warp][d] + rank;
+      kd[dst] = key;
+      id[dst] = idv;
+    }
+    __syncthreads();
+    if (tid < kDigits) base[tid] += tot[tid];
+  }
+}
+
+// weights of the top min(k, V) candidates, their in-order running sum, the kept count and the draw
+constexpr int kFinalThreads = 1024;
+constexpr int kRunChunk = 8192;
+
+__global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const SampleArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int V = a.V;
+  const float* lg = a.logits + (size_t)b * a.logits_stride;
+  const int32_t* is = a.idx + (size_t)b * 2 * a.V_pad;  // after 8 passes the sorted row is in buffer 0
+  float* pre = a.pre + (size_t)b * a.V_pad;
+  __shared__ float chunk[kRunChunk];
+  const float temp = a.step->temp;
   const int k = min(a.step->k, V);
   const float top = lg[is[0]];
   const float ttop = __fdiv_rn(top, temp);
-  for (int j = tid; j < k; j += kSampThreads) pre[j] = exp_s(__fsub_rn(__fdiv_rn(lg[is[j]], temp), ttop));
+  for (int j = tid; j < k; j += kFinalThreads) pre[j] = exp_s(__fsub_rn(__fdiv_rn(lg[is[j]], temp), ttop));
   __syncthreads();
-  if (tid == 0) {
-    float s = 0.0f;
-    int j = 0;
-    for (; j + 8 <= k; j += 8) {
-      float w[8];
+  // the running sum is sequential by definition: one thread adds, in order, chunk by chunk
+  float run = 0.0f;
+  for (int c0 = 0; c0 < k; c0 += kRunChunk) {
+    const int n = min(kRunChunk, k - c0);
+    for (int j = tid; j < n; j += kFinalThreads) chunk[j] = pre[c0 + j];
+    __syncthreads();
+    if (tid == 0) {
+      int j = 0;
+      for (; j + 8 <= n; j += 8) {
+        float w[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) w[q] = pre[j + q];
+        for (int q = 0; q < 8; ++q) w[q] = chunk[j + q];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        s = __fadd_rn(s, w[q]);
-        pre[j + q] = s;
+        for (int q = 0; q < 8; ++q) {
+          run = __fadd_rn(run, w[q]);
+          chunk[j + q] = run;
+        }
+      }
+      for (; j < n; ++j) {
+        run = __fadd_rn(run, chunk[j]);
+        chunk[j] = run;
       }
     }
-    for (; j < k; ++j) {
-      s = __fadd_rn(s, pre[j]);
-      pre[j] = s;
-    }
-    const float Z = s;
+    __syncthreads();
+    for (int j = tid; j < n; j += kFinalThreads) pre[c0 + j] = chunk[j];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const float Z = pre[k - 1];
     const float lim = __fmul_rn(a.step->p, Z);
     // kept = 1 + number of leading running sums below lim, at most k
-    int lo_ = 0, hi_ = k;  // first j with pre[j] >= lim
-    while (lo_ < hi_) {
-      const int mid = (lo_ + hi_) >> 1;
-      if (pre[mid] < lim) lo_ = mid + 1;
-      else hi_ = mid;
+    int lo = 0, hi = k;  // first j with pre[j] >= lim
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] < lim) lo = mid + 1;
+      else hi = mid;
     }
-    const int kept = min(k, lo_ + 1);
+    const int kept = min(k, lo + 1);
     const float zp = pre[kept - 1];
     const float target = __fmul_rn(a.u[b], zp);
-    lo_ = 0;
-    hi_ = kept - 1;  // first j < kept-1 with target < pre[j], else kept-1
-    while (lo_ < hi_) {
-      const int mid = (lo_ + hi_) >> 1;
-      if (target < pre[mid]) hi_ = mid;
-      else lo_ = mid + 1;
+    lo = 0;
+    hi = kept - 1;  // first j < kept-1 with target < pre[j], else kept-1
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (target < pre[mid]) hi = mid;
+      else lo = mid + 1;
     }
-    s_id = is[lo_];
+    a.ids[b] = is[lo];
   }
-  __syncthreads();
-  if (tid == 0) a.ids[b] = s_id;
 }
 
-size_t sample_smem() { return (size_t)kDigits * kSampThreads * 4; }
-
-cudaError_t sample_prepare() {
-  return cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sample_smem());
-}
-
-cudaError_t launch_sample(const SampleArgs& a, int B, cudaStream_t s, bool pdl) {
+static cudaError_t launch(void (*fn)(const SampleArgs), dim3 grid, int threads, const SampleArgs& a,
+                          cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(B);
-  cfg.blockDim = dim3(kSampThreads);
-  cfg.dynamicSmemBytes = sample_smem();
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sample_kernel, a);
+  return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
+template <class Arg>
+static cudaError_t launch2(void (*fn)(const SampleArgs, Arg), dim3 grid, int threads, const SampleArgs& a,
+                           Arg x, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, a, x);
+}
+
+int sample_slices(int V) { return (V + sort_slice(V) - 1) / sort_slice(V); }
+
+cudaError_t launch_sample(const SampleArgs& a, int B, bool greedy, cudaStream_t s, bool pdl) {
+  if (greedy) return launch(sample_kernel, dim3(B), kSampThreads, a, s, pdl);
+  const int NB = sample_slices(a.V);
+  cudaError_t e = launch(sort_init_kernel, dim3(NB, B), kSortThreads, a, s, pdl);
+  for (int pass = 0; pass < 8 && e == cudaSuccess; ++pass) {
+    e = launch2(sort_count_kernel, dim3(NB, B), kSortThreads, a, pass, s, true);
+    if (e == cudaSuccess) e = launch2(sort_scan_kernel, dim3(B), kSortThreads, a, NB, s, true);
+    if (e == cudaSuccess) e = launch2(sort_scatter_kernel, dim3(NB, B), kSortThreads, a, pass, s, true);
+  }
+  if (e == cudaSuccess) e = launch(sample_final_kernel, dim3(B), kFinalThreads, a, s, true);
+  return e;
 }
 
 }  // namespace llm

@@ -12,13 +12,17 @@ struct SampleArgs {
   uint32_t* keys;        // scratch [B][2][V_pad]
   int32_t* idx;          // scratch [B][2][V_pad]
   float* pre;            // scratch [B][V_pad]: weights, then their running sums
+  uint32_t* hist;        // scratch [B][16][sample_slices(V)]: digit counts, then offsets, per CTA slice
   const float* u;        // [B] uniform draws
   int32_t* ids;          // [B] drawn ids
   const StepState* step; // temp, k, p
 };
 
-size_t sample_smem();
-cudaError_t sample_prepare();
-cudaError_t launch_sample(const SampleArgs& a, int B, cudaStream_t s, bool pdl);
+constexpr int kSortMaxSlicesPerRow = 64;
+constexpr size_t kSampleHistPerRow = 16 * kSortMaxSlicesPerRow;  // uint32 entries a row needs at most
+
+int sample_slices(int V);
+// greedy: one argmax kernel; otherwise the sort chain and the draw (temp, k, p from *step)
+cudaError_t launch_sample(const SampleArgs& a, int B, bool greedy, cudaStream_t s, bool pdl);
 
 }  // namespace llm
