@@ -376,7 +376,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (weights %.1f GB per step)" % (wbytes / 1e9),
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
-        "clocks": clk, "gpu_launches": K * (5 * s.layers + 4),
+        "clocks": clk, "gpu_launches": K * pkg.llm_step_kernels(h, B, temp),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -75,6 +75,9 @@ typedef struct llm_config {
   int32_t max_seq;      /* cache positions per row                            */
   int32_t dtype;        /* LLM_DTYPE_BF16: bf16 weights and bf16 cache; LLM_DTYPE_F32: both f32 */
   int32_t debug_trace;  /* 1: keep per-layer intermediates (slow path, for llm_debug_trace) */
+  int32_t tc_min_batch; /* bf16 only: steps of at least this many rows run the projections on the
+                           tensor cores (TMA-fed tcgen05 GEMM), fewer rows on the weight-streaming
+                           GEMV; 0: the library default (16); above max_batch: never */
 } llm_config;
 
 typedef struct llm_handle llm_handle;
@@ -205,6 +208,14 @@ llm_status llm_debug_trace(llm_handle* h, int32_t layer, const char* name, float
  */
 llm_status llm_profile_kernel(llm_handle* h, int32_t which, int32_t B, int32_t pos, int32_t reps,
                               float* ms_per_launch);
+
+/*
+ * How many kernels one llm_step / llm_step_dev of B rows launches at temperature temp (greedy
+ * when temp == 0): the step prologue plus the kernels of the step's CUDA graph, which this call
+ * captures if it does not exist yet (no kernel runs).  LLM_ERR_BATCH for B outside
+ * 1..max_batch; LLM_ERR_ARG for handles created with debug_trace (they run without a graph).
+ */
+llm_status llm_step_kernels(llm_handle* h, int32_t B, float temp, int32_t* kernels);
 
 /*
  * Sampling without a handle and without allocating: the same draw as llm_sample_dev (greedy

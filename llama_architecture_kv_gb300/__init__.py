@@ -21,7 +21,8 @@ EXPORTS = ("llm_weight_count", "llm_create", "llm_destroy", "llm_reset", "llm_pr
            "llm_sample", "llm_step", "llm_prefill_dev", "llm_decode_dev", "llm_sample_dev",
            "llm_step_dev", "llm_synchronize", "llm_stream", "llm_logits_buffer", "llm_filled",
            "llm_last_error", "llm_status_string", "llm_kv_import", "llm_kv_export",
-           "llm_debug_trace", "llm_profile_kernel", "llm_sample_noalloc")
+           "llm_debug_trace", "llm_profile_kernel", "llm_sample_noalloc",
+           "llm_step_kernels")
 
 
 class LlmConfig(ctypes.Structure):
@@ -32,7 +33,7 @@ class LlmConfig(ctypes.Structure):
                 ("rope_low_freq", ctypes.c_float), ("rope_high_freq", ctypes.c_float),
                 ("rope_orig_max_pos", ctypes.c_float), ("max_batch", ctypes.c_int32),
                 ("max_seq", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("debug_trace", ctypes.c_int32)]
+                ("debug_trace", ctypes.c_int32), ("tc_min_batch", ctypes.c_int32)]
 
 
 class LlmError(RuntimeError):
@@ -78,6 +79,7 @@ def lib():
             "llm_debug_trace": ([vp, i32, ctypes.c_char_p, vp], i32),
             "llm_profile_kernel": ([vp, i32, i32, i32, i32, ctypes.POINTER(f32)], i32),
             "llm_sample_noalloc": ([vp, i32, i32, f32, i32, f32, vp, vp, vp], i32),
+            "llm_step_kernels": ([vp, i32, f32, ctypes.POINTER(i32)], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -87,13 +89,14 @@ def lib():
     return _lib
 
 
-def config(shape, max_batch, max_seq, debug_trace=False) -> LlmConfig:
+def config(shape, max_batch, max_seq, debug_trace=False, tc_min_batch=0) -> LlmConfig:
     """An llm_config from a shape description (fields kv, g, half, ffn, layers, vocab, eps,
     theta, tied, llama3, factor, low_freq, high_freq, orig_max, bf16)."""
     return LlmConfig(shape.kv, shape.g, shape.half, shape.ffn, shape.layers, shape.vocab,
                      shape.eps, shape.theta, int(shape.tied), int(shape.llama3), shape.factor,
                      shape.low_freq, shape.high_freq, shape.orig_max, max_batch, max_seq,
-                     LLM_DTYPE_BF16 if shape.bf16 else LLM_DTYPE_F32, int(debug_trace))
+                     LLM_DTYPE_BF16 if shape.bf16 else LLM_DTYPE_F32, int(debug_trace),
+                     int(tc_min_batch))
 
 
 def _ptr(a):
@@ -214,6 +217,12 @@ def llm_profile_kernel(h, which, B, pos, reps) -> float:
     return float(ms.value)
 
 
+def llm_step_kernels(h, B, temp) -> int:
+    n = ctypes.c_int32()
+    _check(h, lib().llm_step_kernels(h, B, temp, ctypes.byref(n)))
+    return int(n.value)
+
+
 SAMPLE_NOALLOC_MAX_ELEMS = 262144
 
 
@@ -231,9 +240,9 @@ class Model:
     """One handle: host-memory entry points with numpy arrays."""
 
     def __init__(self, shape, weights, max_batch, max_seq, stream=None, debug_trace=False,
-                 weights_on_device=False):
+                 weights_on_device=False, tc_min_batch=0):
         self.shape = shape
-        self.cfg = config(shape, max_batch, max_seq, debug_trace)
+        self.cfg = config(shape, max_batch, max_seq, debug_trace, tc_min_batch)
         self.h = llm_create(self.cfg, weights, weights_on_device, stream)
         self.V = shape.vocab
         self.cache_dtype = np.uint16 if shape.bf16 else np.float32

@@ -19,6 +19,7 @@
 
 #include "attention.cuh"
 #include "common.cuh"
+#include "gemm.cuh"
 #include "gemv.cuh"
 #include "llm.h"
 #include "sampler.cuh"
@@ -144,6 +145,10 @@ struct LayerW {
   void* down;  // [d][f]
 };
 
+struct TcMaps {
+  CUtensorMap qkv, o, gu, down;
+};
+
 struct GraphKey {
   int B, mode;
   bool operator<(const GraphKey& o) const { return B != o.B ? B < o.B : mode < o.mode; }
@@ -182,8 +187,16 @@ struct llm_handle {
   uint32_t* s_hist = nullptr;
   int V_pad = 0;
   float* trace = nullptr;  // [L][5][max_batch][max(d, f)]
+  // tensor-core projections (bf16, steps of at least tc_min rows)
+  int tc_min = 0;          // 0: the tensor-core path is off for this handle
+  std::vector<TcMaps> tmaps;
+  CUtensorMap tmap_head;
+  uint16_t* tc_xs = nullptr;    // split activations [2][Ntot][max(d, f)]
+  float* tc_part = nullptr;     // stream-K partials
+  uint32_t* tc_ticket = nullptr;
+  std::map<std::pair<int, int>, CUtensorMap> xmaps;  // (K, B) -> map over tc_xs
   std::vector<int32_t> filled;
-  std::map<GraphKey, cudaGraphExec_t> graphs;
+  std::map<GraphKey, std::pair<cudaGraphExec_t, int>> graphs;  // executable graph, kernels in it
   std::string err;
 };
 
@@ -345,7 +358,37 @@ SampleArgs sample_args(const llm_handle* h) {
   return s;
 }
 
-// launch one kernel of the decode step (layer l where it applies)
+// the activation map of a B-row step over K-wide rows (built on first use; host only)
+const CUtensorMap* tc_xmap(llm_handle* h, int K, int B) {
+  auto key = std::make_pair(K, B);
+  auto it = h->xmaps.find(key);
+  if (it != h->xmaps.end()) return &it->second;
+  const TcPlan p = plan_tc(kTcM, K, B, h->num_sms);
+  CUtensorMap m;
+  if (!tc_make_map(&m, h->tc_xs, (uint64_t)K, 2 * (uint64_t)p.Ntot, kTcK, (uint32_t)p.NP)) return nullptr;
+  return &h->xmaps.emplace(key, m).first->second;
+}
+
+// x' = x or RMSNorm(x) split into bf16 halves, then out = W x' on the tensor cores with epilogue
+// epi; `a` carries the epilogue's pointers
+llm_status launch_tc(llm_handle* h, const CUtensorMap& tw, int rows, int K, const float* x, int x_stride,
+                     const float* gain, int epi, TcArgs a, int B, bool pdl) {
+  const TcPlan p = plan_tc(rows, K, B, h->num_sms);
+  const CUtensorMap* tx = tc_xmap(h, K, B);
+  if (!tx) return fail(h, LLM_ERR_CUDA, "tensor map of the activations (K %d, B %d)", K, B);
+  TcSplitArgs sa = {};
+  sa.x = x; sa.x_stride = x_stride; sa.gain = gain; sa.eps = h->cfg.eps;
+  sa.K = K; sa.B = B; sa.Ntot = p.Ntot; sa.xs = h->tc_xs;
+  CUDA_TRY(h, launch_tc_split(sa, h->stream, pdl));
+  a.rows = rows; a.K = K; a.N = B; a.NP = p.NP; a.Ntot = p.Ntot; a.MT = p.MT; a.KB = p.KB;
+  a.stages = p.stages; a.tmem_cols = p.tmem_cols; a.part = h->tc_part; a.ticket = h->tc_ticket;
+  a.status = h->status; a.step = h->st;
+  CUDA_TRY(h, launch_tc_gemm(tw, *tx, a, p, epi, h->stream, pdl));
+  return LLM_OK;
+}
+
+// launch one kernel of the decode step (layer l where it applies); on the tensor-core path a
+// projection is two kernels (activation split, then the GEMM)
 llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
   const int wt = h->wt;
   const int cps = 2;
@@ -364,6 +407,12 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     else CUDA_TRY(h, cudaLaunchKernelEx(&lc, embed_kernel<0>, (const void*)h->emb, (const int32_t*)h->tok_buf, h->xa, h->d, h->d));
     return LLM_OK;
   }
+  const bool tc = h->tc_min > 0 && B >= h->tc_min;
+  if (which == K_HEAD && tc) {
+    TcArgs a = {};
+    a.out = h->logits; a.out_stride = h->V;
+    return launch_tc(h, h->tmap_head, h->V, h->d, h->xa, h->d, h->lnf, EPI_STORE, a, B, pdl);
+  }
   if (which == K_HEAD) {
     const GemvPlan p_h = plan_gemv(h->V, h->d, 1, wt, B, h->num_sms, cps);
     GemvArgs hd = {};
@@ -381,6 +430,28 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
   const LayerW& w = h->lw[l];
   char* kcl = (char*)h->kc + (size_t)l * h->layer_cache_elems * h->es;
   char* vcl = (char*)h->vc + (size_t)l * h->layer_cache_elems * h->es;
+  if (tc && which != K_ATTN) {
+    const TcMaps& tm = h->tmaps[l];
+    TcArgs a = {};
+    if (which == K_QKV) {
+      a.q_out = h->q; a.q_stride = h->d; a.kc = kcl; a.vc = vcl;
+      a.H = h->H; a.kv = c.kv_heads; a.hd = h->hd; a.cap = c.max_seq;
+      a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin;
+      return launch_tc(h, tm.qkv, (h->H + 2 * c.kv_heads) * h->hd, h->d, h->xa, h->d, w.ln1, EPI_QKV, a, B, pdl);
+    }
+    if (which == K_O) {
+      a.out = h->xb; a.out_stride = h->d; a.resid = h->xa; a.resid_stride = h->d;
+      return launch_tc(h, tm.o, h->d, h->d, h->attn, h->d, nullptr, EPI_RESID, a, B, pdl);
+    }
+    if (which == K_GATEUP) {
+      a.out = h->m; a.out_stride = h->f;
+      return launch_tc(h, tm.gu, 2 * h->f, h->d, h->xb, h->d, w.ln2, EPI_SWIGLU, a, B, pdl);
+    }
+    if (which == K_DOWN) {
+      a.out = h->xa; a.out_stride = h->d; a.resid = h->xb; a.resid_stride = h->d;
+      return launch_tc(h, tm.down, h->d, h->f, h->m, h->f, nullptr, EPI_RESID, a, B, pdl);
+    }
+  }
   if (which == K_QKV) {
     const int qkv_rows = (h->H + 2 * c.kv_heads) * h->hd;
     const GemvPlan p = plan_gemv(qkv_rows, h->d, 2, wt, B, h->num_sms, cps);
@@ -456,8 +527,8 @@ llm_status launch_layer_kernels(llm_handle* h, int B, int mode, bool pdl, bool t
   return LLM_OK;
 }
 
-llm_status run_step(llm_handle* h, int B, int mode) {
-  if (h->cfg.debug_trace) return launch_layer_kernels(h, B, mode, false, true);
+// the step graph of (B, mode), captured on first use
+llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t, int>** out) {
   GraphKey key{B, mode};
   auto it = h->graphs.find(key);
   if (it == h->graphs.end()) {
@@ -474,13 +545,23 @@ llm_status run_step(llm_handle* h, int B, int mode) {
       return s;
     }
     if (e != cudaSuccess) return fail(h, LLM_ERR_CUDA, "stream capture: %s", cudaGetErrorString(e));
+    size_t nodes = 0;  // every node of the step graph is a kernel launch
+    e = cudaGraphGetNodes(graph, nullptr, &nodes);
     cudaGraphExec_t exec = nullptr;
-    e = cudaGraphInstantiate(&exec, graph, 0);
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
     if (e != cudaSuccess) return fail(h, LLM_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
-    it = h->graphs.emplace(key, exec).first;
+    it = h->graphs.emplace(key, std::make_pair(exec, (int)nodes)).first;
   }
-  CUDA_TRY(h, cudaGraphLaunch(it->second, h->stream));
+  *out = &it->second;
+  return LLM_OK;
+}
+
+llm_status run_step(llm_handle* h, int B, int mode) {
+  if (h->cfg.debug_trace) return launch_layer_kernels(h, B, mode, false, true);
+  std::pair<cudaGraphExec_t, int>* g = nullptr;
+  TRY(step_graph(h, B, mode, &g));
+  CUDA_TRY(h, cudaGraphLaunch(g->first, h->stream));
   return LLM_OK;
 }
 
@@ -576,7 +657,7 @@ const char* llm_last_error(const llm_handle* h) { return h ? h->err.c_str() : g_
 llm_status llm_destroy(llm_handle* h) {
   if (!h) return LLM_ERR_ARG;
   if (h->stream) cudaStreamSynchronize(h->stream);
-  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second.first);
   for (void* p : h->allocs) cudaFree(p);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->own_stream && h->stream) cudaStreamDestroy(h->stream);
@@ -641,6 +722,12 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   }
   if ((ce = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking)) != cudaSuccess) return cuda_bail("capture stream", ce);
   if ((ce = gemv_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("gemv kernel attributes", ce);
+  // tensor-core path: bf16 weights, rows a whole number of 16-byte chunks (checked above)
+  const int tc_min = c.tc_min_batch > 0 ? c.tc_min_batch : kTcDefaultMinBatch;
+  if (h->wt && tc_min <= c.max_batch && tc_available()) {
+    if ((ce = tc_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("tensor-core kernel attributes", ce);
+    h->tc_min = tc_min;
+  }
   if ((ce = attn_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("attention kernel attributes", ce);
   // weights: a device copy of the blob when it is on the host, then repacked
   const char* blob = (const char*)weights;
@@ -684,6 +771,29 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   if ((st = dalloc(h, &h->s_keys, B * 2 * h->V_pad * 4)) || (st = dalloc(h, &h->s_idx, B * 2 * h->V_pad * 4)) ||
       (st = dalloc(h, &h->s_pre, B * h->V_pad * 4)) || (st = dalloc(h, &h->s_hist, B * kSampleHistPerRow * 4)))
     return bail(st);
+  if (h->tc_min) {
+    const TcPlan pm = plan_tc(kTcM, std::max(h->d, h->f), c.max_batch, h->num_sms);
+    const int64_t rows_max = std::max<int64_t>(std::max<int64_t>(h->V, 2 * (int64_t)h->f), (int64_t)(h->H + 2 * c.kv_heads) * h->hd);
+    const size_t tickets = (size_t)pm.ntiles * (size_t)((rows_max + kTcM - 1) / kTcM);
+    if ((st = dalloc(h, &h->tc_xs, (size_t)2 * pm.Ntot * std::max(h->d, h->f) * 2)) ||
+        (st = dalloc(h, &h->tc_part, (size_t)pm.ntiles * h->num_sms * 2 * pm.NP * kTcM * 4)) ||
+        (st = dalloc(h, &h->tc_ticket, tickets * 4)))
+      return bail(st);
+    if (cudaMemsetAsync(h->tc_xs, 0, (size_t)2 * pm.Ntot * std::max(h->d, h->f) * 2, h->stream) != cudaSuccess ||
+        cudaMemsetAsync(h->tc_ticket, 0, tickets * 4, h->stream) != cudaSuccess)
+      return cuda_bail("clearing the tensor-core scratch", cudaGetLastError());
+    h->tmaps.resize(h->L);
+    bool ok = true;
+    for (int l = 0; l < h->L && ok; ++l) {
+      const LayerW& w = h->lw[l];
+      TcMaps& m = h->tmaps[l];
+      ok = tc_make_map(&m.qkv, w.qkv, h->d, (uint64_t)(h->H + 2 * c.kv_heads) * h->hd, kTcK, kTcM) &&
+           tc_make_map(&m.o, w.o, h->d, h->d, kTcK, kTcM) && tc_make_map(&m.gu, w.gu, h->d, 2 * (uint64_t)h->f, kTcK, kTcM) &&
+           tc_make_map(&m.down, w.down, h->f, h->d, kTcK, kTcM);
+    }
+    // a shape the tensor maps cannot describe keeps every step on the GEMV
+    if (!ok || !tc_make_map(&h->tmap_head, h->head, h->d, h->V, kTcK, kTcM)) h->tc_min = 0;
+  }
   if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * 5 * B * std::max(h->d, h->f) * 4))) return bail(st);
   if (cudaMemsetAsync(h->ticket, 0, B * c.kv_heads * 4, h->stream) != cudaSuccess ||
       cudaMemsetAsync(h->status, 0, 16, h->stream) != cudaSuccess ||
@@ -873,6 +983,16 @@ llm_status llm_kv_import(llm_handle* h, int32_t layer, int32_t row, int32_t pos0
 
 llm_status llm_kv_export(llm_handle* h, int32_t layer, int32_t row, int32_t pos0, int32_t n, void* k_host, void* v_host) {
   return kv_copy(h, layer, row, pos0, n, k_host, v_host, false);
+}
+
+llm_status llm_step_kernels(llm_handle* h, int32_t B, float temp, int32_t* kernels) {
+  if (!h || !kernels) return LLM_ERR_ARG;
+  if (B < 1 || B > h->cfg.max_batch) return fail(h, LLM_ERR_BATCH, "batch %d outside 1..%d", B, h->cfg.max_batch);
+  if (h->cfg.debug_trace) return fail(h, LLM_ERR_ARG, "debug_trace handles run without a step graph");
+  std::pair<cudaGraphExec_t, int>* g = nullptr;
+  TRY(step_graph(h, B, temp > 0.0f ? MODE_TOPP : MODE_GREEDY, &g));
+  *kernels = 1 + g->second;  // the step prologue, then the graph
+  return LLM_OK;
 }
 
 llm_status llm_profile_kernel(llm_handle* h, int32_t which, int32_t B, int32_t pos, int32_t reps, float* ms_per_launch) {

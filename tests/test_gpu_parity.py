@@ -282,3 +282,78 @@ def test_smollm2_135m_short():
     agree = run_teacher_forced(w.shape, blob, g, prompt, 12, f32=False)
     assert np.mean(agree) >= ARGMAX_AGREE
     g.close()
+
+
+# ---------------------------------------------------------------------------------------
+# tensor-core projections (bf16 steps of at least tc_min_batch rows)
+# ---------------------------------------------------------------------------------------
+
+TC_SHAPES = [
+    # 135M-like: Q/K/V rows 960 (a ragged last 128-row tile), K = 576 (9 blocks of 64)
+    ("smol135_like", shrink(WORKLOADS["smollm2_135m"].shape, layers=2, vocab=8192)),
+    # 8B-like: head dim 128, g 4, untied head with a ragged vocabulary, llama3 RoPE
+    ("llama_like", shrink(WORKLOADS["llama8b_b1"].shape, layers=2, kv=2, ffn=1024, vocab=3000)),
+    # 1.7B-like: g 1, head dim 64, MLP width 712 (a partial last K block in down)
+    ("smol17_like", shrink(WORKLOADS["smollm2_1_7b_b16"].shape, layers=2, kv=4, ffn=712, vocab=2500)),
+]
+
+
+@pytest.mark.parametrize("name,shape", TC_SHAPES, ids=lambda x: x if isinstance(x, str) else "")
+@pytest.mark.parametrize("B", [3, 17, 40])
+def test_tensor_core_path_teacher_forced(name, shape, B):
+    # tc_min_batch = 1 puts every step of this handle on the tensor-core path (16-, 32- and
+    # 48-column tiles for B = 3, 17, 40)
+    S, steps, cap = 5, 4, 12
+    blob = synth.model_blob(shape, 91)
+    g = pkg.Model(shape, blob, max_batch=B, max_seq=cap, tc_min_batch=1)
+    prompts = synth.tokens(92, 0, B * S, shape.vocab).reshape(B, S)
+    rows = sorted({0, B // 2, B - 1})
+    refs = {b: oracle.Model(oracle.cfg_of(shape, 1, cap), blob) for b in rows}
+    lg = g.prefill(prompts, 0)
+    agree = []
+    for b in rows:
+        check_bf16(lg[b], refs[b].prefill(0, prompts[b], 0), agree)
+    toks = np.array([np.argmax(lg[b]) for b in range(B)], np.int32)
+    for t in range(S, S + steps):
+        ids, lg = g.step(toks, t, logits=True)
+        for b in rows:
+            check_bf16(lg[b], refs[b].forward(0, int(toks[b]), t), agree)
+            assert int(ids[b]) == oracle.argmax(lg[b])
+        toks = ids
+    assert np.mean(agree) >= ARGMAX_AGREE
+    for r in refs.values():
+        r.close()
+    g.close()
+
+
+def test_tensor_core_and_gemv_paths_agree():
+    shape = TC_SHAPES[1][1]
+    B, S, cap = 16, 6, 10
+    blob = synth.model_blob(shape, 93)
+    prompts = synth.tokens(94, 0, B * S, shape.vocab).reshape(B, S)
+    outs = []
+    for tc_min in (1, 1 << 20):
+        g = pkg.Model(shape, blob, max_batch=B, max_seq=cap, tc_min_batch=tc_min)
+        lg = g.prefill(prompts, 0)
+        ids, lg2 = g.step(np.argmax(lg, axis=1).astype(np.int32), S, logits=True)
+        outs.append((lg, lg2, ids))
+        g.close()
+    # the activations reach the tensor cores as bf16 hi + lo pairs (about 2^-17 relative)
+    for a, b in zip(outs[0][:2], outs[1][:2]):
+        assert float(np.max(np.abs(a - b))) <= 2e-3
+    rng_ = outs[1][1].max(axis=1) - outs[1][1].min(axis=1)
+    assert np.all(rng_ > 0)
+
+
+def test_step_kernel_counts():
+    shape = TC_SHAPES[0][1]
+    L = shape.layers
+    blob = synth.model_blob(shape, 95)
+    g = pkg.Model(shape, blob, max_batch=20, max_seq=8, tc_min_batch=16)
+    greedy_gemv = pkg.llm_step_kernels(g.h, 4, 0.0)
+    assert greedy_gemv == 5 * L + 4  # prologue, embedding, 5 per layer, head, argmax
+    assert pkg.llm_step_kernels(g.h, 16, 0.0) == greedy_gemv + 4 * L + 1  # an activation split per projection
+    assert pkg.llm_step_kernels(g.h, 4, 0.8) == greedy_gemv + 25  # 8 passes x 3 sort kernels + init + draw
+    with pytest.raises(pkg.LlmError):
+        pkg.llm_step_kernels(g.h, 21, 0.0)
+    g.close()
