@@ -7,52 +7,84 @@
 // attention.linnet decode: seen[s] = s <= pos).
 //
 // Layout: the cache of one layer is [max_batch][kv][cap][hd] (attention.linnet cache_k), so the
-// positions of one (row, key/value head) are contiguous.  Grid: (splits, kv, B).  A CTA takes
-// one contiguous slice of positions of one (row, kv head) and streams it through shared memory
-// in tiles (cp.async, a ring of 2..4 tiles, all but one in flight); the g query heads of the
-// group are served from the same tile, so the cache is read from HBM once.  Inside a tile all eight warps work on it together,
-// which keeps the dependent chains short (decode attention at small batch is latency-bound):
-//   scores   one thread per (head, position): a dot product of hd with four accumulators;
-//   softmax  one warp per head: tile maximum, running max m, weights exp(s - m), running sum l;
-//   values   one thread per (head, two dimensions), or a few threads splitting the positions
-//            when heads x dimensions is small; outputs stay in registers across tiles.
-// Merging the splits of one (row, kv head) (log-sum-exp, in split order, so the result does not
-// depend on timing):
-//   up to attn_max_cluster() splits (8, or 16 where the device allows) form one cluster; each CTA leaves its partial in
-//   its shared memory and, after a cluster barrier, CTA 0 of the cluster reads the others'
-//   through distributed shared memory;
-//   more splits (long contexts) write partials to global memory, and the last CTA to finish --
-//   found with an atomic ticket, nobody waits -- merges them.
+// positions of one (row, key/value head) are contiguous.  Grid: (splits, kv, B); a CTA takes a
+// contiguous slice of positions of one (row, kv head) and its warps take 32-position chunks of
+// it in turn.  Each warp streams its own chunks through a private ring of shared-memory buffers
+// (a TMA tensor copy of the keys with the 128-byte swizzle, a bulk copy of the values; one
+// mbarrier per buffer), so warps never wait for one another inside the loop.  Per chunk:
+//   scores   lane = position: the g dot products q_h . K[p] (the key row is read once for the
+//            whole group; the queries are shared-memory broadcasts; the swizzle keeps the 32
+//            lanes' row reads on distinct banks);
+//   softmax  per head, across the warp: chunk maximum, running max m, weights exp(s - m),
+//            per-lane running sums l, rescaled when m grows;
+//   values   lane = hd/32 consecutive dimensions of every head; per position one value load and
+//            one broadcast of the g weights.
+// The warps' (o, m, l) merge in warp order, then the splits of one (row, kv head) merge by
+// log-sum-exp in split order (the result does not depend on timing): up to attn_max_cluster()
+// splits form one thread-block cluster and CTA 0 reads the others' partials through distributed
+// shared memory; more splits (long contexts) write partials to global memory and the last CTA to
+// finish -- found with an atomic ticket, nobody waits -- merges them.
+// Chunks that lie entirely below position t were written by earlier steps, so their copies start
+// before the wait on the previous kernel (which writes position t).
 #include "attention.cuh"
+#include "gemm.cuh"
+#include "tc.cuh"
 
 namespace llm {
 
-constexpr int kAttnThreads = 256;
-constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kChunk = 32;      // positions per chunk: one per lane
 constexpr int kMinChunk = 64;   // fewest positions a split takes
-constexpr int kMaxPairs = 4;    // output pairs (two dimensions each) per thread
+constexpr int kAttnMaxThreads = 128;
+constexpr uint64_t kAttnWaitCycles = 1000000000ull;  // about 0.5 s at 2 GHz
 
-// Tile shape: about 256 (head, position) scores per tile, and a ring of 2..4 tile buffers
-// (ring - 1 tiles in flight ahead of the one in use) within 160 KB of shared memory.
-struct TileCfg {
-  int tp, ring;
+template <int KT, int HD>
+struct AttnShape {
+  static constexpr int ES = Elem<KT>::bytes;
+  static constexpr int ROWB = HD * ES;               // bytes of one cached row
+  static constexpr bool SWZ = ROWB >= 128;           // keys staged with the 128-byte swizzle
+  static constexpr int BOXB = SWZ ? 128 : ROWB;      // bytes of a key row inside one copy box
+  static constexpr int NBOX = ROWB / BOXB;           // boxes per key chunk
+  static constexpr int BUF = 2 * kChunk * ROWB;      // one chunk: keys, then values
+  static constexpr int CPR = ROWB / 16;              // 16-byte pieces of a row
+  static constexpr int EPC = 16 / ES;                // elements per piece
+  static constexpr int DPL = HD >= 32 ? HD / 32 : 1; // value dimensions per lane
+  static constexpr int VL = HD >= 32 ? 32 : HD;      // lanes that hold value dimensions
 };
-LLM_HD TileCfg tile_cfg(int g, int rowb) {
-  int tp = g >= 8 ? 32 : g >= 2 ? 32 * (8 / g) : 128;
-  const size_t per = 2 * (size_t)rowb + 16;  // a padded key row and a value row
-  const size_t budget = 160 * 1024;
-  int ring = 4;
-  while (ring > 2 && ring * tp * per > budget) --ring;
-  while (tp > 32 && ring * tp * per > budget) tp -= 32;
-  return {tp, ring};
+
+// warps per CTA and buffers per warp for a chunk of buf bytes (within 192 KB)
+struct AttnGeom {
+  int nw, nr;
+};
+LLM_HD AttnGeom attn_geom(int buf) {
+  const int budget = 192 * 1024;
+  int nw = 4;
+  while (nw > 1 && nw * 2 * buf > budget) nw >>= 1;
+  int nr = 3;
+  while (nr > 2 && nw * nr * buf > budget) --nr;
+  return {nw, nr};
 }
 
-LLM_D void cp_async16(void* smem, const void* gmem) {
-  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+template <int KT, int HD>
+LLM_HD size_t attn_region(int g, int ns) {  // ring buffers; the global merge reuses them
+  const AttnGeom geo = attn_geom(AttnShape<KT, HD>::BUF);
+  size_t r = (size_t)geo.nw * geo.nr * AttnShape<KT, HD>::BUF;
+  if (r < (size_t)g * ns * 8) r = (size_t)g * ns * 8;
+  return (r + 1023) & ~(size_t)1023;
 }
-LLM_D void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> LLM_D void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int KT, int HD, int GM>
+LLM_HD size_t attn_smem(int g, int ns) {
+  const AttnGeom geo = attn_geom(AttnShape<KT, HD>::BUF);
+  size_t s = 1024 + attn_region<KT, HD>(g, ns);
+  s += (size_t)g * HD * 4;                    // queries
+  s += (size_t)geo.nw * kChunk * GM * 4;      // weights of the chunk in use, per warp
+  s += (size_t)geo.nw * g * (HD + 2) * 4;     // warp partials
+  s += (size_t)g * (HD + 2) * 4;              // CTA partial
+  s += (size_t)g * kAttnMaxCluster * 4;       // merge factors
+  s = (s + 7) & ~(size_t)7;
+  s += (size_t)geo.nw * geo.nr * 8;           // mbarriers
+  return s;
+}
 
 LLM_D void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -71,259 +103,99 @@ LLM_D float ld_cluster(const float* p, uint32_t rank) {
   return v;
 }
 
-template <int KT> LLM_D float2 load2(const void* base, int idx) {
-  if constexpr (KT == 0) {
-    return *reinterpret_cast<const float2*>((const float*)base + idx);
+// DPL consecutive cached elements as f32
+template <int KT, int DPL>
+LLM_D void load_dims(const unsigned char* p, float (&v)[DPL]) {
+  if constexpr (KT == 1) {
+    if constexpr (DPL == 1) {
+      v[0] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(p));
+    } else if constexpr (DPL == 2) {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+      v[0] = bf16_lo(u);
+      v[1] = bf16_hi(u);
+    } else if constexpr (DPL == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+    } else {
+#pragma unroll
+      for (int q = 0; q < DPL; q += 8) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p + q * 2);
+        v[q + 0] = bf16_lo(u.x); v[q + 1] = bf16_hi(u.x); v[q + 2] = bf16_lo(u.y); v[q + 3] = bf16_hi(u.y);
+        v[q + 4] = bf16_lo(u.z); v[q + 5] = bf16_hi(u.z); v[q + 6] = bf16_lo(u.w); v[q + 7] = bf16_hi(u.w);
+      }
+    }
   } else {
-    const uint32_t u = *reinterpret_cast<const uint32_t*>((const uint16_t*)base + idx);
-    return make_float2(bf16_lo(u), bf16_hi(u));
+    if constexpr (DPL == 1) {
+      v[0] = *reinterpret_cast<const float*>(p);
+    } else if constexpr (DPL == 2) {
+      const float2 f = *reinterpret_cast<const float2*>(p);
+      v[0] = f.x; v[1] = f.y;
+    } else {
+#pragma unroll
+      for (int q = 0; q < DPL; q += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(p + q * 4);
+        v[q] = f.x; v[q + 1] = f.y; v[q + 2] = f.z; v[q + 3] = f.w;
+      }
+    }
   }
 }
 
-template <int KT, int HD>
-struct AttnSmem {
-  static constexpr int ES = Elem<KT>::bytes;
-  static constexpr int ROWB = HD * ES;    // bytes of one cached row
-  static constexpr int KPAD = ROWB + 16;  // padded key row: lanes reading different rows do not collide
-  // qs [g][HD] | tiles: kbuf [ring][TP][KPAD], vbuf [ring][TP][ROWB] | sw [g][TP] | m, l, corr [g] |
-  // part [g][HD+2] | fac [g][kAttnMaxCluster]
-  static LLM_HD size_t tiles(int g, int ns) {
-    const TileCfg tc = tile_cfg(g, ROWB);
-    size_t t = (size_t)tc.ring * tc.tp * KPAD + (size_t)tc.ring * tc.tp * ROWB;
-    if (t < (size_t)g * ns * 8) t = (size_t)g * ns * 8;  // the global merge reuses the tile space
-    return t;
-  }
-  static LLM_HD size_t bytes(int g, int ns) {
-    return (size_t)g * HD * 4 + tiles(g, ns) + (size_t)g * tile_cfg(g, ROWB).tp * 4 + 3 * (size_t)g * 4 +
-           (size_t)g * (HD + 2) * 4 + (size_t)g * kAttnMaxCluster * 4;
-  }
-};
-
-// KT: cache element type (0 f32, 1 bf16); HD: head size; CLUSTER: splits merged in a cluster
-template <int KT, int HD, bool CLUSTER>
-__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs a) {
-  using S = AttnSmem<KT, HD>;
-  constexpr int ROWB = S::ROWB, KPAD = S::KPAD, CPR = ROWB / 16, EPC = 16 / S::ES;
-  extern __shared__ __align__(16) unsigned char smraw[];
-
-  const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+// Combines the warps' partials (wpart [NW][g][HD+2]: o, m, l) into the CTA's partial, then
+// merges the splits of this (row, kv head) and writes the output.  Every thread calls it.
+template <int HD>
+LLM_D void attn_finish(const AttnArgs& a, unsigned char* base, const float* wpart, float* mypart, float* fac, int nact,
+                       int split, int b, int j) {
   const int g = a.g, H = a.kv * a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const TileCfg tc = tile_cfg(g, ROWB);
-  const int TP = tc.tp, NR = tc.ring;
-
-  float* qs = reinterpret_cast<float*>(smraw);
-  unsigned char* kbuf = smraw + (size_t)g * HD * 4;
-  unsigned char* vbuf = kbuf + (size_t)NR * TP * KPAD;
-  float* sw = reinterpret_cast<float*>(kbuf + S::tiles(g, a.ns));  // scores, then weights [g][TP]
-  float* mst = sw + g * TP;
-  float* lst = mst + g;
-  float* cst = lst + g;
-  float* mypart = cst + g;                // [g][HD+2]: unnormalized o, m, l
-  float* fac = mypart + g * (HD + 2);     // [g][kAttnMaxCluster]
+  const int NT = blockDim.x, NW = NT >> 5;
   __shared__ int s_last;
-
-  grid_dep_wait();
-  grid_dep_launch();
-
-  // positions 0..t in contiguous slices of at least kMinChunk
-  const int t = a.step->pos;
-  const int npos = t + 1;
-  int chunk = (npos + a.ns - 1) / a.ns;
-  chunk = (chunk + 31) & ~31;
-  if (chunk < kMinChunk) chunk = kMinChunk;
-  const int nact = (npos + chunk - 1) / chunk;
-  if (!CLUSTER && split >= nact) return;  // (a cluster's CTAs all take part in its barriers)
-  const int p0 = split * chunk;
-  const int p1 = min(npos, p0 + chunk);
-
-  // output ownership: pairs (head, 2 dimensions); T threads per pair split the positions
-  const int pairs = g * HD / 2;
-  int T = 1;
-  while (T * 2 * pairs <= kAttnThreads) T *= 2;
-  const int npt = pairs > kAttnThreads ? (pairs + kAttnThreads - 1) / kAttnThreads : 1;
-  const int sub = tid % T;
-  float o[kMaxPairs][2];
-#pragma unroll
-  for (int k = 0; k < kMaxPairs; ++k) o[k][0] = o[k][1] = 0.f;
-
-  const size_t head_off = (((size_t)b * a.kv + j) * a.cap) * HD;  // element offset of position 0
-  const unsigned char* kg = (const unsigned char*)a.kc + head_off * S::ES;
-  const unsigned char* vg = (const unsigned char*)a.vc + head_off * S::ES;
-  auto stage = [&](int buf, int tb) {
-    const int rows = min(TP, p1 - tb);
-    for (int i = tid; i < rows * CPR; i += kAttnThreads) {
-      const int r = i / CPR, c = i - r * CPR;
-      cp_async16(kbuf + ((size_t)buf * TP + r) * KPAD + c * 16, kg + (size_t)(tb + r) * ROWB + c * 16);
-      cp_async16(vbuf + ((size_t)buf * TP + r) * ROWB + c * 16, vg + (size_t)(tb + r) * ROWB + c * 16);
+  for (int idx = tid; idx < g * (HD + 2); idx += NT) {
+    const int h = idx / (HD + 2), e = idx - h * (HD + 2);
+    float M = -INFINITY;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wpart[(w * g + h) * (HD + 2) + HD]);
+    float r = M;
+    if (e != HD) {
+      r = 0.f;
+      for (int w = 0; w < NW; ++w) {
+        const float mw = wpart[(w * g + h) * (HD + 2) + HD];
+        const float f = mw == -INFINITY ? 0.f : expf(mw - M);
+        r = fmaf(f, wpart[(w * g + h) * (HD + 2) + e], r);
+      }
     }
-  };
-
-  // the first NR - 1 tiles go out before anything else, then the queries
-  const int ntiles = p0 < p1 ? (p1 - p0 + TP - 1) / TP : 0;
-  for (int r = 0; r < NR - 1; ++r) {
-    if (r < ntiles) stage(r, p0 + r * TP);
-    cp_async_commit();
+    mypart[idx] = r;
   }
-  // queries of the group: 16-byte loads issued together
-  {
-    const float4* src = reinterpret_cast<const float4*>(a.q + (size_t)b * a.q_stride + (size_t)j * g * HD);
-    float4* dst = reinterpret_cast<float4*>(qs);
-    const int n4 = g * HD / 4;
-    float4 v[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = tid + r * kAttnThreads;
-      if (i < n4) v[r] = src[i];
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = tid + r * kAttnThreads;
-      if (i < n4) dst[i] = v[r];
-    }
-  }
-  for (int h = tid; h < g; h += kAttnThreads) {
-    mst[h] = -INFINITY;
-    lst[h] = 0.f;
-  }
-
   __syncthreads();
-  for (int it = 0; it < ntiles; ++it) {
-    const int tb = p0 + it * TP;
-    const int nv = min(TP, p1 - tb);
-    if (it + NR - 1 < ntiles) stage((it + NR - 1) % NR, tb + (NR - 1) * TP);
-    cp_async_commit();
-    // tile it has landed once at most NR - 1 of the groups committed so far are pending
-    if (NR == 4) cp_async_wait<3>();
-    else if (NR == 3) cp_async_wait<2>();
-    else cp_async_wait<1>();
-    __syncthreads();
-    const int buf = it % NR;
-    // scores: one (head, position) per thread
-    for (int item = tid; item < g * TP; item += kAttnThreads) {
-      const int h = item / TP, p = item - h * TP;
-      float s = -INFINITY;
-      if (p < nv) {
-        const unsigned char* krow = kbuf + ((size_t)buf * TP + p) * KPAD;
-        const float* qh = qs + h * HD;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int c = 0; c < CPR; ++c) {
-          const uint4 kv4 = *reinterpret_cast<const uint4*>(krow + c * 16);
-          float kf[EPC];
-          unpack16<KT>(kv4, kf);
-          const float4* q4 = reinterpret_cast<const float4*>(qh + c * EPC);
-#pragma unroll
-          for (int e4 = 0; e4 < EPC / 4; ++e4) {
-            const float4 qv = q4[e4];
-            float& r = acc[(c * (EPC / 4) + e4) & 3];
-            r = fmaf(qv.x, kf[4 * e4 + 0], r);
-            r = fmaf(qv.y, kf[4 * e4 + 1], r);
-            r = fmaf(qv.z, kf[4 * e4 + 2], r);
-            r = fmaf(qv.w, kf[4 * e4 + 3], r);
-          }
-        }
-        s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * a.scale;
-      }
-      sw[h * TP + p] = s;
-    }
-    __syncthreads();
-    // online softmax: one warp per head
-    for (int h = warp; h < g; h += kAttnWarps) {
-      float mx = -INFINITY;
-      for (int p = lane; p < TP; p += 32) mx = fmaxf(mx, sw[h * TP + p]);
-      mx = warp_max(mx);
-      const float mold = mst[h];
-      const float mnew = fmaxf(mold, mx);  // finite: the tile holds at least one position
-      const float corr = mold == -INFINITY ? 0.f : expf(mold - mnew);
-      float sum = 0.f;
-      for (int p = lane; p < TP; p += 32) {
-        const float sc = sw[h * TP + p];
-        const float w = sc == -INFINITY ? 0.f : expf(sc - mnew);
-        sw[h * TP + p] = w;
-        sum += w;
-      }
-      sum = warp_sum(sum);
-      if (lane == 0) {
-        mst[h] = mnew;
-        lst[h] = lst[h] * corr + sum;
-        cst[h] = corr;
-      }
-    }
-    __syncthreads();
-    // weighted values
-#pragma unroll
-    for (int k = 0; k < kMaxPairs; ++k) {
-      if (k >= npt) break;
-      const int pi = T == 1 ? tid + k * kAttnThreads : tid / T;
-      if (pi < pairs) {
-        const int h = pi / (HD / 2), e = 2 * (pi - h * (HD / 2));
-        const float c = cst[h];
-        float o0 = o[k][0] * c, o1 = o[k][1] * c;
-        const float* wh = sw + h * TP;
-        const unsigned char* vb = vbuf + (size_t)buf * TP * ROWB;
-#pragma unroll 4
-        for (int p = sub; p < nv; p += T) {
-          const float w = wh[p];
-          const float2 v2 = load2<KT>(vb + (size_t)p * ROWB, e);
-          o0 = fmaf(w, v2.x, o0);
-          o1 = fmaf(w, v2.y, o1);
-        }
-        o[k][0] = o0;
-        o[k][1] = o1;
-      }
-    }
-    __syncthreads();  // this buffer is refilled NR - 1 tiles later
-  }
-  cp_async_wait<0>();
-
-  // the CTA's partial: sum the position sub-splits, then (o, m, l) per head
-  if (T > 1) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      float v = o[0][r];
-      for (int off = T >> 1; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      o[0][r] = v;
-    }
-  }
-  if (sub == 0) {
-#pragma unroll
-    for (int k = 0; k < kMaxPairs; ++k) {
-      if (k >= npt) break;
-      const int pi = T == 1 ? tid + k * kAttnThreads : tid / T;
-      if (pi < pairs) {
-        const int h = pi / (HD / 2), e = 2 * (pi - h * (HD / 2));
-        mypart[h * (HD + 2) + e] = o[k][0];
-        mypart[h * (HD + 2) + e + 1] = o[k][1];
-      }
-    }
-  }
-  for (int h = tid; h < g; h += kAttnThreads) {
-    mypart[h * (HD + 2) + HD] = mst[h];
-    mypart[h * (HD + 2) + HD + 1] = lst[h];
-  }
   float* outb = a.out + (size_t)b * a.out_stride + (size_t)j * g * HD;
 
-  if constexpr (CLUSTER) {
+  if (a.cluster) {
     // ---- merge inside the cluster (CTA rank = split) through distributed shared memory ----
     const int nr = a.ns;
     cluster_sync_all();
     if (cluster_rank() == 0) {
-      for (int h = tid; h < g; h += kAttnThreads) {
+      // every rank's (m, l) of every head, fetched together (the ring is idle scratch now)
+      float* cm = reinterpret_cast<float*>(base);  // [g][nr]
+      float* cl = cm + g * nr;                     // [g][nr]
+      for (int idx = tid; idx < g * nr; idx += NT) {
+        const int h = idx / nr, r = idx - h * nr;
+        cm[idx] = ld_cluster(mypart + h * (HD + 2) + HD, r);
+        cl[idx] = ld_cluster(mypart + h * (HD + 2) + HD + 1, r);
+      }
+      __syncthreads();
+      for (int h = tid; h < g; h += NT) {
         float M = -INFINITY;
-        for (int r = 0; r < nr; ++r) M = fmaxf(M, ld_cluster(mypart + h * (HD + 2) + HD, r));
+        for (int r = 0; r < nr; ++r) M = fmaxf(M, cm[h * nr + r]);
         float L = 0.f;
         for (int r = 0; r < nr; ++r) {
-          const float mr = ld_cluster(mypart + h * (HD + 2) + HD, r);
+          const float mr = cm[h * nr + r];
           const float f = mr == -INFINITY ? 0.f : expf(mr - M);
           fac[h * kAttnMaxCluster + r] = f;
-          L += ld_cluster(mypart + h * (HD + 2) + HD + 1, r) * f;
+          L += cl[h * nr + r] * f;
         }
         const float rl = 1.0f / L;
         for (int r = 0; r < nr; ++r) fac[h * kAttnMaxCluster + r] *= rl;
       }
       __syncthreads();
-      for (int idx = tid; idx < g * HD; idx += kAttnThreads) {
+      for (int idx = tid; idx < g * HD; idx += NT) {
         const int h = idx / HD, e = idx - h * HD;
         float ov[kAttnMaxCluster];
 #pragma unroll
@@ -338,126 +210,640 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     }
     cluster_sync_all();  // the other CTAs keep their shared memory until CTA 0 has read it
     return;
-  } else {
-    // ---- global partials; the last CTA of this (row, kv head) merges them in order ----
-    __syncthreads();
-    float* pglob = a.part + (((size_t)b * H + (size_t)j * g) * a.ns) * (HD + 2);
-    for (int idx = tid; idx < g * (HD + 2); idx += kAttnThreads) {
-      const int h = idx / (HD + 2), e = idx - h * (HD + 2);
-      pglob[((size_t)h * a.ns + split) * (HD + 2) + e] = mypart[idx];
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const unsigned int prev = atomicAdd(a.ticket + (size_t)b * a.kv + j, 1u);
-      s_last = (prev == (unsigned int)(nact - 1));
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    float* fm = reinterpret_cast<float*>(kbuf);  // [g][nact] maxima, then factors
-    float* fl = fm + g * nact;                   // [g][nact] sums
-    for (int idx = tid; idx < g * nact; idx += kAttnThreads) {
-      const int h = idx / nact, s2 = idx - h * nact;
-      const float* pp = pglob + ((size_t)h * a.ns + s2) * (HD + 2);
-      fm[idx] = __ldcg(pp + HD);
-      fl[idx] = __ldcg(pp + HD + 1);
-    }
-    __syncthreads();
-    for (int h = warp; h < g; h += kAttnWarps) {
-      float M = -INFINITY;
-      for (int s2 = lane; s2 < nact; s2 += 32) M = fmaxf(M, fm[h * nact + s2]);
-      M = warp_max(M);
-      float L = 0.f;
-      for (int s2 = lane; s2 < nact; s2 += 32) {
-        const float ms = fm[h * nact + s2];
-        const float f = ms == -INFINITY ? 0.f : expf(ms - M);
-        fm[h * nact + s2] = f;
-        L += fl[h * nact + s2] * f;
-      }
-      L = warp_sum(L);
-      const float rl = 1.0f / L;
-      for (int s2 = lane; s2 < nact; s2 += 32) fm[h * nact + s2] *= rl;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < g * HD; idx += kAttnThreads) {
-      const int h = idx / HD, e = idx - h * HD;
-      const float* pb = pglob + (size_t)h * a.ns * (HD + 2) + e;
-      float O = 0.f;
-      int s2 = 0;
-      for (; s2 + 8 <= nact; s2 += 8) {
-        float ov[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) ov[q] = __ldcg(pb + (size_t)(s2 + q) * (HD + 2));
-#pragma unroll
-        for (int q = 0; q < 8; ++q) O = fmaf(fm[h * nact + s2 + q], ov[q], O);
-      }
-      for (; s2 < nact; ++s2) O = fmaf(fm[h * nact + s2], __ldcg(pb + (size_t)s2 * (HD + 2)), O);
-      outb[(size_t)h * HD + e] = O;
-    }
-    if (tid == 0) a.ticket[(size_t)b * a.kv + j] = 0u;
   }
+  // ---- global partials; the last CTA of this (row, kv head) merges them in order ----
+  float* pglob = a.part + (((size_t)b * H + (size_t)j * g) * a.ns) * (HD + 2);
+  for (int idx = tid; idx < g * (HD + 2); idx += NT) {
+    const int h = idx / (HD + 2), e = idx - h * (HD + 2);
+    pglob[((size_t)h * a.ns + split) * (HD + 2) + e] = mypart[idx];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned int prev = atomicAdd(a.ticket + (size_t)b * a.kv + j, 1u);
+    s_last = (prev == (unsigned int)(nact - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  float* fm = reinterpret_cast<float*>(base);  // [g][nact] maxima, then factors (the ring is idle)
+  float* fl = fm + g * nact;                   // [g][nact] sums
+  for (int idx = tid; idx < g * nact; idx += NT) {
+    const int h = idx / nact, s2 = idx - h * nact;
+    const float* pp = pglob + ((size_t)h * a.ns + s2) * (HD + 2);
+    fm[idx] = __ldcg(pp + HD);
+    fl[idx] = __ldcg(pp + HD + 1);
+  }
+  __syncthreads();
+  for (int h = warp; h < g; h += NW) {
+    float M = -INFINITY;
+    for (int s2 = lane; s2 < nact; s2 += 32) M = fmaxf(M, fm[h * nact + s2]);
+    M = warp_max(M);
+    float L = 0.f;
+    for (int s2 = lane; s2 < nact; s2 += 32) {
+      const float ms = fm[h * nact + s2];
+      const float f = ms == -INFINITY ? 0.f : expf(ms - M);
+      fm[h * nact + s2] = f;
+      L += fl[h * nact + s2] * f;
+    }
+    L = warp_sum(L);
+    const float rl = 1.0f / L;
+    for (int s2 = lane; s2 < nact; s2 += 32) fm[h * nact + s2] *= rl;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < g * HD; idx += NT) {
+    const int h = idx / HD, e = idx - h * HD;
+    const float* pb = pglob + (size_t)h * a.ns * (HD + 2) + e;
+    float O = 0.f;
+    int s2 = 0;
+    for (; s2 + 8 <= nact; s2 += 8) {
+      float ov[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ov[q] = __ldcg(pb + (size_t)(s2 + q) * (HD + 2));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) O = fmaf(fm[h * nact + s2 + q], ov[q], O);
+    }
+    for (; s2 < nact; ++s2) O = fmaf(fm[h * nact + s2], __ldcg(pb + (size_t)s2 * (HD + 2)), O);
+    outb[(size_t)h * HD + e] = O;
+  }
+  if (tid == 0) a.ticket[(size_t)b * a.kv + j] = 0u;
+}
+
+// KT: cache element type (0 f32, 1 bf16); HD: head size; GM: group size bound (g <= GM)
+template <int KT, int HD, int GM>
+__global__ void __launch_bounds__(kAttnMaxThreads)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const AttnArgs a) {
+  using S = AttnShape<KT, HD>;
+  constexpr int ROWB = S::ROWB, BUF = S::BUF, DPL = S::DPL;
+  extern __shared__ unsigned char araw[];
+  const uint32_t s_raw = smem_u32(araw);
+  unsigned char* base = araw + (((s_raw + 1023u) & ~1023u) - s_raw);
+  const uint32_t s_base = smem_u32(base);
+
+  const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  const int g = a.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NT = blockDim.x, NW = NT >> 5;
+  const int NR = attn_geom(BUF).nr;
+  const size_t region = attn_region<KT, HD>(g, a.ns);
+  float* qs = reinterpret_cast<float*>(base + region);  // [g][HD]
+  float* wb = qs + g * HD;                               // [NW][32][GM]
+  float* wpart = wb + NW * kChunk * GM;                  // [NW][g][HD+2]
+  float* mypart = wpart + NW * g * (HD + 2);             // [g][HD+2]: unnormalized o, m, l
+  float* fac = mypart + g * (HD + 2);                    // [g][kAttnMaxCluster]
+  const uint32_t bars = (smem_u32(fac + g * kAttnMaxCluster) + 7u) & ~7u;
+
+  // positions 0..t in contiguous slices of at least kMinChunk (multiples of 32)
+  const int t = a.step->pos;
+  const int npos = t + 1;
+  int chunk = (npos + a.ns - 1) / a.ns;
+  chunk = (chunk + 31) & ~31;
+  if (chunk < kMinChunk) chunk = kMinChunk;
+  const int nact = (npos + chunk - 1) / chunk;
+  if (!a.cluster && split >= nact) return;  // (a cluster's CTAs all take part in its barriers)
+  const int p0 = split * chunk;
+  const int p1 = min(npos, p0 + chunk);
+  const int nch = p0 < p1 ? (p1 - p0 + kChunk - 1) / kChunk : 0;
+  const int cnt = nch > warp ? (nch - warp + NW - 1) / NW : 0;  // chunks of this warp
+
+  if (tid == 0) {
+    for (int i = 0; i < NW * NR; ++i) mbar_init(bars + 8u * i, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  const int row0 = a.krow0 + (b * a.kv + j) * a.cap;  // key-map row of position 0
+  const unsigned char* vg = (const unsigned char*)a.vc + ((size_t)(b * a.kv + j) * a.cap) * ROWB;
+  auto issue = [&](int k) {  // lane 0: chunk k of this warp into its ring slot
+    const int slot = k % NR;
+    const int pb = p0 + (warp + k * NW) * kChunk;
+    const int nv = min(kChunk, p1 - pb);
+    const uint32_t bar = bars + 8u * (warp * NR + slot);
+    const uint32_t dst = s_base + (uint32_t)((warp * NR + slot) * BUF);
+    fence_proxy_async_smem();
+    mbar_expect_tx(bar, (uint32_t)(kChunk * ROWB + nv * ROWB));
+#pragma unroll
+    for (int bx = 0; bx < S::NBOX; ++bx)
+      tma_load_2d(dst + (uint32_t)(bx * kChunk * S::BOXB), &kmap, bar, bx * (S::BOXB / S::ES), row0 + pb);
+    bulk_load(dst + (uint32_t)(kChunk * ROWB), vg + (size_t)pb * ROWB, (uint32_t)(nv * ROWB), bar);
+  };
+  // chunks below position t do not depend on the previous kernel
+  const int npre = cnt < NR ? cnt : NR;
+  int issued = 0;
+  if (lane == 0) {
+    while (issued < npre) {
+      const int pb = p0 + (warp + issued * NW) * kChunk;
+      if (pb + min(kChunk, p1 - pb) > t) break;  // holds position t
+      issue(issued++);
+    }
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  if (lane == 0)
+    while (issued < npre) issue(issued++);
+  {
+    const float4* src = reinterpret_cast<const float4*>(a.q + (size_t)b * a.q_stride + (size_t)j * g * HD);
+    float4* dst = reinterpret_cast<float4*>(qs);
+    for (int i = tid; i < g * HD / 4; i += NT) dst[i] = src[i];
+  }
+  __syncthreads();
+
+  float m[GM], l[GM], o[GM][DPL];
+#pragma unroll
+  for (int h = 0; h < GM; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
+  }
+  float* wme = wb + warp * kChunk * GM;
+  bool ok = true;
+  int consumed = 0;
+  for (int k = 0; k < cnt; ++k) {
+    const int slot = k % NR;
+    const uint32_t bar = bars + 8u * (warp * NR + slot);
+    ok = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)(k / NR) & 1u, kAttnWaitCycles));
+    if (!ok) break;
+    consumed = k + 1;
+    const int pb = p0 + (warp + k * NW) * kChunk;
+    const int nv = min(kChunk, p1 - pb);
+    const unsigned char* kreg = base + (size_t)(warp * NR + slot) * BUF;
+    const unsigned char* vreg = kreg + kChunk * ROWB;
+    const bool valid = lane < nv;
+    // scores: lane = position
+    float acc[GM][2];
+#pragma unroll
+    for (int h = 0; h < GM; ++h) acc[h][0] = acc[h][1] = 0.f;
+#pragma unroll
+    for (int c = 0; c < S::CPR; ++c) {
+      const unsigned char* kp;
+      if constexpr (S::SWZ)
+        kp = kreg + (c >> 3) * (kChunk * 128) + lane * 128 + (((c & 7) ^ (lane & 7)) << 4);
+      else
+        kp = kreg + lane * ROWB + c * 16;
+      float kf[S::EPC];
+      unpack16<KT>(*reinterpret_cast<const uint4*>(kp), kf);
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
+        if (h < g) {
+          const float4* q4 = reinterpret_cast<const float4*>(qs + h * HD + c * S::EPC);
+#pragma unroll
+          for (int e4 = 0; e4 < S::EPC / 4; ++e4) {
+            const float4 qv = q4[e4];
+            float& r = acc[h][c & 1];
+            r = fmaf(qv.x, kf[4 * e4 + 0], r);
+            r = fmaf(qv.y, kf[4 * e4 + 1], r);
+            r = fmaf(qv.z, kf[4 * e4 + 2], r);
+            r = fmaf(qv.w, kf[4 * e4 + 3], r);
+          }
+        }
+      }
+    }
+    // online softmax, per head across the warp
+#pragma unroll
+    for (int h = 0; h < GM; ++h) {
+      if (h < g) {
+        const float s = valid ? (acc[h][0] + acc[h][1]) * a.scale : -INFINITY;
+        const float mnew = fmaxf(m[h], warp_max(s));  // finite: lane 0 holds a position
+        const float corr = m[h] == -INFINITY ? 0.f : expf(m[h] - mnew);
+        const float w = valid ? expf(s - mnew) : 0.f;
+        l[h] = fmaf(l[h], corr, w);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[h][e] *= corr;
+        m[h] = mnew;
+        wme[lane * GM + h] = w;
+      }
+    }
+    __syncwarp();
+    // values: lane = DPL dimensions of every head
+    if (lane < S::VL) {
+      const unsigned char* vp = vreg + lane * DPL * S::ES;
+#pragma unroll 2
+      for (int pp = 0; pp < nv; ++pp) {
+        float wv[GM];
+#pragma unroll
+        for (int h4 = 0; h4 < GM; h4 += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(wme + pp * GM + h4);
+          wv[h4] = w4.x; wv[h4 + 1] = w4.y; wv[h4 + 2] = w4.z; wv[h4 + 3] = w4.w;
+        }
+        float v[DPL];
+        load_dims<KT, DPL>(vp + (size_t)pp * ROWB, v);
+#pragma unroll
+        for (int h = 0; h < GM; ++h)
+          if (h < g)
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(wv[h], v[e], o[h][e]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && issued < cnt) issue(issued++);
+  }
+  if (!ok) {
+    if (lane == 0) atomicCAS(a.status, 0, kErrDeviceTimeout);
+  }
+  // no copy may still be writing shared memory when the CTA moves on or exits
+  if (lane == 0)
+    for (int k = consumed; k < issued; ++k)
+      if (!mbar_wait(bars + 8u * (warp * NR + k % NR), (uint32_t)(k / NR) & 1u, kAttnWaitCycles))
+        atomicCAS(a.status, 0, kErrDeviceTimeout);
+  __syncwarp();
+
+  // the warp's partial, then the CTA's: warps merged in order
+#pragma unroll
+  for (int h = 0; h < GM; ++h) {
+    if (h < g) {
+      const float lsum = warp_sum(l[h]);
+      float* wp = wpart + (warp * g + h) * (HD + 2);
+      if (lane < S::VL)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) wp[lane * DPL + e] = o[h][e];
+      if (lane == 0) {
+        wp[HD] = m[h];
+        wp[HD + 1] = lsum;
+      }
+    }
+  }
+  __syncthreads();
+  attn_finish<HD>(a, base, wpart, mypart, fac, nact, split, b, j);
+}
+
+
+// ---------------------------------------------------------------------------------------
+// bf16 caches, hd 64 or 128: the two contractions of a chunk on warp-level tensor-core MMAs
+// (m16n8k16, bf16 in, f32 accumulate).  Rows of the MMA are the g query heads (padded to 16).
+//   scores  S[16][32] = Q K^T: Q as bf16 hi + lo (two MMAs into separate accumulators, so
+//           each query enters to about 2^-17 relative), K fragments by ldmatrix from the
+//           swizzled key tile;
+//   softmax on the accumulator fragments (a row's 32 positions live in one quad of lanes);
+//   values  O[16][hd] += P V: the weights P as bf16 hi + lo (the score fragments reused as the
+//           A operand), V fragments by transposing ldmatrix from the swizzled value tile.
+// ---------------------------------------------------------------------------------------
+
+LLM_D void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+LLM_D void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += a * b, m16n8k16, bf16 inputs, f32 accumulators
+LLM_D void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// two f32 as bf16 hi parts (x0 in the low half) and the bf16 of what they leave over
+LLM_D void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(x1), "f"(x0));
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(__fsub_rn(x1, h1)), "f"(__fsub_rn(x0, h0)));
+}
+
+template <int HD>
+struct MmaShape {
+  static constexpr int ROWB = HD * 2;
+  static constexpr int NBOX = ROWB / 128;   // 128-byte column boxes per row
+  static constexpr int BUF = 2 * kChunk * ROWB;
+  static constexpr int QP = HD + 8;         // padded query row (elements): ldmatrix rows on distinct banks
+  static constexpr int NTO = HD / 8;        // output n-tiles
+  static constexpr int KS = HD / 16;        // k-steps of the scores
+};
+
+template <int HD>
+LLM_HD size_t attn_mma_smem(int g, int ns) {
+  using M = MmaShape<HD>;
+  const AttnGeom geo = attn_geom(M::BUF);
+  size_t r = (size_t)geo.nw * geo.nr * M::BUF;
+  if (r < (size_t)g * ns * 8) r = (size_t)g * ns * 8;
+  r = (r + 1023) & ~(size_t)1023;
+  size_t s = 1024 + r;
+  s += 2 * 16 * (size_t)M::QP * 2;            // queries hi, lo
+  s += (size_t)geo.nw * g * (HD + 2) * 4;     // warp partials
+  s += (size_t)g * (HD + 2) * 4;              // CTA partial
+  s += (size_t)g * kAttnMaxCluster * 4;       // merge factors
+  s = (s + 7) & ~(size_t)7;
+  s += (size_t)geo.nw * geo.nr * 8;           // mbarriers
+  return s;
+}
+
+// byte offset of 16-byte piece c of row r in a chunk tile stored as 128-byte-wide swizzled boxes
+LLM_D uint32_t swz_off(int r, int c) { return (uint32_t)((c >> 3) * (kChunk * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)); }
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnMaxThreads)
+    attn_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  using M = MmaShape<HD>;
+  constexpr int ROWB = M::ROWB, BUF = M::BUF, QP = M::QP, NTO = M::NTO, KS = M::KS;
+  extern __shared__ unsigned char araw[];
+  const uint32_t s_raw = smem_u32(araw);
+  unsigned char* base = araw + (((s_raw + 1023u) & ~1023u) - s_raw);
+  const uint32_t s_base = smem_u32(base);
+
+  const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  const int g = a.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int NT = blockDim.x, NW = NT >> 5;
+  const int NR = attn_geom(BUF).nr;
+  size_t region = (size_t)NW * NR * BUF;
+  if (region < (size_t)g * a.ns * 8) region = (size_t)g * a.ns * 8;
+  region = (region + 1023) & ~(size_t)1023;
+  uint16_t* qh = reinterpret_cast<uint16_t*>(base + region);  // [16][QP] bf16
+  uint16_t* ql = qh + 16 * QP;
+  float* wpart = reinterpret_cast<float*>(ql + 16 * QP);      // [NW][g][HD+2]
+  float* mypart = wpart + NW * g * (HD + 2);
+  float* fac = mypart + g * (HD + 2);
+  const uint32_t bars = (smem_u32(fac + g * kAttnMaxCluster) + 7u) & ~7u;
+
+  const int t = a.step->pos;
+  const int npos = t + 1;
+  int chunk = (npos + a.ns - 1) / a.ns;
+  chunk = (chunk + 31) & ~31;
+  if (chunk < kMinChunk) chunk = kMinChunk;
+  const int nact = (npos + chunk - 1) / chunk;
+  if (!a.cluster && split >= nact) return;
+  const int p0 = split * chunk;
+  const int p1 = min(npos, p0 + chunk);
+  const int nch = p0 < p1 ? (p1 - p0 + kChunk - 1) / kChunk : 0;
+  const int cnt = nch > warp ? (nch - warp + NW - 1) / NW : 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < NW * NR; ++i) mbar_init(bars + 8u * i, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  const int row0 = a.krow0 + (b * a.kv + j) * a.cap;
+  auto issue = [&](int k) {
+    const int slot = k % NR;
+    const int pb = p0 + (warp + k * NW) * kChunk;
+    const uint32_t bar = bars + 8u * (warp * NR + slot);
+    const uint32_t dst = s_base + (uint32_t)((warp * NR + slot) * BUF);
+    fence_proxy_async_smem();
+    mbar_expect_tx(bar, (uint32_t)(2 * kChunk * ROWB));
+#pragma unroll
+    for (int bx = 0; bx < M::NBOX; ++bx) {
+      tma_load_2d(dst + (uint32_t)(bx * kChunk * 128), &kmap, bar, bx * 64, row0 + pb);
+      tma_load_2d(dst + (uint32_t)(kChunk * ROWB + bx * kChunk * 128), &vmap, bar, bx * 64, row0 + pb);
+    }
+  };
+  const int npre = cnt < NR ? cnt : NR;
+  int issued = 0;
+  if (lane == 0) {
+    tma_prefetch_map(&kmap);
+    tma_prefetch_map(&vmap);
+    while (issued < npre) {
+      const int pb = p0 + (warp + issued * NW) * kChunk;
+      if (pb + min(kChunk, p1 - pb) > t) break;  // holds position t
+      issue(issued++);
+    }
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  if (lane == 0)
+    while (issued < npre) issue(issued++);
+  // queries of the group as bf16 hi + lo, rows g..15 zero
+  {
+    const float* qsrc = a.q + (size_t)b * a.q_stride + (size_t)j * g * HD;
+    for (int i = tid; i < 16 * HD / 2; i += NT) {
+      const int r = (2 * i) / HD, e = (2 * i) - r * HD;
+      float x0 = 0.f, x1 = 0.f;
+      if (r < g) {
+        const float2 v = *reinterpret_cast<const float2*>(qsrc + (size_t)r * HD + e);
+        x0 = v.x;
+        x1 = v.y;
+      }
+      uint32_t hi, lo;
+      split_bf16x2(x0, x1, hi, lo);
+      *reinterpret_cast<uint32_t*>(qh + r * QP + e) = hi;
+      *reinterpret_cast<uint32_t*>(ql + r * QP + e) = lo;
+    }
+  }
+  __syncthreads();
+
+  float o[NTO][4];
+#pragma unroll
+  for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  // this lane's ldmatrix row addresses: queries (A operand)
+  const int qr = (lane & 7) + ((lane >> 3) & 1) * 8, qc = (lane >> 4) * 8;
+  const uint32_t qh_addr = smem_u32(qh + qr * QP + qc), ql_addr = smem_u32(ql + qr * QP + qc);
+  const int mi = lane >> 3, mr = lane & 7;
+  bool ok = true;
+  int consumed = 0;
+  for (int k = 0; k < cnt; ++k) {
+    const int slot = k % NR;
+    const uint32_t bar = bars + 8u * (warp * NR + slot);
+    ok = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)(k / NR) & 1u, kAttnWaitCycles));
+    if (!ok) break;
+    consumed = k + 1;
+    const int pb = p0 + (warp + k * NW) * kChunk;
+    const int nv = min(kChunk, p1 - pb);
+    const uint32_t kreg = s_base + (uint32_t)((warp * NR + slot) * BUF);
+    const uint32_t vreg = kreg + (uint32_t)(kChunk * ROWB);
+    if (nv < kChunk) {
+      // rows past the last position hold other data (possibly not finite): zero the values
+      unsigned char* vz = base + (size_t)(warp * NR + slot) * BUF + kChunk * ROWB;
+      for (int i = lane; i < (kChunk - nv) * (ROWB / 16); i += 32) {
+        const int r = nv + i / (ROWB / 16), c = i - (i / (ROWB / 16)) * (ROWB / 16);
+        *reinterpret_cast<uint4*>(vz + swz_off(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+    // ---- scores S = Q K^T: 4 n-tiles of 8 positions, separate hi and lo accumulators ----
+    float sh[4][4], sl[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sh[n][i] = sl[n][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ks += 2) {
+      uint32_t ah0[4], al0[4], ah1[4], al1[4];
+      ldsm_x4(qh_addr + ks * 32, ah0);
+      ldsm_x4(ql_addr + ks * 32, al0);
+      ldsm_x4(qh_addr + (ks + 1) * 32, ah1);
+      ldsm_x4(ql_addr + (ks + 1) * 32, al1);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        // matrices: (ks, dims 0-7), (ks, dims 8-15), (ks+1, 0-7), (ks+1, 8-15) of positions n*8..
+        uint32_t bk[4];
+        ldsm_x4(kreg + swz_off(n * 8 + mr, 2 * (ks + (mi >> 1)) + (mi & 1)), bk);
+        mma_bf16_16816(sh[n], ah0, bk[0], bk[1]);
+        mma_bf16_16816(sl[n], al0, bk[0], bk[1]);
+        mma_bf16_16816(sh[n], ah1, bk[2], bk[3]);
+        mma_bf16_16816(sl[n], al1, bk[2], bk[3]);
+      }
+    }
+    // ---- online softmax: row gid (entries 0, 1) and row gid + 8 (entries 2, 3) ----
+    float p[4][4];
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int pos = n * 8 + tig * 2 + (i & 1);
+        const float sv = pos < nv ? (sh[n][i] + sl[n][i]) * a.scale : -INFINITY;
+        p[n][i] = sv;
+        mx[i >> 1] = fmaxf(mx[i >> 1], sv);
+      }
+    float corr[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float mnew = fmaxf(mrow[r], mx[r]);  // finite: position 0 of the chunk is valid
+      corr[r] = mrow[r] == -INFINITY ? 0.f : expf(mrow[r] - mnew);
+      mrow[r] = mnew;
+    }
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float w = p[n][i] == -INFINITY ? 0.f : expf(p[n][i] - mrow[i >> 1]);
+        p[n][i] = w;
+        rs[i >> 1] += w;
+      }
+    lrow[0] = fmaf(lrow[0], corr[0], rs[0]);
+    lrow[1] = fmaf(lrow[1], corr[1], rs[1]);
+#pragma unroll
+    for (int n = 0; n < NTO; ++n) {
+      o[n][0] *= corr[0];
+      o[n][1] *= corr[0];
+      o[n][2] *= corr[1];
+      o[n][3] *= corr[1];
+    }
+    // ---- values O += P V: two k-steps of 16 positions, P as bf16 hi + lo ----
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+      uint32_t ph[4], pl[4];
+      split_bf16x2(p[2 * s2][0], p[2 * s2][1], ph[0], pl[0]);
+      split_bf16x2(p[2 * s2][2], p[2 * s2][3], ph[1], pl[1]);
+      split_bf16x2(p[2 * s2 + 1][0], p[2 * s2 + 1][1], ph[2], pl[2]);
+      split_bf16x2(p[2 * s2 + 1][2], p[2 * s2 + 1][3], ph[3], pl[3]);
+#pragma unroll
+      for (int n = 0; n < NTO; n += 2) {
+        // matrices: positions 0-7 and 8-15 of this k-step for dims n*8.., then for dims (n+1)*8..
+        uint32_t bv[4];
+        ldsm_x4_t(vreg + swz_off(16 * s2 + (mi & 1) * 8 + mr, n + (mi >> 1)), bv);
+        mma_bf16_16816(o[n], ph, bv[0], bv[1]);
+        mma_bf16_16816(o[n], pl, bv[0], bv[1]);
+        mma_bf16_16816(o[n + 1], ph, bv[2], bv[3]);
+        mma_bf16_16816(o[n + 1], pl, bv[2], bv[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && issued < cnt) issue(issued++);
+  }
+  if (!ok && lane == 0) atomicCAS(a.status, 0, kErrDeviceTimeout);
+  if (lane == 0)
+    for (int k = consumed; k < issued; ++k)
+      if (!mbar_wait(bars + 8u * (warp * NR + k % NR), (uint32_t)(k / NR) & 1u, kAttnWaitCycles))
+        atomicCAS(a.status, 0, kErrDeviceTimeout);
+  __syncwarp();
+
+  // the warp's partial: rows gid and gid + 8 of the fragments
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
+    const int h = gid + 8 * r;
+    if (h < g) {
+      float* wp = wpart + (warp * g + h) * (HD + 2);
+#pragma unroll
+      for (int n = 0; n < NTO; ++n) {
+        wp[n * 8 + tig * 2] = o[n][2 * r];
+        wp[n * 8 + tig * 2 + 1] = o[n][2 * r + 1];
+      }
+      if (tig == 0) {
+        wp[HD] = mrow[r];
+        wp[HD + 1] = lrow[r];
+      }
+    }
+  }
+  __syncthreads();
+  attn_finish<HD>(a, base, wpart, mypart, fac, nact, split, b, j);
 }
 
 // ---------------------------------------------------------------------------------------
 
-using AttnFn = void (*)(const AttnArgs);
+using AttnFn = void (*)(const CUtensorMap, const AttnArgs);
 
-template <int KT, bool CL>
-static AttnFn pick_hd(int hd, size_t* smem, int g, int ns) {
+template <int KT, int HD>
+static AttnFn pick_gm(int g, size_t* smem, int ns, int* nw) {
+  *nw = attn_geom(AttnShape<KT, HD>::BUF).nw;
+  if (g <= 4) {
+    *smem = attn_smem<KT, HD, 4>(g, ns);
+    return attn_decode_kernel<KT, HD, 4>;
+  }
+  if constexpr (HD <= 128) {
+    if (g <= 8) {
+      *smem = attn_smem<KT, HD, 8>(g, ns);
+      return attn_decode_kernel<KT, HD, 8>;
+    }
+  }
+  if constexpr (HD <= 64) {
+    if (g <= 16) {
+      *smem = attn_smem<KT, HD, 16>(g, ns);
+      return attn_decode_kernel<KT, HD, 16>;
+    }
+  }
+  return nullptr;
+}
+
+template <int KT>
+static AttnFn pick_hd(int hd, int g, size_t* smem, int ns, int* nw) {
   switch (hd) {
-    case 16: *smem = AttnSmem<KT, 16>::bytes(g, ns); return attn_decode_kernel<KT, 16, CL>;
-    case 32: *smem = AttnSmem<KT, 32>::bytes(g, ns); return attn_decode_kernel<KT, 32, CL>;
-    case 64: *smem = AttnSmem<KT, 64>::bytes(g, ns); return attn_decode_kernel<KT, 64, CL>;
-    case 128: *smem = AttnSmem<KT, 128>::bytes(g, ns); return attn_decode_kernel<KT, 128, CL>;
-    case 256: *smem = AttnSmem<KT, 256>::bytes(g, ns); return attn_decode_kernel<KT, 256, CL>;
+    case 16: return pick_gm<KT, 16>(g, smem, ns, nw);
+    case 32: return pick_gm<KT, 32>(g, smem, ns, nw);
+    case 64: return pick_gm<KT, 64>(g, smem, ns, nw);
+    case 128: return pick_gm<KT, 128>(g, smem, ns, nw);
+    case 256: return pick_gm<KT, 256>(g, smem, ns, nw);
     default: return nullptr;
   }
 }
 
-static AttnFn pick(int kt, bool cl, int hd, size_t* smem, int g, int ns) {
-  if (kt) return cl ? pick_hd<1, true>(hd, smem, g, ns) : pick_hd<1, false>(hd, smem, g, ns);
-  return cl ? pick_hd<0, true>(hd, smem, g, ns) : pick_hd<0, false>(hd, smem, g, ns);
+static AttnFn pick(int kt, int hd, int g, size_t* smem, int ns, int* nw) {
+  return kt ? pick_hd<1>(hd, g, smem, ns, nw) : pick_hd<0>(hd, g, smem, ns, nw);
 }
 
 static int g_max_cluster = 8;  // 16 once attn_prepare finds the device can schedule it
 int attn_max_cluster() { return g_max_cluster; }
 
 bool attn_supported(int hd, int g) {
-  return (hd == 16 || hd == 32 || hd == 64 || hd == 128 || hd == 256) && g >= 1 && g <= 16 &&
-         g * hd <= 2 * kAttnThreads * kMaxPairs;
+  return (hd == 16 || hd == 32 || hd == 64 || hd == 128 || hd == 256) && g >= 1 && g <= 16 && g * hd <= 1024;
 }
 
 cudaError_t attn_prepare(int max_smem_optin) {
   for (int kt = 0; kt < 2; ++kt)
-    for (int cl = 0; cl < 2; ++cl)
-      for (int hd : {16, 32, 64, 128, 256}) {
+    for (int hd : {16, 32, 64, 128, 256})
+      for (int g : {4, 8, 16}) {
+        if (!attn_supported(hd, g)) continue;
         size_t sm = 0;
-        AttnFn fn = pick(kt, cl != 0, hd, &sm, 1, 1);
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        int nw = 0;
+        AttnFn fn = pick(kt, hd, g, &sm, 1, &nw);
+        if (!fn) continue;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin - 64);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin - (int)fa.sharedSizeBytes);
-        if (e != cudaSuccess) return e;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) cudaGetLastError();
       }
+  for (auto fn : {attn_mma_kernel<64>, attn_mma_kernel<128>}) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin - 64);
+    if (e != cudaSuccess) return e;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) cudaGetLastError();
+  }
   // clusters of 16 (beyond the portable 8) where the device can run them with this kernel
   g_max_cluster = 8;
-  for (int kt = 0; kt < 2; ++kt)
-    for (int hd : {16, 32, 64, 128, 256}) {
-      size_t sm = 0;
-      AttnFn fn = pick(kt, true, hd, &sm, 1, 1);
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-        cudaGetLastError();
-        return cudaSuccess;
-      }
-    }
   {
-    size_t sm = 0;
-    AttnFn fn = pick(1, true, 128, &sm, 4, 16);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(16, 8, 1);
-    cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = sm;
+    cfg.blockDim = dim3(attn_geom(MmaShape<128>::BUF).nw * 32);
+    cfg.dynamicSmemBytes = attn_mma_smem<128>(4, 16);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 16;
@@ -466,10 +852,20 @@ cudaError_t attn_prepare(int max_smem_optin) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, fn, &cfg) == cudaSuccess && nclusters >= 1) g_max_cluster = 16;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, attn_mma_kernel<128>, &cfg) == cudaSuccess && nclusters >= 1)
+      g_max_cluster = 16;
     cudaGetLastError();
   }
   return cudaSuccess;
+}
+
+bool attn_make_kmap(CUtensorMap* map, const void* kc, int kt, int hd, uint64_t rows) {
+  const int es = kt ? 2 : 4;
+  const int rowb = hd * es;
+  const bool swz = rowb >= 128;
+  const int boxb = swz ? 128 : rowb;
+  return make_map_2d(map, kc, es, (uint64_t)hd, rows, (uint32_t)(boxb / es), (uint32_t)kChunk,
+                     swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int attn_splits(int B, int kv, int cap, int num_sms) {
@@ -487,21 +883,34 @@ int attn_splits(int B, int kv, int cap, int num_sms) {
   return ns;
 }
 
-cudaError_t launch_attn(const AttnArgs& a, int kt, cudaStream_t s, bool pdl) {
-  const bool cl = a.ns <= attn_max_cluster();
+bool attn_uses_mma(int kt, int hd) { return kt == 1 && (hd == 64 || hd == 128); }
+
+cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a0, int kt, cudaStream_t s,
+                        bool pdl) {
+  AttnArgs a = a0;
+  a.cluster = a.ns <= attn_max_cluster() ? 1 : 0;
   size_t smem = 0;
-  AttnFn fn = pick(kt, cl, a.hd, &smem, a.g, a.ns);
-  if (!fn) return cudaErrorInvalidValue;
+  int nw = 0;
+  AttnFn fn = nullptr;
+  void (*mfn)(const CUtensorMap, const CUtensorMap, const AttnArgs) = nullptr;
+  if (attn_uses_mma(kt, a.hd)) {
+    mfn = a.hd == 64 ? attn_mma_kernel<64> : attn_mma_kernel<128>;
+    smem = a.hd == 64 ? attn_mma_smem<64>(a.g, a.ns) : attn_mma_smem<128>(a.g, a.ns);
+    nw = attn_geom(a.hd == 64 ? MmaShape<64>::BUF : MmaShape<128>::BUF).nw;
+  } else {
+    fn = pick(kt, a.hd, a.g, &smem, a.ns, &nw);
+    if (!fn) return cudaErrorInvalidValue;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ns, a.kv, a.B);
-  cfg.blockDim = dim3(kAttnThreads);
+  cfg.blockDim = dim3(nw * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   int na = 1;
-  if (cl) {
+  if (a.cluster) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = a.ns;
     attr[1].val.clusterDim.y = 1;
@@ -510,7 +919,8 @@ cudaError_t launch_attn(const AttnArgs& a, int kt, cudaStream_t s, bool pdl) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, fn, a);
+  if (mfn) return cudaLaunchKernelEx(&cfg, mfn, kmap, vmap, a);
+  return cudaLaunchKernelEx(&cfg, fn, kmap, a);
 }
 
 }  // namespace llm

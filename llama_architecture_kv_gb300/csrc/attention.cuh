@@ -1,5 +1,7 @@
 // Split-K decode attention over the KV cache (declarations).
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace llm {
@@ -7,8 +9,8 @@ namespace llm {
 struct AttnArgs {
   const float* q;      // rotated queries [B][q_stride]
   int32_t q_stride;
-  const void* kc;      // this layer's key cache [max_batch][kv][cap][hd]
-  const void* vc;      // this layer's value cache
+  const void* vc;      // this layer's value cache [max_batch][kv][cap][hd]
+  int32_t krow0;       // row of this layer's position 0 of (row 0, kv head 0) in the key map
   float* out;          // attention output [B][out_stride], heads concatenated
   int32_t out_stride;
   float* part;         // partials [B][H][ns][hd + 2]: unnormalized o, running max, running sum
@@ -16,6 +18,8 @@ struct AttnArgs {
   int32_t B, kv, g, hd, cap, ns;
   float scale;         // 1 / sqrt(hd), rounded to f32
   const StepState* step;
+  int32_t* status;     // device error flag
+  int32_t cluster;     // set by launch_attn: the splits form one thread-block cluster
 };
 
 constexpr int kAttnMaxCluster = 16;  // most splits merged inside one thread-block cluster
@@ -25,6 +29,12 @@ bool attn_supported(int hd, int g);
 int attn_max_cluster();
 int attn_splits(int B, int kv, int cap, int num_sms);
 cudaError_t attn_prepare(int max_smem_optin);
-cudaError_t launch_attn(const AttnArgs& a, int kt, cudaStream_t s, bool pdl);
+// tensor map over a whole key (or value) cache viewed as [rows][hd]
+// (rows = layers * max_batch * kv * cap), boxes of 32 rows
+bool attn_make_kmap(CUtensorMap* map, const void* kc, int kt, int hd, uint64_t rows);
+// bf16 caches with hd 64 or 128 run the tensor-core kernel (which also reads the values by map)
+bool attn_uses_mma(int kt, int hd);
+cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a, int kt, cudaStream_t s,
+                        bool pdl);
 
 }  // namespace llm

@@ -62,6 +62,9 @@ TcPlan plan_tc(int rows, int K, int B, int num_sms);
 // 128-byte swizzle
 bool tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                  uint32_t box_outer);
+// general 2D tensor map (elements of elem_bytes: 2 = bf16, 4 = f32) with the given swizzle
+bool make_map_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 cudaError_t launch_tc_split(const TcSplitArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_tc_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, const TcPlan& p, int epi,
                            cudaStream_t s, bool pdl);

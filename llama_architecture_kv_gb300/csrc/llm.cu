@@ -176,6 +176,7 @@ struct llm_handle {
   float* part = nullptr;
   uint32_t* ticket = nullptr;
   int part_ns = 0;
+  CUtensorMap kmap, vmap;  // the key and value caches as [layers * max_batch * kv * max_seq][hd]
   StepState* st = nullptr;
   int32_t* status = nullptr;
   int32_t* tok_buf = nullptr;
@@ -468,10 +469,11 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     const int ns = attn_splits(B, c.kv_heads, c.max_seq, h->num_sms);
     if (ns > h->part_ns) return fail(h, LLM_ERR_ARG, "internal: attention splits %d > %d", ns, h->part_ns);
     AttnArgs at = {};
-    at.q = h->q; at.q_stride = h->d; at.kc = kcl; at.vc = vcl; at.out = h->attn; at.out_stride = h->d;
+    at.q = h->q; at.q_stride = h->d; at.vc = vcl; at.out = h->attn; at.out_stride = h->d;
+    at.krow0 = (int32_t)((size_t)l * c.max_batch * c.kv_heads * c.max_seq); at.status = h->status;
     at.part = h->part; at.ticket = h->ticket; at.B = B; at.kv = c.kv_heads; at.g = c.group; at.hd = h->hd;
     at.cap = c.max_seq; at.ns = ns; at.scale = 1.0f / sqrtf((float)h->hd); at.step = h->st;
-    CUDA_TRY(h, launch_attn(at, wt, h->stream, pdl));
+    CUDA_TRY(h, launch_attn(h->kmap, h->vmap, at, wt, h->stream, pdl));
   } else if (which == K_O) {
     // o_proj + residual: x1 (xb) = x (xa) + W_o attn
     const GemvPlan p = plan_gemv(h->d, h->d, 1, wt, B, h->num_sms, cps);
@@ -751,6 +753,12 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   h->layer_cache_elems = (size_t)c.max_batch * c.kv_heads * c.max_seq * h->hd;
   const size_t cache_bytes = (size_t)h->L * h->layer_cache_elems * es;
   if ((st = dalloc(h, &h->kc, cache_bytes)) || (st = dalloc(h, &h->vc, cache_bytes))) return bail(st);
+  if ((uint64_t)h->L * c.max_batch * c.kv_heads * c.max_seq >= (1ull << 31) ||
+      !attn_make_kmap(&h->kmap, h->kc, h->wt, h->hd, (uint64_t)h->L * c.max_batch * c.kv_heads * c.max_seq) ||
+      !attn_make_kmap(&h->vmap, h->vc, h->wt, h->hd, (uint64_t)h->L * c.max_batch * c.kv_heads * c.max_seq)) {
+    fail(h, LLM_ERR_CONFIG, "the key cache does not fit a tensor map (layers x rows x kv heads x positions < 2^31)");
+    return bail(LLM_ERR_CONFIG);
+  }
   if ((st = dalloc(h, &h->rope_cos, (size_t)c.max_seq * c.half * 4)) ||
       (st = dalloc(h, &h->rope_sin, (size_t)c.max_seq * c.half * 4)))
     return bail(st);

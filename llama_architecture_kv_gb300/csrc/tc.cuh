@@ -78,6 +78,15 @@ LLM_D void tma_load_2d(uint32_t dst, const void* map, uint32_t bar, int32_t x, i
       : "memory");
 }
 
+// 1D bulk copy global -> shared (addresses 16-byte aligned, bytes a multiple of 16)
+LLM_D void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// order this thread's earlier generic-proxy shared-memory accesses before later bulk copies
+LLM_D void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ---- tcgen05 ----------------------------------------------------------------------------
 LLM_D void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)

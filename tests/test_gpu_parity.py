@@ -357,3 +357,60 @@ def test_step_kernel_counts():
     with pytest.raises(pkg.LlmError):
         pkg.llm_step_kernels(g.h, 21, 0.0)
     g.close()
+
+
+# ---------------------------------------------------------------------------------------
+# bf16 caches (the tensor-core attention kernel: head sizes 64 and 128)
+# ---------------------------------------------------------------------------------------
+
+BF16_ATTN_SHAPES = [
+    ("hd128_g4", shrink(WORKLOADS["llama8b_b1"].shape, layers=1, kv=2, ffn=256, vocab=512)),
+    ("hd64_g3", shrink(WORKLOADS["smollm2_135m"].shape, layers=1, ffn=256, vocab=512)),
+]
+
+
+def bf16_bits(x):
+    return np.asarray(x, np.float32).view(np.uint32).astype(np.uint64).__rshift__(16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("name,shape", BF16_ATTN_SHAPES, ids=lambda x: x if isinstance(x, str) else "")
+@pytest.mark.parametrize("t", [5, 70, 300])
+def test_gqa_markers_bf16_cache(name, shape, t):
+    # as the f32 marker test: zero Q/K/V weights make every score 0, so query head h's output
+    # is marker(h // g) * t / (t + 1); t spans one chunk, a ragged third chunk and many splits
+    s = shape
+    blob = synth.model_blob(s, 6)
+    v = views(s, blob)
+    for nm in ("q", "k", "v"):
+        v[(0, nm)][...] = 0
+    g = pkg.Model(s, blob, max_batch=1, max_seq=t + 1, debug_trace=True)
+    kk = np.zeros((s.kv, t, s.hd), np.uint16)
+    vv = np.zeros((s.kv, t, s.hd), np.float32)
+    for j in range(s.kv):
+        vv[j, :, j] = j + 1
+    g.kv_import(0, 0, 0, kk, bf16_bits(vv))
+    g.decode(np.array([3], np.int32), t)
+    att = g.trace(0, "attn")[0].reshape(s.heads, s.hd)
+    for h in range(s.heads):
+        want = np.zeros(s.hd, np.float32)
+        want[h // s.g] = (h // s.g + 1) * t / (t + 1)
+        np.testing.assert_allclose(att[h], want, rtol=2e-6, atol=1e-7)
+    g.close()
+
+
+@pytest.mark.parametrize("name,shape", BF16_ATTN_SHAPES, ids=lambda x: x if isinstance(x, str) else "")
+def test_causality_bf16_cache(name, shape):
+    s = shape
+    B, cap, t = 2, 100, 40
+    blob = synth.model_blob(s, 7)
+    g = pkg.Model(s, blob, max_batch=B, max_seq=cap)
+    toks = synth.tokens(8, 0, B * (t + 1), s.vocab).reshape(B, t + 1)
+    g.prefill(toks[:, :t], 0, logits=False)
+    a = g.decode(toks[:, t], t)
+    junk = np.full((s.kv, cap - t - 1, s.hd), 0x7FC0, np.uint16)  # bf16 NaN
+    for layer in range(s.layers):
+        for b in range(B):
+            g.kv_import(layer, b, t + 1, junk, junk)
+    b_ = g.decode(toks[:, t], t)
+    assert np.array_equal(a.view(np.uint32), b_.view(np.uint32))
+    g.close()
