@@ -26,6 +26,10 @@
 // finish -- found with an atomic ticket, nobody waits -- merges them.
 // Chunks that lie entirely below position t were written by earlier steps, so their copies start
 // before the wait on the previous kernel (which writes position t).
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "attention.cuh"
 #include "gemm.cuh"
 #include "tc.cuh"
@@ -885,10 +889,56 @@ int attn_splits(int B, int kv, int cap, int num_sms) {
 
 bool attn_uses_mma(int kt, int hd) { return kt == 1 && (hd == 64 || hd == 128); }
 
+// clusters of cs CTAs of this kernel that the device runs at once (queried once per shape)
+static int max_active_clusters(const void* fn, size_t smem, int threads, int cs) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, size_t, int, int>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(fn, smem, threads, cs);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, 1, 1);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache.emplace(key, n);
+  return n;
+}
+
+// The splits merge inside a cluster only when every cluster of the launch runs at once (a second
+// wave of clusters would double the time); otherwise through global partials.
+bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters) {
+  if (ns == 1) return true;
+  if (ns > attn_max_cluster()) return false;
+  size_t smem = 0;
+  int nw = 0;
+  const void* f = nullptr;
+  if (attn_uses_mma(kt, hd)) {
+    f = hd == 64 ? (const void*)attn_mma_kernel<64> : (const void*)attn_mma_kernel<128>;
+    smem = hd == 64 ? attn_mma_smem<64>(g, ns) : attn_mma_smem<128>(g, ns);
+    nw = attn_geom(hd == 64 ? MmaShape<64>::BUF : MmaShape<128>::BUF).nw;
+  } else {
+    f = (const void*)pick(kt, hd, g, &smem, ns, &nw);
+    if (!f) return false;
+  }
+  return clusters <= max_active_clusters(f, smem, nw * 32, ns);
+}
+
 cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a0, int kt, cudaStream_t s,
                         bool pdl) {
   AttnArgs a = a0;
-  a.cluster = a.ns <= attn_max_cluster() ? 1 : 0;
   size_t smem = 0;
   int nw = 0;
   AttnFn fn = nullptr;
@@ -901,6 +951,7 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
     fn = pick(kt, a.hd, a.g, &smem, a.ns, &nw);
     if (!fn) return cudaErrorInvalidValue;
   }
+  a.cluster = attn_cluster_merge(kt, a.hd, a.g, a.ns, a.B * a.kv) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ns, a.kv, a.B);
   cfg.blockDim = dim3(nw * 32);

@@ -34,6 +34,9 @@ cudaError_t attn_prepare(int max_smem_optin);
 bool attn_make_kmap(CUtensorMap* map, const void* kc, int kt, int hd, uint64_t rows);
 // bf16 caches with hd 64 or 128 run the tensor-core kernel (which also reads the values by map)
 bool attn_uses_mma(int kt, int hd);
+// whether ns splits of `clusters` (row, kv head) pairs merge inside thread-block clusters; the
+// first call for a shape queries the device (make it outside stream capture)
+bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters);
 cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a, int kt, cudaStream_t s,
                         bool pdl);
 

@@ -768,7 +768,11 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
       (st = dalloc(h, &h->m, B * h->f * 4)) || (st = dalloc(h, &h->logits, B * h->V * 4)))
     return bail(st);
   int maxns = 1;
-  for (int b = 1; b <= c.max_batch; ++b) maxns = std::max(maxns, attn_splits(b, c.kv_heads, c.max_seq, h->num_sms));
+  for (int b = 1; b <= c.max_batch; ++b) {
+    const int ns = attn_splits(b, c.kv_heads, c.max_seq, h->num_sms);
+    maxns = std::max(maxns, ns);
+    attn_cluster_merge(h->wt, h->hd, c.group, ns, b * c.kv_heads);  // device queries before any capture
+  }
   h->part_ns = maxns;
   if ((st = dalloc(h, &h->part, B * h->H * maxns * (h->hd + 2) * 4)) ||
       (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, sizeof(StepState))) ||
