@@ -508,73 +508,85 @@ LLM_D void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(__fsub_rn(x1, h1)), "f"(__fsub_rn(x0, h0)));
 }
 
+constexpr int kMmaChunk = 16;   // positions per chunk of a warp (one MMA k-step of the values)
+constexpr int kMmaWarps = 8;
+
 template <int HD>
 struct MmaShape {
   static constexpr int ROWB = HD * 2;
   static constexpr int NBOX = ROWB / 128;   // 128-byte column boxes per row
-  static constexpr int BUF = 2 * kChunk * ROWB;
+  static constexpr int BUF = 2 * kMmaChunk * ROWB;
+  static constexpr int NR = HD <= 64 ? 3 : 2;  // ring slots per warp (within the shared memory)
   static constexpr int QP = HD + 8;         // padded query row (elements): ldmatrix rows on distinct banks
   static constexpr int NTO = HD / 8;        // output n-tiles
   static constexpr int KS = HD / 16;        // k-steps of the scores
 };
 
+constexpr int kMmaMaxSplits = 64;  // splits of one (row, kv head) the persistent kernel merges
+
 template <int HD>
-LLM_HD size_t attn_mma_smem(int g, int ns) {
+LLM_HD size_t attn_mma_smem(int g) {
   using M = MmaShape<HD>;
-  const AttnGeom geo = attn_geom(M::BUF);
-  size_t r = (size_t)geo.nw * geo.nr * M::BUF;
-  if (r < (size_t)g * ns * 8) r = (size_t)g * ns * 8;
-  r = (r + 1023) & ~(size_t)1023;
-  size_t s = 1024 + r;
-  s += 2 * 16 * (size_t)M::QP * 2;            // queries hi, lo
-  s += (size_t)geo.nw * g * (HD + 2) * 4;     // warp partials
+  size_t s = 1024 + (size_t)kMmaWarps * M::NR * M::BUF;
+  s += 2 * 2 * 16 * (size_t)M::QP * 2;        // queries hi, lo (two units)
+  s += (size_t)kMmaWarps * g * (HD + 2) * 4;  // warp partials
   s += (size_t)g * (HD + 2) * 4;              // CTA partial
-  s += (size_t)g * kAttnMaxCluster * 4;       // merge factors
+  s += (size_t)g * kMmaMaxSplits * 4;         // merge factors
   s = (s + 7) & ~(size_t)7;
-  s += (size_t)geo.nw * geo.nr * 8;           // mbarriers
+  s += (size_t)kMmaWarps * M::NR * 8;         // mbarriers
   return s;
 }
 
 // byte offset of 16-byte piece c of row r in a chunk tile stored as 128-byte-wide swizzled boxes
-LLM_D uint32_t swz_off(int r, int c) { return (uint32_t)((c >> 3) * (kChunk * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)); }
+// of kMmaChunk rows
+LLM_D uint32_t swz_off(int r, int c) {
+  return (uint32_t)((c >> 3) * (kMmaChunk * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
 
+// Persistent and evenly split: the (row, kv head, 16-position chunk) sequence, rows and heads
+// outermost, is cut into one contiguous run per CTA; a run crosses into at most a few
+// (row, kv head) segments, and each warp's ring runs ahead across segment boundaries, so copies
+// never stop.  A (row, kv head) shared by several CTAs is finished by the last of them (atomic
+// ticket), which merges their partials in CTA order (the order of the positions).
 template <int HD>
-__global__ void __launch_bounds__(kAttnMaxThreads)
+__global__ void __launch_bounds__(kMmaWarps * 32, 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
   using M = MmaShape<HD>;
-  constexpr int ROWB = M::ROWB, BUF = M::BUF, QP = M::QP, NTO = M::NTO, KS = M::KS;
+  constexpr int ROWB = M::ROWB, BUF = M::BUF, QP = M::QP, NTO = M::NTO, KS = M::KS, NR = M::NR;
+  constexpr int CH = kMmaChunk;
   extern __shared__ unsigned char araw[];
   const uint32_t s_raw = smem_u32(araw);
   unsigned char* base = araw + (((s_raw + 1023u) & ~1023u) - s_raw);
   const uint32_t s_base = smem_u32(base);
 
-  const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
-  const int g = a.g;
+  const int g = a.g, H = a.kv * a.g, ns = kMmaMaxSplits;  // partial slots per (row, kv head)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int NT = blockDim.x, NW = NT >> 5;
-  const int NR = attn_geom(BUF).nr;
-  size_t region = (size_t)NW * NR * BUF;
-  if (region < (size_t)g * a.ns * 8) region = (size_t)g * a.ns * 8;
-  region = (region + 1023) & ~(size_t)1023;
-  uint16_t* qh = reinterpret_cast<uint16_t*>(base + region);  // [16][QP] bf16
-  uint16_t* ql = qh + 16 * QP;
-  float* wpart = reinterpret_cast<float*>(ql + 16 * QP);      // [NW][g][HD+2]
-  float* mypart = wpart + NW * g * (HD + 2);
-  float* fac = mypart + g * (HD + 2);
-  const uint32_t bars = (smem_u32(fac + g * kAttnMaxCluster) + 7u) & ~7u;
+  const int c = blockIdx.x, G = gridDim.x;
+  uint16_t* qbase = reinterpret_cast<uint16_t*>(base + (size_t)kMmaWarps * NR * BUF);  // [2][hi, lo][16][QP]
+  float* wpart = reinterpret_cast<float*>(qbase + 2 * 2 * 16 * QP);                   // [NW][g][HD+2]
+  float* mypart = wpart + NW * g * (HD + 2);                                           // [g][HD+2]
+  float* fac = mypart + g * (HD + 2);                                                  // [g][kMmaMaxSplits]
+  const uint32_t bars = (smem_u32(fac + g * kMmaMaxSplits) + 7u) & ~7u;
+  __shared__ int s_last;
 
   const int t = a.step->pos;
   const int npos = t + 1;
-  int chunk = (npos + a.ns - 1) / a.ns;
-  chunk = (chunk + 31) & ~31;
-  if (chunk < kMinChunk) chunk = kMinChunk;
-  const int nact = (npos + chunk - 1) / chunk;
-  if (!a.cluster && split >= nact) return;
-  const int p0 = split * chunk;
-  const int p1 = min(npos, p0 + chunk);
-  const int nch = p0 < p1 ? (p1 - p0 + kChunk - 1) / kChunk : 0;
-  const int cnt = nch > warp ? (nch - warp + NW - 1) / NW : 0;
+  const int nchk = (npos + CH - 1) / CH;              // chunks of one (row, kv head)
+  const long long T = (long long)a.B * a.kv * nchk;   // chunks of the launch
+  const long long c0 = T * c / G, c1 = T * (c + 1) / G;
+  auto owner = [&](long long it) { return (int)(((it + 1) * G + T - 1) / T - 1); };
+  // the segment starting at chunk st of the sequence: (row b, kv head j), chunks [k0, k1)
+  auto seg = [&](long long st, int& b, int& j, int& k0, int& k1, long long& next) {
+    const long long bj = st / nchk;
+    k0 = (int)(st - bj * nchk);
+    const long long end = c1 < (bj + 1) * nchk ? c1 : (bj + 1) * nchk;
+    k1 = k0 + (int)(end - st);
+    j = (int)(bj % a.kv);
+    b = (int)(bj / a.kv);
+    next = end;
+  };
 
   if (tid == 0) {
     for (int i = 0; i < NW * NR; ++i) mbar_init(bars + 8u * i, 1);
@@ -582,37 +594,48 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   }
   __syncthreads();
 
-  const int row0 = a.krow0 + (b * a.kv + j) * a.cap;
-  auto issue = [&](int k) {
-    const int slot = k % NR;
-    const int pb = p0 + (warp + k * NW) * kChunk;
+  // the issuing side of this warp (lane 0): cursor over (segment, chunk) pairs
+  long long ist = c0, inext = c0;
+  int iq = warp, issued = 0, ib = 0, ij = 0, ik0 = 0, ik1 = 0;
+  if (ist < c1) seg(ist, ib, ij, ik0, ik1, inext);
+  auto settle = [&]() {  // move the cursor to a pair that exists (or past the run)
+    while (ist < c1 && iq >= ik1 - ik0) {
+      ist = inext;
+      iq = warp;
+      if (ist < c1) seg(ist, ib, ij, ik0, ik1, inext);
+    }
+  };
+  settle();
+  auto issue = [&]() {
+    const int slot = issued % NR;
+    const int pb = (ik0 + iq) * CH;
+    const int row0 = a.krow0 + (ib * a.kv + ij) * a.cap;
     const uint32_t bar = bars + 8u * (warp * NR + slot);
     const uint32_t dst = s_base + (uint32_t)((warp * NR + slot) * BUF);
     fence_proxy_async_smem();
-    mbar_expect_tx(bar, (uint32_t)(2 * kChunk * ROWB));
+    mbar_expect_tx(bar, (uint32_t)(2 * CH * ROWB));
 #pragma unroll
     for (int bx = 0; bx < M::NBOX; ++bx) {
-      tma_load_2d(dst + (uint32_t)(bx * kChunk * 128), &kmap, bar, bx * 64, row0 + pb);
-      tma_load_2d(dst + (uint32_t)(kChunk * ROWB + bx * kChunk * 128), &vmap, bar, bx * 64, row0 + pb);
+      tma_load_2d(dst + (uint32_t)(bx * CH * 128), &kmap, bar, bx * 64, row0 + pb);
+      tma_load_2d(dst + (uint32_t)(CH * ROWB + bx * CH * 128), &vmap, bar, bx * 64, row0 + pb);
     }
+    ++issued;
+    iq += NW;
+    settle();
   };
-  const int npre = cnt < NR ? cnt : NR;
-  int issued = 0;
   if (lane == 0) {
     tma_prefetch_map(&kmap);
     tma_prefetch_map(&vmap);
-    while (issued < npre) {
-      const int pb = p0 + (warp + issued * NW) * kChunk;
-      if (pb + min(kChunk, p1 - pb) > t) break;  // holds position t
-      issue(issued++);
-    }
+    // chunks below position t do not depend on the previous kernel
+    while (issued < NR && ist < c1 && (ik0 + iq) * CH + min(CH, npos - (ik0 + iq) * CH) <= t) issue();
   }
   grid_dep_wait();
   grid_dep_launch();
   if (lane == 0)
-    while (issued < npre) issue(issued++);
-  // queries of the group as bf16 hi + lo, rows g..15 zero
-  {
+    while (issued < NR && ist < c1) issue();
+  auto load_q = [&](int buf, int b, int j) {  // queries of (b, j) as bf16 hi + lo, rows g..15 zero
+    uint16_t* qh = qbase + buf * 2 * 16 * QP;
+    uint16_t* ql = qh + 16 * QP;
     const float* qsrc = a.q + (size_t)b * a.q_stride + (size_t)j * g * HD;
     for (int i = tid; i < 16 * HD / 2; i += NT) {
       const int r = (2 * i) / HD, e = (2 * i) - r * HD;
@@ -627,151 +650,264 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
       *reinterpret_cast<uint32_t*>(qh + r * QP + e) = hi;
       *reinterpret_cast<uint32_t*>(ql + r * QP + e) = lo;
     }
+  };
+  if (c0 < c1) {
+    int b, j, k0, k1;
+    long long nx;
+    seg(c0, b, j, k0, k1, nx);
+    load_q(0, b, j);
   }
   __syncthreads();
 
-  float o[NTO][4];
-#pragma unroll
-  for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  // this lane's ldmatrix row addresses: queries (A operand)
+  const bool row1 = g > 8;     // MMA rows 8..15 hold heads (else padding)
+  const bool row0v = gid < g;  // this lane's row 0 holds a head
   const int qr = (lane & 7) + ((lane >> 3) & 1) * 8, qc = (lane >> 4) * 8;
-  const uint32_t qh_addr = smem_u32(qh + qr * QP + qc), ql_addr = smem_u32(ql + qr * QP + qc);
   const int mi = lane >> 3, mr = lane & 7;
   bool ok = true;
   int consumed = 0;
-  for (int k = 0; k < cnt; ++k) {
-    const int slot = k % NR;
-    const uint32_t bar = bars + 8u * (warp * NR + slot);
-    ok = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)(k / NR) & 1u, kAttnWaitCycles));
-    if (!ok) break;
-    consumed = k + 1;
-    const int pb = p0 + (warp + k * NW) * kChunk;
-    const int nv = min(kChunk, p1 - pb);
-    const uint32_t kreg = s_base + (uint32_t)((warp * NR + slot) * BUF);
-    const uint32_t vreg = kreg + (uint32_t)(kChunk * ROWB);
-    if (nv < kChunk) {
-      // rows past the last position hold other data (possibly not finite): zero the values
-      unsigned char* vz = base + (size_t)(warp * NR + slot) * BUF + kChunk * ROWB;
-      for (int i = lane; i < (kChunk - nv) * (ROWB / 16); i += 32) {
-        const int r = nv + i / (ROWB / 16), c = i - (i / (ROWB / 16)) * (ROWB / 16);
-        *reinterpret_cast<uint4*>(vz + swz_off(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+
+  int lu = 0;
+  long long next = c0;
+  for (long long st = c0; st < c1; st = next, ++lu) {
+    int b, j, k0, k1;
+    seg(st, b, j, k0, k1, next);
+    const int p0 = k0 * CH, p1 = min(npos, k1 * CH), nch = k1 - k0;
+    const uint16_t* qh = qbase + (lu & 1) * 2 * 16 * QP;
+    const uint32_t qh_addr = smem_u32(qh + qr * QP + qc), ql_addr = smem_u32(qh + 16 * QP + qr * QP + qc);
+    float o[NTO][4];
+#pragma unroll
+    for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    for (int ci = warp; ci < nch && ok; ci += NW) {
+      const int slot = consumed % NR;
+      const uint32_t bar = bars + 8u * (warp * NR + slot);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)(consumed / NR) & 1u, kAttnWaitCycles));
+      if (!ok) break;
+      ++consumed;
+      const int pb = p0 + ci * CH;
+      const int nv = min(CH, p1 - pb);
+      const uint32_t kreg = s_base + (uint32_t)((warp * NR + slot) * BUF);
+      const uint32_t vreg = kreg + (uint32_t)(CH * ROWB);
+      if (nv < CH) {
+        // rows past the last position hold other data (possibly not finite): zero the values
+        unsigned char* vz = base + (size_t)(warp * NR + slot) * BUF + CH * ROWB;
+        for (int i = lane; i < (CH - nv) * (ROWB / 16); i += 32) {
+          const int r = nv + i / (ROWB / 16), cc = i - (i / (ROWB / 16)) * (ROWB / 16);
+          *reinterpret_cast<uint4*>(vz + swz_off(r, cc)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
+      // ---- scores S = Q K^T: 2 n-tiles of 8 positions, separate hi and lo accumulators ----
+      float sh[2][4], sl[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sh[n][i] = sl[n][i] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ks += 2) {
+        uint32_t ah0[4], al0[4], ah1[4], al1[4], bk[2][4];
+        ldsm_x4(qh_addr + ks * 32, ah0);
+        ldsm_x4(ql_addr + ks * 32, al0);
+        ldsm_x4(qh_addr + (ks + 1) * 32, ah1);
+        ldsm_x4(ql_addr + (ks + 1) * 32, al1);
+        // matrices: (ks, dims 0-7), (ks, dims 8-15), (ks+1, 0-7), (ks+1, 8-15) of positions n*8..
+#pragma unroll
+        for (int n = 0; n < 2; ++n) ldsm_x4(kreg + swz_off(n * 8 + mr, 2 * (ks + (mi >> 1)) + (mi & 1)), bk[n]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) mma_bf16_16816(sh[n], ah0, bk[n][0], bk[n][1]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) mma_bf16_16816(sl[n], al0, bk[n][0], bk[n][1]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) mma_bf16_16816(sh[n], ah1, bk[n][2], bk[n][3]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) mma_bf16_16816(sl[n], al1, bk[n][2], bk[n][3]);
+      }
+      // ---- online softmax: row gid (entries 0, 1) and row gid + 8 (entries 2, 3) ----
+      float p[2][4];
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int pos = n * 8 + tig * 2 + (i & 1);
+          const float sv = pos < nv ? (sh[n][i] + sl[n][i]) * a.scale : -INFINITY;
+          p[n][i] = sv;
+          mx[i >> 1] = fmaxf(mx[i >> 1], sv);
+        }
+      float corr[2] = {1.f, 1.f};
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (r == 1 && !row1) break;
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        const float mnew = fmaxf(mrow[r], mx[r]);  // finite: position 0 of the chunk is valid
+        corr[r] = mrow[r] == -INFINITY ? 0.f : expf(mrow[r] - mnew);
+        mrow[r] = mnew;
+      }
+      float rs[2] = {0.f, 0.f};
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = i >> 1;
+          const bool live = r == 0 ? row0v : row1;
+          const float w = (!live || p[n][i] == -INFINITY) ? 0.f : expf(p[n][i] - mrow[r]);
+          p[n][i] = w;
+          rs[r] += w;
+        }
+      lrow[0] = fmaf(lrow[0], corr[0], rs[0]);
+      lrow[1] = fmaf(lrow[1], corr[1], rs[1]);
+      // the outputs need rescaling only when a running maximum moved
+      if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
+#pragma unroll
+        for (int n = 0; n < NTO; ++n) {
+          o[n][0] *= corr[0];
+          o[n][1] *= corr[0];
+          o[n][2] *= corr[1];
+          o[n][3] *= corr[1];
+        }
+      }
+      // ---- values O += P V: one k-step of 16 positions, P as bf16 hi + lo ----
+      {
+        uint32_t ph[4], pl[4];
+        split_bf16x2(p[0][0], p[0][1], ph[0], pl[0]);
+        split_bf16x2(p[0][2], p[0][3], ph[1], pl[1]);
+        split_bf16x2(p[1][0], p[1][1], ph[2], pl[2]);
+        split_bf16x2(p[1][2], p[1][3], ph[3], pl[3]);
+        // matrices: positions 0-7 and 8-15 for dims n*8.., then for dims (n+1)*8..
+        uint32_t bv[NTO / 2][4];
+#pragma unroll
+        for (int n = 0; n < NTO; n += 2) ldsm_x4_t(vreg + swz_off((mi & 1) * 8 + mr, n + (mi >> 1)), bv[n / 2]);
+        // the hi products of every output tile, then the lo products: NTO issues apart
+#pragma unroll
+        for (int n = 0; n < NTO; n += 2) {
+          mma_bf16_16816(o[n], ph, bv[n / 2][0], bv[n / 2][1]);
+          mma_bf16_16816(o[n + 1], ph, bv[n / 2][2], bv[n / 2][3]);
+        }
+#pragma unroll
+        for (int n = 0; n < NTO; n += 2) {
+          mma_bf16_16816(o[n], pl, bv[n / 2][0], bv[n / 2][1]);
+          mma_bf16_16816(o[n + 1], pl, bv[n / 2][2], bv[n / 2][3]);
+        }
       }
       __syncwarp();
+      if (lane == 0)
+        while (issued - consumed < NR && ist < c1) issue();
     }
-    // ---- scores S = Q K^T: 4 n-tiles of 8 positions, separate hi and lo accumulators ----
-    float sh[4][4], sl[4][4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sh[n][i] = sl[n][i] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ks += 2) {
-      uint32_t ah0[4], al0[4], ah1[4], al1[4];
-      ldsm_x4(qh_addr + ks * 32, ah0);
-      ldsm_x4(ql_addr + ks * 32, al0);
-      ldsm_x4(qh_addr + (ks + 1) * 32, ah1);
-      ldsm_x4(ql_addr + (ks + 1) * 32, al1);
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        // matrices: (ks, dims 0-7), (ks, dims 8-15), (ks+1, 0-7), (ks+1, 8-15) of positions n*8..
-        uint32_t bk[4];
-        ldsm_x4(kreg + swz_off(n * 8 + mr, 2 * (ks + (mi >> 1)) + (mi & 1)), bk);
-        mma_bf16_16816(sh[n], ah0, bk[0], bk[1]);
-        mma_bf16_16816(sl[n], al0, bk[0], bk[1]);
-        mma_bf16_16816(sh[n], ah1, bk[2], bk[3]);
-        mma_bf16_16816(sl[n], al1, bk[2], bk[3]);
-      }
-    }
-    // ---- online softmax: row gid (entries 0, 1) and row gid + 8 (entries 2, 3) ----
-    float p[4][4];
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int pos = n * 8 + tig * 2 + (i & 1);
-        const float sv = pos < nv ? (sh[n][i] + sl[n][i]) * a.scale : -INFINITY;
-        p[n][i] = sv;
-        mx[i >> 1] = fmaxf(mx[i >> 1], sv);
-      }
-    float corr[2];
+    // ---- the unit's end: warp partials, the CTA's partial, the split merge ----
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float mnew = fmaxf(mrow[r], mx[r]);  // finite: position 0 of the chunk is valid
-      corr[r] = mrow[r] == -INFINITY ? 0.f : expf(mrow[r] - mnew);
-      mrow[r] = mnew;
-    }
-    float rs[2] = {0.f, 0.f};
+      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
+      const int h = gid + 8 * r;
+      if (h < g) {
+        float* wp = wpart + (warp * g + h) * (HD + 2);
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float w = p[n][i] == -INFINITY ? 0.f : expf(p[n][i] - mrow[i >> 1]);
-        p[n][i] = w;
-        rs[i >> 1] += w;
-      }
-    lrow[0] = fmaf(lrow[0], corr[0], rs[0]);
-    lrow[1] = fmaf(lrow[1], corr[1], rs[1]);
-#pragma unroll
-    for (int n = 0; n < NTO; ++n) {
-      o[n][0] *= corr[0];
-      o[n][1] *= corr[0];
-      o[n][2] *= corr[1];
-      o[n][3] *= corr[1];
-    }
-    // ---- values O += P V: two k-steps of 16 positions, P as bf16 hi + lo ----
-#pragma unroll
-    for (int s2 = 0; s2 < 2; ++s2) {
-      uint32_t ph[4], pl[4];
-      split_bf16x2(p[2 * s2][0], p[2 * s2][1], ph[0], pl[0]);
-      split_bf16x2(p[2 * s2][2], p[2 * s2][3], ph[1], pl[1]);
-      split_bf16x2(p[2 * s2 + 1][0], p[2 * s2 + 1][1], ph[2], pl[2]);
-      split_bf16x2(p[2 * s2 + 1][2], p[2 * s2 + 1][3], ph[3], pl[3]);
-#pragma unroll
-      for (int n = 0; n < NTO; n += 2) {
-        // matrices: positions 0-7 and 8-15 of this k-step for dims n*8.., then for dims (n+1)*8..
-        uint32_t bv[4];
-        ldsm_x4_t(vreg + swz_off(16 * s2 + (mi & 1) * 8 + mr, n + (mi >> 1)), bv);
-        mma_bf16_16816(o[n], ph, bv[0], bv[1]);
-        mma_bf16_16816(o[n], pl, bv[0], bv[1]);
-        mma_bf16_16816(o[n + 1], ph, bv[2], bv[3]);
-        mma_bf16_16816(o[n + 1], pl, bv[2], bv[3]);
+        for (int n = 0; n < NTO; ++n) {
+          wp[n * 8 + tig * 2] = o[n][2 * r];
+          wp[n * 8 + tig * 2 + 1] = o[n][2 * r + 1];
+        }
+        if (tig == 0) {
+          wp[HD] = mrow[r];
+          wp[HD + 1] = lrow[r];
+        }
       }
     }
-    __syncwarp();
-    if (lane == 0 && issued < cnt) issue(issued++);
+    __syncthreads();
+    for (int idx = tid; idx < g * (HD + 2); idx += NT) {
+      const int h = idx / (HD + 2), e = idx - h * (HD + 2);
+      float Mx = -INFINITY;
+      for (int w = 0; w < NW; ++w) Mx = fmaxf(Mx, wpart[(w * g + h) * (HD + 2) + HD]);
+      float r = Mx;
+      if (e != HD) {
+        r = 0.f;
+        for (int w = 0; w < NW; ++w) {
+          const float mw = wpart[(w * g + h) * (HD + 2) + HD];
+          const float f = mw == -INFINITY ? 0.f : expf(mw - Mx);
+          r = fmaf(f, wpart[(w * g + h) * (HD + 2) + e], r);
+        }
+      }
+      mypart[idx] = r;
+    }
+    if (next < c1) {
+      int b2, j2, k02, k12;
+      long long nx2;
+      seg(next, b2, j2, k02, k12, nx2);
+      load_q((lu + 1) & 1, b2, j2);
+    }
+    __syncthreads();
+    float* outb = a.out + (size_t)b * a.out_stride + (size_t)j * g * HD;
+    // the CTAs holding chunks of this (row, kv head): with at least one chunk per CTA they are
+    // first..last; with fewer chunks than CTAs each holds one chunk
+    const long long bj0 = ((long long)b * a.kv + j) * nchk;
+    const int first = owner(bj0), last = owner(bj0 + nchk - 1);
+    const int nc = T >= G ? last - first + 1 : nchk, sp = T >= G ? c - first : k0;
+    if (nc == 1) {
+      // this CTA holds all positions: the output is o / l (the merge's factor for one part)
+      for (int idx = tid; idx < g * HD; idx += NT) {
+        const int h = idx / HD, e = idx - h * HD;
+        const float rl = 1.0f / mypart[h * (HD + 2) + HD + 1];
+        outb[(size_t)h * HD + e] = fmaf(rl, mypart[h * (HD + 2) + e], 0.f);
+      }
+    } else {
+      // global partials; the last CTA of this (row, kv head) merges them in CTA order
+      float* pglob = a.part + (((size_t)b * H + (size_t)j * g) * ns) * (HD + 2);
+      for (int idx = tid; idx < g * (HD + 2); idx += NT) {
+        const int h = idx / (HD + 2), e = idx - h * (HD + 2);
+        pglob[((size_t)h * ns + sp) * (HD + 2) + e] = mypart[idx];
+      }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const unsigned int prev = atomicAdd(a.ticket + (size_t)b * a.kv + j, 1u);
+        s_last = (prev == (unsigned int)(nc - 1));
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        for (int h = warp; h < g; h += NW) {
+          float Mx = -INFINITY;
+          for (int s2 = lane; s2 < nc; s2 += 32) Mx = fmaxf(Mx, __ldcg(pglob + ((size_t)h * ns + s2) * (HD + 2) + HD));
+          Mx = warp_max(Mx);
+          float L = 0.f;
+          for (int s2 = lane; s2 < nc; s2 += 32) {
+            const float* pp = pglob + ((size_t)h * ns + s2) * (HD + 2);
+            const float ms = __ldcg(pp + HD);
+            const float f = ms == -INFINITY ? 0.f : expf(ms - Mx);
+            fac[h * kMmaMaxSplits + s2] = f;
+            L += __ldcg(pp + HD + 1) * f;
+          }
+          L = warp_sum(L);
+          const float rl = 1.0f / L;
+          for (int s2 = lane; s2 < nc; s2 += 32) fac[h * kMmaMaxSplits + s2] *= rl;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < g * HD; idx += NT) {
+          const int h = idx / HD, e = idx - h * HD;
+          const float* pb = pglob + (size_t)h * ns * (HD + 2) + e;
+          float O = 0.f;
+          int s2 = 0;
+          for (; s2 + 8 <= nc; s2 += 8) {
+            float ov[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) ov[q] = __ldcg(pb + (size_t)(s2 + q) * (HD + 2));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) O = fmaf(fac[h * kMmaMaxSplits + s2 + q], ov[q], O);
+          }
+          for (; s2 < nc; ++s2) O = fmaf(fac[h * kMmaMaxSplits + s2], __ldcg(pb + (size_t)s2 * (HD + 2)), O);
+          outb[(size_t)h * HD + e] = O;
+        }
+        if (tid == 0) a.ticket[(size_t)b * a.kv + j] = 0u;
+      }
+      __syncthreads();
+    }
   }
   if (!ok && lane == 0) atomicCAS(a.status, 0, kErrDeviceTimeout);
+  // no copy may still be writing shared memory when the CTA exits
   if (lane == 0)
     for (int k = consumed; k < issued; ++k)
       if (!mbar_wait(bars + 8u * (warp * NR + k % NR), (uint32_t)(k / NR) & 1u, kAttnWaitCycles))
         atomicCAS(a.status, 0, kErrDeviceTimeout);
-  __syncwarp();
-
-  // the warp's partial: rows gid and gid + 8 of the fragments
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    const int h = gid + 8 * r;
-    if (h < g) {
-      float* wp = wpart + (warp * g + h) * (HD + 2);
-#pragma unroll
-      for (int n = 0; n < NTO; ++n) {
-        wp[n * 8 + tig * 2] = o[n][2 * r];
-        wp[n * 8 + tig * 2 + 1] = o[n][2 * r + 1];
-      }
-      if (tig == 0) {
-        wp[HD] = mrow[r];
-        wp[HD + 1] = lrow[r];
-      }
-    }
-  }
-  __syncthreads();
-  attn_finish<HD>(a, base, wpart, mypart, fac, nact, split, b, j);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -846,8 +982,8 @@ cudaError_t attn_prepare(int max_smem_optin) {
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(16, 8, 1);
-    cfg.blockDim = dim3(attn_geom(MmaShape<128>::BUF).nw * 32);
-    cfg.dynamicSmemBytes = attn_mma_smem<128>(4, 16);
+    cfg.blockDim = dim3(kMmaWarps * 32);
+    cfg.dynamicSmemBytes = attn_mma_smem<128>(4);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 16;
@@ -868,26 +1004,38 @@ bool attn_make_kmap(CUtensorMap* map, const void* kc, int kt, int hd, uint64_t r
   const int rowb = hd * es;
   const bool swz = rowb >= 128;
   const int boxb = swz ? 128 : rowb;
-  return make_map_2d(map, kc, es, (uint64_t)hd, rows, (uint32_t)(boxb / es), (uint32_t)kChunk,
+  const int box_rows = attn_uses_mma(kt, hd) ? kMmaChunk : kChunk;
+  return make_map_2d(map, kc, es, (uint64_t)hd, rows, (uint32_t)(boxb / es), (uint32_t)box_rows,
                      swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int attn_splits(int B, int kv, int cap, int num_sms) {
-  // enough CTAs to cover the GPU twice, each split at least kMinChunk positions of the capacity;
-  // up to kAttnMaxCluster splits merge inside a cluster, which is cheaper than a global merge,
-  // so a short cache uses one cluster of kAttnMaxCluster splits instead of more global ones
-  int ns = (2 * num_sms + B * kv - 1) / (B * kv);
+  // about two CTAs per SM, each split at least kMinChunk positions of the capacity; among nearby
+  // counts the one whose CTAs fill whole waves of one CTA per SM
+  const int units = B * kv;
   int by_cap = cap / kMinChunk;
   if (by_cap < 1) by_cap = 1;
-  if (ns > by_cap) ns = by_cap;
-  const int mc = attn_max_cluster();
-  if (ns > mc && cap / mc <= 4096) ns = mc;
-  if (ns > 1024) ns = 1024;
-  if (ns < 1) ns = 1;
-  return ns;
+  if (by_cap > 64) by_cap = 64;  // (the persistent kernel merges at most 64 splits)
+  const int ns0 = (2 * num_sms + units - 1) / units;
+  int best = 1;
+  double best_eff = -1.0;
+  int lo = ns0 / 2 > 1 ? ns0 / 2 : 1;
+  if (lo > by_cap) lo = by_cap;
+  for (int ns = lo; ns <= 2 * ns0 && ns <= by_cap; ++ns) {
+    const long long ctas = (long long)units * ns;
+    const long long waves = (ctas + num_sms - 1) / num_sms;
+    const double eff = (double)ctas / (double)(waves * num_sms);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = ns;
+    }
+  }
+  return best;
 }
 
 bool attn_uses_mma(int kt, int hd) { return kt == 1 && (hd == 64 || hd == 128); }
+
+int attn_part_slots(int kt, int hd, int ns) { return attn_uses_mma(kt, hd) ? kMmaMaxSplits : ns; }
 
 // clusters of cs CTAs of this kernel that the device runs at once (queried once per shape)
 static int max_active_clusters(const void* fn, size_t smem, int threads, int cs) {
@@ -926,9 +1074,7 @@ bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters) {
   int nw = 0;
   const void* f = nullptr;
   if (attn_uses_mma(kt, hd)) {
-    f = hd == 64 ? (const void*)attn_mma_kernel<64> : (const void*)attn_mma_kernel<128>;
-    smem = hd == 64 ? attn_mma_smem<64>(g, ns) : attn_mma_smem<128>(g, ns);
-    nw = attn_geom(hd == 64 ? MmaShape<64>::BUF : MmaShape<128>::BUF).nw;
+    return false;  // the persistent kernel merges through global partials
   } else {
     f = (const void*)pick(kt, hd, g, &smem, ns, &nw);
     if (!f) return false;
@@ -945,8 +1091,8 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   void (*mfn)(const CUtensorMap, const CUtensorMap, const AttnArgs) = nullptr;
   if (attn_uses_mma(kt, a.hd)) {
     mfn = a.hd == 64 ? attn_mma_kernel<64> : attn_mma_kernel<128>;
-    smem = a.hd == 64 ? attn_mma_smem<64>(a.g, a.ns) : attn_mma_smem<128>(a.g, a.ns);
-    nw = attn_geom(a.hd == 64 ? MmaShape<64>::BUF : MmaShape<128>::BUF).nw;
+    smem = a.hd == 64 ? attn_mma_smem<64>(a.g) : attn_mma_smem<128>(a.g);
+    nw = kMmaWarps;
   } else {
     fn = pick(kt, a.hd, a.g, &smem, a.ns, &nw);
     if (!fn) return cudaErrorInvalidValue;
@@ -954,6 +1100,19 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   a.cluster = attn_cluster_merge(kt, a.hd, a.g, a.ns, a.B * a.kv) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ns, a.kv, a.B);
+  if (mfn) {
+    // persistent: one CTA per SM, each walking (row, kv head, split) units
+    static int sms = 0;
+    if (!sms) {
+      int dev = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (sms < 1) sms = 1;
+    }
+    // at most kMmaMaxSplits - 1 CTAs per (row, kv head) keeps every one's parts within its slots
+    const int cap = (kMmaMaxSplits - 1) * a.B * a.kv;
+    cfg.gridDim = dim3(cap < sms ? cap : sms);
+  }
   cfg.blockDim = dim3(nw * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

@@ -34,6 +34,8 @@ cudaError_t attn_prepare(int max_smem_optin);
 bool attn_make_kmap(CUtensorMap* map, const void* kc, int kt, int hd, uint64_t rows);
 // bf16 caches with hd 64 or 128 run the tensor-core kernel (which also reads the values by map)
 bool attn_uses_mma(int kt, int hd);
+// partial slots per (row, kv head) the kernels need for ns splits
+int attn_part_slots(int kt, int hd, int ns);
 // whether ns splits of `clusters` (row, kv head) pairs merge inside thread-block clusters; the
 // first call for a shape queries the device (make it outside stream capture)
 bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters);

@@ -1,27 +1,30 @@
-// Tensor-core projections of batched decode: out[j][r] = sum_c W[r][c] * x'[j][c] for B >= 16
+// Tensor-core projections of batched decode: out[j][r] = sum_c W[r][c] * x'[j][c] for batches of
 // activation rows, on the 5th-generation tensor core (tcgen05.mma, accumulators in tensor memory,
-// operands staged by TMA), with the same fused epilogues as the weight-streaming GEMV
-// (bend-ml-llama "A layer", block: RoPE + KV write after Q/K/V, residual adds, SwiGLU; the LM
-// head after the final norm).
+// operands staged by TMA).  The steps around each projection (bend-ml-llama "A layer", block:
+// RMSNorm before Q/K/V and gate/up, RoPE and the KV write after Q/K/V, the residual adds, SwiGLU;
+// the final norm before the LM head) run in the small kernels that read the projection's output.
 //
-// Precision.  The weights are bf16; the activations are f32.  Each activation is split into
-// two bf16 numbers, hi = bf16(x') and lo = bf16(x' - hi), and the product runs as W*hi + W*lo
-// into one f32 accumulator: x' is represented to about 2^-17 relative, close to the f32 inputs
-// of the plain matrix-vector product, at twice the tensor work (still far below the weight
-// stream's time).  x' is x or RMSNorm(x) (bend-ml-llama "The numeric pieces", rmsnorm),
-// computed by tc_split_kernel before the product.
+// Precision.  The weights are bf16; the activations are f32.  Each activation is split into two
+// bf16 numbers, hi = bf16(x') and lo = bf16(x' - hi) (about 2^-17 relative together), and both
+// multiply the weights in one MMA: hi rows sit in MMA rows 0..63, lo rows in 64..127, and the two
+// accumulator rows of an activation are added in the epilogue.
 //
-// Work split.  The weight tiles (128 rows x 64 K) of all row tiles, K innermost, form one
-// sequence; each CTA (one per SM) takes an equal contiguous run of it (stream-K).  A CTA whose
-// run covers a whole row tile applies the epilogue from tensor memory; row tiles shared by
-// several CTAs are finished by the last CTA to arrive (atomic ticket, nobody waits), which adds
-// the partials in CTA order, so results do not depend on timing.
+// Shape of the MMA: M = 128 (the stacked activation rows), N = 256 (weight rows), K = 16; the
+// weights are the N operand, so one MMA covers 256 weight rows and a 64-element K block of a
+// 32 KB weight tile takes four MMAs.
+//
+// Work split.  The K range of every 256-row weight tile is cut into S equal splits (S chosen per
+// shape so that tiles x splits fills the GPU's SMs evenly); a unit (activation tile, weight tile,
+// split) writes its raw sums to out[s].  CTAs are persistent, one per SM, and take units
+// c, c + grid, ...; the reader of the projection adds the S splits in split order, so results do
+// not depend on timing.
 //
 // Roles: warp 0 issues TMA copies into a ring of shared-memory stages (mbarrier full/empty),
 // warp 1 issues the MMAs (one thread) into two tensor-memory accumulators so the epilogue of one
-// run overlaps the next, warps 2..5 read the accumulator (tcgen05.ld, one row per thread) and
-// run the epilogue.  Every wait is bounded: on timeout the kernel records kErrDeviceTimeout,
-// lets its copies and MMAs drain (bounded again), frees its tensor memory and returns.
+// unit overlaps the next, warps 2..5 read the accumulators (tcgen05.ld, one MMA row per thread):
+// the lo rows pass their values through shared memory to the hi rows, which add and store.  Every
+// wait is bounded: on timeout the kernel records kErrDeviceTimeout, lets its copies and MMAs
+// drain (bounded again), frees its tensor memory and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -31,78 +34,35 @@
 
 namespace llm {
 
-constexpr uint64_t kTcWaitNs = 4000000000ull;  // SM cycles: about 2 s at 2 GHz
+constexpr uint64_t kTcWaitCycles = 4000000000ull;  // SM cycles: about 2 s at 2 GHz
+constexpr int kTcStages = 4;
+constexpr uint32_t kTcA = 128 * 128;               // activation tile: 128 MMA rows x 128 bytes
+constexpr uint32_t kTcW = kTcN * 128;              // weight tile: 256 rows x 128 bytes
+constexpr uint32_t kTcStage = kTcA + kTcW;
+constexpr int kXchgPitch = 33;                     // floats per exchange row (conflict-free)
 
-LLM_HD int tc_owner(int64_t it, int64_t T, int G) { return (int)(((it + 1) * G + T - 1) / T - 1); }
-LLM_HD int64_t tc_first(int64_t T, int G, int c) { return T * c / G; }
-
-// epilogue of column j (batch row), weight row R, accumulated value v; lanes hold consecutive
-// rows, so RoPE and SwiGLU partners (rows 2i, 2i+1) are neighbouring lanes
-template <int EPI>
-LLM_D void tc_epi(const TcArgs& a, int R, int j, float v) {
-  const bool ok = R < a.rows;
-  if constexpr (EPI == EPI_STORE) {
-    if (ok) a.out[(size_t)j * a.out_stride + R] = v;
-  } else if constexpr (EPI == EPI_RESID) {
-    if (ok) a.out[(size_t)j * a.out_stride + R] = __fadd_rn(a.resid[(size_t)j * a.resid_stride + R], v);
-  } else if constexpr (EPI == EPI_SWIGLU) {
-    const float up = __shfl_xor_sync(0xffffffffu, v, 1);
-    if (ok && !(R & 1)) {
-      const float si = __fdiv_rn(v, __fadd_rn(1.0f, expf(-v)));
-      a.out[(size_t)j * a.out_stride + (R >> 1)] = __fmul_rn(si, up);
-    }
-  } else {
-    const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-    if (ok) {
-      const bool odd = (R & 1) != 0;
-      const float x0 = odd ? other : v, x1 = odd ? v : other;
-      const int head = R / a.hd, e = (R - head * a.hd) >> 1, half = a.hd >> 1;
-      const int pos = a.step->pos;
-      const int ee = odd ? e + half : e;
-      const size_t row = (size_t)j;
-      if (head < a.H + a.kv) {
-        const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];
-        const float r = odd ? __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s))
-                            : __fadd_rn(__fmul_rn(x0, c), __fmul_rn(-x1, s));
-        if (head < a.H) {
-          a.q_out[row * a.q_stride + (size_t)head * a.hd + ee] = r;
-        } else {
-          const size_t ci = ((row * a.kv + (size_t)(head - a.H)) * a.cap + pos) * a.hd;
-          store_elem<1>(a.kc, ci + ee, r);
-        }
-      } else {
-        const size_t ci = ((row * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pos) * a.hd;
-        store_elem<1>(a.vc, ci + ee, v);
-      }
-    }
-  }
-}
-
-template <int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, const TcArgs a) {
   extern __shared__ uint8_t tc_smem[];
   const uint32_t s_raw = smem_u32(tc_smem);
   const uint32_t s_base = (s_raw + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 bytes
   uint8_t* g_base = tc_smem + (s_base - s_raw);
-  const int NP = a.NP, S = a.stages, KB = a.KB;
-  const uint32_t bB = (uint32_t)NP * 128u;
-  const uint32_t stage = 16384u + 2u * bB;
-  const uint32_t bars = s_base + (uint32_t)S * stage;
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain
-  const uint32_t FULL0 = bars, EMPTY0 = bars + 8u * S, ACCF0 = bars + 16u * S, ACCE0 = ACCF0 + 16u,
+  const int NP = a.NP, KB = a.KB, S = a.S, MT = a.MT;
+  float* xchg = reinterpret_cast<float*>(g_base + kTcStages * kTcStage);  // [64][kXchgPitch]
+  const uint32_t bars = s_base + kTcStages * kTcStage + kTcRows * kXchgPitch * 4;
+  // barriers: full[stages], empty[stages], acc_full[2], acc_empty[2], drain
+  const uint32_t FULL0 = bars, EMPTY0 = bars + 8u * kTcStages, ACCF0 = bars + 16u * kTcStages, ACCE0 = ACCF0 + 16u,
                  DRAIN = ACCE0 + 16u;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(g_base + (size_t)S * stage + 16u * S + 40u);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [0] abort, [1] last arrival
+  volatile uint32_t* tmem_slot =
+      reinterpret_cast<volatile uint32_t*>(g_base + kTcStages * kTcStage + kTcRows * kXchgPitch * 4 + 16 * kTcStages + 40);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [0] abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x, G = gridDim.x, nt = blockIdx.y;
-  const int64_t T = (int64_t)a.MT * KB;
-  const int64_t it0 = tc_first(T, G, c), it1 = tc_first(T, G, c + 1);
-  const int64_t n_it = it1 - it0;
+  const int c = blockIdx.x, G = gridDim.x;
+  const uint32_t xbytes = 2u * (uint32_t)NP * 128u;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
+    for (int i = 0; i < kTcStages; ++i) {
       mbar_init(FULL0 + 8u * i, 1);
       mbar_init(EMPTY0 + 8u * i, 1);
     }
@@ -112,11 +72,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(ACCE0 + 8u, 128);
     mbar_init(DRAIN, 1);
     flags[0] = 0;
-    flags[1] = 0;
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32((const void*)tmem_slot), a.tmem_cols);
+    tmem_alloc(smem_u32((const void*)tmem_slot), 2 * kTcN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -128,51 +87,64 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     flags[0] = 1;
     atomicCAS(a.status, 0, kErrDeviceTimeout);
   };
+  // unit u = (t * MT + m) * S + s: activation tile t, weight tile m, split s
+  auto unit = [&](int u, int& t, int& m, int& kb0, int& kb1) {
+    const int s = u % S, tm = u / S;
+    m = tm % MT;
+    t = tm / MT;
+    kb0 = KB * s / S;
+    kb1 = KB * (s + 1) / S;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_map(&tw);
       tma_prefetch_map(&tx);
-      const int n = (int)n_it;
-      const int npre = n < S ? n : S;
-      const int m0 = (int)(it0 / KB), kb00 = (int)(it0 - (int64_t)m0 * KB);
       // the weight tiles of the first stages do not depend on the previous kernel
-      int m = m0, kb = kb00;
-      for (int i = 0; i < npre; ++i) {
-        mbar_expect_tx(FULL0 + 8u * i, stage);
-        tma_load_2d(s_base + (uint32_t)i * stage, &tw, FULL0 + 8u * i, kb * kTcK, m * kTcM);
-        if (++kb == KB) kb = 0, ++m;
+      int u = c, t = 0, m = 0, kb0 = 0, kb1 = 0, kb = 0;
+      if (u < a.units) unit(u, t, m, kb0, kb1), kb = kb0;
+      int npre = 0;
+      {
+        int pu = u, pt = t, pm = m, pk0 = kb0, pk1 = kb1, pk = kb;
+        while (npre < kTcStages && pu < a.units) {
+          mbar_expect_tx(FULL0 + 8u * npre, kTcW + xbytes);
+          tma_load_2d(s_base + (uint32_t)npre * kTcStage + kTcA, &tw, FULL0 + 8u * npre, pk * kTcK, pm * kTcN);
+          ++npre;
+          if (++pk == pk1) {
+            pu += G;
+            if (pu < a.units) unit(pu, pt, pm, pk0, pk1), pk = pk0;
+          }
+        }
       }
       grid_dep_wait();
       grid_dep_launch();
-      kb = kb00;
-      for (int i = 0; i < npre; ++i) {
-        const uint32_t sb = s_base + (uint32_t)i * stage + 16384u;
-        tma_load_2d(sb, &tx, FULL0 + 8u * i, kb * kTcK, nt * NP);
-        tma_load_2d(sb + bB, &tx, FULL0 + 8u * i, kb * kTcK, a.Ntot + nt * NP);
-        if (++kb == KB) kb = 0;
-      }
-      // m, kb: the tile of iteration npre; (s, ph): its stage and round parity
-      int s = npre == S ? 0 : npre;
-      uint32_t ph = npre == S ? 1u : 0u;
-      int issued = npre;
-      for (int i = npre; i < n; ++i) {
-        if (flags[0] || !mbar_wait(EMPTY0 + 8u * s, ph ^ 1u, kTcWaitNs)) {
+      int stg = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      while (u < a.units && ok) {
+        if (issued >= kTcStages && (flags[0] || !mbar_wait(EMPTY0 + 8u * stg, ph ^ 1u, kTcWaitCycles))) {
           fail();
+          ok = false;
           break;
         }
-        const uint32_t sa = s_base + (uint32_t)s * stage;
-        mbar_expect_tx(FULL0 + 8u * s, stage);
-        tma_load_2d(sa, &tw, FULL0 + 8u * s, kb * kTcK, m * kTcM);
-        tma_load_2d(sa + 16384u, &tx, FULL0 + 8u * s, kb * kTcK, nt * NP);
-        tma_load_2d(sa + 16384u + bB, &tx, FULL0 + 8u * s, kb * kTcK, a.Ntot + nt * NP);
-        issued = i + 1;
-        if (++kb == KB) kb = 0, ++m;
-        if (++s == S) s = 0, ph ^= 1u;
+        const uint32_t sa = s_base + (uint32_t)stg * kTcStage;
+        if (issued >= npre) {
+          mbar_expect_tx(FULL0 + 8u * stg, kTcW + xbytes);
+          tma_load_2d(sa + kTcA, &tw, FULL0 + 8u * stg, kb * kTcK, m * kTcN);
+        }
+        tma_load_2d(sa, &tx, FULL0 + 8u * stg, kb * kTcK, t * NP);                       // hi rows
+        tma_load_2d(sa + 64u * 128u, &tx, FULL0 + 8u * stg, kb * kTcK, a.Ntot + t * NP);  // lo rows
+        ++issued;
+        if (++stg == kTcStages) stg = 0, ph ^= 1u;
+        if (++kb == kb1) {
+          u += G;
+          if (u < a.units) unit(u, t, m, kb0, kb1), kb = kb0;
+        }
       }
       // no copy may still be writing shared memory when the CTA exits
-      for (int i = issued > S ? issued - S : 0; i < issued; ++i)
-        if (!mbar_wait(FULL0 + 8u * (uint32_t)(i % S), (uint32_t)(i / S) & 1u, kTcWaitNs)) fail();
+      for (int i = issued > kTcStages ? issued - kTcStages : 0; i < issued; ++i)
+        if (!mbar_wait(FULL0 + 8u * (uint32_t)(i % kTcStages), (uint32_t)(i / kTcStages) & 1u, kTcWaitCycles)) fail();
     } else {
       grid_dep_wait();
       grid_dep_launch();
@@ -181,210 +153,286 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     grid_dep_wait();
     grid_dep_launch();
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kTcM, NP);
-      int s = 0;
+      const uint32_t idesc = idesc_bf16_f32(128, kTcN);
+      int stg = 0;
       uint32_t ph = 0;
-      int si = 0;
       bool ok = true;
-      const int n = (int)n_it;
-      int kb0 = (int)(it0 % KB);
-      for (int done = 0; done < n && ok; ++si) {
-        const int kb1 = KB < kb0 + (n - done) ? KB : kb0 + (n - done);
+      int si = 0;
+      for (int u = c; u < a.units && ok; u += G, ++si) {
+        int t, m, kb0, kb1;
+        unit(u, t, m, kb0, kb1);
         const int buf = si & 1, use = si >> 1;
-        if (use > 0 && !mbar_wait(ACCE0 + 8u * buf, (uint32_t)(use - 1) & 1u, kTcWaitNs)) {
+        if (use > 0 && !mbar_wait(ACCE0 + 8u * buf, (uint32_t)(use - 1) & 1u, kTcWaitCycles)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * NP);
+        const uint32_t d = tmem + (uint32_t)(buf * kTcN);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (flags[0] || !mbar_wait(FULL0 + 8u * s, ph, kTcWaitNs)) {
+          if (flags[0] || !mbar_wait(FULL0 + 8u * stg, ph, kTcWaitCycles)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = s_base + (uint32_t)s * stage, sb = sa + 16384u;
-          const uint64_t ad = sw128_kmajor_desc(sa), bh = sw128_kmajor_desc(sb), bl = sw128_kmajor_desc(sb + bB);
+          const uint32_t sa = s_base + (uint32_t)stg * kTcStage;
+          const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sa + kTcA);
 #pragma unroll
-          for (int k = 0; k < kTcK / 16; ++k) {
-            // 16 K elements = 32 bytes = 2 in the descriptor's address field
-            tc_mma_bf16(d, ad + 2 * k, bh + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-            tc_mma_bf16(d, ad + 2 * k, bl + 2 * k, idesc, 1u);
-          }
-          tc_commit(EMPTY0 + 8u * s);
-          if (++s == S) s = 0, ph ^= 1u;
+          for (int k = 0; k < kTcK / 16; ++k)  // 16 K elements = 32 bytes = 2 in the address field
+            tc_mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          tc_commit(EMPTY0 + 8u * stg);
+          if (++stg == kTcStages) stg = 0, ph ^= 1u;
         }
         if (!ok) break;
         tc_commit(ACCF0 + 8u * buf);
-        done += kb1 - kb0;
-        kb0 = 0;
       }
       if (!ok) fail();
       // every MMA has completed before tensor memory is freed
       tc_commit(DRAIN);
-      if (!mbar_wait(DRAIN, 0, kTcWaitNs)) fail();
+      if (!mbar_wait(DRAIN, 0, kTcWaitCycles)) fail();
     }
   } else {
     grid_dep_wait();
     grid_dep_launch();
-    const int q = warp & 3;  // this warp's quarter of the tensor-memory lanes
-    const int rl = q * 32 + lane;
+    const int q = warp & 3;          // this warp's quarter of the tensor-memory lanes
+    const bool hi = q < 2;           // MMA rows 0..63: hi halves; 64..127: lo halves
+    const int j = (q & 1) * 32 + lane;  // activation row within the tile
+    const bool active = (q & 1) == 0 || NP > 32;
+    const bool vec = (a.rows & 3) == 0;
     int si = 0;
-    for (int64_t it = it0; it < it1; ++si) {
-      const int m = (int)(it / KB), kb0 = (int)(it - (int64_t)m * KB);
-      const int kb1 = (int)((int64_t)KB < kb0 + (it1 - it) ? KB : kb0 + (it1 - it));
+    for (int u = c; u < a.units; u += G, ++si) {
+      int t, m, kb0, kb1;
+      unit(u, t, m, kb0, kb1);
+      const int s = u % S;
       const int buf = si & 1, use = si >> 1;
-      bool ok = !flags[0] && mbar_wait(ACCF0 + 8u * buf, (uint32_t)use & 1u, kTcWaitNs);
+      bool ok = !flags[0] && mbar_wait(ACCF0 + 8u * buf, (uint32_t)use & 1u, kTcWaitCycles);
       ok = named_sync_and(1, 128, ok);
       if (!ok) {
         if (threadIdx.x == 64) fail();
         break;
       }
       tc_fence_after();
-      const bool whole = kb0 == 0 && kb1 == KB;
-      const int R = m * kTcM + rl;
-      const int j0 = nt * NP;
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NP);
-      float* mine = a.part + ((size_t)(nt * G + c) * 2 + (si == 0 ? 0 : 1)) * (size_t)NP * kTcM + (size_t)rl * NP;
-      for (int jc = 0; jc < NP; jc += 16) {
-        float v[16];
-        tc_ld16(taddr + (uint32_t)jc, v);
-        tc_wait_ld();
-        if (whole) {
+      const int row = t * NP + j;  // activation (batch) row
+      const bool valid = j < NP && row < a.N;
+      float* orow = a.out + ((size_t)s * a.N + (size_t)(valid ? row : 0)) * a.rows;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kTcN);
+      for (int cc = 0; cc < kTcN / 32; ++cc) {
+        float v[32];
+        if (active) {
+          float w[16];
+          tc_ld16(taddr + (uint32_t)(cc * 32), w);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            if (j0 + jc + jj < a.N) tc_epi<EPI>(a, R, j0 + jc + jj, v[jj]);
-        } else {
+          for (int i = 0; i < 16; ++i) v[i] = w[i];
+          tc_ld16(taddr + (uint32_t)(cc * 32 + 16), w);
 #pragma unroll
-          for (int jj = 0; jj < 16; jj += 4)
-            *reinterpret_cast<float4*>(mine + jc + jj) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(ACCE0 + 8u * buf);
-      if (!whole) {
-        __threadfence();
-        named_sync(1, 128);
-        const int cf = tc_owner((int64_t)m * KB, T, G), cl = tc_owner((int64_t)m * KB + KB - 1, T, G);
-        if (threadIdx.x == 64) {
-          uint32_t* tk = a.ticket + (size_t)nt * a.MT + m;
-          const uint32_t old = atomicAdd(tk, 1u);
-          const int last = old == (uint32_t)(cl - cf) ? 1 : 0;
-          if (last) *tk = 0u;  // ready for the next launch
-          flags[1] = last;
+          for (int i = 0; i < 16; ++i) v[16 + i] = w[i];
+          tc_wait_ld();
+          if (!hi)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xchg[j * kXchgPitch + i] = v[i];
         }
         named_sync(1, 128);
-        if (flags[1]) {
-          __threadfence();
-          // 16 columns at a time; the loads of two contributors are in flight together, and each
-          // column adds the contributors in CTA order
-          for (int jc = 0; jc < NP && j0 + jc < a.N; jc += 16) {
-            float acc[16];
+        if (hi && active && valid) {
+          const int col0 = m * kTcN + cc * 32;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
-            for (int cc = cf; cc <= cl; cc += 2) {
-              float4 p0[4], p1[4];
-              const int slot0 = tc_first(T, G, cc) >= (int64_t)m * KB ? 0 : 1;
-              const float4* q0 = reinterpret_cast<const float4*>(
-                  a.part + ((size_t)(nt * G + cc) * 2 + slot0) * (size_t)NP * kTcM + (size_t)rl * NP + jc);
+          for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(v[i], xchg[j * kXchgPitch + i]);
+          if (vec && col0 + 32 <= a.rows) {
 #pragma unroll
-              for (int u = 0; u < 4; ++u) p0[u] = __ldcg(q0 + u);
-              const bool two = cc + 1 <= cl;
-              if (two) {
-                const int slot1 = tc_first(T, G, cc + 1) >= (int64_t)m * KB ? 0 : 1;
-                const float4* q1 = reinterpret_cast<const float4*>(
-                    a.part + ((size_t)(nt * G + cc + 1) * 2 + slot1) * (size_t)NP * kTcM + (size_t)rl * NP + jc);
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(orow + col0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) p1[u] = __ldcg(q1 + u);
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                acc[4 * u] += p0[u].x;
-                acc[4 * u + 1] += p0[u].y;
-                acc[4 * u + 2] += p0[u].z;
-                acc[4 * u + 3] += p0[u].w;
-              }
-              if (two) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  acc[4 * u] += p1[u].x;
-                  acc[4 * u + 1] += p1[u].y;
-                  acc[4 * u + 2] += p1[u].z;
-                  acc[4 * u + 3] += p1[u].w;
-                }
-              }
-            }
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              if (j0 + jc + jj < a.N) tc_epi<EPI>(a, R, j0 + jc + jj, acc[jj]);
+            for (int i = 0; i < 32; ++i)
+              if (col0 + i < a.rows) orow[col0 + i] = v[i];
           }
         }
         named_sync(1, 128);
       }
-      it += kb1 - kb0;
+      tc_fence_before();
+      mbar_arrive(ACCE0 + 8u * buf);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, a.tmem_cols);
+    tmem_dealloc(tmem, 2 * kTcN);
   }
 }
 
-// x' = x or RMSNorm(x), split into bf16 hi and lo rows; one CTA per activation row
-constexpr int kSplitThreads = 256;
+// ---------------------------------------------------------------------------------------
+// the readers of the split sums
+// ---------------------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kSplitThreads) tc_split_kernel(const TcSplitArgs a) {
+constexpr int kPrepThreads = 128;
+constexpr int kPrepCluster = 8;   // CTAs sharing one activation row (a thread-block cluster)
+constexpr int kPrepMaxV = 4;      // float4 of the row per thread (K <= 8 * 128 * 4 * 4 = 16384)
+constexpr int kMaxSplits = 16;  // K splits a reader adds (plan_tc stays within it)
+
+LLM_D float silu_mul(float g, float u) { return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u); }
+
+// sum_s p[s * stride] in split order; the loads are issued together
+LLM_D float4 sum_splits4(const float* p, size_t stride, int S) {
+  float4 t[kMaxSplits];
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s)
+    if (s < S) t[s] = *reinterpret_cast<const float4*>(p + s * stride);
+  float4 v = t[0];
+#pragma unroll
+  for (int s = 1; s < kMaxSplits; ++s)
+    if (s < S) {
+      v.x = __fadd_rn(v.x, t[s].x); v.y = __fadd_rn(v.y, t[s].y); v.z = __fadd_rn(v.z, t[s].z); v.w = __fadd_rn(v.w, t[s].w);
+    }
+  return v;
+}
+
+// grid (kPrepCluster, B): the CTAs of one row form a cluster and exchange their parts of the
+// sum of squares through distributed shared memory (added in rank order)
+__global__ void __launch_bounds__(kPrepThreads) tc_prep_kernel(const TcPrepArgs a) {
+  __shared__ float red[kPrepThreads / 32];
+  __shared__ float s_part;
   grid_dep_wait();
   grid_dep_launch();
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (b >= a.B) return;
-  const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)b * a.x_stride);
+  const int rank = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k4 = a.K >> 2;
-  __shared__ float red[kSplitThreads / 32];
-  __shared__ float s_inv;
-  float inv = 1.0f;
-  if (a.gain) {
-    float ss = 0.f;
-    for (int i = tid; i < k4; i += kSplitThreads) {
-      const float4 v = __ldg(xr + i);
+  const int per = (k4 + kPrepCluster - 1) / kPrepCluster;  // float4 of this CTA
+  const int i0 = rank * per, i1 = min(k4, i0 + per);
+  const size_t split = (size_t)a.B * a.part_rows;
+  float4 xv[kPrepMaxV];
+  float ss = 0.f;
+#pragma unroll
+  for (int r = 0; r < kPrepMaxV; ++r) {
+    const int i = i0 + tid + r * kPrepThreads;
+    if (i < i1) {
+      float4 v;
+      if (!a.part) {
+        v = *reinterpret_cast<const float4*>(a.x_in + (size_t)b * a.x_stride + 4 * i);
+      } else if (a.swiglu) {
+        const float* p = a.part + (size_t)b * a.part_rows + 8 * i;  // (g, u) pairs of 4 outputs
+        const float4 s0 = sum_splits4(p, split, a.S), s1 = sum_splits4(p + 4, split, a.S);
+        v = make_float4(silu_mul(s0.x, s0.y), silu_mul(s0.z, s0.w), silu_mul(s1.x, s1.y), silu_mul(s1.z, s1.w));
+      } else {
+        v = sum_splits4(a.part + (size_t)b * a.part_rows + 4 * i, split, a.S);
+        if (a.resid) {
+          const float4 rr = *reinterpret_cast<const float4*>(a.resid + (size_t)b * a.resid_stride + 4 * i);
+          v.x = __fadd_rn(rr.x, v.x); v.y = __fadd_rn(rr.y, v.y); v.z = __fadd_rn(rr.z, v.z); v.w = __fadd_rn(rr.w, v.w);
+        }
+      }
+      if (a.xout) *reinterpret_cast<float4*>(a.xout + (size_t)b * a.xout_stride + 4 * i) = v;
       ss = fmaf(v.x, v.x, ss);
       ss = fmaf(v.y, v.y, ss);
       ss = fmaf(v.z, v.z, ss);
       ss = fmaf(v.w, v.w, ss);
+      xv[r] = v;
     }
+  }
+  float inv = 1.0f;
+  if (a.gain) {
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
     if (tid == 0) {
-      float s = 0.f;
-      for (int w = 0; w < kSplitThreads / 32; ++w) s += red[w];
-      s_inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)a.K), a.eps)));
+      float t = 0.f;
+      for (int w = 0; w < kPrepThreads / 32; ++w) t += red[w];
+      s_part = t;
     }
-    __syncthreads();
-    inv = s_inv;
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    // lane r fetches rank r's part; the parts are then added in rank order
+    float pr = 0.f;
+    if (lane < kPrepCluster) {
+      uint32_t remote;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(&s_part)), "r"(lane));
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(pr) : "r"(remote) : "memory");
+    }
+    float tot = 0.f;
+#pragma unroll
+    for (int r = 0; r < kPrepCluster; ++r) tot += __shfl_sync(0xffffffffu, pr, r);
+    inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)a.K), a.eps)));
+    // no CTA leaves while another may still read its part
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   }
   uint16_t* hi = a.xs + (size_t)b * a.K;
   uint16_t* lo = a.xs + ((size_t)a.Ntot + b) * a.K;
-  for (int i = tid; i < k4; i += kSplitThreads) {
-    float4 v = __ldg(xr + i);
-    if (a.gain) {
-      const float4 g = __ldg(reinterpret_cast<const float4*>(a.gain) + i);
-      v.x = __fmul_rn(g.x, __fmul_rn(inv, v.x));
-      v.y = __fmul_rn(g.y, __fmul_rn(inv, v.y));
-      v.z = __fmul_rn(g.z, __fmul_rn(inv, v.z));
-      v.w = __fmul_rn(g.w, __fmul_rn(inv, v.w));
-    }
-    const float f[4] = {v.x, v.y, v.z, v.w};
-    uint16_t h[4], l[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      h[e] = f32_to_bf16(f[e]);
-      l[e] = f32_to_bf16(__fsub_rn(f[e], bf16_to_f32(h[e])));
+  for (int r = 0; r < kPrepMaxV; ++r) {
+    const int i = i0 + tid + r * kPrepThreads;
+    if (i < i1) {
+      float4 v = xv[r];
+      if (a.gain) {
+        const float4 g = *reinterpret_cast<const float4*>(a.gain + 4 * i);
+        v.x = __fmul_rn(g.x, __fmul_rn(inv, v.x));
+        v.y = __fmul_rn(g.y, __fmul_rn(inv, v.y));
+        v.z = __fmul_rn(g.z, __fmul_rn(inv, v.z));
+        v.w = __fmul_rn(g.w, __fmul_rn(inv, v.w));
+      }
+      const float f[4] = {v.x, v.y, v.z, v.w};
+      uint16_t h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[e] = f32_to_bf16(f[e]);
+        l[e] = f32_to_bf16(__fsub_rn(f[e], bf16_to_f32(h[e])));
+      }
+      reinterpret_cast<uint2*>(hi)[i] = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+      reinterpret_cast<uint2*>(lo)[i] = make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
     }
-    reinterpret_cast<uint2*>(hi)[i] = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
-    reinterpret_cast<uint2*>(lo)[i] = make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
+  }
+}
+
+// one thread per (row, RoPE pair): the split sums added in order, then as the GEMV's Q/K/V
+// epilogue (rot_lo = lo*cos - hi*sin, rot_hi = hi*cos + lo*sin; v unrotated; the cache element
+// rounded on write)
+__global__ void tc_qkv_kernel(const TcQkvArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int npairs = a.rows >> 1;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= a.B * npairs) return;
+  const int b = idx / npairs, pr = idx - b * npairs;
+  const int R = 2 * pr;
+  const size_t split = (size_t)a.B * a.rows;
+  const float* p = a.part + (size_t)b * a.rows + R;
+  float2 t[kMaxSplits];
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s)
+    if (s < a.S) t[s] = *reinterpret_cast<const float2*>(p + s * split);
+  float2 x = t[0];
+#pragma unroll
+  for (int s = 1; s < kMaxSplits; ++s)
+    if (s < a.S) {
+      x.x = __fadd_rn(x.x, t[s].x);
+      x.y = __fadd_rn(x.y, t[s].y);
+    }
+  const float x0 = x.x, x1 = x.y;
+  const int pos = a.step->pos, half = a.hd >> 1;
+  const int head = R / a.hd, e = (R - head * a.hd) >> 1;
+  const size_t row = (size_t)b;
+  if (head < a.H + a.kv) {
+    const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];
+    const float lo = __fadd_rn(__fmul_rn(x0, c), __fmul_rn(-x1, s));
+    const float hi = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
+    if (head < a.H) {
+      float* q = a.q_out + row * a.q_stride + (size_t)head * a.hd;
+      q[e] = lo;
+      q[e + half] = hi;
+    } else {
+      const size_t ci = ((row * a.kv + (size_t)(head - a.H)) * a.cap + pos) * a.hd;
+      store_elem<1>(a.kc, ci + e, lo);
+      store_elem<1>(a.kc, ci + e + half, hi);
+    }
+  } else {
+    const size_t ci = ((row * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pos) * a.hd;
+    store_elem<1>(a.vc, ci + e, x0);
+    store_elem<1>(a.vc, ci + e + half, x1);
+  }
+}
+
+__global__ void tc_sum_kernel(const float* part, int S, int B, int rows, float* out, int out_stride) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int r4 = rows >> 2;
+  const size_t split = (size_t)B * rows;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < B * r4; idx += gridDim.x * blockDim.x) {
+    const int b = idx / r4, i = idx - b * r4;
+    *reinterpret_cast<float4*>(out + (size_t)b * out_stride + 4 * i) = sum_splits4(part + (size_t)b * rows + 4 * i, split, S);
   }
 }
 
@@ -425,74 +473,94 @@ bool tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ou
   return make_map_2d(map, base, 2, inner, outer, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+int tc_ntot(int B) {
+  const int np = B >= kTcRows ? kTcRows : (B + 15) / 16 * 16;
+  return (B + np - 1) / np * np;
+}
+
 TcPlan plan_tc(int rows, int K, int B, int num_sms) {
   TcPlan p{};
-  p.NP = (B + 15) / 16 * 16;
-  if (p.NP > kTcMaxNP) p.NP = kTcMaxNP;
+  p.NP = B >= kTcRows ? kTcRows : (B + 15) / 16 * 16;
   p.ntiles = (B + p.NP - 1) / p.NP;
   p.Ntot = p.ntiles * p.NP;
-  p.MT = (rows + kTcM - 1) / kTcM;
+  p.MT = (rows + kTcN - 1) / kTcN;
   p.KB = (K + kTcK - 1) / kTcK;
-  const int64_t T = (int64_t)p.MT * p.KB;
-  p.grid = (int)(T < num_sms ? T : num_sms);
-  const size_t stage = 16384 + 2 * (size_t)p.NP * 128;
-  int st = (int)((200 * 1024) / stage);
-  p.stages = st > 8 ? 8 : st < 2 ? 2 : st;
-  uint32_t cols = 32;
-  while (cols < 2u * (uint32_t)p.NP) cols <<= 1;
-  p.tmem_cols = cols;
-  // at least 116 KB keeps one CTA per SM, so tensor-memory allocations never queue
-  size_t smem = 1024 + (size_t)p.stages * stage + 16 * (size_t)p.stages + 64;
-  if (smem < 116 * 1024) smem = 116 * 1024;
-  p.smem = smem;
+  // splits: the most even fill of the SMs (units / (waves * SMs)), at least 4 K blocks a split
+  const int base = p.ntiles * p.MT;
+  double best = -1.0;
+  p.S = 1;
+  for (int S = 1; S <= kMaxSplits && S <= p.KB; ++S) {
+    if (S > 1 && p.KB / S < 4) break;
+    const long long U = (long long)base * S;
+    const long long waves = (U + num_sms - 1) / num_sms;
+    const double eff = (double)U / (double)(waves * num_sms);
+    if (eff > best + 1e-9) {
+      best = eff;
+      p.S = S;
+    }
+  }
+  p.units = base * p.S;
+  p.grid = p.units < num_sms ? p.units : num_sms;
+  p.stages = kTcStages;
+  p.smem = 1024 + (size_t)kTcStages * kTcStage + (size_t)kTcRows * kXchgPitch * 4 + 16 * kTcStages + 64;
   return p;
 }
 
-using TcFn = void (*)(const CUtensorMap, const CUtensorMap, const TcArgs);
-
-static TcFn pick_tc(int epi) {
-  switch (epi) {
-    case EPI_QKV: return tc_gemm_kernel<EPI_QKV>;
-    case EPI_SWIGLU: return tc_gemm_kernel<EPI_SWIGLU>;
-    case EPI_RESID: return tc_gemm_kernel<EPI_RESID>;
-    default: return tc_gemm_kernel<EPI_STORE>;
-  }
-}
-
 cudaError_t tc_prepare(int max_smem_optin) {
-  for (int epi = 0; epi < 4; ++epi) {
-    cudaError_t e = cudaFuncSetAttribute(pick_tc(epi), cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin);
-    if (e != cudaSuccess) return e;
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin);
+  return e;
+}
+
+static cudaLaunchConfig_t cfg_of(dim3 grid, int threads, size_t smem, cudaStream_t s, bool pdl,
+                                 cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+cudaError_t launch_tc_prep(const TcPrepArgs& a, cudaStream_t s, bool pdl) {
+  if (a.K > kPrepCluster * kPrepThreads * kPrepMaxV * 4 || (a.K & 3) || a.S > kMaxSplits) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = cfg_of(dim3(kPrepCluster, a.B), kPrepThreads, 0, s, pdl, attr);
+  if (a.gain) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kPrepCluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
-  return cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, tc_prep_kernel, a);
 }
 
-cudaError_t launch_tc_split(const TcSplitArgs& a, cudaStream_t s, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B);
-  cfg.blockDim = dim3(kSplitThreads);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_split_kernel, a);
-}
-
-cudaError_t launch_tc_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, const TcPlan& p, int epi,
+cudaError_t launch_tc_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, const TcPlan& p,
                            cudaStream_t s, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid, p.ntiles);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = p.smem;
-  cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pick_tc(epi), tw, tx, a);
+  const cudaLaunchConfig_t cfg = cfg_of(dim3(p.grid), kTcThreads, p.smem, s, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, tw, tx, a);
+}
+
+cudaError_t launch_tc_qkv(const TcQkvArgs& a, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  const int n = a.B * (a.rows >> 1);
+  const cudaLaunchConfig_t cfg = cfg_of(dim3((n + 255) / 256), 256, 0, s, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, tc_qkv_kernel, a);
+}
+
+cudaError_t launch_tc_sum(const float* part, int S, int B, int rows, float* out, int out_stride, cudaStream_t s,
+                          bool pdl) {
+  cudaLaunchAttribute attr[1];
+  const int n = B * (rows >> 2);
+  int blocks = (n + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  const cudaLaunchConfig_t cfg = cfg_of(dim3(blocks), 256, 0, s, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, tc_sum_kernel, part, S, B, rows, out, out_stride);
 }
 
 }  // namespace llm

@@ -3,33 +3,53 @@
 #include <cuda.h>
 
 #include "common.cuh"
-#include "gemv.cuh"
 
 namespace llm {
 
-constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kTcM = 128;         // weight rows per tile (TMEM lanes)
+constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 read the accumulators
+constexpr int kTcN = 256;         // weight rows per tile (the MMA's N)
 constexpr int kTcK = 64;          // K elements per stage (one 128-byte swizzle row)
-constexpr int kTcMaxNP = 256;     // columns per tile
+constexpr int kTcRows = 64;       // activation rows per tile (hi in MMA rows 0..63, lo in 64..127)
 constexpr int kTcDefaultMinBatch = 16;  // rows from which a step uses the tensor cores
 
+// out[s][j][r] = sum over K block range s of W[r][c] * x'[j][c]: raw split sums, f32
 struct TcArgs {
   int32_t rows, K;        // W [rows][K] bf16, row-major
-  int32_t N;              // valid columns (batch rows) in total
-  int32_t NP;             // columns per tile: a multiple of 16, at most 256
-  int32_t Ntot;           // columns of the split activations per half (a multiple of NP)
-  int32_t MT, KB;         // 128-row tiles, 64-element K blocks
+  int32_t N;              // activation rows (batch)
+  int32_t NP;             // activation rows per tile: a multiple of 16, at most 64
+  int32_t Ntot;           // rows of each half (hi, lo) of the split activations (ntiles * NP)
+  int32_t MT, KB, S;      // 256-row weight tiles, 64-element K blocks, K splits
+  int32_t units;          // ntiles * MT * S
   int32_t stages;         // shared-memory pipeline depth
-  uint32_t tmem_cols;     // tensor-memory columns allocated (two accumulators of NP)
-  float* part;            // split partials [n tiles][grid][2][128 rows][NP]
-  uint32_t* ticket;       // [n tiles][MT], zero between launches
+  float* out;             // [S][N][rows]
   int32_t* status;        // device error flag
-  const StepState* step;
-  // epilogue (as GemvArgs)
-  float* out;
-  int32_t out_stride;
+};
+
+// the activations of a projection, reduced and normalized, split into bf16 hi and lo:
+//   x = resid + sum_s part[s]         (part given; resid optional)
+//   x = silu(g) * u, (g, u) = sum_s part[s] rows (2i, 2i + 1)   (swiglu)
+//   x = x_in                          (part null)
+// then optionally x is written to xout, and x' = norm ? gain * (x * inv_rms) : x is split
+struct TcPrepArgs {
+  const float* x_in;
+  int32_t x_stride;
+  const float* part;      // [S][B][part_rows]
+  int32_t S, part_rows;
+  int32_t swiglu;
   const float* resid;
   int32_t resid_stride;
+  float* xout;
+  int32_t xout_stride;
+  const float* gain;      // RMSNorm gains [K] or null
+  float eps;
+  int32_t K, B, Ntot;
+  uint16_t* xs;           // [2][Ntot][K]
+};
+
+// Q/K/V from split sums: RoPE on q and k, q to q_out, k and v into the cache at pos
+struct TcQkvArgs {
+  const float* part;      // [S][B][rows], rows in RoPE pairs (q heads, k heads, v heads)
+  int32_t S, rows, B;
   float* q_out;
   int32_t q_stride;
   void* kc;
@@ -37,27 +57,19 @@ struct TcArgs {
   int32_t H, kv, hd, cap;
   const float* rope_cos;
   const float* rope_sin;
-};
-
-struct TcSplitArgs {
-  const float* x;         // [B][x_stride] f32
-  int32_t x_stride;
-  const float* gain;      // RMSNorm gains [K] or nullptr (no norm)
-  float eps;
-  int32_t K, B, Ntot;
-  uint16_t* xs;           // [2][Ntot][K] bf16: hi rows, then lo rows
+  const StepState* step;
 };
 
 struct TcPlan {
-  int NP, Ntot, MT, KB, grid, ntiles, stages;
-  uint32_t tmem_cols;
+  int NP, Ntot, ntiles, MT, KB, S, units, grid, stages;
   size_t smem;
 };
 
-// the tensor-core path needs bf16 weights and rows of K a multiple of 8 elements (16 bytes)
 bool tc_available();
 cudaError_t tc_prepare(int max_smem_optin);
 TcPlan plan_tc(int rows, int K, int B, int num_sms);
+// rows of the split activations buffer for B rows, per half
+int tc_ntot(int B);
 // 2D bf16 tensor map over [outer][inner] (row pitch inner elements), box box_inner x box_outer,
 // 128-byte swizzle
 bool tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
@@ -65,8 +77,12 @@ bool tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ou
 // general 2D tensor map (elements of elem_bytes: 2 = bf16, 4 = f32) with the given swizzle
 bool make_map_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
-cudaError_t launch_tc_split(const TcSplitArgs& a, cudaStream_t s, bool pdl);
-cudaError_t launch_tc_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, const TcPlan& p, int epi,
+cudaError_t launch_tc_prep(const TcPrepArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_tc_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, const TcPlan& p,
                            cudaStream_t s, bool pdl);
+cudaError_t launch_tc_qkv(const TcQkvArgs& a, cudaStream_t s, bool pdl);
+// out[j][r] = sum_s part[s][j][r] (f32, rows a multiple of 4)
+cudaError_t launch_tc_sum(const float* part, int S, int B, int rows, float* out, int out_stride, cudaStream_t s,
+                          bool pdl);
 
 }  // namespace llm

@@ -193,8 +193,7 @@ struct llm_handle {
   std::vector<TcMaps> tmaps;
   CUtensorMap tmap_head;
   uint16_t* tc_xs = nullptr;    // split activations [2][Ntot][max(d, f)]
-  float* tc_part = nullptr;     // stream-K partials
-  uint32_t* tc_ticket = nullptr;
+  float* tc_part = nullptr;     // split sums of the last projection [S][B][rows]
   std::map<std::pair<int, int>, CUtensorMap> xmaps;  // (K, B) -> map over tc_xs
   std::vector<int32_t> filled;
   std::map<GraphKey, std::pair<cudaGraphExec_t, int>> graphs;  // executable graph, kernels in it
@@ -364,27 +363,49 @@ const CUtensorMap* tc_xmap(llm_handle* h, int K, int B) {
   auto key = std::make_pair(K, B);
   auto it = h->xmaps.find(key);
   if (it != h->xmaps.end()) return &it->second;
-  const TcPlan p = plan_tc(kTcM, K, B, h->num_sms);
+  const TcPlan p = plan_tc(kTcN, K, B, h->num_sms);
   CUtensorMap m;
   if (!tc_make_map(&m, h->tc_xs, (uint64_t)K, 2 * (uint64_t)p.Ntot, kTcK, (uint32_t)p.NP)) return nullptr;
   return &h->xmaps.emplace(key, m).first->second;
 }
 
-// x' = x or RMSNorm(x) split into bf16 halves, then out = W x' on the tensor cores with epilogue
-// epi; `a` carries the epilogue's pointers
-llm_status launch_tc(llm_handle* h, const CUtensorMap& tw, int rows, int K, const float* x, int x_stride,
-                     const float* gain, int epi, TcArgs a, int B, bool pdl) {
+// the reader of a projection's split sums: x reduced (plus the residual, or SwiGLU), optionally
+// written to xout and normalized, then split into bf16 halves for the next projection
+struct PrepIn {
+  const float* x = nullptr;  // plain rows (no split sums)
+  int x_stride = 0;
+  int src_rows = 0, src_K = 0;  // shape of the projection whose split sums are read
+  bool swiglu = false;
+  const float* resid = nullptr;
+  float* xout = nullptr;
+  const float* gain = nullptr;
+};
+
+llm_status launch_prep(llm_handle* h, const PrepIn& in, int K, int B, bool pdl) {
+  TcPrepArgs pa = {};
+  pa.x_in = in.x; pa.x_stride = in.x_stride;
+  if (!in.x) {
+    const TcPlan src = plan_tc(in.src_rows, in.src_K, B, h->num_sms);
+    pa.part = h->tc_part; pa.S = src.S; pa.part_rows = in.src_rows;
+  }
+  pa.swiglu = in.swiglu ? 1 : 0;
+  pa.resid = in.resid; pa.resid_stride = K;
+  pa.xout = in.xout; pa.xout_stride = K;
+  pa.gain = in.gain; pa.eps = h->cfg.eps;
+  pa.K = K; pa.B = B; pa.Ntot = tc_ntot(B); pa.xs = h->tc_xs;
+  CUDA_TRY(h, launch_tc_prep(pa, h->stream, pdl));
+  return LLM_OK;
+}
+
+// out (split sums, [S][B][rows]) = W x' for the split activations of K-wide rows
+llm_status launch_gemm(llm_handle* h, const CUtensorMap& tw, int rows, int K, int B, float* out, bool pdl) {
   const TcPlan p = plan_tc(rows, K, B, h->num_sms);
   const CUtensorMap* tx = tc_xmap(h, K, B);
   if (!tx) return fail(h, LLM_ERR_CUDA, "tensor map of the activations (K %d, B %d)", K, B);
-  TcSplitArgs sa = {};
-  sa.x = x; sa.x_stride = x_stride; sa.gain = gain; sa.eps = h->cfg.eps;
-  sa.K = K; sa.B = B; sa.Ntot = p.Ntot; sa.xs = h->tc_xs;
-  CUDA_TRY(h, launch_tc_split(sa, h->stream, pdl));
-  a.rows = rows; a.K = K; a.N = B; a.NP = p.NP; a.Ntot = p.Ntot; a.MT = p.MT; a.KB = p.KB;
-  a.stages = p.stages; a.tmem_cols = p.tmem_cols; a.part = h->tc_part; a.ticket = h->tc_ticket;
-  a.status = h->status; a.step = h->st;
-  CUDA_TRY(h, launch_tc_gemm(tw, *tx, a, p, epi, h->stream, pdl));
+  TcArgs a = {};
+  a.rows = rows; a.K = K; a.N = B; a.NP = p.NP; a.Ntot = p.Ntot; a.MT = p.MT; a.KB = p.KB; a.S = p.S;
+  a.units = p.units; a.stages = p.stages; a.out = out; a.status = h->status;
+  CUDA_TRY(h, launch_tc_gemm(tw, *tx, a, p, h->stream, pdl));
   return LLM_OK;
 }
 
@@ -410,9 +431,15 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
   }
   const bool tc = h->tc_min > 0 && B >= h->tc_min;
   if (which == K_HEAD && tc) {
-    TcArgs a = {};
-    a.out = h->logits; a.out_stride = h->V;
-    return launch_tc(h, h->tmap_head, h->V, h->d, h->xa, h->d, h->lnf, EPI_STORE, a, B, pdl);
+    // x = the last layer's residual stream (its down projection's split sums + x1), final norm
+    PrepIn in;
+    in.src_rows = h->d; in.src_K = h->f; in.resid = h->xb; in.xout = h->xa; in.gain = h->lnf;
+    TRY(launch_prep(h, in, h->d, B, pdl));
+    const TcPlan p = plan_tc(h->V, h->d, B, h->num_sms);
+    if (p.S == 1) return launch_gemm(h, h->tmap_head, h->V, h->d, B, h->logits, pdl);
+    TRY(launch_gemm(h, h->tmap_head, h->V, h->d, B, h->tc_part, pdl));
+    CUDA_TRY(h, launch_tc_sum(h->tc_part, p.S, B, h->V, h->logits, h->V, h->stream, pdl));
+    return LLM_OK;
   }
   if (which == K_HEAD) {
     const GemvPlan p_h = plan_gemv(h->V, h->d, 1, wt, B, h->num_sms, cps);
@@ -433,24 +460,42 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
   char* vcl = (char*)h->vc + (size_t)l * h->layer_cache_elems * h->es;
   if (tc && which != K_ATTN) {
     const TcMaps& tm = h->tmaps[l];
-    TcArgs a = {};
+    const int qkv_rows = (h->H + 2 * c.kv_heads) * h->hd;
+    PrepIn in;
     if (which == K_QKV) {
-      a.q_out = h->q; a.q_stride = h->d; a.kc = kcl; a.vc = vcl;
-      a.H = h->H; a.kv = c.kv_heads; a.hd = h->hd; a.cap = c.max_seq;
-      a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin;
-      return launch_tc(h, tm.qkv, (h->H + 2 * c.kv_heads) * h->hd, h->d, h->xa, h->d, w.ln1, EPI_QKV, a, B, pdl);
+      // x: the embedding (layer 0) or the previous layer's down split sums + x1; then norm 1
+      if (l == 0) {
+        in.x = h->xa; in.x_stride = h->d;
+      } else {
+        in.src_rows = h->d; in.src_K = h->f; in.resid = h->xb; in.xout = h->xa;
+      }
+      in.gain = w.ln1;
+      TRY(launch_prep(h, in, h->d, B, pdl));
+      TRY(launch_gemm(h, tm.qkv, qkv_rows, h->d, B, h->tc_part, pdl));
+      TcQkvArgs qa = {};
+      qa.part = h->tc_part; qa.S = plan_tc(qkv_rows, h->d, B, h->num_sms).S; qa.rows = qkv_rows; qa.B = B;
+      qa.q_out = h->q; qa.q_stride = h->d; qa.kc = kcl; qa.vc = vcl;
+      qa.H = h->H; qa.kv = c.kv_heads; qa.hd = h->hd; qa.cap = c.max_seq;
+      qa.rope_cos = h->rope_cos; qa.rope_sin = h->rope_sin; qa.step = h->st;
+      CUDA_TRY(h, launch_tc_qkv(qa, h->stream, pdl));
+      return LLM_OK;
     }
     if (which == K_O) {
-      a.out = h->xb; a.out_stride = h->d; a.resid = h->xa; a.resid_stride = h->d;
-      return launch_tc(h, tm.o, h->d, h->d, h->attn, h->d, nullptr, EPI_RESID, a, B, pdl);
+      in.x = h->attn; in.x_stride = h->d;
+      TRY(launch_prep(h, in, h->d, B, pdl));
+      return launch_gemm(h, tm.o, h->d, h->d, B, h->tc_part, pdl);
     }
     if (which == K_GATEUP) {
-      a.out = h->m; a.out_stride = h->f;
-      return launch_tc(h, tm.gu, 2 * h->f, h->d, h->xb, h->d, w.ln2, EPI_SWIGLU, a, B, pdl);
+      // x1 = x + o_proj split sums (kept in xb for the down residual), norm 2
+      in.src_rows = h->d; in.src_K = h->d; in.resid = h->xa; in.xout = h->xb; in.gain = w.ln2;
+      TRY(launch_prep(h, in, h->d, B, pdl));
+      return launch_gemm(h, tm.gu, 2 * h->f, h->d, B, h->tc_part, pdl);
     }
     if (which == K_DOWN) {
-      a.out = h->xa; a.out_stride = h->d; a.resid = h->xb; a.resid_stride = h->d;
-      return launch_tc(h, tm.down, h->d, h->f, h->m, h->f, nullptr, EPI_RESID, a, B, pdl);
+      // m = silu(gate) * up from the gate/up split sums
+      in.src_rows = 2 * h->f; in.src_K = h->d; in.swiglu = true; in.xout = h->m;
+      TRY(launch_prep(h, in, h->f, B, pdl));
+      return launch_gemm(h, tm.down, h->d, h->f, B, h->tc_part, pdl);
     }
   }
   if (which == K_QKV) {
@@ -726,7 +771,8 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   if ((ce = gemv_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("gemv kernel attributes", ce);
   // tensor-core path: bf16 weights, rows a whole number of 16-byte chunks (checked above)
   const int tc_min = c.tc_min_batch > 0 ? c.tc_min_batch : kTcDefaultMinBatch;
-  if (h->wt && tc_min <= c.max_batch && tc_available()) {
+  // (debug_trace handles keep every step on the GEMV: the traced buffers are written in order there)
+  if (h->wt && !c.debug_trace && tc_min <= c.max_batch && tc_available()) {
     if ((ce = tc_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("tensor-core kernel attributes", ce);
     h->tc_min = tc_min;
   }
@@ -774,7 +820,8 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     attn_cluster_merge(h->wt, h->hd, c.group, ns, b * c.kv_heads);  // device queries before any capture
   }
   h->part_ns = maxns;
-  if ((st = dalloc(h, &h->part, B * h->H * maxns * (h->hd + 2) * 4)) ||
+  const int slots = attn_part_slots(h->wt, h->hd, maxns);
+  if ((st = dalloc(h, &h->part, B * h->H * slots * (h->hd + 2) * 4)) ||
       (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, sizeof(StepState))) ||
       (st = dalloc(h, &h->status, 16)) || (st = dalloc(h, &h->tok_buf, B * 4)) || (st = dalloc(h, &h->u_buf, B * 4)) ||
       (st = dalloc(h, &h->ids_buf, B * 4)))
@@ -784,27 +831,32 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
       (st = dalloc(h, &h->s_pre, B * h->V_pad * 4)) || (st = dalloc(h, &h->s_hist, B * kSampleHistPerRow * 4)))
     return bail(st);
   if (h->tc_min) {
-    const TcPlan pm = plan_tc(kTcM, std::max(h->d, h->f), c.max_batch, h->num_sms);
-    const int64_t rows_max = std::max<int64_t>(std::max<int64_t>(h->V, 2 * (int64_t)h->f), (int64_t)(h->H + 2 * c.kv_heads) * h->hd);
-    const size_t tickets = (size_t)pm.ntiles * (size_t)((rows_max + kTcM - 1) / kTcM);
-    if ((st = dalloc(h, &h->tc_xs, (size_t)2 * pm.Ntot * std::max(h->d, h->f) * 2)) ||
-        (st = dalloc(h, &h->tc_part, (size_t)pm.ntiles * h->num_sms * 2 * pm.NP * kTcM * 4)) ||
-        (st = dalloc(h, &h->tc_ticket, tickets * 4)))
-      return bail(st);
-    if (cudaMemsetAsync(h->tc_xs, 0, (size_t)2 * pm.Ntot * std::max(h->d, h->f) * 2, h->stream) != cudaSuccess ||
-        cudaMemsetAsync(h->tc_ticket, 0, tickets * 4, h->stream) != cudaSuccess)
+    // split activations for up to max_batch rows; split sums of the largest projection
+    const int64_t qkv_rows = (int64_t)(h->H + 2 * c.kv_heads) * h->hd;
+    size_t part = 0;
+    for (int b = h->tc_min; b <= c.max_batch; ++b) {
+      const int64_t shapes[5][2] = {{qkv_rows, h->d}, {h->d, h->d}, {2 * (int64_t)h->f, h->d}, {h->d, h->f}, {h->V, h->d}};
+      for (auto& sh : shapes) {
+        const TcPlan p = plan_tc((int)sh[0], (int)sh[1], b, h->num_sms);
+        part = std::max(part, (size_t)p.S * b * (size_t)sh[0]);
+      }
+    }
+    const size_t xs_elems = (size_t)2 * tc_ntot(c.max_batch) * std::max(h->d, h->f);
+    if ((st = dalloc(h, &h->tc_xs, xs_elems * 2)) || (st = dalloc(h, &h->tc_part, part * 4))) return bail(st);
+    if (cudaMemsetAsync(h->tc_xs, 0, xs_elems * 2, h->stream) != cudaSuccess ||
+        cudaMemsetAsync(h->tc_part, 0, part * 4, h->stream) != cudaSuccess)
       return cuda_bail("clearing the tensor-core scratch", cudaGetLastError());
     h->tmaps.resize(h->L);
     bool ok = true;
     for (int l = 0; l < h->L && ok; ++l) {
       const LayerW& w = h->lw[l];
       TcMaps& m = h->tmaps[l];
-      ok = tc_make_map(&m.qkv, w.qkv, h->d, (uint64_t)(h->H + 2 * c.kv_heads) * h->hd, kTcK, kTcM) &&
-           tc_make_map(&m.o, w.o, h->d, h->d, kTcK, kTcM) && tc_make_map(&m.gu, w.gu, h->d, 2 * (uint64_t)h->f, kTcK, kTcM) &&
-           tc_make_map(&m.down, w.down, h->f, h->d, kTcK, kTcM);
+      ok = tc_make_map(&m.qkv, w.qkv, h->d, (uint64_t)qkv_rows, kTcK, kTcN) &&
+           tc_make_map(&m.o, w.o, h->d, h->d, kTcK, kTcN) && tc_make_map(&m.gu, w.gu, h->d, 2 * (uint64_t)h->f, kTcK, kTcN) &&
+           tc_make_map(&m.down, w.down, h->f, h->d, kTcK, kTcN);
     }
     // a shape the tensor maps cannot describe keeps every step on the GEMV
-    if (!ok || !tc_make_map(&h->tmap_head, h->head, h->d, h->V, kTcK, kTcM)) h->tc_min = 0;
+    if (!ok || !tc_make_map(&h->tmap_head, h->head, h->d, h->V, kTcK, kTcN)) h->tc_min = 0;
   }
   if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * 5 * B * std::max(h->d, h->f) * 4))) return bail(st);
   if (cudaMemsetAsync(h->ticket, 0, B * c.kv_heads * 4, h->stream) != cudaSuccess ||
