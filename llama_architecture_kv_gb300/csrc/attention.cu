@@ -516,26 +516,33 @@ struct MmaShape {
   static constexpr int ROWB = HD * 2;
   static constexpr int NBOX = ROWB / 128;   // 128-byte column boxes per row
   static constexpr int BUF = 2 * kMmaChunk * ROWB;
-  static constexpr int NR = HD <= 64 ? 3 : 2;  // ring slots per warp (within the shared memory)
   static constexpr int QP = HD + 8;         // padded query row (elements): ldmatrix rows on distinct banks
   static constexpr int NTO = HD / 8;        // output n-tiles
   static constexpr int KS = HD / 16;        // k-steps of the scores
 };
 
+// shared memory of the kernel with nr ring slots per warp
+template <int HD>
+LLM_HD size_t attn_mma_smem_nr(int g, int nr) {
+  using M = MmaShape<HD>;
+  size_t s = 1024 + (size_t)kMmaWarps * nr * M::BUF;
+  s += 2 * 16 * (size_t)M::QP * 2;            // queries hi, lo
+  s += (size_t)kMmaWarps * g * (HD + 2) * 4;  // warp partials
+  s += (size_t)g * (HD + 2) * 4;              // CTA partial
+  s += (size_t)g * 64 * 4;                    // merge factors
+  s = (s + 7) & ~(size_t)7;
+  s += (size_t)kMmaWarps * nr * 8;            // mbarriers
+  return s;
+}
+// ring slots per warp: three for 64-dimension heads, two for 128 (measured faster than three at
+// both batch 1 and 32 on the 8B shape), two wherever three would not fit
+template <int HD>
+LLM_HD int attn_mma_nr(int g) { return HD <= 64 && attn_mma_smem_nr<HD>(g, 3) <= 232448 - 64 ? 3 : 2; }
+
 constexpr int kMmaMaxSplits = 64;  // splits of one (row, kv head) the persistent kernel merges
 
 template <int HD>
-LLM_HD size_t attn_mma_smem(int g) {
-  using M = MmaShape<HD>;
-  size_t s = 1024 + (size_t)kMmaWarps * M::NR * M::BUF;
-  s += 2 * 2 * 16 * (size_t)M::QP * 2;        // queries hi, lo (two units)
-  s += (size_t)kMmaWarps * g * (HD + 2) * 4;  // warp partials
-  s += (size_t)g * (HD + 2) * 4;              // CTA partial
-  s += (size_t)g * kMmaMaxSplits * 4;         // merge factors
-  s = (s + 7) & ~(size_t)7;
-  s += (size_t)kMmaWarps * M::NR * 8;         // mbarriers
-  return s;
-}
+LLM_HD size_t attn_mma_smem(int g) { return attn_mma_smem_nr<HD>(g, attn_mma_nr<HD>(g)); }
 
 // byte offset of 16-byte piece c of row r in a chunk tile stored as 128-byte-wide swizzled boxes
 // of kMmaChunk rows
@@ -552,8 +559,9 @@ template <int HD>
 __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
   using M = MmaShape<HD>;
-  constexpr int ROWB = M::ROWB, BUF = M::BUF, QP = M::QP, NTO = M::NTO, KS = M::KS, NR = M::NR;
+  constexpr int ROWB = M::ROWB, BUF = M::BUF, QP = M::QP, NTO = M::NTO, KS = M::KS;
   constexpr int CH = kMmaChunk;
+  const int NR = attn_mma_nr<HD>(a.g);
   extern __shared__ unsigned char araw[];
   const uint32_t s_raw = smem_u32(araw);
   unsigned char* base = araw + (((s_raw + 1023u) & ~1023u) - s_raw);
@@ -564,8 +572,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   const int gid = lane >> 2, tig = lane & 3;
   const int NT = blockDim.x, NW = NT >> 5;
   const int c = blockIdx.x, G = gridDim.x;
-  uint16_t* qbase = reinterpret_cast<uint16_t*>(base + (size_t)kMmaWarps * NR * BUF);  // [2][hi, lo][16][QP]
-  float* wpart = reinterpret_cast<float*>(qbase + 2 * 2 * 16 * QP);                   // [NW][g][HD+2]
+  uint16_t* qbase = reinterpret_cast<uint16_t*>(base + (size_t)kMmaWarps * NR * BUF);  // [hi, lo][16][QP]
+  float* wpart = reinterpret_cast<float*>(qbase + 2 * 16 * QP);                       // [NW][g][HD+2]
   float* mypart = wpart + NW * g * (HD + 2);                                           // [g][HD+2]
   float* fac = mypart + g * (HD + 2);                                                  // [g][kMmaMaxSplits]
   const uint32_t bars = (smem_u32(fac + g * kMmaMaxSplits) + 7u) & ~7u;
@@ -633,8 +641,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   grid_dep_launch();
   if (lane == 0)
     while (issued < NR && ist < c1) issue();
-  auto load_q = [&](int buf, int b, int j) {  // queries of (b, j) as bf16 hi + lo, rows g..15 zero
-    uint16_t* qh = qbase + buf * 2 * 16 * QP;
+  auto load_q = [&](int b, int j) {  // queries of (b, j) as bf16 hi + lo, rows g..15 zero
+    uint16_t* qh = qbase;
     uint16_t* ql = qh + 16 * QP;
     const float* qsrc = a.q + (size_t)b * a.q_stride + (size_t)j * g * HD;
     for (int i = tid; i < 16 * HD / 2; i += NT) {
@@ -655,7 +663,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     int b, j, k0, k1;
     long long nx;
     seg(c0, b, j, k0, k1, nx);
-    load_q(0, b, j);
+    load_q(b, j);
   }
   __syncthreads();
 
@@ -672,7 +680,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     int b, j, k0, k1;
     seg(st, b, j, k0, k1, next);
     const int p0 = k0 * CH, p1 = min(npos, k1 * CH), nch = k1 - k0;
-    const uint16_t* qh = qbase + (lu & 1) * 2 * 16 * QP;
+    const uint16_t* qh = qbase;
     const uint32_t qh_addr = smem_u32(qh + qr * QP + qc), ql_addr = smem_u32(qh + 16 * QP + qr * QP + qc);
     float o[NTO][4];
 #pragma unroll
@@ -829,11 +837,11 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
       }
       mypart[idx] = r;
     }
-    if (next < c1) {
+    if (next < c1) {  // (every warp is past this segment's chunks: the query buffer is free)
       int b2, j2, k02, k12;
       long long nx2;
       seg(next, b2, j2, k02, k12, nx2);
-      load_q((lu + 1) & 1, b2, j2);
+      load_q(b2, j2);
     }
     __syncthreads();
     float* outb = a.out + (size_t)b * a.out_stride + (size_t)j * g * HD;

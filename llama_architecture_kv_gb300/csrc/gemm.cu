@@ -37,8 +37,7 @@ namespace llm {
 constexpr uint64_t kTcWaitCycles = 4000000000ull;  // SM cycles: about 2 s at 2 GHz
 constexpr int kTcStages = 4;
 constexpr uint32_t kTcA = 128 * 128;               // activation tile: 128 MMA rows x 128 bytes
-constexpr uint32_t kTcW = kTcN * 128;              // weight tile: 256 rows x 128 bytes
-constexpr uint32_t kTcStage = kTcA + kTcW;
+constexpr uint32_t kTcStageMax = kTcA + kTcN * 128;  // activation tile + a weight tile of up to 256 rows
 constexpr int kXchgPitch = 33;                     // floats per exchange row (conflict-free)
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -47,7 +46,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t s_raw = smem_u32(tc_smem);
   const uint32_t s_base = (s_raw + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 bytes
   uint8_t* g_base = tc_smem + (s_base - s_raw);
-  const int NP = a.NP, KB = a.KB, S = a.S, MT = a.MT;
+  const int NP = a.NP, KB = a.KB, S = a.S, MT = a.MT, NT = a.n_tile;
+  const uint32_t kTcW = (uint32_t)NT * 128u;   // weight tile: NT rows x 128 bytes
+  const uint32_t kTcStage = kTcA + kTcW;
   float* xchg = reinterpret_cast<float*>(g_base + kTcStages * kTcStage);  // [64][kXchgPitch]
   const uint32_t bars = s_base + kTcStages * kTcStage + kTcRows * kXchgPitch * 4;
   // barriers: full[stages], empty[stages], acc_full[2], acc_empty[2], drain
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int pu = u, pt = t, pm = m, pk0 = kb0, pk1 = kb1, pk = kb;
         while (npre < kTcStages && pu < a.units) {
           mbar_expect_tx(FULL0 + 8u * npre, kTcW + xbytes);
-          tma_load_2d(s_base + (uint32_t)npre * kTcStage + kTcA, &tw, FULL0 + 8u * npre, pk * kTcK, pm * kTcN);
+          tma_load_2d(s_base + (uint32_t)npre * kTcStage + kTcA, &tw, FULL0 + 8u * npre, pk * kTcK, pm * NT);
           ++npre;
           if (++pk == pk1) {
             pu += G;
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t sa = s_base + (uint32_t)stg * kTcStage;
         if (issued >= npre) {
           mbar_expect_tx(FULL0 + 8u * stg, kTcW + xbytes);
-          tma_load_2d(sa + kTcA, &tw, FULL0 + 8u * stg, kb * kTcK, m * kTcN);
+          tma_load_2d(sa + kTcA, &tw, FULL0 + 8u * stg, kb * kTcK, m * NT);
         }
         tma_load_2d(sa, &tx, FULL0 + 8u * stg, kb * kTcK, t * NP);                       // hi rows
         tma_load_2d(sa + 64u * 128u, &tx, FULL0 + 8u * stg, kb * kTcK, a.Ntot + t * NP);  // lo rows
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     grid_dep_wait();
     grid_dep_launch();
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, kTcN);
+      const uint32_t idesc = idesc_bf16_f32(128, NT);
       int stg = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool valid = j < NP && row < a.N;
       float* orow = a.out + ((size_t)s * a.N + (size_t)(valid ? row : 0)) * a.rows;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kTcN);
-      for (int cc = 0; cc < kTcN / 32; ++cc) {
+      for (int cc = 0; cc < NT / 32; ++cc) {
         float v[32];
         if (active) {
           float w[16];
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_sync(1, 128);
         if (hi && active && valid) {
-          const int col0 = m * kTcN + cc * 32;
+          const int col0 = m * NT + cc * 32;
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(v[i], xchg[j * kXchgPitch + i]);
           if (vec && col0 + 32 <= a.rows) {
@@ -425,17 +426,6 @@ __global__ void tc_qkv_kernel(const TcQkvArgs a) {
   }
 }
 
-__global__ void tc_sum_kernel(const float* part, int S, int B, int rows, float* out, int out_stride) {
-  grid_dep_wait();
-  grid_dep_launch();
-  const int r4 = rows >> 2;
-  const size_t split = (size_t)B * rows;
-  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < B * r4; idx += gridDim.x * blockDim.x) {
-    const int b = idx / r4, i = idx - b * r4;
-    *reinterpret_cast<float4*>(out + (size_t)b * out_stride + 4 * i) = sum_splits4(part + (size_t)b * rows + 4 * i, split, S);
-  }
-}
-
 // ---------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------
@@ -478,31 +468,42 @@ int tc_ntot(int B) {
   return (B + np - 1) / np * np;
 }
 
-TcPlan plan_tc(int rows, int K, int B, int num_sms) {
+TcPlan plan_tc(int rows, int K, int B, int num_sms, bool whole) {
   TcPlan p{};
   p.NP = B >= kTcRows ? kTcRows : (B + 15) / 16 * 16;
   p.ntiles = (B + p.NP - 1) / p.NP;
   p.Ntot = p.ntiles * p.NP;
-  p.MT = (rows + kTcN - 1) / kTcN;
   p.KB = (K + kTcK - 1) / kTcK;
-  // splits: the most even fill of the SMs (units / (waves * SMs)), at least 4 K blocks a split
-  const int base = p.ntiles * p.MT;
-  double best = -1.0;
-  p.S = 1;
-  for (int S = 1; S <= kMaxSplits && S <= p.KB; ++S) {
-    if (S > 1 && p.KB / S < 4) break;
-    const long long U = (long long)base * S;
+  auto eff = [&](long long U) {
     const long long waves = (U + num_sms - 1) / num_sms;
-    const double eff = (double)U / (double)(waves * num_sms);
-    if (eff > best + 1e-9) {
-      best = eff;
-      p.S = S;
+    return (double)U / (double)(waves * num_sms);
+  };
+  if (whole) {
+    // no K split (the reader takes the output as it is): 256- or 128-row tiles, whichever fills
+    // the SMs more evenly
+    const int m256 = (rows + 255) / 256, m128 = (rows + 127) / 128;
+    p.n_tile = eff((long long)m128 * p.ntiles) > eff((long long)m256 * p.ntiles) + 1e-9 ? 128 : 256;
+    p.S = 1;
+  } else {
+    // splits: the most even fill of the SMs (units / (waves * SMs)), at least 4 K blocks a split
+    p.n_tile = kTcN;
+    const int base = p.ntiles * ((rows + kTcN - 1) / kTcN);
+    double best = -1.0;
+    p.S = 1;
+    for (int S = 1; S <= kMaxSplits && S <= p.KB; ++S) {
+      if (S > 1 && p.KB / S < 4) break;
+      const double e = eff((long long)base * S);
+      if (e > best + 1e-9) {
+        best = e;
+        p.S = S;
+      }
     }
   }
-  p.units = base * p.S;
+  p.MT = (rows + p.n_tile - 1) / p.n_tile;
+  p.units = p.ntiles * p.MT * p.S;
   p.grid = p.units < num_sms ? p.units : num_sms;
   p.stages = kTcStages;
-  p.smem = 1024 + (size_t)kTcStages * kTcStage + (size_t)kTcRows * kXchgPitch * 4 + 16 * kTcStages + 64;
+  p.smem = 1024 + (size_t)kTcStages * (kTcA + (size_t)p.n_tile * 128) + (size_t)kTcRows * kXchgPitch * 4 + 16 * kTcStages + 64;
   return p;
 }
 
@@ -553,14 +554,5 @@ cudaError_t launch_tc_qkv(const TcQkvArgs& a, cudaStream_t s, bool pdl) {
   return cudaLaunchKernelEx(&cfg, tc_qkv_kernel, a);
 }
 
-cudaError_t launch_tc_sum(const float* part, int S, int B, int rows, float* out, int out_stride, cudaStream_t s,
-                          bool pdl) {
-  cudaLaunchAttribute attr[1];
-  const int n = B * (rows >> 2);
-  int blocks = (n + 255) / 256;
-  if (blocks > 1024) blocks = 1024;
-  const cudaLaunchConfig_t cfg = cfg_of(dim3(blocks), 256, 0, s, pdl, attr);
-  return cudaLaunchKernelEx(&cfg, tc_sum_kernel, part, S, B, rows, out, out_stride);
-}
 
 }  // namespace llm

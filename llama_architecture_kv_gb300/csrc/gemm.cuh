@@ -18,7 +18,8 @@ struct TcArgs {
   int32_t N;              // activation rows (batch)
   int32_t NP;             // activation rows per tile: a multiple of 16, at most 64
   int32_t Ntot;           // rows of each half (hi, lo) of the split activations (ntiles * NP)
-  int32_t MT, KB, S;      // 256-row weight tiles, 64-element K blocks, K splits
+  int32_t MT, KB, S;      // weight tiles, 64-element K blocks, K splits
+  int32_t n_tile;         // weight rows per tile (the MMA's N): 256 or 128
   int32_t units;          // ntiles * MT * S
   int32_t stages;         // shared-memory pipeline depth
   float* out;             // [S][N][rows]
@@ -61,13 +62,14 @@ struct TcQkvArgs {
 };
 
 struct TcPlan {
-  int NP, Ntot, ntiles, MT, KB, S, units, grid, stages;
+  int NP, Ntot, ntiles, MT, KB, S, units, grid, stages, n_tile;
   size_t smem;
 };
 
 bool tc_available();
 cudaError_t tc_prepare(int max_smem_optin);
-TcPlan plan_tc(int rows, int K, int B, int num_sms);
+// whole: one split (the output is final); the tile height is chosen for an even fill
+TcPlan plan_tc(int rows, int K, int B, int num_sms, bool whole = false);
 // rows of the split activations buffer for B rows, per half
 int tc_ntot(int B);
 // 2D bf16 tensor map over [outer][inner] (row pitch inner elements), box box_inner x box_outer,
@@ -81,8 +83,5 @@ cudaError_t launch_tc_prep(const TcPrepArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_tc_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, const TcPlan& p,
                            cudaStream_t s, bool pdl);
 cudaError_t launch_tc_qkv(const TcQkvArgs& a, cudaStream_t s, bool pdl);
-// out[j][r] = sum_s part[s][j][r] (f32, rows a multiple of 4)
-cudaError_t launch_tc_sum(const float* part, int S, int B, int rows, float* out, int out_stride, cudaStream_t s,
-                          bool pdl);
 
 }  // namespace llm

@@ -398,12 +398,14 @@ llm_status launch_prep(llm_handle* h, const PrepIn& in, int K, int B, bool pdl) 
 }
 
 // out (split sums, [S][B][rows]) = W x' for the split activations of K-wide rows
-llm_status launch_gemm(llm_handle* h, const CUtensorMap& tw, int rows, int K, int B, float* out, bool pdl) {
-  const TcPlan p = plan_tc(rows, K, B, h->num_sms);
+llm_status launch_gemm(llm_handle* h, const CUtensorMap& tw, int rows, int K, int B, float* out, bool pdl,
+                       bool whole = false) {
+  const TcPlan p = plan_tc(rows, K, B, h->num_sms, whole);
   const CUtensorMap* tx = tc_xmap(h, K, B);
   if (!tx) return fail(h, LLM_ERR_CUDA, "tensor map of the activations (K %d, B %d)", K, B);
   TcArgs a = {};
   a.rows = rows; a.K = K; a.N = B; a.NP = p.NP; a.Ntot = p.Ntot; a.MT = p.MT; a.KB = p.KB; a.S = p.S;
+  a.n_tile = p.n_tile;
   a.units = p.units; a.stages = p.stages; a.out = out; a.status = h->status;
   CUDA_TRY(h, launch_tc_gemm(tw, *tx, a, p, h->stream, pdl));
   return LLM_OK;
@@ -435,11 +437,8 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     PrepIn in;
     in.src_rows = h->d; in.src_K = h->f; in.resid = h->xb; in.xout = h->xa; in.gain = h->lnf;
     TRY(launch_prep(h, in, h->d, B, pdl));
-    const TcPlan p = plan_tc(h->V, h->d, B, h->num_sms);
-    if (p.S == 1) return launch_gemm(h, h->tmap_head, h->V, h->d, B, h->logits, pdl);
-    TRY(launch_gemm(h, h->tmap_head, h->V, h->d, B, h->tc_part, pdl));
-    CUDA_TRY(h, launch_tc_sum(h->tc_part, p.S, B, h->V, h->logits, h->V, h->stream, pdl));
-    return LLM_OK;
+    // one K split: the GEMM writes the logits themselves
+    return launch_gemm(h, h->tmap_head, h->V, h->d, B, h->logits, pdl, true);
   }
   if (which == K_HEAD) {
     const GemvPlan p_h = plan_gemv(h->V, h->d, 1, wt, B, h->num_sms, cps);
@@ -835,7 +834,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     const int64_t qkv_rows = (int64_t)(h->H + 2 * c.kv_heads) * h->hd;
     size_t part = 0;
     for (int b = h->tc_min; b <= c.max_batch; ++b) {
-      const int64_t shapes[5][2] = {{qkv_rows, h->d}, {h->d, h->d}, {2 * (int64_t)h->f, h->d}, {h->d, h->f}, {h->V, h->d}};
+      const int64_t shapes[4][2] = {{qkv_rows, h->d}, {h->d, h->d}, {2 * (int64_t)h->f, h->d}, {h->d, h->f}};
       for (auto& sh : shapes) {
         const TcPlan p = plan_tc((int)sh[0], (int)sh[1], b, h->num_sms);
         part = std::max(part, (size_t)p.S * b * (size_t)sh[0]);
@@ -856,7 +855,9 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
            tc_make_map(&m.down, w.down, h->f, h->d, kTcK, kTcN);
     }
     // a shape the tensor maps cannot describe keeps every step on the GEMV
-    if (!ok || !tc_make_map(&h->tmap_head, h->head, h->d, h->V, kTcK, kTcN)) h->tc_min = 0;
+    // the head runs unsplit; its tile height (the map's box) depends only on the vocabulary
+    const int head_rows = plan_tc(h->V, h->d, 1, h->num_sms, true).n_tile;
+    if (!ok || !tc_make_map(&h->tmap_head, h->head, h->d, h->V, kTcK, (uint32_t)head_rows)) h->tc_min = 0;
   }
   if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * 5 * B * std::max(h->d, h->f) * 4))) return bail(st);
   if (cudaMemsetAsync(h->ticket, 0, B * c.kv_heads * 4, h->stream) != cudaSuccess ||
