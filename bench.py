@@ -333,8 +333,14 @@ def run_ours(args):
     bytes_gu = 2 * s.ffn * s.d * (2 if s.bf16 else 4)  # algorithmic: the gate and up weights
     achieved = bytes_gu / (kms / 1e3) / 1e9
     peak, peak_kind = peaks()
-    traffic = traffic_from_profile("gemv.cu", "gate_up_gemv_llama8b_b1.md") if w.name == "llama8b_b1" else None
-    roofline = {"bound": "hbm", "kernel": "gemv_kernel<bf16, EPI_SWIGLU> (norm + gate/up + SwiGLU)",
+    tc = s.bf16 and B >= 16  # the handle's default tensor-core threshold
+    if tc:
+        kname = "tc_gemm_kernel (gate/up, timed with its tc_prep_kernel: x1 = x + o_proj, norm, bf16 split)"
+        traffic = traffic_from_profile("gemm.cu", "tc_gemm_gate_up_llama8b_b32.md") if w.name == "llama8b_b32" else None
+    else:
+        kname = "gemv_kernel<bf16, EPI_SWIGLU> (norm + gate/up + SwiGLU)"
+        traffic = traffic_from_profile("gemv.cu", "gate_up_gemv_llama8b_b1.md") if w.name == "llama8b_b1" else None
+    roofline = {"bound": "hbm", "kernel": kname,
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": peak_kind, "traffic": traffic, "ms_per_launch": kms,
                 "algorithmic_bytes_per_launch": bytes_gu}
