@@ -21,6 +21,7 @@
 // the (normalized) input lives in shared memory as f32.  Partial dot products are reduced
 // with warp shuffles and a fixed-order sum across warps, so results are deterministic.
 #include "gemv.cuh"
+#include "tc.cuh"
 
 namespace llm {
 
@@ -322,6 +323,200 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
 }
 
 // ---------------------------------------------------------------------------------------
+// batch 1, bf16: each warp streams its rows through its own ring of bulk copies
+// ---------------------------------------------------------------------------------------
+// Rows are taken two at a time (a "group": a RoPE pair, a (gate, up) pair, or two neighbouring
+// rows); a CTA owns a contiguous, balanced range of groups and warp w takes groups w, w + 8, ...
+// A step of a warp is the same 4 KB piece of both rows of a group, copied by lane 0 into a ring
+// slot with two cp.async.bulk copies on one mbarrier; `ns` steps are in flight per warp, so the
+// bytes in flight no longer depend on registers.  The first steps are requested before the wait
+// on the previous kernel (the weights do not depend on it).  Lane l multiplies 16-byte chunks
+// l, l + 32, ... of both pieces with the (normalized) input, which sits in shared memory as f32
+// in two planes (elements 0-3 and 4-7 of every 8-element chunk) so that the loads of a warp are
+// contiguous; each input load serves both rows.  A row's sum is a warp reduction; the epilogues
+// are those of gemv_kernel.
+constexpr int kTmaWarps = 8;
+constexpr int kPiece = 4096;              // bytes of one row per step
+constexpr int kStepBytes = 2 * kPiece;    // both rows of a group
+constexpr int kTmaMaxSteps = 3;           // steps in flight per warp, at most
+constexpr uint64_t kTmaWaitCycles = 4000000000ull;  // SM cycles: about 2 s at 2 GHz
+static int g_smem_optin = 0;              // set by gemv_prepare
+
+static LLM_HD size_t gemv_tma_x_bytes(int cols) { return ((size_t)cols * 4 + 1023) & ~(size_t)1023; }
+static size_t gemv_tma_smem(int cols, int ns) {
+  return gemv_tma_x_bytes(cols) + (size_t)kTmaWarps * ns * (kStepBytes + 8);
+}
+
+template <int EPI, bool NORM>
+__global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvArgs a, const int ns) {
+  extern __shared__ __align__(1024) uint8_t gsm[];
+  constexpr int NW = kTmaWarps;
+  const int cols = a.cols;
+  float* xlo = reinterpret_cast<float*>(gsm);  // [cols / 2]: elements 0..3 of each chunk
+  float* xhi = xlo + (cols >> 1);              // elements 4..7
+  uint8_t* ring = gsm + gemv_tma_x_bytes(cols);
+  const uint32_t ring_s = smem_u32(ring);
+  const uint32_t bars = ring_s + (uint32_t)(NW * ns * kStepBytes);
+  __shared__ float red[NW];
+  __shared__ float s_inv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int groups = (a.rows + 1) >> 1;
+  const int g0 = (int)(((long long)groups * blockIdx.x) / gridDim.x);
+  const int g1 = (int)(((long long)groups * (blockIdx.x + 1)) / gridDim.x);
+  const size_t row_bytes = (size_t)cols * 2;
+  const int ppr = (int)((row_bytes + kPiece - 1) / kPiece);  // pieces per row
+  const int ng = g1 - g0 > warp ? (g1 - g0 - warp + NW - 1) / NW : 0;
+  const int total = ng * ppr;  // steps of this warp
+  const char* W = (const char*)a.W;
+
+  if (tid == 0) {
+    for (int i = 0; i < NW * ns; ++i) mbar_init(bars + 8u * i, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // step t of this warp: piece t % ppr of the rows of group g0 + warp + (t / ppr) * NW
+  auto issue = [&](int t) {
+    const int ig = t / ppr, pc = t - ig * ppr;
+    const size_t r0 = 2 * (size_t)(g0 + warp + ig * NW);
+    const size_t r1 = r0 + 1 < (size_t)a.rows ? r0 + 1 : r0;  // an odd last row is read twice
+    const size_t off = (size_t)pc * kPiece;
+    const uint32_t bytes = (uint32_t)(row_bytes - off < (size_t)kPiece ? row_bytes - off : (size_t)kPiece);
+    const int slot = t % ns;
+    const uint32_t bar = bars + 8u * (warp * ns + slot);
+    const uint32_t dst = ring_s + (uint32_t)((warp * ns + slot) * kStepBytes);
+    mbar_expect_tx(bar, 2 * bytes);
+    bulk_load(dst, W + r0 * row_bytes + off, bytes, bar);
+    bulk_load(dst + kPiece, W + r1 * row_bytes + off, bytes, bar);
+  };
+  if (lane == 0)
+    for (int t = 0; t < ns && t < total; ++t) issue(t);
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // the (normalized) input, f32, in its two planes
+  const int c4 = cols >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(a.x);
+  float inv = 1.f;
+  if constexpr (NORM) {
+    float ss = 0.f;
+    for (int i = tid; i < c4; i += NW * 32) {
+      const float4 v = __ldg(xr + i);
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < NW; ++w) t += red[w];
+      s_inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)cols), a.eps)));
+    }
+    __syncthreads();
+    inv = s_inv;
+  }
+  for (int i = tid; i < c4; i += NW * 32) {
+    float4 v = __ldg(xr + i);
+    if constexpr (NORM) {
+      const float4 g = __ldg(reinterpret_cast<const float4*>(a.gain) + i);
+      v.x = __fmul_rn(g.x, __fmul_rn(inv, v.x));
+      v.y = __fmul_rn(g.y, __fmul_rn(inv, v.y));
+      v.z = __fmul_rn(g.z, __fmul_rn(inv, v.z));
+      v.w = __fmul_rn(g.w, __fmul_rn(inv, v.w));
+    }
+    reinterpret_cast<float4*>((i & 1) ? xhi : xlo)[i >> 1] = v;
+  }
+  __syncthreads();
+
+  bool ok = true;
+  int consumed = 0;
+  float a0[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f};  // the group's two rows
+  auto chunk = [&](const uint8_t* w0, const float* xl, const float* xh, int j, int par) {
+    float f0[8], f1[8];
+    unpack16<1>(*reinterpret_cast<const uint4*>(w0 + j * 16), f0);
+    unpack16<1>(*reinterpret_cast<const uint4*>(w0 + kPiece + j * 16), f1);
+    const float4 lo = *reinterpret_cast<const float4*>(xl + j * 4);
+    const float4 hi = *reinterpret_cast<const float4*>(xh + j * 4);
+    const float xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      a0[par] = fmaf(f0[e], xv[e], a0[par]);
+      a1[par] = fmaf(f1[e], xv[e], a1[par]);
+    }
+  };
+  for (int t = 0; t < total; ++t) {
+    const int slot = t % ns;
+    ok = __all_sync(0xffffffffu, mbar_wait(bars + 8u * (warp * ns + slot), (uint32_t)(t / ns) & 1u, kTmaWaitCycles));
+    if (!ok) break;
+    consumed = t + 1;
+    const int ig = t / ppr, pc = t - ig * ppr;
+    const size_t off = (size_t)pc * kPiece;
+    const int nch = (int)((row_bytes - off < (size_t)kPiece ? row_bytes - off : (size_t)kPiece) >> 4);
+    const uint8_t* w0 = ring + (size_t)(warp * ns + slot) * kStepBytes;
+    const float* xl = xlo + (size_t)pc * (kPiece / 4);
+    const float* xh = xhi + (size_t)pc * (kPiece / 4);
+    if (nch == kPiece / 16) {
+#pragma unroll
+      for (int i = 0; i < kPiece / 16 / 32; ++i) chunk(w0, xl, xh, lane + 32 * i, i & 1);
+    } else {
+      for (int j = lane; j < nch; j += 32) chunk(w0, xl, xh, j, 0);
+    }
+    __syncwarp();
+    if (lane == 0 && t + ns < total) {
+      fence_proxy_async_smem();  // this slot's reads come before the copy that refills it
+      issue(t + ns);
+    }
+    if (pc == ppr - 1) {
+      const float v0 = warp_sum(a0[0] + a0[1]);
+      const float v1 = warp_sum(a1[0] + a1[1]);
+      a0[0] = a0[1] = a1[0] = a1[1] = 0.f;
+      const int g = g0 + warp + ig * NW;
+      if (lane == 0) {
+        if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+          const int r0 = 2 * g;
+          a.out[r0] = EPI == EPI_RESID ? __fadd_rn(a.resid[r0], v0) : v0;
+          if (r0 + 1 < a.rows) a.out[r0 + 1] = EPI == EPI_RESID ? __fadd_rn(a.resid[r0 + 1], v1) : v1;
+        } else if constexpr (EPI == EPI_SWIGLU) {
+          const float si = __fdiv_rn(v0, __fadd_rn(1.0f, expf(-v0)));
+          a.out[g] = __fmul_rn(si, v1);
+        } else {
+          const int R = 2 * g;
+          const int pos = a.step->pos, half = a.hd >> 1;
+          const int head = R / a.hd, e = (R - head * a.hd) >> 1;
+          if (head < a.H + a.kv) {
+            const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];
+            const float lo = __fadd_rn(__fmul_rn(v0, c), __fmul_rn(-v1, s));
+            const float hi = __fadd_rn(__fmul_rn(v1, c), __fmul_rn(v0, s));
+            if (head < a.H) {
+              float* q = a.q_out + (size_t)head * a.hd;
+              q[e] = lo;
+              q[e + half] = hi;
+            } else {
+              const size_t ci = ((size_t)(head - a.H) * a.cap + pos) * a.hd;
+              store_elem<1>(a.kc, ci + e, lo);
+              store_elem<1>(a.kc, ci + e + half, hi);
+            }
+          } else {
+            const size_t ci = ((size_t)(head - a.H - a.kv) * a.cap + pos) * a.hd;
+            store_elem<1>(a.vc, ci + e, v0);
+            store_elem<1>(a.vc, ci + e + half, v1);
+          }
+        }
+      }
+    }
+  }
+  if (!ok && lane == 0) {
+    atomicCAS(a.status, 0, kErrDeviceTimeout);
+    // no copy may still be writing shared memory when the CTA exits
+    for (int t = consumed; t < total && t < consumed + ns; ++t)
+      mbar_wait(bars + 8u * (warp * ns + t % ns), (uint32_t)(t / ns) & 1u, kTmaWaitCycles);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------
 
@@ -364,6 +559,19 @@ GemvPlan plan_gemv(int rows, int cols, int rg, int wt, int B, int num_sms, int c
   p.ws = (lpr >= 32 && ws_floats * 4 <= 48 * 1024) ? 1 : 0;
   p.smem = ((size_t)p.bt * p.seg_ch * E + (size_t)p.rows_cap * p.bt + 2 * 8 * RB * p.bt + 8 + 8 * 8 +
             (p.ws ? ws_floats : 0)) * 4;
+  // batch 1, bf16, rows of whole 16-byte chunks: as many steps in flight per warp as shared
+  // memory holds, up to kTmaMaxSteps; one CTA per SM
+  p.tma_ns = 0;
+  if (B == 1 && wt == 1 && cols % 8 == 0 && g_smem_optin > 0) {
+    int ns = kTmaMaxSteps;
+    while (ns >= 2 && gemv_tma_smem(cols, ns) + 1024 > (size_t)g_smem_optin) --ns;
+    if (ns >= 2) {
+      const int groups = (rows + 1) / 2;
+      p.tma_ns = ns;
+      p.tma_grid = groups < num_sms ? groups : num_sms;
+      p.tma_smem = gemv_tma_smem(cols, ns);
+    }
+  }
   return p;
 }
 
@@ -393,6 +601,17 @@ static GemvFn pick(int wt, int bt, int epi, bool norm) {
   return wt ? pick_bt<1>(bt, epi, norm) : pick_bt<0>(bt, epi, norm);
 }
 
+using GemvTmaFn = void (*)(const GemvArgs, const int);
+
+static GemvTmaFn pick_tma(int epi, bool norm) {
+  switch (epi) {
+    case EPI_QKV: return gemv_tma_kernel<EPI_QKV, true>;
+    case EPI_SWIGLU: return gemv_tma_kernel<EPI_SWIGLU, true>;
+    case EPI_RESID: return gemv_tma_kernel<EPI_RESID, false>;
+    default: return norm ? gemv_tma_kernel<EPI_STORE, true> : gemv_tma_kernel<EPI_STORE, false>;
+  }
+}
+
 cudaError_t gemv_prepare(int max_smem_optin) {
   for (int wt = 0; wt < 2; ++wt)
     for (int bt : {1, 2, 4, 8})
@@ -406,11 +625,35 @@ cudaError_t gemv_prepare(int max_smem_optin) {
                                    max_smem_optin - (int)fa.sharedSizeBytes);
           if (e != cudaSuccess) return e;
         }
+  for (int epi = 0; epi < 4; ++epi)
+    for (int norm = 0; norm < 2; ++norm) {
+      GemvTmaFn fn = pick_tma(epi, norm != 0);
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               max_smem_optin - (int)fa.sharedSizeBytes);
+      if (e != cudaSuccess) return e;
+    }
+  g_smem_optin = max_smem_optin;
   return cudaSuccess;
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, const GemvPlan& p, int wt, int epi, bool norm,
                         cudaStream_t s, bool pdl) {
+  if (p.tma_ns > 0 && a.B == 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.tma_grid);
+    cfg.blockDim = dim3(kTmaWarps * 32);
+    cfg.dynamicSmemBytes = p.tma_smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pick_tma(epi, norm), a, p.tma_ns);
+  }
   GemvFn fn = pick(wt, p.bt, epi, norm);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);

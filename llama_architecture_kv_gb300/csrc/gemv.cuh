@@ -38,11 +38,15 @@ struct GemvArgs {
   int32_t H, kv, hd, cap;
   const float* rope_cos;  // [cap][hd/2]
   const float* rope_sin;
+  int32_t* status;      // device error flag (a bounded wait that ran out)
 };
 
 struct GemvPlan {
   int bt, lpr, seg_ch, nseg, grid, rows_cap, ws;
   size_t smem;
+  // batch 1 with bf16 weights: the bulk-copy kernel (tma_ns > 0 steps in flight per warp)
+  int tma_ns, tma_grid;
+  size_t tma_smem;
 };
 
 constexpr int kGemvThreads = 256;

@@ -447,6 +447,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     hd.x = h->xa; hd.x_stride = h->d; hd.gain = h->lnf;
     hd.lpr = p_h.lpr; hd.seg_ch = p_h.seg_ch; hd.nseg = p_h.nseg; hd.rows_cap = p_h.rows_cap; hd.ws = p_h.ws;
     hd.out = h->logits; hd.out_stride = h->V;
+    hd.status = h->status;
     CUDA_TRY(h, launch_gemv(hd, p_h, wt, EPI_STORE, true, h->stream, pdl));
     return LLM_OK;
   }
@@ -508,6 +509,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     a.q_out = h->q; a.q_stride = h->d; a.kc = kcl; a.vc = vcl;
     a.H = h->H; a.kv = c.kv_heads; a.hd = h->hd; a.cap = c.max_seq;
     a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin;
+    a.status = h->status;
     CUDA_TRY(h, launch_gemv(a, p, wt, EPI_QKV, true, h->stream, pdl));
   } else if (which == K_ATTN) {
     const int ns = attn_splits(B, c.kv_heads, c.max_seq, h->num_sms);
@@ -526,6 +528,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     o.x = h->attn; o.x_stride = h->d;
     o.lpr = p.lpr; o.seg_ch = p.seg_ch; o.nseg = p.nseg; o.rows_cap = p.rows_cap; o.ws = p.ws;
     o.out = h->xb; o.out_stride = h->d; o.resid = h->xa; o.resid_stride = h->d;
+    o.status = h->status;
     CUDA_TRY(h, launch_gemv(o, p, wt, EPI_RESID, false, h->stream, pdl));
   } else if (which == K_GATEUP) {
     // RMSNorm + gate/up + SwiGLU: m = silu(W_g n2) * (W_u n2)
@@ -535,6 +538,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     g.x = h->xb; g.x_stride = h->d; g.gain = w.ln2;
     g.lpr = p.lpr; g.seg_ch = p.seg_ch; g.nseg = p.nseg; g.rows_cap = p.rows_cap; g.ws = p.ws;
     g.out = h->m; g.out_stride = h->f;
+    g.status = h->status;
     CUDA_TRY(h, launch_gemv(g, p, wt, EPI_SWIGLU, true, h->stream, pdl));
   } else if (which == K_DOWN) {
     // down + residual: y (xa) = x1 (xb) + W_down m
@@ -544,6 +548,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     dn.x = h->m; dn.x_stride = h->f;
     dn.lpr = p.lpr; dn.seg_ch = p.seg_ch; dn.nseg = p.nseg; dn.rows_cap = p.rows_cap; dn.ws = p.ws;
     dn.out = h->xa; dn.out_stride = h->d; dn.resid = h->xb; dn.resid_stride = h->d;
+    dn.status = h->status;
     CUDA_TRY(h, launch_gemv(dn, p, wt, EPI_RESID, false, h->stream, pdl));
   } else {
     return fail(h, LLM_ERR_ARG, "unknown kernel %d", which);
