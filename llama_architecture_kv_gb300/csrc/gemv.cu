@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
 constexpr int kTmaWarps = 8;
 constexpr int kPiece = 4096;              // bytes of one row per step
 constexpr int kStepBytes = 2 * kPiece;    // both rows of a group
-constexpr int kTmaMaxSteps = 3;           // steps in flight per warp, at most
+constexpr int kTmaMaxSteps = 2;           // steps in flight per warp
 constexpr uint64_t kTmaWaitCycles = 4000000000ull;  // SM cycles: about 2 s at 2 GHz
 static int g_smem_optin = 0;              // set by gemv_prepare
 
@@ -559,8 +559,9 @@ GemvPlan plan_gemv(int rows, int cols, int rg, int wt, int B, int num_sms, int c
   p.ws = (lpr >= 32 && ws_floats * 4 <= 48 * 1024) ? 1 : 0;
   p.smem = ((size_t)p.bt * p.seg_ch * E + (size_t)p.rows_cap * p.bt + 2 * 8 * RB * p.bt + 8 + 8 * 8 +
             (p.ws ? ws_floats : 0)) * 4;
-  // batch 1, bf16, rows of whole 16-byte chunks: as many steps in flight per warp as shared
-  // memory holds, up to kTmaMaxSteps; one CTA per SM
+  // batch 1, bf16, rows of whole 16-byte chunks: kTmaMaxSteps steps in flight per warp (fewer
+  // if shared memory does not hold them; two measured faster than three at the 8B shape, the
+  // smaller footprint leaving room for the next kernel's CTAs); one CTA per SM
   p.tma_ns = 0;
   if (B == 1 && wt == 1 && cols % 8 == 0 && g_smem_optin > 0) {
     int ns = kTmaMaxSteps;
