@@ -474,13 +474,16 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
 
 // ---------------------------------------------------------------------------------------
 // bf16 caches, hd 64 or 128: the two contractions of a chunk on warp-level tensor-core MMAs
-// (m16n8k16, bf16 in, f32 accumulate).  Rows of the MMA are the g query heads (padded to 16).
-//   scores  S[16][32] = Q K^T: Q as bf16 hi + lo (two MMAs into separate accumulators, so
-//           each query enters to about 2^-17 relative), K fragments by ldmatrix from the
-//           swizzled key tile;
-//   softmax on the accumulator fragments (a row's 32 positions live in one quad of lanes);
-//   values  O[16][hd] += P V: the weights P as bf16 hi + lo (the score fragments reused as the
-//           A operand), V fragments by transposing ldmatrix from the swizzled value tile.
+// (m16n8k16, bf16 in, f32 accumulate).  Rows of the MMA are the chunk's 16 positions, columns
+// the query heads of the group (one 8-column tile for g <= 8, two for g <= 16), so a small group
+// wastes at most half of each MMA:
+//   scores  S^T[16][8] = K Q^T: K fragments by ldmatrix from the swizzled key tile, Q as bf16
+//           hi + lo fragments kept in registers for the whole segment (two MMAs into separate
+//           accumulators, so each query enters to about 2^-17 relative);
+//   softmax per head = per column: 16 positions over the 8 lanes of one quad column;
+//   values  O^T[hd][8] += V^T P^T: V fragments by transposing ldmatrix from the swizzled value
+//           tile, the weights P as bf16 hi + lo B fragments gathered from the score fragments
+//           with shuffles.
 // ---------------------------------------------------------------------------------------
 
 LLM_D void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -517,7 +520,7 @@ struct MmaShape {
   static constexpr int NBOX = ROWB / 128;   // 128-byte column boxes per row
   static constexpr int BUF = 2 * kMmaChunk * ROWB;
   static constexpr int QP = HD + 8;         // padded query row (elements): ldmatrix rows on distinct banks
-  static constexpr int NTO = HD / 8;        // output n-tiles
+  static constexpr int DT = HD / 16;        // 16-dimension tiles of the output
   static constexpr int KS = HD / 16;        // k-steps of the scores
 };
 
@@ -540,6 +543,9 @@ template <int HD>
 LLM_HD int attn_mma_nr(int g) { return HD <= 64 && attn_mma_smem_nr<HD>(g, 3) <= 232448 - 64 ? 3 : 2; }
 
 constexpr int kMmaMaxSplits = 64;  // splits of one (row, kv head) the persistent kernel merges
+constexpr int kMmaMaxCluster = 16; // most CTAs of one cluster in cluster mode
+constexpr int kMmaCluster = 8;     // the cluster size used (portable)
+constexpr size_t kMmaClusterMaxBytes = 1u << 20;  // most cache bytes per CTA in cluster mode
 
 template <int HD>
 LLM_HD size_t attn_mma_smem(int g) { return attn_mma_smem_nr<HD>(g, attn_mma_nr<HD>(g)); }
@@ -555,11 +561,11 @@ LLM_D uint32_t swz_off(int r, int c) {
 // (row, kv head) segments, and each warp's ring runs ahead across segment boundaries, so copies
 // never stop.  A (row, kv head) shared by several CTAs is finished by the last of them (atomic
 // ticket), which merges their partials in CTA order (the order of the positions).
-template <int HD>
+template <int HD, int NG>
 __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
   using M = MmaShape<HD>;
-  constexpr int ROWB = M::ROWB, BUF = M::BUF, QP = M::QP, NTO = M::NTO, KS = M::KS;
+  constexpr int ROWB = M::ROWB, BUF = M::BUF, QP = M::QP, DT = M::DT, KS = M::KS;
   constexpr int CH = kMmaChunk;
   const int NR = attn_mma_nr<HD>(a.g);
   extern __shared__ unsigned char araw[];
@@ -583,7 +589,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   const int npos = t + 1;
   const int nchk = (npos + CH - 1) / CH;              // chunks of one (row, kv head)
   const long long T = (long long)a.B * a.kv * nchk;   // chunks of the launch
-  const long long c0 = T * c / G, c1 = T * (c + 1) / G;
+  // cluster mode: cluster bj takes (row, kv head) bj and its CTA of rank r the r-th of a.ns
+  // even parts of the chunks (possibly none)
+  const bool clus = a.cluster != 0;
+  const int crank = clus ? (int)cluster_rank() : 0;
+  const long long cbj = clus ? c / a.ns : 0;
+  const long long c0 = clus ? cbj * nchk + (long long)nchk * crank / a.ns : T * c / G;
+  const long long c1 = clus ? cbj * nchk + (long long)nchk * (crank + 1) / a.ns : T * (c + 1) / G;
   auto owner = [&](long long it) { return (int)(((it + 1) * G + T - 1) / T - 1); };
   // the segment starting at chunk st of the sequence: (row b, kv head j), chunks [k0, k1)
   auto seg = [&](long long st, int& b, int& j, int& k0, int& k1, long long& next) {
@@ -667,12 +679,57 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   }
   __syncthreads();
 
-  const bool row1 = g > 8;     // MMA rows 8..15 hold heads (else padding)
-  const bool row0v = gid < g;  // this lane's row 0 holds a head
-  const int qr = (lane & 7) + ((lane >> 3) & 1) * 8, qc = (lane >> 4) * 8;
   const int mi = lane >> 3, mr = lane & 7;
   bool ok = true;
   int consumed = 0;
+
+  // the splits of (row b, kv head j) merge through distributed shared memory: every CTA of the
+  // cluster reads all ranks' (m, l), forms the factors, and writes its share of the outputs
+  auto cluster_merge = [&](int b, int j) {
+    const int cs = a.ns;
+    cluster_sync_all();
+    for (int idx = tid; idx < g * cs; idx += NT) {
+      const int h = idx / cs, r = idx - h * cs;
+      fac[h * kMmaMaxSplits + r] = ld_cluster(mypart + h * (HD + 2) + HD, r);
+      fac[h * kMmaMaxSplits + 32 + r] = ld_cluster(mypart + h * (HD + 2) + HD + 1, r);
+    }
+    __syncthreads();
+    for (int h = tid; h < g; h += NT) {
+      float Mx = -INFINITY;
+      for (int r = 0; r < cs; ++r) Mx = fmaxf(Mx, fac[h * kMmaMaxSplits + r]);
+      float L = 0.f;
+      for (int r = 0; r < cs; ++r) {
+        const float mr = fac[h * kMmaMaxSplits + r];
+        const float f = mr == -INFINITY ? 0.f : expf(mr - Mx);
+        fac[h * kMmaMaxSplits + r] = f;
+        L += fac[h * kMmaMaxSplits + 32 + r] * f;
+      }
+      const float rl = 1.0f / L;
+      for (int r = 0; r < cs; ++r) fac[h * kMmaMaxSplits + r] *= rl;
+    }
+    __syncthreads();
+    float* outb = a.out + (size_t)b * a.out_stride + (size_t)j * g * HD;
+    const int n_out = g * HD, i0 = n_out * crank / cs, i1 = n_out * (crank + 1) / cs;
+    for (int idx = i0 + tid; idx < i1; idx += NT) {
+      const int h = idx / HD, e = idx - h * HD;
+      float ov[kMmaMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMmaMaxCluster; ++r)
+        if (r < cs) ov[r] = ld_cluster(mypart + h * (HD + 2) + e, r);
+      float O = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMmaMaxCluster; ++r)
+        if (r < cs) O = fmaf(fac[h * kMmaMaxSplits + r], ov[r], O);
+      outb[(size_t)h * HD + e] = O;
+    }
+    cluster_sync_all();  // every CTA keeps its shared memory until the others have read it
+  };
+  if (clus && c0 == c1) {
+    // no chunks here: an empty part (o = 0, m = -inf, l = 0) joins the merge
+    for (int idx = tid; idx < g * (HD + 2); idx += NT) mypart[idx] = (idx % (HD + 2)) == HD ? -INFINITY : 0.f;
+    __syncthreads();
+    cluster_merge((int)(cbj / a.kv), (int)(cbj % a.kv));
+  }
 
   int lu = 0;
   long long next = c0;
@@ -680,12 +737,30 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     int b, j, k0, k1;
     seg(st, b, j, k0, k1, next);
     const int p0 = k0 * CH, p1 = min(npos, k1 * CH), nch = k1 - k0;
-    const uint16_t* qh = qbase;
-    const uint32_t qh_addr = smem_u32(qh + qr * QP + qc), ql_addr = smem_u32(qh + 16 * QP + qr * QP + qc);
-    float o[NTO][4];
+    // this segment's queries as B fragments (k = dimensions, n = heads), hi and lo, kept in
+    // registers: x4 loads give (b0, b1) of two consecutive k-steps
+    uint32_t qfh[NG][KS][2], qfl[NG][KS][2];
 #pragma unroll
-    for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    for (int n = 0; n < NG; ++n)
+#pragma unroll
+      for (int ks = 0; ks < KS; ks += 2) {
+        const uint32_t off = (uint32_t)(((n * 8 + mr) * QP + ks * 16 + mi * 8) * 2);
+        uint32_t r[4];
+        ldsm_x4(smem_u32(qbase) + off, r);
+        qfh[n][ks][0] = r[0]; qfh[n][ks][1] = r[1]; qfh[n][ks + 1][0] = r[2]; qfh[n][ks + 1][1] = r[3];
+        ldsm_x4(smem_u32(qbase + 16 * QP) + off, r);
+        qfl[n][ks][0] = r[0]; qfl[n][ks][1] = r[1]; qfl[n][ks + 1][0] = r[2]; qfl[n][ks + 1][1] = r[3];
+      }
+    // O^T tiles: o[n][dt] = (dims dt*16 + gid (+8), heads n*8 + 2 tig (+1))
+    float o[NG][DT][4];
+#pragma unroll
+    for (int n = 0; n < NG; ++n)
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) o[n][dt][0] = o[n][dt][1] = o[n][dt][2] = o[n][dt][3] = 0.f;
+    // running max and this lane's share of the running sum, per head n*8 + 2 tig + hc
+    float mrow[NG][2], lrow[NG][2];
+#pragma unroll
+    for (int n = 0; n < NG; ++n) mrow[n][0] = mrow[n][1] = -INFINITY, lrow[n][0] = lrow[n][1] = 0.f;
     for (int ci = warp; ci < nch && ok; ci += NW) {
       const int slot = consumed % NR;
       const uint32_t bar = bars + 8u * (warp * NR + slot);
@@ -705,98 +780,89 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
         }
         __syncwarp();
       }
-      // ---- scores S = Q K^T: 2 n-tiles of 8 positions, separate hi and lo accumulators ----
-      float sh[2][4], sl[2][4];
+      // ---- scores S^T = K Q^T: rows = the 16 positions, columns = heads; separate hi and lo
+      // accumulators ----
+      float sh[NG][4], sl[NG][4];
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < NG; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) sh[n][i] = sl[n][i] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < KS; ks += 2) {
-        uint32_t ah0[4], al0[4], ah1[4], al1[4], bk[2][4];
-        ldsm_x4(qh_addr + ks * 32, ah0);
-        ldsm_x4(ql_addr + ks * 32, al0);
-        ldsm_x4(qh_addr + (ks + 1) * 32, ah1);
-        ldsm_x4(ql_addr + (ks + 1) * 32, al1);
-        // matrices: (ks, dims 0-7), (ks, dims 8-15), (ks+1, 0-7), (ks+1, 8-15) of positions n*8..
+      for (int ks = 0; ks < KS; ++ks) {
+        // matrices: positions 0-7 and 8-15 of dims ks*16 + 0..7, then of dims ks*16 + 8..15
+        uint32_t ka[4];
+        ldsm_x4(kreg + swz_off((mi & 1) * 8 + mr, 2 * ks + (mi >> 1)), ka);
 #pragma unroll
-        for (int n = 0; n < 2; ++n) ldsm_x4(kreg + swz_off(n * 8 + mr, 2 * (ks + (mi >> 1)) + (mi & 1)), bk[n]);
+        for (int n = 0; n < NG; ++n) mma_bf16_16816(sh[n], ka, qfh[n][ks][0], qfh[n][ks][1]);
 #pragma unroll
-        for (int n = 0; n < 2; ++n) mma_bf16_16816(sh[n], ah0, bk[n][0], bk[n][1]);
-#pragma unroll
-        for (int n = 0; n < 2; ++n) mma_bf16_16816(sl[n], al0, bk[n][0], bk[n][1]);
-#pragma unroll
-        for (int n = 0; n < 2; ++n) mma_bf16_16816(sh[n], ah1, bk[n][2], bk[n][3]);
-#pragma unroll
-        for (int n = 0; n < 2; ++n) mma_bf16_16816(sl[n], al1, bk[n][2], bk[n][3]);
+        for (int n = 0; n < NG; ++n) mma_bf16_16816(sl[n], ka, qfl[n][ks][0], qfl[n][ks][1]);
       }
-      // ---- online softmax: row gid (entries 0, 1) and row gid + 8 (entries 2, 3) ----
-      float p[2][4];
-      float mx[2] = {-INFINITY, -INFINITY};
+      // ---- online softmax per head (a column: the 8 lanes of one tig, two rows each) ----
+      float p[NG][4], corr[NG][2];
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < NG; ++n) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int pos = n * 8 + tig * 2 + (i & 1);
-          const float sv = pos < nv ? (sh[n][i] + sl[n][i]) * a.scale : -INFINITY;
-          p[n][i] = sv;
-          mx[i >> 1] = fmaxf(mx[i >> 1], sv);
+          const int pos = gid + 8 * (i >> 1), hh = n * 8 + 2 * tig + (i & 1);
+          p[n][i] = (pos < nv && hh < g) ? (sh[n][i] + sl[n][i]) * a.scale : -INFINITY;
         }
-      float corr[2] = {1.f, 1.f};
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        if (r == 1 && !row1) break;
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        const float mnew = fmaxf(mrow[r], mx[r]);  // finite: position 0 of the chunk is valid
-        corr[r] = mrow[r] == -INFINITY ? 0.f : expf(mrow[r] - mnew);
-        mrow[r] = mnew;
+        for (int hc = 0; hc < 2; ++hc) {
+          float mx = fmaxf(p[n][hc], p[n][2 + hc]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(mrow[n][hc], mx);  // -inf only for a padding head
+          corr[n][hc] = mrow[n][hc] == -INFINITY ? 0.f : expf(mrow[n][hc] - mnew);
+          mrow[n][hc] = mnew;
+          const float w0 = p[n][hc] == -INFINITY ? 0.f : expf(p[n][hc] - mnew);
+          const float w1 = p[n][2 + hc] == -INFINITY ? 0.f : expf(p[n][2 + hc] - mnew);
+          p[n][hc] = w0;
+          p[n][2 + hc] = w1;
+          lrow[n][hc] = fmaf(lrow[n][hc], corr[n][hc], w0 + w1);
+        }
       }
-      float rs[2] = {0.f, 0.f};
-#pragma unroll
-      for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = i >> 1;
-          const bool live = r == 0 ? row0v : row1;
-          const float w = (!live || p[n][i] == -INFINITY) ? 0.f : expf(p[n][i] - mrow[r]);
-          p[n][i] = w;
-          rs[r] += w;
-        }
-      lrow[0] = fmaf(lrow[0], corr[0], rs[0]);
-      lrow[1] = fmaf(lrow[1], corr[1], rs[1]);
       // the outputs need rescaling only when a running maximum moved
-      if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
+      bool same = true;
 #pragma unroll
-        for (int n = 0; n < NTO; ++n) {
-          o[n][0] *= corr[0];
-          o[n][1] *= corr[0];
-          o[n][2] *= corr[1];
-          o[n][3] *= corr[1];
+      for (int n = 0; n < NG; ++n) same = same && corr[n][0] == 1.f && corr[n][1] == 1.f;
+      if (!__all_sync(0xffffffffu, same)) {
+#pragma unroll
+        for (int n = 0; n < NG; ++n)
+#pragma unroll
+          for (int dt = 0; dt < DT; ++dt) {
+            o[n][dt][0] *= corr[n][0];
+            o[n][dt][1] *= corr[n][1];
+            o[n][dt][2] *= corr[n][0];
+            o[n][dt][3] *= corr[n][1];
+          }
+      }
+      // ---- values O^T += V^T P^T: the weights as the B operand (k = positions, n = heads),
+      // gathered from the score fragments: lane (gid = head, tig = t) takes positions 2t, 2t + 1
+      // from lane 8t + gid/2 and lane 8t + 4 + gid/2, rows gid and gid + 8 ----
+      uint32_t pfh[NG][2], pfl[NG][2];
+      {
+        const int sa = 8 * tig + (gid >> 1), sb = sa + 4;
+        const bool odd = gid & 1;
+#pragma unroll
+        for (int n = 0; n < NG; ++n) {
+          const float a0 = __shfl_sync(0xffffffffu, p[n][0], sa), a1 = __shfl_sync(0xffffffffu, p[n][1], sa);
+          const float a2 = __shfl_sync(0xffffffffu, p[n][2], sa), a3 = __shfl_sync(0xffffffffu, p[n][3], sa);
+          const float b0 = __shfl_sync(0xffffffffu, p[n][0], sb), b1 = __shfl_sync(0xffffffffu, p[n][1], sb);
+          const float b2 = __shfl_sync(0xffffffffu, p[n][2], sb), b3 = __shfl_sync(0xffffffffu, p[n][3], sb);
+          split_bf16x2(odd ? a1 : a0, odd ? b1 : b0, pfh[n][0], pfl[n][0]);  // positions 2t, 2t + 1
+          split_bf16x2(odd ? a3 : a2, odd ? b3 : b2, pfh[n][1], pfl[n][1]);  // positions 2t + 8, 2t + 9
         }
       }
-      // ---- values O += P V: one k-step of 16 positions, P as bf16 hi + lo ----
-      {
-        uint32_t ph[4], pl[4];
-        split_bf16x2(p[0][0], p[0][1], ph[0], pl[0]);
-        split_bf16x2(p[0][2], p[0][3], ph[1], pl[1]);
-        split_bf16x2(p[1][0], p[1][1], ph[2], pl[2]);
-        split_bf16x2(p[1][2], p[1][3], ph[3], pl[3]);
-        // matrices: positions 0-7 and 8-15 for dims n*8.., then for dims (n+1)*8..
-        uint32_t bv[NTO / 2][4];
 #pragma unroll
-        for (int n = 0; n < NTO; n += 2) ldsm_x4_t(vreg + swz_off((mi & 1) * 8 + mr, n + (mi >> 1)), bv[n / 2]);
-        // the hi products of every output tile, then the lo products: NTO issues apart
+      for (int dt = 0; dt < DT; ++dt) {
+        // matrices (transposed): positions 0-7 of dims dt*16 + 0..7 and + 8..15, then 8-15
+        uint32_t va[4];
+        ldsm_x4_t(vreg + swz_off((mi >> 1) * 8 + mr, 2 * dt + (mi & 1)), va);
 #pragma unroll
-        for (int n = 0; n < NTO; n += 2) {
-          mma_bf16_16816(o[n], ph, bv[n / 2][0], bv[n / 2][1]);
-          mma_bf16_16816(o[n + 1], ph, bv[n / 2][2], bv[n / 2][3]);
-        }
+        for (int n = 0; n < NG; ++n) mma_bf16_16816(o[n][dt], va, pfh[n][0], pfh[n][1]);
 #pragma unroll
-        for (int n = 0; n < NTO; n += 2) {
-          mma_bf16_16816(o[n], pl, bv[n / 2][0], bv[n / 2][1]);
-          mma_bf16_16816(o[n + 1], pl, bv[n / 2][2], bv[n / 2][3]);
-        }
+        for (int n = 0; n < NG; ++n) mma_bf16_16816(o[n][dt], va, pfl[n][0], pfl[n][1]);
       }
       __syncwarp();
       if (lane == 0)
@@ -804,23 +870,27 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     }
     // ---- the unit's end: warp partials, the CTA's partial, the split merge ----
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-      const int h = gid + 8 * r;
-      if (h < g) {
-        float* wp = wpart + (warp * g + h) * (HD + 2);
+    for (int n = 0; n < NG; ++n)
 #pragma unroll
-        for (int n = 0; n < NTO; ++n) {
-          wp[n * 8 + tig * 2] = o[n][2 * r];
-          wp[n * 8 + tig * 2 + 1] = o[n][2 * r + 1];
-        }
-        if (tig == 0) {
-          wp[HD] = mrow[r];
-          wp[HD + 1] = lrow[r];
+      for (int hc = 0; hc < 2; ++hc) {
+        float l = lrow[n][hc];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int h = n * 8 + 2 * tig + hc;
+        if (h < g) {
+          float* wp = wpart + (warp * g + h) * (HD + 2);
+#pragma unroll
+          for (int dt = 0; dt < DT; ++dt) {
+            wp[dt * 16 + gid] = o[n][dt][hc];
+            wp[dt * 16 + gid + 8] = o[n][dt][2 + hc];
+          }
+          if (gid == 0) {
+            wp[HD] = mrow[n][hc];
+            wp[HD + 1] = l;
+          }
         }
       }
-    }
     __syncthreads();
     for (int idx = tid; idx < g * (HD + 2); idx += NT) {
       const int h = idx / (HD + 2), e = idx - h * (HD + 2);
@@ -844,6 +914,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
       load_q(b2, j2);
     }
     __syncthreads();
+    if (clus) {
+      cluster_merge(b, j);
+      continue;
+    }
     float* outb = a.out + (size_t)b * a.out_stride + (size_t)j * g * HD;
     // the CTAs holding chunks of this (row, kv head): with at least one chunk per CTA they are
     // first..last; with fewer chunks than CTAs each holds one chunk
@@ -921,6 +995,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
 // ---------------------------------------------------------------------------------------
 
 using AttnFn = void (*)(const CUtensorMap, const AttnArgs);
+using MmaFn = void (*)(const CUtensorMap, const CUtensorMap, const AttnArgs);
+
+// the tensor-core kernel for a head size (64 or 128) and group size (one or two 8-head tiles)
+static MmaFn mma_fn(int hd, int g) {
+  if (hd == 64) return g <= 8 ? attn_mma_kernel<64, 1> : attn_mma_kernel<64, 2>;
+  return g <= 8 ? attn_mma_kernel<128, 1> : attn_mma_kernel<128, 2>;
+}
 
 template <int KT, int HD>
 static AttnFn pick_gm(int g, size_t* smem, int ns, int* nw) {
@@ -980,7 +1061,7 @@ cudaError_t attn_prepare(int max_smem_optin) {
         if (e != cudaSuccess) return e;
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) cudaGetLastError();
       }
-  for (auto fn : {attn_mma_kernel<64>, attn_mma_kernel<128>}) {
+  for (auto fn : {attn_mma_kernel<64, 1>, attn_mma_kernel<64, 2>, attn_mma_kernel<128, 1>, attn_mma_kernel<128, 2>}) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin - 64);
     if (e != cudaSuccess) return e;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) cudaGetLastError();
@@ -1000,7 +1081,7 @@ cudaError_t attn_prepare(int max_smem_optin) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, attn_mma_kernel<128>, &cfg) == cudaSuccess && nclusters >= 1)
+    if (cudaOccupancyMaxActiveClusters(&nclusters, attn_mma_kernel<128, 1>, &cfg) == cudaSuccess && nclusters >= 1)
       g_max_cluster = 16;
     cudaGetLastError();
   }
@@ -1075,18 +1156,22 @@ static int max_active_clusters(const void* fn, size_t smem, int threads, int cs)
 
 // The splits merge inside a cluster only when every cluster of the launch runs at once (a second
 // wave of clusters would double the time); otherwise through global partials.
-bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters) {
+bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters, int cap) {
+  if (attn_uses_mma(kt, hd)) {
+    // the tensor-core kernel: clusters of kMmaCluster CTAs per (row, kv head) when they all run at
+    // once and each CTA's share of a full cache is small (a long cache wants every SM streaming
+    // it), else the persistent split over every SM with global partials
+    if ((size_t)cap * hd * 2 * 2 / kMmaCluster > kMmaClusterMaxBytes) return false;
+    const void* f = (const void*)mma_fn(hd, g);
+    const size_t smem = hd == 64 ? attn_mma_smem<64>(g) : attn_mma_smem<128>(g);
+    return clusters <= max_active_clusters(f, smem, kMmaWarps * 32, kMmaCluster);
+  }
   if (ns == 1) return true;
   if (ns > attn_max_cluster()) return false;
   size_t smem = 0;
   int nw = 0;
-  const void* f = nullptr;
-  if (attn_uses_mma(kt, hd)) {
-    return false;  // the persistent kernel merges through global partials
-  } else {
-    f = (const void*)pick(kt, hd, g, &smem, ns, &nw);
-    if (!f) return false;
-  }
+  const void* f = (const void*)pick(kt, hd, g, &smem, ns, &nw);
+  if (!f) return false;
   return clusters <= max_active_clusters(f, smem, nw * 32, ns);
 }
 
@@ -1096,19 +1181,23 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   size_t smem = 0;
   int nw = 0;
   AttnFn fn = nullptr;
-  void (*mfn)(const CUtensorMap, const CUtensorMap, const AttnArgs) = nullptr;
+  MmaFn mfn = nullptr;
   if (attn_uses_mma(kt, a.hd)) {
-    mfn = a.hd == 64 ? attn_mma_kernel<64> : attn_mma_kernel<128>;
+    mfn = mma_fn(a.hd, a.g);
     smem = a.hd == 64 ? attn_mma_smem<64>(a.g) : attn_mma_smem<128>(a.g);
     nw = kMmaWarps;
   } else {
     fn = pick(kt, a.hd, a.g, &smem, a.ns, &nw);
     if (!fn) return cudaErrorInvalidValue;
   }
-  a.cluster = attn_cluster_merge(kt, a.hd, a.g, a.ns, a.B * a.kv) ? 1 : 0;
+  a.cluster = attn_cluster_merge(kt, a.hd, a.g, a.ns, a.B * a.kv, a.cap) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ns, a.kv, a.B);
-  if (mfn) {
+  if (mfn && a.cluster) {
+    // one cluster per (row, kv head)
+    a.ns = kMmaCluster;
+    cfg.gridDim = dim3(a.B * a.kv * kMmaCluster);
+  } else if (mfn) {
     // persistent: one CTA per SM, each walking (row, kv head, split) units
     static int sms = 0;
     if (!sms) {

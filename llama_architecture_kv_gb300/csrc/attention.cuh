@@ -36,9 +36,10 @@ bool attn_make_kmap(CUtensorMap* map, const void* kc, int kt, int hd, uint64_t r
 bool attn_uses_mma(int kt, int hd);
 // partial slots per (row, kv head) the kernels need for ns splits
 int attn_part_slots(int kt, int hd, int ns);
-// whether ns splits of `clusters` (row, kv head) pairs merge inside thread-block clusters; the
-// first call for a shape queries the device (make it outside stream capture)
-bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters);
+// whether ns splits of `clusters` (row, kv head) pairs merge inside thread-block clusters (the
+// tensor-core kernel: clusters of its own size, for caches of at most cap positions); the first
+// call for a shape queries the device (make it outside stream capture)
+bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters, int cap);
 cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a, int kt, cudaStream_t s,
                         bool pdl);
 

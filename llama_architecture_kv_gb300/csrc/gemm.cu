@@ -37,7 +37,6 @@ namespace llm {
 constexpr uint64_t kTcWaitCycles = 4000000000ull;  // SM cycles: about 2 s at 2 GHz
 constexpr int kTcStages = 4;
 constexpr uint32_t kTcA = 128 * 128;               // activation tile: 128 MMA rows x 128 bytes
-constexpr uint32_t kTcStageMax = kTcA + kTcN * 128;  // activation tile + a weight tile of up to 256 rows
 constexpr int kXchgPitch = 33;                     // floats per exchange row (conflict-free)
 
 __global__ void __launch_bounds__(kTcThreads, 1)

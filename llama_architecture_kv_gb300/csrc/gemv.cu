@@ -326,15 +326,16 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
 // batch 1, bf16: each warp streams its rows through its own ring of bulk copies
 // ---------------------------------------------------------------------------------------
 // Rows are taken two at a time (a "group": a RoPE pair, a (gate, up) pair, or two neighbouring
-// rows); a CTA owns a contiguous, balanced range of groups and warp w takes groups w, w + 8, ...
-// A step of a warp is the same 4 KB piece of both rows of a group, copied by lane 0 into a ring
-// slot with two cp.async.bulk copies on one mbarrier; `ns` steps are in flight per warp, so the
-// bytes in flight no longer depend on registers.  The first steps are requested before the wait
-// on the previous kernel (the weights do not depend on it).  Lane l multiplies 16-byte chunks
-// l, l + 32, ... of both pieces with the (normalized) input, which sits in shared memory as f32
-// in two planes (elements 0-3 and 4-7 of every 8-element chunk) so that the loads of a warp are
-// contiguous; each input load serves both rows.  A row's sum is a warp reduction; the epilogues
-// are those of gemv_kernel.
+// rows); a CTA owns a contiguous, balanced range of groups.  A step is the same 4 KB piece of
+// both rows of a group; the CTA's steps (group-major) are dealt to its warps in turn, so warps
+// differ by at most one step.  Lane 0 of a warp copies its steps into a private ring of slots
+// (two cp.async.bulk copies on one mbarrier per slot), `ns` steps ahead, so the bytes in flight
+// no longer depend on registers; the first steps are requested before the wait on the previous
+// kernel (the weights do not depend on it).  Lane l multiplies 16-byte chunks l, l + 32, ... of
+// both pieces with the (normalized) input, which sits in shared memory as f32 in two planes
+// (elements 0-3 and 4-7 of every 8-element chunk) so that the loads of a warp are contiguous and
+// each serves both rows.  A step's two sums (warp reductions) go to shared memory; at the end the
+// threads add each row's pieces in order and run the epilogues of gemv_kernel.
 constexpr int kTmaWarps = 8;
 constexpr int kPiece = 4096;              // bytes of one row per step
 constexpr int kStepBytes = 2 * kPiece;    // both rows of a group
@@ -343,8 +344,10 @@ constexpr uint64_t kTmaWaitCycles = 4000000000ull;  // SM cycles: about 2 s at 2
 static int g_smem_optin = 0;              // set by gemv_prepare
 
 static LLM_HD size_t gemv_tma_x_bytes(int cols) { return ((size_t)cols * 4 + 1023) & ~(size_t)1023; }
-static size_t gemv_tma_smem(int cols, int ns) {
-  return gemv_tma_x_bytes(cols) + (size_t)kTmaWarps * ns * (kStepBytes + 8);
+static LLM_HD int gemv_tma_ppr(int cols) { return (int)(((size_t)cols * 2 + kPiece - 1) / kPiece); }
+// input planes, ring slots, their mbarriers, and two partial sums per step of at most maxg groups
+static size_t gemv_tma_smem(int cols, int ns, int maxg) {
+  return gemv_tma_x_bytes(cols) + (size_t)kTmaWarps * ns * (kStepBytes + 8) + (size_t)maxg * gemv_tma_ppr(cols) * 8;
 }
 
 template <int EPI, bool NORM>
@@ -357,6 +360,7 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
   uint8_t* ring = gsm + gemv_tma_x_bytes(cols);
   const uint32_t ring_s = smem_u32(ring);
   const uint32_t bars = ring_s + (uint32_t)(NW * ns * kStepBytes);
+  float* part = reinterpret_cast<float*>(ring + (size_t)NW * ns * (kStepBytes + 8));  // [steps][2]
   __shared__ float red[NW];
   __shared__ float s_inv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -365,9 +369,9 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
   const int g0 = (int)(((long long)groups * blockIdx.x) / gridDim.x);
   const int g1 = (int)(((long long)groups * (blockIdx.x + 1)) / gridDim.x);
   const size_t row_bytes = (size_t)cols * 2;
-  const int ppr = (int)((row_bytes + kPiece - 1) / kPiece);  // pieces per row
-  const int ng = g1 - g0 > warp ? (g1 - g0 - warp + NW - 1) / NW : 0;
-  const int total = ng * ppr;  // steps of this warp
+  const int ppr = gemv_tma_ppr(cols);  // pieces per row
+  const int nsteps = (g1 - g0) * ppr;  // steps of the CTA; this warp's are warp, warp + NW, ...
+  const int total = nsteps > warp ? (nsteps - warp + NW - 1) / NW : 0;
   const char* W = (const char*)a.W;
 
   if (tid == 0) {
@@ -375,10 +379,11 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
     mbar_fence_init();
   }
   __syncthreads();
-  // step t of this warp: piece t % ppr of the rows of group g0 + warp + (t / ppr) * NW
+  // step t of this warp: CTA step q = warp + t * NW, piece q % ppr of the rows of group g0 + q / ppr
   auto issue = [&](int t) {
-    const int ig = t / ppr, pc = t - ig * ppr;
-    const size_t r0 = 2 * (size_t)(g0 + warp + ig * NW);
+    const int q = warp + t * NW;
+    const int ig = q / ppr, pc = q - ig * ppr;
+    const size_t r0 = 2 * (size_t)(g0 + ig);
     const size_t r1 = r0 + 1 < (size_t)a.rows ? r0 + 1 : r0;  // an odd last row is read twice
     const size_t off = (size_t)pc * kPiece;
     const uint32_t bytes = (uint32_t)(row_bytes - off < (size_t)kPiece ? row_bytes - off : (size_t)kPiece);
@@ -452,7 +457,8 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
     ok = __all_sync(0xffffffffu, mbar_wait(bars + 8u * (warp * ns + slot), (uint32_t)(t / ns) & 1u, kTmaWaitCycles));
     if (!ok) break;
     consumed = t + 1;
-    const int ig = t / ppr, pc = t - ig * ppr;
+    const int q = warp + t * NW;
+    const int pc = q - (q / ppr) * ppr;
     const size_t off = (size_t)pc * kPiece;
     const int nch = (int)((row_bytes - off < (size_t)kPiece ? row_bytes - off : (size_t)kPiece) >> 4);
     const uint8_t* w0 = ring + (size_t)(warp * ns + slot) * kStepBytes;
@@ -469,42 +475,13 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
       fence_proxy_async_smem();  // this slot's reads come before the copy that refills it
       issue(t + ns);
     }
-    if (pc == ppr - 1) {
+    {
       const float v0 = warp_sum(a0[0] + a0[1]);
       const float v1 = warp_sum(a1[0] + a1[1]);
       a0[0] = a0[1] = a1[0] = a1[1] = 0.f;
-      const int g = g0 + warp + ig * NW;
       if (lane == 0) {
-        if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
-          const int r0 = 2 * g;
-          a.out[r0] = EPI == EPI_RESID ? __fadd_rn(a.resid[r0], v0) : v0;
-          if (r0 + 1 < a.rows) a.out[r0 + 1] = EPI == EPI_RESID ? __fadd_rn(a.resid[r0 + 1], v1) : v1;
-        } else if constexpr (EPI == EPI_SWIGLU) {
-          const float si = __fdiv_rn(v0, __fadd_rn(1.0f, expf(-v0)));
-          a.out[g] = __fmul_rn(si, v1);
-        } else {
-          const int R = 2 * g;
-          const int pos = a.step->pos, half = a.hd >> 1;
-          const int head = R / a.hd, e = (R - head * a.hd) >> 1;
-          if (head < a.H + a.kv) {
-            const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];
-            const float lo = __fadd_rn(__fmul_rn(v0, c), __fmul_rn(-v1, s));
-            const float hi = __fadd_rn(__fmul_rn(v1, c), __fmul_rn(v0, s));
-            if (head < a.H) {
-              float* q = a.q_out + (size_t)head * a.hd;
-              q[e] = lo;
-              q[e + half] = hi;
-            } else {
-              const size_t ci = ((size_t)(head - a.H) * a.cap + pos) * a.hd;
-              store_elem<1>(a.kc, ci + e, lo);
-              store_elem<1>(a.kc, ci + e + half, hi);
-            }
-          } else {
-            const size_t ci = ((size_t)(head - a.H - a.kv) * a.cap + pos) * a.hd;
-            store_elem<1>(a.vc, ci + e, v0);
-            store_elem<1>(a.vc, ci + e + half, v1);
-          }
-        }
+        part[2 * q] = v0;
+        part[2 * q + 1] = v1;
       }
     }
   }
@@ -513,6 +490,46 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
     // no copy may still be writing shared memory when the CTA exits
     for (int t = consumed; t < total && t < consumed + ns; ++t)
       mbar_wait(bars + 8u * (warp * ns + t % ns), (uint32_t)(t / ns) & 1u, kTmaWaitCycles);
+  }
+  __syncthreads();
+  // ---- epilogue: each group's two rows, pieces added in order ----
+  for (int i = tid; i < g1 - g0; i += NW * 32) {
+    float v0 = 0.f, v1 = 0.f;
+    for (int pc = 0; pc < ppr; ++pc) {
+      v0 += part[2 * (i * ppr + pc)];
+      v1 += part[2 * (i * ppr + pc) + 1];
+    }
+    const int g = g0 + i;
+    if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+      const int r0 = 2 * g;
+      a.out[r0] = EPI == EPI_RESID ? __fadd_rn(a.resid[r0], v0) : v0;
+      if (r0 + 1 < a.rows) a.out[r0 + 1] = EPI == EPI_RESID ? __fadd_rn(a.resid[r0 + 1], v1) : v1;
+    } else if constexpr (EPI == EPI_SWIGLU) {
+      const float si = __fdiv_rn(v0, __fadd_rn(1.0f, expf(-v0)));
+      a.out[g] = __fmul_rn(si, v1);
+    } else {
+      const int R = 2 * g;
+      const int pos = a.step->pos, half = a.hd >> 1;
+      const int head = R / a.hd, e = (R - head * a.hd) >> 1;
+      if (head < a.H + a.kv) {
+        const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];
+        const float lo = __fadd_rn(__fmul_rn(v0, c), __fmul_rn(-v1, s));
+        const float hi = __fadd_rn(__fmul_rn(v1, c), __fmul_rn(v0, s));
+        if (head < a.H) {
+          float* qo = a.q_out + (size_t)head * a.hd;
+          qo[e] = lo;
+          qo[e + half] = hi;
+        } else {
+          const size_t ci = ((size_t)(head - a.H) * a.cap + pos) * a.hd;
+          store_elem<1>(a.kc, ci + e, lo);
+          store_elem<1>(a.kc, ci + e + half, hi);
+        }
+      } else {
+        const size_t ci = ((size_t)(head - a.H - a.kv) * a.cap + pos) * a.hd;
+        store_elem<1>(a.vc, ci + e, v0);
+        store_elem<1>(a.vc, ci + e + half, v1);
+      }
+    }
   }
 }
 
@@ -564,13 +581,15 @@ GemvPlan plan_gemv(int rows, int cols, int rg, int wt, int B, int num_sms, int c
   // smaller footprint leaving room for the next kernel's CTAs); one CTA per SM
   p.tma_ns = 0;
   if (B == 1 && wt == 1 && cols % 8 == 0 && g_smem_optin > 0) {
+    const int groups = (rows + 1) / 2;
+    const int grid = groups < num_sms ? groups : num_sms;
+    const int maxg = (groups + grid - 1) / grid;
     int ns = kTmaMaxSteps;
-    while (ns >= 2 && gemv_tma_smem(cols, ns) + 1024 > (size_t)g_smem_optin) --ns;
+    while (ns >= 2 && gemv_tma_smem(cols, ns, maxg) + 1024 > (size_t)g_smem_optin) --ns;
     if (ns >= 2) {
-      const int groups = (rows + 1) / 2;
       p.tma_ns = ns;
-      p.tma_grid = groups < num_sms ? groups : num_sms;
-      p.tma_smem = gemv_tma_smem(cols, ns);
+      p.tma_grid = grid;
+      p.tma_smem = gemv_tma_smem(cols, ns, maxg);
     }
   }
   return p;

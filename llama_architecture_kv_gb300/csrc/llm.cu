@@ -821,7 +821,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   for (int b = 1; b <= c.max_batch; ++b) {
     const int ns = attn_splits(b, c.kv_heads, c.max_seq, h->num_sms);
     maxns = std::max(maxns, ns);
-    attn_cluster_merge(h->wt, h->hd, c.group, ns, b * c.kv_heads);  // device queries before any capture
+    attn_cluster_merge(h->wt, h->hd, c.group, ns, b * c.kv_heads, c.max_seq);  // device queries before any capture
   }
   h->part_ns = maxns;
   const int slots = attn_part_slots(h->wt, h->hd, maxns);
