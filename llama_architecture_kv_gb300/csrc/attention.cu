@@ -98,6 +98,18 @@ LLM_D uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
+LLM_D void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+LLM_D void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+LLM_D void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// the address in CTA `rank`'s shared memory of the one `local` has here
+LLM_D uint32_t map_rank(uint32_t local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+LLM_D void st_cluster(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 // a float in the shared memory of CTA `rank` of this cluster, at the address `p` has here
 LLM_D float ld_cluster(const float* p, uint32_t rank) {
   uint32_t local = (uint32_t)__cvta_generic_to_shared(p), remote;
@@ -524,15 +536,18 @@ struct MmaShape {
   static constexpr int KS = HD / 16;        // k-steps of the scores
 };
 
+constexpr int kMmaCluster = 8;     // CTAs per (row, kv head) in cluster mode (portable size)
+
 // shared memory of the kernel with nr ring slots per warp
 template <int HD>
-LLM_HD size_t attn_mma_smem_nr(int g, int nr) {
+LLM_HD size_t attn_mma_smem_nr(int g, int nr, bool cluster = false) {
   using M = MmaShape<HD>;
   size_t s = 1024 + (size_t)kMmaWarps * nr * M::BUF;
   s += 2 * 16 * (size_t)M::QP * 2;            // queries hi, lo
   s += (size_t)kMmaWarps * g * (HD + 2) * 4;  // warp partials
   s += (size_t)g * (HD + 2) * 4;              // CTA partial
   s += (size_t)g * 64 * 4;                    // merge factors
+  if (cluster) s += (size_t)kMmaCluster * g * (HD + 2) * 4;  // cluster mode: every rank's partial
   s = (s + 7) & ~(size_t)7;
   s += (size_t)kMmaWarps * nr * 8;            // mbarriers
   return s;
@@ -540,15 +555,13 @@ LLM_HD size_t attn_mma_smem_nr(int g, int nr) {
 // ring slots per warp: three for 64-dimension heads, two for 128 (measured faster than three at
 // both batch 1 and 32 on the 8B shape), two wherever three would not fit
 template <int HD>
-LLM_HD int attn_mma_nr(int g) { return HD <= 64 && attn_mma_smem_nr<HD>(g, 3) <= 232448 - 64 ? 3 : 2; }
+LLM_HD int attn_mma_nr(int g) { return HD <= 64 && attn_mma_smem_nr<HD>(g, 3) <= 232448 - 1024 ? 3 : 2; }
 
 constexpr int kMmaMaxSplits = 64;  // splits of one (row, kv head) the persistent kernel merges
-constexpr int kMmaMaxCluster = 16; // most CTAs of one cluster in cluster mode
-constexpr int kMmaCluster = 8;     // the cluster size used (portable)
 constexpr size_t kMmaClusterMaxBytes = 1u << 20;  // most cache bytes per CTA in cluster mode
 
 template <int HD>
-LLM_HD size_t attn_mma_smem(int g) { return attn_mma_smem_nr<HD>(g, attn_mma_nr<HD>(g)); }
+LLM_HD size_t attn_mma_smem(int g, bool cluster = false) { return attn_mma_smem_nr<HD>(g, attn_mma_nr<HD>(g), cluster); }
 
 // byte offset of 16-byte piece c of row r in a chunk tile stored as 128-byte-wide swizzled boxes
 // of kMmaChunk rows
@@ -582,8 +595,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   float* wpart = reinterpret_cast<float*>(qbase + 2 * 16 * QP);                       // [NW][g][HD+2]
   float* mypart = wpart + NW * g * (HD + 2);                                           // [g][HD+2]
   float* fac = mypart + g * (HD + 2);                                                  // [g][kMmaMaxSplits]
-  const uint32_t bars = (smem_u32(fac + g * kMmaMaxSplits) + 7u) & ~7u;
+  float* cpart = fac + g * kMmaMaxSplits;  // cluster mode: [rank][g][HD+2], filled in rank 0
+  const uint32_t bars = (smem_u32(cpart + (a.cluster ? kMmaCluster * g * (HD + 2) : 0)) + 7u) & ~7u;
   __shared__ int s_last;
+  __shared__ float wfac[kMmaWarps * 16];   // per head, each warp's factor exp(m_w - M)
 
   const int t = a.step->pos;
   const int npos = t + 1;
@@ -613,6 +628,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     mbar_fence_init();
   }
   __syncthreads();
+  if (clus) cluster_arrive_relaxed();  // waited for before the first access to another CTA
 
   // the issuing side of this warp (lane 0): cursor over (segment, chunk) pairs
   long long ist = c0, inext = c0;
@@ -683,46 +699,38 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   bool ok = true;
   int consumed = 0;
 
-  // the splits of (row b, kv head j) merge through distributed shared memory: every CTA of the
-  // cluster reads all ranks' (m, l), forms the factors, and writes its share of the outputs
+  // the splits of (row b, kv head j) merge in rank 0: every CTA stores its partial into rank 0's
+  // shared memory (distributed shared memory), one cluster barrier publishes them, and rank 0
+  // merges them in rank order (the order of the positions) and writes the output
   auto cluster_merge = [&](int b, int j) {
     const int cs = a.ns;
-    cluster_sync_all();
-    for (int idx = tid; idx < g * cs; idx += NT) {
-      const int h = idx / cs, r = idx - h * cs;
-      fac[h * kMmaMaxSplits + r] = ld_cluster(mypart + h * (HD + 2) + HD, r);
-      fac[h * kMmaMaxSplits + 32 + r] = ld_cluster(mypart + h * (HD + 2) + HD + 1, r);
-    }
-    __syncthreads();
+    cluster_wait();  // every CTA of the cluster has started
+    const uint32_t dst = map_rank(smem_u32(cpart + crank * g * (HD + 2)), 0);
+    for (int idx = tid; idx < g * (HD + 2); idx += NT) st_cluster(dst + 4u * idx, mypart[idx]);
+    cluster_arrive();
+    cluster_wait();  // every partial is in rank 0 (and no CTA leaves with its stores in flight)
+    if (crank != 0) return;
     for (int h = tid; h < g; h += NT) {
       float Mx = -INFINITY;
-      for (int r = 0; r < cs; ++r) Mx = fmaxf(Mx, fac[h * kMmaMaxSplits + r]);
+      for (int r = 0; r < cs; ++r) Mx = fmaxf(Mx, cpart[(r * g + h) * (HD + 2) + HD]);
       float L = 0.f;
       for (int r = 0; r < cs; ++r) {
-        const float mr = fac[h * kMmaMaxSplits + r];
+        const float mr = cpart[(r * g + h) * (HD + 2) + HD];
         const float f = mr == -INFINITY ? 0.f : expf(mr - Mx);
         fac[h * kMmaMaxSplits + r] = f;
-        L += fac[h * kMmaMaxSplits + 32 + r] * f;
+        L += cpart[(r * g + h) * (HD + 2) + HD + 1] * f;
       }
       const float rl = 1.0f / L;
       for (int r = 0; r < cs; ++r) fac[h * kMmaMaxSplits + r] *= rl;
     }
     __syncthreads();
     float* outb = a.out + (size_t)b * a.out_stride + (size_t)j * g * HD;
-    const int n_out = g * HD, i0 = n_out * crank / cs, i1 = n_out * (crank + 1) / cs;
-    for (int idx = i0 + tid; idx < i1; idx += NT) {
+    for (int idx = tid; idx < g * HD; idx += NT) {
       const int h = idx / HD, e = idx - h * HD;
-      float ov[kMmaMaxCluster];
-#pragma unroll
-      for (int r = 0; r < kMmaMaxCluster; ++r)
-        if (r < cs) ov[r] = ld_cluster(mypart + h * (HD + 2) + e, r);
       float O = 0.f;
-#pragma unroll
-      for (int r = 0; r < kMmaMaxCluster; ++r)
-        if (r < cs) O = fmaf(fac[h * kMmaMaxSplits + r], ov[r], O);
+      for (int r = 0; r < cs; ++r) O = fmaf(fac[h * kMmaMaxSplits + r], cpart[(r * g + h) * (HD + 2) + e], O);
       outb[(size_t)h * HD + e] = O;
     }
-    cluster_sync_all();  // every CTA keeps its shared memory until the others have read it
   };
   if (clus && c0 == c1) {
     // no chunks here: an empty part (o = 0, m = -inf, l = 0) joins the merge
@@ -892,19 +900,22 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
         }
       }
     __syncthreads();
+    // the CTA's partial: per head the maximum M over the warps and each warp's factor
+    // exp(m_w - M), then the factor-weighted sums of o and l in warp order
+    for (int i = tid; i < g * NW; i += NT) {
+      const int h = i / NW, w = i - h * NW;
+      float Mx = -INFINITY;
+      for (int w2 = 0; w2 < NW; ++w2) Mx = fmaxf(Mx, wpart[(w2 * g + h) * (HD + 2) + HD]);
+      const float mw = wpart[(w * g + h) * (HD + 2) + HD];
+      wfac[i] = mw == -INFINITY ? 0.f : expf(mw - Mx);
+      if (w == 0) mypart[h * (HD + 2) + HD] = Mx;
+    }
+    __syncthreads();
     for (int idx = tid; idx < g * (HD + 2); idx += NT) {
       const int h = idx / (HD + 2), e = idx - h * (HD + 2);
-      float Mx = -INFINITY;
-      for (int w = 0; w < NW; ++w) Mx = fmaxf(Mx, wpart[(w * g + h) * (HD + 2) + HD]);
-      float r = Mx;
-      if (e != HD) {
-        r = 0.f;
-        for (int w = 0; w < NW; ++w) {
-          const float mw = wpart[(w * g + h) * (HD + 2) + HD];
-          const float f = mw == -INFINITY ? 0.f : expf(mw - Mx);
-          r = fmaf(f, wpart[(w * g + h) * (HD + 2) + e], r);
-        }
-      }
+      if (e == HD) continue;
+      float r = 0.f;
+      for (int w = 0; w < NW; ++w) r = fmaf(wfac[h * NW + w], wpart[(w * g + h) * (HD + 2) + e], r);
       mypart[idx] = r;
     }
     if (next < c1) {  // (every warp is past this segment's chunks: the query buffer is free)
@@ -1042,6 +1053,7 @@ static AttnFn pick(int kt, int hd, int g, size_t* smem, int ns, int* nw) {
 }
 
 static int g_max_cluster = 8;  // 16 once attn_prepare finds the device can schedule it
+static int g_smem_limit = 0;   // dynamic shared memory a kernel of this file may use
 int attn_max_cluster() { return g_max_cluster; }
 
 bool attn_supported(int hd, int g) {
@@ -1061,8 +1073,12 @@ cudaError_t attn_prepare(int max_smem_optin) {
         if (e != cudaSuccess) return e;
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) cudaGetLastError();
       }
+  g_smem_limit = max_smem_optin - 1024;  // (the kernels' static shared memory is far below this margin)
   for (auto fn : {attn_mma_kernel<64, 1>, attn_mma_kernel<64, 2>, attn_mma_kernel<128, 1>, attn_mma_kernel<128, 2>}) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin - 64);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin - (int)fa.sharedSizeBytes);
     if (e != cudaSuccess) return e;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) cudaGetLastError();
   }
@@ -1163,7 +1179,8 @@ bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters, int cap) {
     // it), else the persistent split over every SM with global partials
     if ((size_t)cap * hd * 2 * 2 / kMmaCluster > kMmaClusterMaxBytes) return false;
     const void* f = (const void*)mma_fn(hd, g);
-    const size_t smem = hd == 64 ? attn_mma_smem<64>(g) : attn_mma_smem<128>(g);
+    const size_t smem = hd == 64 ? attn_mma_smem<64>(g, true) : attn_mma_smem<128>(g, true);
+    if (smem > (size_t)g_smem_limit) return false;
     return clusters <= max_active_clusters(f, smem, kMmaWarps * 32, kMmaCluster);
   }
   if (ns == 1) return true;
@@ -1191,6 +1208,7 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
     if (!fn) return cudaErrorInvalidValue;
   }
   a.cluster = attn_cluster_merge(kt, a.hd, a.g, a.ns, a.B * a.kv, a.cap) ? 1 : 0;
+  if (mfn && a.cluster) smem = a.hd == 64 ? attn_mma_smem<64>(a.g, true) : attn_mma_smem<128>(a.g, true);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ns, a.kv, a.B);
   if (mfn && a.cluster) {
