@@ -338,7 +338,8 @@ def run_ours(args):
         kname = "tc_gemm_kernel (gate/up, timed with its tc_prep_kernel: x1 = x + o_proj, norm, bf16 split)"
         traffic = traffic_from_profile("gemm.cu", "tc_gemm_gate_up_llama8b_b32.md") if w.name == "llama8b_b32" else None
     else:
-        kname = "gemv_kernel<bf16, EPI_SWIGLU> (norm + gate/up + SwiGLU)"
+        kname = ("gemv_tma_kernel<EPI_SWIGLU> (norm + gate/up + SwiGLU, bulk-copy rings)" if s.bf16 and B == 1
+                 else "gemv_kernel<EPI_SWIGLU> (norm + gate/up + SwiGLU)")
         traffic = traffic_from_profile("gemv.cu", "gate_up_gemv_llama8b_b1.md") if w.name == "llama8b_b1" else None
     roofline = {"bound": "hbm", "kernel": kname,
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
