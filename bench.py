@@ -53,6 +53,8 @@ def parse():
                     help="reference arm: layers of the model run per timed step")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--prompt", type=int, default=-1, help="override the prompt length (profiling)")
+    ap.add_argument("--rows", action="store_true",
+                    help="rows at their own positions (decode_rows): row b at P - b * (P // 2B)")
     ap.add_argument("--kernels", action="store_true",
                     help="print each kernel's isolated launch time (CUDA events) and exit")
     return ap.parse_args()
@@ -287,9 +289,18 @@ def run_ours(args):
     u_all = synth.uniforms(w.seed_uniform, 0, B * (W + K)).reshape(W + K, B)
     u_dev = torch.from_numpy(u_all).to(dev)
     temp, k_, p_ = w.temp, (w.top_k or s.vocab), w.top_p
+    # rows at their own positions: spread over the upper half of the cache
+    rowpos = (pos0 - np.arange(B, dtype=np.int32) * (pos0 // (2 * B))).astype(np.int32) if args.rows else None
+
+    def step_dev(tk, i, u, ids):
+        if rowpos is None:
+            pkg.llm_step_dev(h, tk, B, pos0 + i, temp, k_, p_, u, ids)
+        else:
+            pkg.llm_step_rows_dev(h, tk, B, rowpos + i, temp, k_, p_, u, ids)
+
     with torch.cuda.stream(stream):
         for i in range(W):  # warm-up: rewind to the prompt end every time
-            pkg.llm_step_dev(h, tok[0], B, pos0, temp, k_, p_, u_dev[i], tok[1])
+            step_dev(tok[0], 0, u_dev[i], tok[1])
         pkg.llm_synchronize(h)
         if world > 1:
             torch.distributed.barrier()
@@ -298,7 +309,7 @@ def run_ours(args):
         with ClockSampler(local) as clocks:
             e0.record(stream)
             for i in range(K):
-                pkg.llm_step_dev(h, tok[i % 2], B, pos0 + i, temp, k_, p_, u_dev[W + i], tok[(i + 1) % 2])
+                step_dev(tok[i % 2], i, u_dev[W + i], tok[(i + 1) % 2])
             e1.record(stream)
             e1.synchronize()
         pkg.llm_synchronize(h)
@@ -321,15 +332,20 @@ def run_ours(args):
     torch.cuda.synchronize()
     te = time.perf_counter()
     for i in range(E):
-        pkg.llm_step(h, tok_h if i == 0 else ids_h, B, pos0 + i, temp, k_, p_,
-                     u_h if temp > 0 else None, ids_h)
+        if rowpos is None:
+            pkg.llm_step(h, tok_h if i == 0 else ids_h, B, pos0 + i, temp, k_, p_,
+                         u_h if temp > 0 else None, ids_h)
+        else:
+            pkg.llm_step_rows(h, tok_h if i == 0 else ids_h, B, rowpos + i, temp, k_, p_,
+                              u_h if temp > 0 else None, ids_h)
     e2e_s = time.perf_counter() - te
     e2e = {"value": B * E / e2e_s, "unit": "tok/s",
            "h2d_bytes_per_step": 4 * B + (4 * B if temp > 0 else 0), "d2h_bytes_per_step": 4 * B}
 
     # the dominant kernel, timed alone (consecutive launches walk the layers: weights from HBM)
     reps = 4 * s.layers
-    kms = pkg.llm_profile_kernel(h, GATEUP, B, pos0, reps)
+    # (at a position every row has reached: rows at their own positions sit at or above their minimum)
+    kms = pkg.llm_profile_kernel(h, GATEUP, B, int(rowpos.min()) if rowpos is not None else pos0, reps)
     bytes_gu = 2 * s.ffn * s.d * (2 if s.bf16 else 4)  # algorithmic: the gate and up weights
     achieved = bytes_gu / (kms / 1e3) / 1e9
     peak, peak_kind = peaks()
@@ -350,7 +366,7 @@ def run_ours(args):
     wbytes = (pkg.llm_weight_count(model.cfg) - s.vocab * s.d) * es  # all but the embedding table
     if s.tied:
         wbytes += s.vocab * s.d * es  # the tied LM head is that table, read in full every step
-    mean_pos = pos0 + (K - 1) / 2
+    mean_pos = (float(np.mean(rowpos)) if rowpos is not None else pos0) + (K - 1) / 2
     kv_bytes = B * 2 * s.layers * s.kv * s.hd * es * (mean_pos + 1)
     step_bytes = wbytes + kv_bytes
     step_roof = {"bytes_per_step": step_bytes, "roofline_tok_s": B * peak * 1e9 / step_bytes,
@@ -380,6 +396,8 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": B, "prompt": P, "cache_positions": pos0,
                    "weights": "bf16" if s.bf16 else "f32", "kv_cache": "bf16" if s.bf16 else "f32",
                    "sampling": "greedy" if temp == 0 else f"temp {temp} top-k {k_} top-p {p_}",
+                   "positions": ("own per row (decode_rows): row b at %d - %d b" % (pos0, pos0 // (2 * B))
+                                 if rowpos is not None else "shared"),
                    "l2": "inputs larger than L2 (weights %.1f GB per step)" % (wbytes / 1e9),
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,

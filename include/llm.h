@@ -162,6 +162,30 @@ llm_status llm_sample_dev(llm_handle* h, const float* logits_dev, int32_t B, flo
 llm_status llm_step_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t pos, float temp,
                         int32_t k, float p, const float* u_dev, int32_t* ids_dev, float* logits_dev);
 
+/*
+ * Rows at their own positions (continuous batching; Llama 3.1 8B Instruct card, "Entries":
+ * decode_rows(tokens, positions)):
+ * row b takes tokens[b] at position positions_host[b], writes its key and value there and
+ * attends over its own cache positions 0..positions_host[b] inclusive; the other rows' positions
+ * do not affect it.  positions_host [B] is always host memory (read before the call returns).
+ * Checks: 1 <= B <= max_batch (else LLM_ERR_BATCH); 0 <= positions_host[b] < max_seq and
+ * positions_host[b] <= filled length of row b (else LLM_ERR_POS_RANGE); tokens in [0, vocab)
+ * (host tokens: LLM_ERR_TOKEN_RANGE; device tokens: as llm_decode_dev).  After success the
+ * filled length of row b is positions_host[b] + 1.  With every position equal these are
+ * llm_decode / llm_step bit for bit.  llm_decode_rows writes logits [B][V]; llm_step_rows
+ * samples as llm_step (ids [B], logits optional, u may be NULL when temp == 0).
+ */
+llm_status llm_decode_rows(llm_handle* h, const int32_t* tokens_host, int32_t B,
+                           const int32_t* positions_host, float* logits_host);
+llm_status llm_decode_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B,
+                               const int32_t* positions_host, float* logits_dev);
+llm_status llm_step_rows(llm_handle* h, const int32_t* tokens_host, int32_t B,
+                         const int32_t* positions_host, float temp, int32_t k, float p,
+                         const float* u_host, int32_t* ids_host, float* logits_host);
+llm_status llm_step_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B,
+                             const int32_t* positions_host, float temp, int32_t k, float p,
+                             const float* u_dev, int32_t* ids_dev, float* logits_dev);
+
 /* Wait for the handle's stream; return the first error recorded on the device since the last
  * call (LLM_ERR_TOKEN_RANGE, LLM_ERR_DEVICE_TIMEOUT) and clear it. */
 llm_status llm_synchronize(llm_handle* h);

@@ -22,7 +22,8 @@ EXPORTS = ("llm_weight_count", "llm_create", "llm_destroy", "llm_reset", "llm_pr
            "llm_step_dev", "llm_synchronize", "llm_stream", "llm_logits_buffer", "llm_filled",
            "llm_last_error", "llm_status_string", "llm_kv_import", "llm_kv_export",
            "llm_debug_trace", "llm_profile_kernel", "llm_sample_noalloc",
-           "llm_step_kernels")
+           "llm_step_kernels", "llm_decode_rows", "llm_decode_rows_dev", "llm_step_rows",
+           "llm_step_rows_dev")
 
 
 class LlmConfig(ctypes.Structure):
@@ -68,6 +69,10 @@ def lib():
             "llm_decode_dev": ([vp, vp, i32, i32, vp], i32),
             "llm_sample_dev": ([vp, vp, i32, f32, i32, f32, vp, vp], i32),
             "llm_step_dev": ([vp, vp, i32, i32, f32, i32, f32, vp, vp, vp], i32),
+            "llm_decode_rows": ([vp, vp, i32, vp, vp], i32),
+            "llm_decode_rows_dev": ([vp, vp, i32, vp, vp], i32),
+            "llm_step_rows": ([vp, vp, i32, vp, f32, i32, f32, vp, vp, vp], i32),
+            "llm_step_rows_dev": ([vp, vp, i32, vp, f32, i32, f32, vp, vp, vp], i32),
             "llm_synchronize": ([vp], i32),
             "llm_stream": ([vp], vp),
             "llm_logits_buffer": ([vp], vp),
@@ -178,6 +183,24 @@ def llm_step_dev(h, tokens, B, pos, temp, k, p, u, ids, logits=None):
     _check(h, lib().llm_step_dev(h, _ptr(tokens), B, pos, temp, k, p, _ptr(u), _ptr(ids), _ptr(logits)))
 
 
+def llm_decode_rows(h, tokens, B, positions, logits):
+    _check(h, lib().llm_decode_rows(h, _ptr(tokens), B, _ptr(positions), _ptr(logits)))
+
+
+def llm_decode_rows_dev(h, tokens, B, positions, logits):
+    _check(h, lib().llm_decode_rows_dev(h, _ptr(tokens), B, _ptr(positions), _ptr(logits)))
+
+
+def llm_step_rows(h, tokens, B, positions, temp, k, p, u, ids, logits=None):
+    _check(h, lib().llm_step_rows(h, _ptr(tokens), B, _ptr(positions), temp, k, p, _ptr(u), _ptr(ids),
+                                  _ptr(logits)))
+
+
+def llm_step_rows_dev(h, tokens, B, positions, temp, k, p, u, ids, logits=None):
+    _check(h, lib().llm_step_rows_dev(h, _ptr(tokens), B, _ptr(positions), temp, k, p, _ptr(u), _ptr(ids),
+                                      _ptr(logits)))
+
+
 def llm_synchronize(h):
     _check(h, lib().llm_synchronize(h))
 
@@ -270,6 +293,26 @@ class Model:
         out = np.empty((tokens.size, self.V), np.float32)
         llm_decode(self.h, tokens, tokens.size, pos, out)
         return out
+
+    def decode_rows(self, tokens, positions):
+        """One token per row, row b at its own position positions[b]."""
+        tokens = np.ascontiguousarray(tokens, np.int32).reshape(-1)
+        positions = np.ascontiguousarray(positions, np.int32).reshape(-1)
+        assert positions.size == tokens.size
+        out = np.empty((tokens.size, self.V), np.float32)
+        llm_decode_rows(self.h, tokens, tokens.size, positions, out)
+        return out
+
+    def step_rows(self, tokens, positions, temp=0.0, k=1, p=1.0, u=None, logits=False):
+        tokens = np.ascontiguousarray(tokens, np.int32).reshape(-1)
+        positions = np.ascontiguousarray(positions, np.int32).reshape(-1)
+        assert positions.size == tokens.size
+        B = tokens.size
+        ids = np.empty(B, np.int32)
+        out = np.empty((B, self.V), np.float32) if logits else None
+        u = None if u is None else np.ascontiguousarray(u, np.float32)
+        llm_step_rows(self.h, tokens, B, positions, temp, k, p, u, ids, out)
+        return (ids, out) if logits else ids
 
     def sample(self, logits, temp, k, p, u):
         logits = np.ascontiguousarray(logits, np.float32)

@@ -309,8 +309,8 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   float* fac = mypart + g * (HD + 2);                    // [g][kAttnMaxCluster]
   const uint32_t bars = (smem_u32(fac + g * kAttnMaxCluster) + 7u) & ~7u;
 
-  // positions 0..t in contiguous slices of at least kMinChunk (multiples of 32)
-  const int t = a.step->pos;
+  // positions 0..t of row b in contiguous slices of at least kMinChunk (multiples of 32)
+  const int t = row_pos(a.step, b);
   const int npos = t + 1;
   int chunk = (npos + a.ns - 1) / a.ns;
   chunk = (chunk + 31) & ~31;
@@ -600,9 +600,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   __shared__ int s_last;
   __shared__ float wfac[kMmaWarps * 16];   // per head, each warp's factor exp(m_w - M)
 
-  const int t = a.step->pos;
-  const int npos = t + 1;
-  const int nchk = (npos + CH - 1) / CH;              // chunks of one (row, kv head)
+  // Every (row, kv head) gets the chunk count of the longest row (rows may sit at different
+  // positions); a row's chunks past its own position are empty: never copied, never computed,
+  // but their CTAs still take part in the merge (with empty partials).
+  const int nchk = (a.step->pos + 1 + CH - 1) / CH;   // chunks of one (row, kv head)
   const long long T = (long long)a.B * a.kv * nchk;   // chunks of the launch
   // cluster mode: cluster bj takes (row, kv head) bj and its CTA of rank r the r-th of a.ns
   // even parts of the chunks (possibly none)
@@ -612,14 +613,18 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   const long long c0 = clus ? cbj * nchk + (long long)nchk * crank / a.ns : T * c / G;
   const long long c1 = clus ? cbj * nchk + (long long)nchk * (crank + 1) / a.ns : T * (c + 1) / G;
   auto owner = [&](long long it) { return (int)(((it + 1) * G + T - 1) / T - 1); };
-  // the segment starting at chunk st of the sequence: (row b, kv head j), chunks [k0, k1)
-  auto seg = [&](long long st, int& b, int& j, int& k0, int& k1, long long& next) {
+  // the segment starting at chunk st of the sequence: (row b, kv head j), chunks [k0, k1), of
+  // which [k0, kv1) hold positions 0..tb of row b
+  auto seg = [&](long long st, int& b, int& j, int& k0, int& k1, int& kv1, int& tb, long long& next) {
     const long long bj = st / nchk;
     k0 = (int)(st - bj * nchk);
     const long long end = c1 < (bj + 1) * nchk ? c1 : (bj + 1) * nchk;
     k1 = k0 + (int)(end - st);
     j = (int)(bj % a.kv);
     b = (int)(bj / a.kv);
+    tb = row_pos(a.step, b);
+    const int nb = (tb + 1 + CH - 1) / CH;
+    kv1 = k1 < nb ? k1 : (k0 > nb ? k0 : nb);
     next = end;
   };
 
@@ -632,13 +637,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
 
   // the issuing side of this warp (lane 0): cursor over (segment, chunk) pairs
   long long ist = c0, inext = c0;
-  int iq = warp, issued = 0, ib = 0, ij = 0, ik0 = 0, ik1 = 0;
-  if (ist < c1) seg(ist, ib, ij, ik0, ik1, inext);
+  int iq = warp, issued = 0, ib = 0, ij = 0, ik0 = 0, ik1 = 0, ikv1 = 0, itb = 0;
+  if (ist < c1) seg(ist, ib, ij, ik0, ik1, ikv1, itb, inext);
   auto settle = [&]() {  // move the cursor to a pair that exists (or past the run)
-    while (ist < c1 && iq >= ik1 - ik0) {
+    while (ist < c1 && iq >= ikv1 - ik0) {
       ist = inext;
       iq = warp;
-      if (ist < c1) seg(ist, ib, ij, ik0, ik1, inext);
+      if (ist < c1) seg(ist, ib, ij, ik0, ik1, ikv1, itb, inext);
     }
   };
   settle();
@@ -662,8 +667,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   if (lane == 0) {
     tma_prefetch_map(&kmap);
     tma_prefetch_map(&vmap);
-    // chunks below position t do not depend on the previous kernel
-    while (issued < NR && ist < c1 && (ik0 + iq) * CH + min(CH, npos - (ik0 + iq) * CH) <= t) issue();
+    // chunks below the row's position do not depend on the previous kernel
+    while (issued < NR && ist < c1 && (ik0 + iq) * CH + min(CH, itb + 1 - (ik0 + iq) * CH) <= itb) issue();
   }
   grid_dep_wait();
   grid_dep_launch();
@@ -688,9 +693,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     }
   };
   if (c0 < c1) {
-    int b, j, k0, k1;
+    int b, j, k0, k1, kv1, tb;
     long long nx;
-    seg(c0, b, j, k0, k1, nx);
+    seg(c0, b, j, k0, k1, kv1, tb, nx);
     load_q(b, j);
   }
   __syncthreads();
@@ -742,9 +747,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   int lu = 0;
   long long next = c0;
   for (long long st = c0; st < c1; st = next, ++lu) {
-    int b, j, k0, k1;
-    seg(st, b, j, k0, k1, next);
-    const int p0 = k0 * CH, p1 = min(npos, k1 * CH), nch = k1 - k0;
+    int b, j, k0, k1, kv1, tb;
+    seg(st, b, j, k0, k1, kv1, tb, next);
+    const int p0 = k0 * CH, p1 = min(tb + 1, kv1 * CH), nch = kv1 - k0;  // nch may be 0
     // this segment's queries as B fragments (k = dimensions, n = heads), hi and lo, kept in
     // registers: x4 loads give (b0, b1) of two consecutive k-steps
     uint32_t qfh[NG][KS][2], qfl[NG][KS][2];
@@ -919,9 +924,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
       mypart[idx] = r;
     }
     if (next < c1) {  // (every warp is past this segment's chunks: the query buffer is free)
-      int b2, j2, k02, k12;
+      int b2, j2, k02, k12, kv12, tb2;
       long long nx2;
-      seg(next, b2, j2, k02, k12, nx2);
+      seg(next, b2, j2, k02, k12, kv12, tb2, nx2);
       load_q(b2, j2);
     }
     __syncthreads();

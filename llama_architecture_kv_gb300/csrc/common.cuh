@@ -97,16 +97,22 @@ LLM_D float warp_max(float v) {
 }
 
 // ---- step parameters written by the step prologue --------------------------------------
+// The state is followed in memory by the position of every row ([max_batch] int32): rows may
+// sit at different positions (a decode of rows at their own positions); pos is their maximum.
 struct StepState {
-  int32_t pos;     // position of this step
+  int32_t pos;     // the largest position of this step's rows
   int32_t B;       // rows in this step
   float temp;      // sampling: temperature (0: greedy)
   int32_t k;       // sampling: top-k
   float p;         // sampling: top-p
   int32_t pad[3];
 };
+// position of row b in this step
+LLM_D int32_t row_pos(const StepState* s, int b) { return reinterpret_cast<const int32_t*>(s + 1)[b]; }
+LLM_HD size_t step_state_bytes(int max_batch) { return sizeof(StepState) + (size_t)max_batch * 4; }
 
 // device error codes (same values as llm.h)
+
 constexpr int32_t kErrTokenRange = 5;
 constexpr int32_t kErrDeviceTimeout = 9;
 

@@ -402,7 +402,7 @@ __global__ void tc_qkv_kernel(const TcQkvArgs a) {
       x.y = __fadd_rn(x.y, t[s].y);
     }
   const float x0 = x.x, x1 = x.y;
-  const int pos = a.step->pos, half = a.hd >> 1;
+  const int pos = row_pos(a.step, b), half = a.hd >> 1;
   const int head = R / a.hd, e = (R - head * a.hd) >> 1;
   const size_t row = (size_t)b;
   if (head < a.H + a.kv) {

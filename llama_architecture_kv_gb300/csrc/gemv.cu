@@ -271,10 +271,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
 
     // ---- epilogue ----
     if constexpr (EPI == EPI_QKV) {
-      const int pos = a.step->pos, half = a.hd >> 1;
+      const int half = a.hd >> 1;
       const int npairs = nrows >> 1;
       for (int i = tid; i < npairs * nb; i += kGemvThreads) {
         const int b = i / npairs, p = i - b * npairs;
+        const int pos = row_pos(a.step, b0 + b);
         const int R = r0 + 2 * p;
         const int head = R / a.hd, e = (R - head * a.hd) >> 1;
         const float x0 = acc[(2 * p) * BT + b], x1 = acc[(2 * p + 1) * BT + b];
@@ -509,7 +510,7 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
       a.out[g] = __fmul_rn(si, v1);
     } else {
       const int R = 2 * g;
-      const int pos = a.step->pos, half = a.hd >> 1;
+      const int pos = row_pos(a.step, 0), half = a.hd >> 1;
       const int head = R / a.hd, e = (R - head * a.hd) >> 1;
       if (head < a.H + a.kv) {
         const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];

@@ -32,7 +32,9 @@ constexpr int kInline = 64;  // rows whose token / draw travel inside the prolog
 
 struct BeginArgs {
   StepState* st;
-  int32_t pos, B;
+  int32_t pos, B;          // pos: every row's position, unless the rows sit at their own:
+  int32_t own_pos;         //   then pos_dev[b] (B > kInline) or pos_inline[b]
+  const int32_t* pos_dev;
   float temp;
   int32_t k;
   float p;
@@ -45,17 +47,28 @@ struct BeginArgs {
   int32_t* status;
   int32_t tok_inline[kInline];
   float u_inline[kInline];
+  int32_t pos_inline[kInline];
 };
 
 __global__ void step_begin_kernel(const BeginArgs a) {
   const int t = threadIdx.x;
+  __shared__ int32_t s_max;
   if (t == 0) {
-    a.st->pos = a.pos;
+    s_max = 0;
     a.st->B = a.B;
     a.st->temp = a.temp;
     a.st->k = a.k;
     a.st->p = a.p;
   }
+  __syncthreads();
+  int32_t* rowpos = reinterpret_cast<int32_t*>(a.st + 1);
+  for (int b = t; b < a.B; b += blockDim.x) {
+    const int32_t pb = !a.own_pos ? a.pos : a.pos_dev ? a.pos_dev[b] : a.pos_inline[b];  // validated by the host
+    rowpos[b] = pb;
+    atomicMax(&s_max, pb);
+  }
+  __syncthreads();
+  if (t == 0) a.st->pos = s_max;
   for (int b = t; b < a.B; b += blockDim.x) {
     int tok = a.tok_dev ? a.tok_dev[(size_t)b * a.tok_stride + a.tok_col] : a.tok_inline[b];
     if (tok < 0 || tok >= a.vocab) {
@@ -178,6 +191,7 @@ struct llm_handle {
   int part_ns = 0;
   CUtensorMap kmap, vmap;  // the key and value caches as [layers * max_batch * kv * max_seq][hd]
   StepState* st = nullptr;
+  int32_t* pos_buf = nullptr;  // [max_batch] positions of a decode of rows at their own positions
   int32_t* status = nullptr;
   int32_t* tok_buf = nullptr;
   float* u_buf = nullptr;
@@ -616,10 +630,21 @@ llm_status run_step(llm_handle* h, int B, int mode) {
   return LLM_OK;
 }
 
+// the step prologue; rows at their own positions when pos_host is given (copied to pos_buf)
 llm_status begin(llm_handle* h, int pos, int B, const int32_t* tok_host, const int32_t* tok_dev, int tok_stride,
-                 int tok_col, float temp, int k, float p, const float* u_host, const float* u_dev) {
+                 int tok_col, float temp, int k, float p, const float* u_host, const float* u_dev,
+                 const int32_t* pos_host = nullptr) {
   BeginArgs a = {};
   a.st = h->st; a.pos = pos; a.B = B; a.temp = temp; a.k = k; a.p = p; a.vocab = h->V;
+  if (pos_host) {
+    a.own_pos = 1;
+    if (B <= kInline) {
+      for (int b = 0; b < B; ++b) a.pos_inline[b] = pos_host[b];
+    } else {
+      CUDA_TRY(h, cudaMemcpyAsync(h->pos_buf, pos_host, (size_t)B * 4, cudaMemcpyHostToDevice, h->stream));
+      a.pos_dev = h->pos_buf;
+    }
+  }
   a.tok_buf = h->tok_buf; a.u_buf = h->u_buf; a.status = h->status;
   a.tok_stride = tok_stride; a.tok_col = tok_col;
   if (tok_dev) {
@@ -675,6 +700,18 @@ llm_status check_sample_args(llm_handle* h, float temp, int k, float p) {
 
 void set_filled(llm_handle* h, int B, int v) {
   for (int b = 0; b < B; ++b) h->filled[b] = v;
+}
+
+// rows at their own positions: 0 <= pos[b] <= filled length of row b, pos[b] < max_seq
+llm_status check_row_positions(llm_handle* h, int B, const int32_t* pos) {
+  if (B < 1 || B > h->cfg.max_batch) return fail(h, LLM_ERR_BATCH, "batch %d outside 1..%d", B, h->cfg.max_batch);
+  for (int b = 0; b < B; ++b) {
+    if (pos[b] < 0 || pos[b] >= h->cfg.max_seq)
+      return fail(h, LLM_ERR_POS_RANGE, "row %d: position %d outside the cache of %d", b, pos[b], h->cfg.max_seq);
+    if (pos[b] > h->filled[b])
+      return fail(h, LLM_ERR_POS_RANGE, "row %d: position %d after its filled length %d", b, pos[b], h->filled[b]);
+  }
+  return LLM_OK;
 }
 
 }  // namespace
@@ -826,7 +863,8 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   h->part_ns = maxns;
   const int slots = attn_part_slots(h->wt, h->hd, maxns);
   if ((st = dalloc(h, &h->part, B * h->H * slots * (h->hd + 2) * 4)) ||
-      (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, sizeof(StepState))) ||
+      (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, step_state_bytes(c.max_batch))) ||
+      (st = dalloc(h, &h->pos_buf, B * 4)) ||
       (st = dalloc(h, &h->status, 16)) || (st = dalloc(h, &h->tok_buf, B * 4)) || (st = dalloc(h, &h->u_buf, B * 4)) ||
       (st = dalloc(h, &h->ids_buf, B * 4)))
     return bail(st);
@@ -945,6 +983,35 @@ llm_status llm_decode_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, i
   return prefill_impl(h, nullptr, tokens_dev, B, 1, pos, logits_dev, false);
 }
 
+// one token per row, each row at its own position; logits of every row
+static llm_status decode_rows_impl(llm_handle* h, const int32_t* tok_host, const int32_t* tok_dev, int32_t B,
+                                   const int32_t* pos, float* logits, bool host) {
+  TRY(check_row_positions(h, B, pos));
+  if (tok_host) TRY(check_tokens(h, tok_host, (size_t)B));
+  TRY(begin(h, 0, B, tok_host, tok_dev, 1, 0, 0.0f, 1, 1.0f, nullptr, nullptr, pos));
+  TRY(run_step(h, B, MODE_HEAD));
+  if (host) {
+    CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  } else if (logits != h->logits) {
+    CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToDevice, h->stream));
+  }
+  for (int b = 0; b < B; ++b) h->filled[b] = pos[b] + 1;
+  return LLM_OK;
+}
+
+llm_status llm_decode_rows(llm_handle* h, const int32_t* tokens_host, int32_t B, const int32_t* positions_host,
+                           float* logits_host) {
+  if (!h || !tokens_host || !positions_host || !logits_host) return LLM_ERR_ARG;
+  return decode_rows_impl(h, tokens_host, nullptr, B, positions_host, logits_host, true);
+}
+
+llm_status llm_decode_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, const int32_t* positions_host,
+                               float* logits_dev) {
+  if (!h || !tokens_dev || !positions_host || !logits_dev) return LLM_ERR_ARG;
+  return decode_rows_impl(h, nullptr, tokens_dev, B, positions_host, logits_dev, false);
+}
+
 static llm_status sample_impl(llm_handle* h, const float* logits, bool logits_on_host, int32_t B, float temp, int32_t k,
                               float p, const float* u, bool u_on_host, int32_t* ids, bool ids_on_host) {
   if (B < 1 || B > h->cfg.max_batch) return fail(h, LLM_ERR_BATCH, "batch %d outside 1..%d", B, h->cfg.max_batch);
@@ -983,15 +1050,16 @@ llm_status llm_sample_dev(llm_handle* h, const float* logits_dev, int32_t B, flo
 
 static llm_status step_impl(llm_handle* h, const int32_t* tok_host, const int32_t* tok_dev, int32_t B, int32_t pos,
                             float temp, int32_t k, float p, const float* u_host, const float* u_dev, int32_t* ids,
-                            float* logits, bool host) {
-  TRY(check_rows(h, B, pos, 1));
+                            float* logits, bool host, const int32_t* pos_rows = nullptr) {
+  if (pos_rows) TRY(check_row_positions(h, B, pos_rows));
+  else TRY(check_rows(h, B, pos, 1));
   TRY(check_sample_args(h, temp, k, p));
   if (temp > 0.0f && !u_host && !u_dev) return fail(h, LLM_ERR_ARG, "sampling needs uniform draws u");
   if (tok_host) TRY(check_tokens(h, tok_host, (size_t)B));
   if (u_host && temp > 0.0f)
     for (int b = 0; b < B; ++b)
       if (!(u_host[b] >= 0.0f && u_host[b] < 1.0f)) return fail(h, LLM_ERR_ARG, "u[%d] outside [0, 1)", b);
-  TRY(begin(h, pos, B, tok_host, tok_dev, 1, 0, temp, k, p, u_host, u_dev));
+  TRY(begin(h, pos, B, tok_host, tok_dev, 1, 0, temp, k, p, u_host, u_dev, pos_rows));
   TRY(run_step(h, B, temp > 0.0f ? MODE_TOPP : MODE_GREEDY));
   if (host) {
     if (logits) CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
@@ -1002,7 +1070,11 @@ static llm_status step_impl(llm_handle* h, const int32_t* tok_host, const int32_
       CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToDevice, h->stream));
     if (ids != h->ids_buf) CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToDevice, h->stream));
   }
-  set_filled(h, B, pos + 1);
+  if (pos_rows) {
+    for (int b = 0; b < B; ++b) h->filled[b] = pos_rows[b] + 1;
+  } else {
+    set_filled(h, B, pos + 1);
+  }
   return LLM_OK;
 }
 
@@ -1016,6 +1088,20 @@ llm_status llm_step_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int
                         float p, const float* u_dev, int32_t* ids_dev, float* logits_dev) {
   if (!h || !tokens_dev || !ids_dev) return LLM_ERR_ARG;
   return step_impl(h, nullptr, tokens_dev, B, pos, temp, k, p, nullptr, u_dev, ids_dev, logits_dev, false);
+}
+
+llm_status llm_step_rows(llm_handle* h, const int32_t* tokens_host, int32_t B, const int32_t* positions_host,
+                         float temp, int32_t k, float p, const float* u_host, int32_t* ids_host, float* logits_host) {
+  if (!h || !tokens_host || !positions_host || !ids_host) return LLM_ERR_ARG;
+  return step_impl(h, tokens_host, nullptr, B, 0, temp, k, p, u_host, nullptr, ids_host, logits_host, true,
+                   positions_host);
+}
+
+llm_status llm_step_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, const int32_t* positions_host,
+                             float temp, int32_t k, float p, const float* u_dev, int32_t* ids_dev, float* logits_dev) {
+  if (!h || !tokens_dev || !positions_host || !ids_dev) return LLM_ERR_ARG;
+  return step_impl(h, nullptr, tokens_dev, B, 0, temp, k, p, nullptr, u_dev, ids_dev, logits_dev, false,
+                   positions_host);
 }
 
 static llm_status kv_copy(llm_handle* h, int32_t layer, int32_t row, int32_t pos0, int32_t n, void* k, void* v,
