@@ -53,6 +53,8 @@ def parse():
                     help="reference arm: layers of the model run per timed step")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--prompt", type=int, default=-1, help="override the prompt length (profiling)")
+    ap.add_argument("--generate", action="store_true",
+                    help="time llm_generate_dev: the K steps as CUDA graphs of 8 chained steps")
     ap.add_argument("--rows", action="store_true",
                     help="rows at their own positions (decode_rows): row b at P - b * (P // 2B)")
     ap.add_argument("--kernels", action="store_true",
@@ -298,9 +300,12 @@ def run_ours(args):
         else:
             pkg.llm_step_rows_dev(h, tk, B, rowpos + i, temp, k_, p_, u, ids)
 
+    gen_ids = torch.empty((max(W, K), B), dtype=torch.int32, device=dev) if args.generate else None
     with torch.cuda.stream(stream):
         for i in range(W):  # warm-up: rewind to the prompt end every time
             step_dev(tok[0], 0, u_dev[i], tok[1])
+        if args.generate:  # captures the generation graphs
+            pkg.llm_generate_dev(h, tok[0], B, pos0, W, temp, k_, p_, u_dev[:W], gen_ids[:W])
         pkg.llm_synchronize(h)
         if world > 1:
             torch.distributed.barrier()
@@ -308,8 +313,11 @@ def run_ours(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(local) as clocks:
             e0.record(stream)
-            for i in range(K):
-                step_dev(tok[i % 2], i, u_dev[W + i], tok[(i + 1) % 2])
+            if args.generate:
+                pkg.llm_generate_dev(h, tok[0], B, pos0, K, temp, k_, p_, u_dev[W:W + K], gen_ids[:K])
+            else:
+                for i in range(K):
+                    step_dev(tok[i % 2], i, u_dev[W + i], tok[(i + 1) % 2])
             e1.record(stream)
             e1.synchronize()
         pkg.llm_synchronize(h)
@@ -329,9 +337,13 @@ def run_ours(args):
     ids_h = torch.empty(B, dtype=torch.int32).pin_memory()
     u_h = torch.from_numpy(u_all[:1].reshape(-1).copy()).pin_memory()
     E = min(K, 100)
+    gen_h = torch.empty((E, B), dtype=torch.int32).pin_memory() if args.generate else None
+    u_e = torch.from_numpy(np.ascontiguousarray(u_all[:E])).pin_memory() if args.generate else None
     torch.cuda.synchronize()
     te = time.perf_counter()
-    for i in range(E):
+    if args.generate:
+        pkg.llm_generate(h, tok_h, B, pos0, E, temp, k_, p_, u_e if temp > 0 else None, gen_h)
+    for i in range(0 if args.generate else E):
         if rowpos is None:
             pkg.llm_step(h, tok_h if i == 0 else ids_h, B, pos0 + i, temp, k_, p_,
                          u_h if temp > 0 else None, ids_h)
@@ -340,7 +352,8 @@ def run_ours(args):
                               u_h if temp > 0 else None, ids_h)
     e2e_s = time.perf_counter() - te
     e2e = {"value": B * E / e2e_s, "unit": "tok/s",
-           "h2d_bytes_per_step": 4 * B + (4 * B if temp > 0 else 0), "d2h_bytes_per_step": 4 * B}
+           "h2d_bytes_per_step": (4 * B / E if args.generate else 4 * B) + (4 * B if temp > 0 else 0),
+           "d2h_bytes_per_step": 4 * B}
 
     # the dominant kernel, timed alone (consecutive launches walk the layers: weights from HBM)
     reps = 4 * s.layers
@@ -398,10 +411,15 @@ def run_ours(args):
                    "sampling": "greedy" if temp == 0 else f"temp {temp} top-k {k_} top-p {p_}",
                    "positions": ("own per row (decode_rows): row b at %d - %d b" % (pos0, pos0 // (2 * B))
                                  if rowpos is not None else "shared"),
+                   "loop": "llm_generate_dev (graphs of 8 chained steps)" if args.generate else "llm_step_dev per step",
                    "l2": "inputs larger than L2 (weights %.1f GB per step)" % (wbytes / 1e9),
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
-        "clocks": clk, "gpu_launches": K * pkg.llm_step_kernels(h, B, temp),
+        "clocks": clk,
+        # a generation step replaces the prologue by its own and ends with one copy of its draws;
+        # each graph launch (8 steps, then single steps) is preceded by one state update
+        "gpu_launches": (K * (pkg.llm_step_kernels(h, B, temp) + 1) + K // 8 + K % 8 if args.generate
+                         else K * pkg.llm_step_kernels(h, B, temp)),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

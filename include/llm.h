@@ -186,6 +186,26 @@ llm_status llm_step_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B
                              const int32_t* positions_host, float temp, int32_t k, float p,
                              const float* u_dev, int32_t* ids_dev, float* logits_dev);
 
+/*
+ * Generation inside CUDA graphs (Llama 3.1 8B Instruct card, "Entries": generate<Steps>(token,
+ * pos), sample<Steps>(...)): n_steps decode + draw steps; step s (0 <= s < n_steps) runs every row
+ * b < B at position pos + s on the token drawn by step s - 1 (tokens[b] for s = 0) and draws
+ * ids[s*B + b] as llm_step would with u[s*B + b] (u may be NULL when temp == 0).  The steps run
+ * as graphs of 8 steps (then single steps) with no host work between the steps of a graph; the
+ * ids equal those of n_steps chained llm_step calls bit for bit.  Checks as llm_step for every
+ * step: n_steps >= 1 (else LLM_ERR_ARG), pos <= filled length of every row and pos + n_steps <=
+ * max_seq (else LLM_ERR_POS_RANGE); handles created with debug_trace = 1 are refused
+ * (LLM_ERR_ARG).  ids [n_steps][B]; after success the filled length of rows b < B is
+ * pos + n_steps and the logits buffer holds the last step's logits.  llm_generate: host tokens,
+ * draws and ids (returns when done); llm_generate_dev: device buffers, stream-ordered.
+ */
+llm_status llm_generate(llm_handle* h, const int32_t* tokens_host, int32_t B, int32_t pos,
+                        int32_t n_steps, float temp, int32_t k, float p, const float* u_host,
+                        int32_t* ids_host);
+llm_status llm_generate_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t pos,
+                            int32_t n_steps, float temp, int32_t k, float p, const float* u_dev,
+                            int32_t* ids_dev);
+
 /* Wait for the handle's stream; return the first error recorded on the device since the last
  * call (LLM_ERR_TOKEN_RANGE, LLM_ERR_DEVICE_TIMEOUT) and clear it. */
 llm_status llm_synchronize(llm_handle* h);

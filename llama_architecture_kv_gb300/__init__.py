@@ -23,7 +23,7 @@ EXPORTS = ("llm_weight_count", "llm_create", "llm_destroy", "llm_reset", "llm_pr
            "llm_last_error", "llm_status_string", "llm_kv_import", "llm_kv_export",
            "llm_debug_trace", "llm_profile_kernel", "llm_sample_noalloc",
            "llm_step_kernels", "llm_decode_rows", "llm_decode_rows_dev", "llm_step_rows",
-           "llm_step_rows_dev")
+           "llm_step_rows_dev", "llm_generate", "llm_generate_dev")
 
 
 class LlmConfig(ctypes.Structure):
@@ -73,6 +73,8 @@ def lib():
             "llm_decode_rows_dev": ([vp, vp, i32, vp, vp], i32),
             "llm_step_rows": ([vp, vp, i32, vp, f32, i32, f32, vp, vp, vp], i32),
             "llm_step_rows_dev": ([vp, vp, i32, vp, f32, i32, f32, vp, vp, vp], i32),
+            "llm_generate": ([vp, vp, i32, i32, i32, f32, i32, f32, vp, vp], i32),
+            "llm_generate_dev": ([vp, vp, i32, i32, i32, f32, i32, f32, vp, vp], i32),
             "llm_synchronize": ([vp], i32),
             "llm_stream": ([vp], vp),
             "llm_logits_buffer": ([vp], vp),
@@ -201,6 +203,14 @@ def llm_step_rows_dev(h, tokens, B, positions, temp, k, p, u, ids, logits=None):
                                       _ptr(logits)))
 
 
+def llm_generate(h, tokens, B, pos, n_steps, temp, k, p, u, ids):
+    _check(h, lib().llm_generate(h, _ptr(tokens), B, pos, n_steps, temp, k, p, _ptr(u), _ptr(ids)))
+
+
+def llm_generate_dev(h, tokens, B, pos, n_steps, temp, k, p, u, ids):
+    _check(h, lib().llm_generate_dev(h, _ptr(tokens), B, pos, n_steps, temp, k, p, _ptr(u), _ptr(ids)))
+
+
 def llm_synchronize(h):
     _check(h, lib().llm_synchronize(h))
 
@@ -313,6 +323,15 @@ class Model:
         u = None if u is None else np.ascontiguousarray(u, np.float32)
         llm_step_rows(self.h, tokens, B, positions, temp, k, p, u, ids, out)
         return (ids, out) if logits else ids
+
+    def generate(self, tokens, pos, n_steps, temp=0.0, k=1, p=1.0, u=None):
+        """n_steps chained decode + draw steps inside CUDA graphs; ids [n_steps][B]."""
+        tokens = np.ascontiguousarray(tokens, np.int32).reshape(-1)
+        B = tokens.size
+        ids = np.empty((n_steps, B), np.int32)
+        u = None if u is None else np.ascontiguousarray(u, np.float32).reshape(n_steps, B)
+        llm_generate(self.h, tokens, B, pos, n_steps, temp, k, p, u, ids)
+        return ids
 
     def sample(self, logits, temp, k, p, u):
         logits = np.ascontiguousarray(logits, np.float32)

@@ -30,6 +30,21 @@ namespace {
 
 constexpr int kInline = 64;  // rows whose token / draw travel inside the prologue's arguments
 
+constexpr int kGenChunk = 8;  // steps per generation graph
+
+// where the steps of one generation graph launch read and write (set before each launch)
+struct GenState {
+  int32_t pos;          // position of the graph's first step
+  int32_t B;
+  float temp;
+  int32_t k;
+  float p;
+  int32_t pad;
+  const int32_t* prev;  // [B] tokens of the first step
+  const float* u;       // [steps][B] draws (temp > 0)
+  int32_t* ids;         // [steps][B] drawn tokens
+};
+
 struct BeginArgs {
   StepState* st;
   int32_t pos, B;          // pos: every row's position, unless the rows sit at their own:
@@ -79,6 +94,35 @@ __global__ void step_begin_kernel(const BeginArgs a) {
     a.u_buf[b] = a.u_dev ? a.u_dev[b] : a.u_inline[b];
   }
 }
+
+// step i of a generation graph: the prologue of a step at position gen.pos + i whose tokens are
+// the previous step's draws (gen.prev for i == 0) and whose draws are gen.u[i]
+__global__ void gen_begin_kernel(StepState* st, const GenState* gen, int32_t* tok_buf, float* u_buf, int i) {
+  const GenState g = *gen;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    st->pos = g.pos + i;
+    st->B = g.B;
+    st->temp = g.temp;
+    st->k = g.k;
+    st->p = g.p;
+  }
+  int32_t* rowpos = reinterpret_cast<int32_t*>(st + 1);
+  for (int b = t; b < g.B; b += blockDim.x) {
+    rowpos[b] = g.pos + i;
+    tok_buf[b] = i == 0 ? g.prev[b] : g.ids[(size_t)(i - 1) * g.B + b];
+    u_buf[b] = g.temp > 0.0f ? g.u[(size_t)i * g.B + b] : 0.0f;
+  }
+}
+
+// the end of step i: its draws into gen.ids[i]
+__global__ void gen_end_kernel(const GenState* gen, const int32_t* ids_buf, int i) {
+  const int B = gen->B;
+  int32_t* out = gen->ids + (size_t)i * B;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) out[b] = ids_buf[b];
+}
+
+__global__ void gen_set_kernel(GenState* gen, const GenState v) { *gen = v; }
 
 template <int WT>
 __global__ void embed_kernel(const void* emb, const int32_t* tok, float* x, int d, int x_stride) {
@@ -163,9 +207,12 @@ struct TcMaps {
 };
 
 struct GraphKey {
-  int B, mode;
-  bool operator<(const GraphKey& o) const { return B != o.B ? B < o.B : mode < o.mode; }
+  int B, mode, gen;  // gen: steps of a generation graph (0: one step after a host prologue)
+  bool operator<(const GraphKey& o) const {
+    return B != o.B ? B < o.B : mode != o.mode ? mode < o.mode : gen < o.gen;
+  }
 };
+
 
 // what follows the layers: nothing, the LM head, or the head and a greedy / top-k top-p draw
 enum { MODE_NOHEAD = 0, MODE_HEAD = 1, MODE_GREEDY = 2, MODE_TOPP = 3 };
@@ -192,6 +239,9 @@ struct llm_handle {
   CUtensorMap kmap, vmap;  // the key and value caches as [layers * max_batch * kv * max_seq][hd]
   StepState* st = nullptr;
   int32_t* pos_buf = nullptr;  // [max_batch] positions of a decode of rows at their own positions
+  GenState* gen = nullptr;     // generation: the state of the graph launch in flight
+  float* u_gen = nullptr;      // [kGenChunk][max_batch] draws of one host-memory generation launch
+  int32_t* ids_gen = nullptr;  // [kGenChunk][max_batch] its drawn tokens
   int32_t* status = nullptr;
   int32_t* tok_buf = nullptr;
   float* u_buf = nullptr;
@@ -592,16 +642,26 @@ llm_status launch_layer_kernels(llm_handle* h, int B, int mode, bool pdl, bool t
   return LLM_OK;
 }
 
-// the step graph of (B, mode), captured on first use
-llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t, int>** out) {
-  GraphKey key{B, mode};
+// the step graph of (B, mode), captured on first use; with gen > 0, a generation graph of gen
+// steps, each its own prologue (gen_begin_kernel), the step's kernels and gen_end_kernel
+llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t, int>** out, int gen = 0) {
+  GraphKey key{B, mode, gen};
   auto it = h->graphs.find(key);
   if (it == h->graphs.end()) {
     // capture on a private stream, then replay on the handle's stream
     cudaStream_t saved = h->stream;
     h->stream = h->cap_stream;
     CUDA_TRY(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
-    llm_status s = launch_layer_kernels(h, B, mode, true, false);
+    llm_status s = LLM_OK;
+    if (gen == 0) {
+      s = launch_layer_kernels(h, B, mode, true, false);
+    } else {
+      for (int i = 0; i < gen && s == LLM_OK; ++i) {
+        gen_begin_kernel<<<1, 128, 0, h->stream>>>(h->st, h->gen, h->tok_buf, h->u_buf, i);
+        s = launch_layer_kernels(h, B, mode, true, false);
+        if (s == LLM_OK) gen_end_kernel<<<1, 128, 0, h->stream>>>(h->gen, h->ids_buf, i);
+      }
+    }
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(h->stream, &graph);
     h->stream = saved;
@@ -864,7 +924,8 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   const int slots = attn_part_slots(h->wt, h->hd, maxns);
   if ((st = dalloc(h, &h->part, B * h->H * slots * (h->hd + 2) * 4)) ||
       (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, step_state_bytes(c.max_batch))) ||
-      (st = dalloc(h, &h->pos_buf, B * 4)) ||
+      (st = dalloc(h, &h->pos_buf, B * 4)) || (st = dalloc(h, &h->gen, sizeof(GenState))) ||
+      (st = dalloc(h, &h->u_gen, (size_t)kGenChunk * B * 4)) || (st = dalloc(h, &h->ids_gen, (size_t)kGenChunk * B * 4)) ||
       (st = dalloc(h, &h->status, 16)) || (st = dalloc(h, &h->tok_buf, B * 4)) || (st = dalloc(h, &h->u_buf, B * 4)) ||
       (st = dalloc(h, &h->ids_buf, B * 4)))
     return bail(st);
@@ -1010,6 +1071,72 @@ llm_status llm_decode_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t
                                float* logits_dev) {
   if (!h || !tokens_dev || !positions_host || !logits_dev) return LLM_ERR_ARG;
   return decode_rows_impl(h, nullptr, tokens_dev, B, positions_host, logits_dev, false);
+}
+
+// n decode steps, each feeding its draws to the next as tokens, as CUDA graphs of kGenChunk
+// steps (then single steps): no host round trip between the steps of a graph
+static llm_status generate_impl(llm_handle* h, const int32_t* tok_host, const int32_t* tok_dev, int32_t B,
+                                int32_t pos, int32_t n, float temp, int32_t k, float p, const float* u_host,
+                                const float* u_dev, int32_t* ids, bool host) {
+  if (n < 1) return fail(h, LLM_ERR_ARG, "steps %d < 1", n);
+  if (h->cfg.debug_trace) return fail(h, LLM_ERR_ARG, "debug_trace handles run without graphs");
+  TRY(check_rows(h, B, pos, n));
+  TRY(check_sample_args(h, temp, k, p));
+  const bool sampled = temp > 0.0f;
+  if (sampled && !u_host && !u_dev) return fail(h, LLM_ERR_ARG, "sampling needs uniform draws u");
+  if (tok_host) TRY(check_tokens(h, tok_host, (size_t)B));
+  if (u_host && sampled)
+    for (size_t i = 0; i < (size_t)n * B; ++i)
+      if (!(u_host[i] >= 0.0f && u_host[i] < 1.0f)) return fail(h, LLM_ERR_ARG, "u[%zu] outside [0, 1)", i);
+  const int mode = sampled ? MODE_TOPP : MODE_GREEDY;
+  const int32_t* prev = tok_dev;
+  if (tok_host) {
+    CUDA_TRY(h, cudaMemcpyAsync(h->tok_buf, tok_host, (size_t)B * 4, cudaMemcpyHostToDevice, h->stream));
+    prev = h->tok_buf;
+  }
+  for (int done = 0; done < n;) {
+    const int c = n - done >= kGenChunk ? kGenChunk : 1;
+    GenState v = {};
+    v.pos = pos + done; v.B = B; v.temp = temp; v.k = k; v.p = p; v.prev = prev;
+    if (host) {
+      if (sampled)
+        CUDA_TRY(h, cudaMemcpyAsync(h->u_gen, u_host + (size_t)done * B, (size_t)c * B * 4, cudaMemcpyHostToDevice,
+                                    h->stream));
+      v.u = h->u_gen;
+      v.ids = h->ids_gen;
+    } else {
+      v.u = sampled ? u_dev + (size_t)done * B : nullptr;
+      v.ids = ids + (size_t)done * B;
+    }
+    gen_set_kernel<<<1, 1, 0, h->stream>>>(h->gen, v);
+    CUDA_TRY(h, cudaGetLastError());
+    std::pair<cudaGraphExec_t, int>* g = nullptr;
+    TRY(step_graph(h, B, mode, &g, c));
+    CUDA_TRY(h, cudaGraphLaunch(g->first, h->stream));
+    if (host) {
+      CUDA_TRY(h, cudaMemcpyAsync(ids + (size_t)done * B, h->ids_gen, (size_t)c * B * 4, cudaMemcpyDeviceToHost,
+                                  h->stream));
+      prev = h->ids_gen + (size_t)(c - 1) * B;  // read by the next launch's first step before it is rewritten
+    } else {
+      prev = ids + (size_t)(done + c - 1) * B;
+    }
+    done += c;
+  }
+  if (host) CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  set_filled(h, B, pos + n);
+  return LLM_OK;
+}
+
+llm_status llm_generate(llm_handle* h, const int32_t* tokens_host, int32_t B, int32_t pos, int32_t n_steps,
+                        float temp, int32_t k, float p, const float* u_host, int32_t* ids_host) {
+  if (!h || !tokens_host || !ids_host) return LLM_ERR_ARG;
+  return generate_impl(h, tokens_host, nullptr, B, pos, n_steps, temp, k, p, u_host, nullptr, ids_host, true);
+}
+
+llm_status llm_generate_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, int32_t pos, int32_t n_steps,
+                            float temp, int32_t k, float p, const float* u_dev, int32_t* ids_dev) {
+  if (!h || !tokens_dev || !ids_dev) return LLM_ERR_ARG;
+  return generate_impl(h, nullptr, tokens_dev, B, pos, n_steps, temp, k, p, nullptr, u_dev, ids_dev, false);
 }
 
 static llm_status sample_impl(llm_handle* h, const float* logits, bool logits_on_host, int32_t B, float temp, int32_t k,
