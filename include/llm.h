@@ -187,6 +187,37 @@ llm_status llm_step_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B
                              const float* u_dev, int32_t* ids_dev, float* logits_dev);
 
 /*
+ * Paged caches (Llama 3.1 8B Instruct card, "Entries": decode_paged(tokens, positions, table)):
+ * the key/value caches of a handle form one pool of max_batch * (max_seq / 64) pages of 64
+ * positions (page q = positions (q % (max_seq/64))*64 .. +63 of cache row q / (max_seq/64)).
+ * Row b takes tokens[b] at position positions_host[b]; its position p lies in pool page
+ * table_host[b*pages_per_row + p/64], where the step writes its key and value and from which
+ * attention reads positions 0..positions_host[b].  Which pages hold which sequence is the
+ * caller's (a serving layer's) to manage: the filled lengths are not consulted or changed, and
+ * pages written by earlier paged steps are read as they are.  Requires max_seq % 64 == 0 (else
+ * LLM_ERR_CONFIG), 1 <= B <= max_batch (LLM_ERR_BATCH), 1 <= pages_per_row <= max_seq/64
+ * (LLM_ERR_ARG), 0 <= positions_host[b] < pages_per_row*64 (LLM_ERR_POS_RANGE), every page
+ * entry for positions 0..positions_host[b] inside the pool (LLM_ERR_ARG), tokens as llm_decode.
+ * positions_host [B] and table_host [B][pages_per_row] are host memory, read before the call
+ * returns.  With table[b][i] = b*(max_seq/64) + i (every row its own pages, in order) the step
+ * is llm_decode_rows bit for bit.  llm_step_paged samples as llm_step.
+ */
+llm_status llm_decode_paged(llm_handle* h, const int32_t* tokens_host, int32_t B,
+                            const int32_t* positions_host, const int32_t* table_host,
+                            int32_t pages_per_row, float* logits_host);
+llm_status llm_decode_paged_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B,
+                                const int32_t* positions_host, const int32_t* table_host,
+                                int32_t pages_per_row, float* logits_dev);
+llm_status llm_step_paged(llm_handle* h, const int32_t* tokens_host, int32_t B,
+                          const int32_t* positions_host, const int32_t* table_host,
+                          int32_t pages_per_row, float temp, int32_t k, float p,
+                          const float* u_host, int32_t* ids_host, float* logits_host);
+llm_status llm_step_paged_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B,
+                              const int32_t* positions_host, const int32_t* table_host,
+                              int32_t pages_per_row, float temp, int32_t k, float p,
+                              const float* u_dev, int32_t* ids_dev, float* logits_dev);
+
+/*
  * Generation inside CUDA graphs (Llama 3.1 8B Instruct card, "Entries": generate<Steps>(token,
  * pos), sample<Steps>(...)): n_steps decode + draw steps; step s (0 <= s < n_steps) runs every row
  * b < B at position pos + s on the token drawn by step s - 1 (tokens[b] for s = 0) and draws

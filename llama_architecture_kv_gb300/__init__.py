@@ -23,7 +23,8 @@ EXPORTS = ("llm_weight_count", "llm_create", "llm_destroy", "llm_reset", "llm_pr
            "llm_last_error", "llm_status_string", "llm_kv_import", "llm_kv_export",
            "llm_debug_trace", "llm_profile_kernel", "llm_sample_noalloc",
            "llm_step_kernels", "llm_decode_rows", "llm_decode_rows_dev", "llm_step_rows",
-           "llm_step_rows_dev", "llm_generate", "llm_generate_dev")
+           "llm_step_rows_dev", "llm_generate", "llm_generate_dev", "llm_decode_paged",
+           "llm_decode_paged_dev", "llm_step_paged", "llm_step_paged_dev")
 
 
 class LlmConfig(ctypes.Structure):
@@ -75,6 +76,10 @@ def lib():
             "llm_step_rows_dev": ([vp, vp, i32, vp, f32, i32, f32, vp, vp, vp], i32),
             "llm_generate": ([vp, vp, i32, i32, i32, f32, i32, f32, vp, vp], i32),
             "llm_generate_dev": ([vp, vp, i32, i32, i32, f32, i32, f32, vp, vp], i32),
+            "llm_decode_paged": ([vp, vp, i32, vp, vp, i32, vp], i32),
+            "llm_decode_paged_dev": ([vp, vp, i32, vp, vp, i32, vp], i32),
+            "llm_step_paged": ([vp, vp, i32, vp, vp, i32, f32, i32, f32, vp, vp, vp], i32),
+            "llm_step_paged_dev": ([vp, vp, i32, vp, vp, i32, f32, i32, f32, vp, vp, vp], i32),
             "llm_synchronize": ([vp], i32),
             "llm_stream": ([vp], vp),
             "llm_logits_buffer": ([vp], vp),
@@ -211,6 +216,26 @@ def llm_generate_dev(h, tokens, B, pos, n_steps, temp, k, p, u, ids):
     _check(h, lib().llm_generate_dev(h, _ptr(tokens), B, pos, n_steps, temp, k, p, _ptr(u), _ptr(ids)))
 
 
+def llm_decode_paged(h, tokens, B, positions, table, pages_per_row, logits):
+    _check(h, lib().llm_decode_paged(h, _ptr(tokens), B, _ptr(positions), _ptr(table), pages_per_row,
+                                     _ptr(logits)))
+
+
+def llm_decode_paged_dev(h, tokens, B, positions, table, pages_per_row, logits):
+    _check(h, lib().llm_decode_paged_dev(h, _ptr(tokens), B, _ptr(positions), _ptr(table), pages_per_row,
+                                         _ptr(logits)))
+
+
+def llm_step_paged(h, tokens, B, positions, table, pages_per_row, temp, k, p, u, ids, logits=None):
+    _check(h, lib().llm_step_paged(h, _ptr(tokens), B, _ptr(positions), _ptr(table), pages_per_row, temp, k, p,
+                                   _ptr(u), _ptr(ids), _ptr(logits)))
+
+
+def llm_step_paged_dev(h, tokens, B, positions, table, pages_per_row, temp, k, p, u, ids, logits=None):
+    _check(h, lib().llm_step_paged_dev(h, _ptr(tokens), B, _ptr(positions), _ptr(table), pages_per_row, temp, k,
+                                       p, _ptr(u), _ptr(ids), _ptr(logits)))
+
+
 def llm_synchronize(h):
     _check(h, lib().llm_synchronize(h))
 
@@ -332,6 +357,28 @@ class Model:
         u = None if u is None else np.ascontiguousarray(u, np.float32).reshape(n_steps, B)
         llm_generate(self.h, tokens, B, pos, n_steps, temp, k, p, u, ids)
         return ids
+
+    def decode_paged(self, tokens, positions, table):
+        """One token per row at its own position, the cache read and written through the row's
+        pages: table [B][pages_per_row] of pool pages (64 positions each)."""
+        tokens = np.ascontiguousarray(tokens, np.int32).reshape(-1)
+        positions = np.ascontiguousarray(positions, np.int32).reshape(-1)
+        table = np.ascontiguousarray(table, np.int32)
+        assert positions.size == tokens.size and table.shape[0] == tokens.size
+        out = np.empty((tokens.size, self.V), np.float32)
+        llm_decode_paged(self.h, tokens, tokens.size, positions, table, table.shape[1], out)
+        return out
+
+    def step_paged(self, tokens, positions, table, temp=0.0, k=1, p=1.0, u=None, logits=False):
+        tokens = np.ascontiguousarray(tokens, np.int32).reshape(-1)
+        positions = np.ascontiguousarray(positions, np.int32).reshape(-1)
+        table = np.ascontiguousarray(table, np.int32)
+        B = tokens.size
+        ids = np.empty(B, np.int32)
+        out = np.empty((B, self.V), np.float32) if logits else None
+        u = None if u is None else np.ascontiguousarray(u, np.float32)
+        llm_step_paged(self.h, tokens, B, positions, table, table.shape[1], temp, k, p, u, ids, out)
+        return (ids, out) if logits else ids
 
     def sample(self, logits, temp, k, p, u):
         logits = np.ascontiguousarray(logits, np.float32)

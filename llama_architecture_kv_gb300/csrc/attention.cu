@@ -328,20 +328,23 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   }
   __syncthreads();
 
-  const int row0 = a.krow0 + (b * a.kv + j) * a.cap;  // key-map row of position 0
-  const unsigned char* vg = (const unsigned char*)a.vc + ((size_t)(b * a.kv + j) * a.cap) * ROWB;
   auto issue = [&](int k) {  // lane 0: chunk k of this warp into its ring slot
     const int slot = k % NR;
     const int pb = p0 + (warp + k * NW) * kChunk;
     const int nv = min(kChunk, p1 - pb);
+    // the cache row and position holding position pb (a chunk never crosses a page)
+    int r, pp;
+    cache_slot(a.step, a.cap, b, pb, r, pp);
+    const int krow = a.krow0 + (r * a.kv + j) * a.cap + pp;  // key-map row
+    const unsigned char* vsrc = (const unsigned char*)a.vc + ((size_t)(r * a.kv + j) * a.cap + pp) * ROWB;
     const uint32_t bar = bars + 8u * (warp * NR + slot);
     const uint32_t dst = s_base + (uint32_t)((warp * NR + slot) * BUF);
     fence_proxy_async_smem();
     mbar_expect_tx(bar, (uint32_t)(kChunk * ROWB + nv * ROWB));
 #pragma unroll
     for (int bx = 0; bx < S::NBOX; ++bx)
-      tma_load_2d(dst + (uint32_t)(bx * kChunk * S::BOXB), &kmap, bar, bx * (S::BOXB / S::ES), row0 + pb);
-    bulk_load(dst + (uint32_t)(kChunk * ROWB), vg + (size_t)pb * ROWB, (uint32_t)(nv * ROWB), bar);
+      tma_load_2d(dst + (uint32_t)(bx * kChunk * S::BOXB), &kmap, bar, bx * (S::BOXB / S::ES), krow);
+    bulk_load(dst + (uint32_t)(kChunk * ROWB), vsrc, (uint32_t)(nv * ROWB), bar);
   };
   // chunks below position t do not depend on the previous kernel
   const int npre = cnt < NR ? cnt : NR;
@@ -650,15 +653,18 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   auto issue = [&]() {
     const int slot = issued % NR;
     const int pb = (ik0 + iq) * CH;
-    const int row0 = a.krow0 + (ib * a.kv + ij) * a.cap;
+    // the cache row and position holding position pb (a chunk never crosses a page)
+    int r, pp;
+    cache_slot(a.step, a.cap, ib, pb, r, pp);
+    const int krow = a.krow0 + (r * a.kv + ij) * a.cap + pp;
     const uint32_t bar = bars + 8u * (warp * NR + slot);
     const uint32_t dst = s_base + (uint32_t)((warp * NR + slot) * BUF);
     fence_proxy_async_smem();
     mbar_expect_tx(bar, (uint32_t)(2 * CH * ROWB));
 #pragma unroll
     for (int bx = 0; bx < M::NBOX; ++bx) {
-      tma_load_2d(dst + (uint32_t)(bx * CH * 128), &kmap, bar, bx * 64, row0 + pb);
-      tma_load_2d(dst + (uint32_t)(CH * ROWB + bx * CH * 128), &vmap, bar, bx * 64, row0 + pb);
+      tma_load_2d(dst + (uint32_t)(bx * CH * 128), &kmap, bar, bx * 64, krow);
+      tma_load_2d(dst + (uint32_t)(CH * ROWB + bx * CH * 128), &vmap, bar, bx * 64, krow);
     }
     ++issued;
     iq += NW;

@@ -105,10 +105,28 @@ struct StepState {
   float temp;      // sampling: temperature (0: greedy)
   int32_t k;       // sampling: top-k
   float p;         // sampling: top-p
-  int32_t pad[3];
+  int32_t table_stride;  // paged steps: entries per row of table
+  const int32_t* table;  // paged steps: [B][table_stride] pool pages of each row's positions, or null
 };
 // position of row b in this step
 LLM_D int32_t row_pos(const StepState* s, int b) { return reinterpret_cast<const int32_t*>(s + 1)[b]; }
+
+// Paged caches (Llama 3.1 8B Instruct card, "Entries": decode_paged): the cache of a layer is a
+// pool of pages of kPage positions; page q is positions [(q % (cap / kPage)) * kPage, + kPage) of
+// cache row q / (cap / kPage).  Position pos of row b lies in page table[b][pos / kPage]; without
+// a table it lies in row b itself.  (r, pp): the cache row and position that hold it.
+constexpr int kPage = 64;
+LLM_D void cache_slot(const StepState* s, int cap, int b, int pos, int& r, int& pp) {
+  if (!s->table) {
+    r = b;
+    pp = pos;
+    return;
+  }
+  const int per_row = cap / kPage;
+  const int page = s->table[(size_t)b * s->table_stride + pos / kPage];
+  r = page / per_row;
+  pp = (page - r * per_row) * kPage + (pos & (kPage - 1));
+}
 LLM_HD size_t step_state_bytes(int max_batch) { return sizeof(StepState) + (size_t)max_batch * 4; }
 
 // device error codes (same values as llm.h)

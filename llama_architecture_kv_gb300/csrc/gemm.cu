@@ -414,12 +414,16 @@ __global__ void tc_qkv_kernel(const TcQkvArgs a) {
       q[e] = lo;
       q[e + half] = hi;
     } else {
-      const size_t ci = ((row * a.kv + (size_t)(head - a.H)) * a.cap + pos) * a.hd;
+      int r, pp;
+      cache_slot(a.step, a.cap, b, pos, r, pp);
+      const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H)) * a.cap + pp) * a.hd;
       store_elem<1>(a.kc, ci + e, lo);
       store_elem<1>(a.kc, ci + e + half, hi);
     }
   } else {
-    const size_t ci = ((row * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pos) * a.hd;
+    int r, pp;
+    cache_slot(a.step, a.cap, b, pos, r, pp);
+    const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pp) * a.hd;
     store_elem<1>(a.vc, ci + e, x0);
     store_elem<1>(a.vc, ci + e + half, x1);
   }

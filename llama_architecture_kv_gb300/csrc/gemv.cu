@@ -289,12 +289,16 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
             q[e] = lo;
             q[e + half] = hi;
           } else {
-            const size_t ci = ((row * a.kv + (size_t)(head - a.H)) * a.cap + pos) * a.hd;
+            int r, pp;
+            cache_slot(a.step, a.cap, (int)row, pos, r, pp);
+            const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H)) * a.cap + pp) * a.hd;
             store_elem<WT>(a.kc, ci + e, lo);
             store_elem<WT>(a.kc, ci + e + half, hi);
           }
         } else {
-          const size_t ci = ((row * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pos) * a.hd;
+          int r, pp;
+          cache_slot(a.step, a.cap, (int)row, pos, r, pp);
+          const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pp) * a.hd;
           store_elem<WT>(a.vc, ci + e, x0);
           store_elem<WT>(a.vc, ci + e + half, x1);
         }
@@ -521,12 +525,16 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
           qo[e] = lo;
           qo[e + half] = hi;
         } else {
-          const size_t ci = ((size_t)(head - a.H) * a.cap + pos) * a.hd;
+          int r, pp;
+          cache_slot(a.step, a.cap, 0, pos, r, pp);
+          const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H)) * a.cap + pp) * a.hd;
           store_elem<1>(a.kc, ci + e, lo);
           store_elem<1>(a.kc, ci + e + half, hi);
         }
       } else {
-        const size_t ci = ((size_t)(head - a.H - a.kv) * a.cap + pos) * a.hd;
+        int r, pp;
+        cache_slot(a.step, a.cap, 0, pos, r, pp);
+        const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pp) * a.hd;
         store_elem<1>(a.vc, ci + e, v0);
         store_elem<1>(a.vc, ci + e + half, v1);
       }

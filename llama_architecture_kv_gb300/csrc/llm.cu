@@ -50,6 +50,8 @@ struct BeginArgs {
   int32_t pos, B;          // pos: every row's position, unless the rows sit at their own:
   int32_t own_pos;         //   then pos_dev[b] (B > kInline) or pos_inline[b]
   const int32_t* pos_dev;
+  const int32_t* table;    // paged step: [B][table_stride] pages, or null
+  int32_t table_stride;
   float temp;
   int32_t k;
   float p;
@@ -74,6 +76,8 @@ __global__ void step_begin_kernel(const BeginArgs a) {
     a.st->temp = a.temp;
     a.st->k = a.k;
     a.st->p = a.p;
+    a.st->table = a.table;
+    a.st->table_stride = a.table_stride;
   }
   __syncthreads();
   int32_t* rowpos = reinterpret_cast<int32_t*>(a.st + 1);
@@ -106,6 +110,8 @@ __global__ void gen_begin_kernel(StepState* st, const GenState* gen, int32_t* to
     st->temp = g.temp;
     st->k = g.k;
     st->p = g.p;
+    st->table = nullptr;
+    st->table_stride = 0;
   }
   int32_t* rowpos = reinterpret_cast<int32_t*>(st + 1);
   for (int b = t; b < g.B; b += blockDim.x) {
@@ -240,6 +246,7 @@ struct llm_handle {
   StepState* st = nullptr;
   int32_t* pos_buf = nullptr;  // [max_batch] positions of a decode of rows at their own positions
   GenState* gen = nullptr;     // generation: the state of the graph launch in flight
+  int32_t* page_table = nullptr;  // paged steps: [max_batch][max_seq / kPage] (max_seq % kPage == 0)
   float* u_gen = nullptr;      // [kGenChunk][max_batch] draws of one host-memory generation launch
   int32_t* ids_gen = nullptr;  // [kGenChunk][max_batch] its drawn tokens
   int32_t* status = nullptr;
@@ -693,9 +700,10 @@ llm_status run_step(llm_handle* h, int B, int mode) {
 // the step prologue; rows at their own positions when pos_host is given (copied to pos_buf)
 llm_status begin(llm_handle* h, int pos, int B, const int32_t* tok_host, const int32_t* tok_dev, int tok_stride,
                  int tok_col, float temp, int k, float p, const float* u_host, const float* u_dev,
-                 const int32_t* pos_host = nullptr) {
+                 const int32_t* pos_host = nullptr, const int32_t* table_dev = nullptr, int table_stride = 0) {
   BeginArgs a = {};
   a.st = h->st; a.pos = pos; a.B = B; a.temp = temp; a.k = k; a.p = p; a.vocab = h->V;
+  a.table = table_dev; a.table_stride = table_stride;
   if (pos_host) {
     a.own_pos = 1;
     if (B <= kInline) {
@@ -926,6 +934,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
       (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, step_state_bytes(c.max_batch))) ||
       (st = dalloc(h, &h->pos_buf, B * 4)) || (st = dalloc(h, &h->gen, sizeof(GenState))) ||
       (st = dalloc(h, &h->u_gen, (size_t)kGenChunk * B * 4)) || (st = dalloc(h, &h->ids_gen, (size_t)kGenChunk * B * 4)) ||
+      (c.max_seq % kPage == 0 && (st = dalloc(h, &h->page_table, B * (size_t)(c.max_seq / kPage) * 4))) ||
       (st = dalloc(h, &h->status, 16)) || (st = dalloc(h, &h->tok_buf, B * 4)) || (st = dalloc(h, &h->u_buf, B * 4)) ||
       (st = dalloc(h, &h->ids_buf, B * 4)))
     return bail(st);
@@ -1071,6 +1080,77 @@ llm_status llm_decode_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t
                                float* logits_dev) {
   if (!h || !tokens_dev || !positions_host || !logits_dev) return LLM_ERR_ARG;
   return decode_rows_impl(h, nullptr, tokens_dev, B, positions_host, logits_dev, false);
+}
+
+// a paged step: rows at their own positions, every position found through the row's pages
+static llm_status paged_impl(llm_handle* h, const int32_t* tok_host, const int32_t* tok_dev, int32_t B,
+                             const int32_t* pos, const int32_t* table, int32_t pages_per_row, int mode, float temp,
+                             int32_t k, float p, const float* u_host, const float* u_dev, int32_t* ids, float* logits,
+                             bool host) {
+  if (!h->page_table)
+    return fail(h, LLM_ERR_CONFIG, "paged steps need max_seq (%d) to be a multiple of %d", h->cfg.max_seq, kPage);
+  if (B < 1 || B > h->cfg.max_batch) return fail(h, LLM_ERR_BATCH, "batch %d outside 1..%d", B, h->cfg.max_batch);
+  const int per_row = h->cfg.max_seq / kPage;
+  if (pages_per_row < 1 || pages_per_row > per_row)
+    return fail(h, LLM_ERR_ARG, "pages per row %d outside 1..%d", pages_per_row, per_row);
+  const int64_t pool = (int64_t)h->cfg.max_batch * per_row;
+  for (int b = 0; b < B; ++b) {
+    if (pos[b] < 0 || pos[b] >= pages_per_row * kPage)
+      return fail(h, LLM_ERR_POS_RANGE, "row %d: position %d outside its %d pages", b, pos[b], pages_per_row);
+    for (int i = 0; i <= pos[b] / kPage; ++i) {
+      const int32_t q = table[(size_t)b * pages_per_row + i];
+      if (q < 0 || q >= pool) return fail(h, LLM_ERR_ARG, "row %d: page %d is %d, outside the pool of %lld", b, i, q, (long long)pool);
+    }
+  }
+  TRY(check_sample_args(h, temp, k, p));
+  if (temp > 0.0f && !u_host && !u_dev) return fail(h, LLM_ERR_ARG, "sampling needs uniform draws u");
+  if (tok_host) TRY(check_tokens(h, tok_host, (size_t)B));
+  if (u_host && temp > 0.0f)
+    for (int b = 0; b < B; ++b)
+      if (!(u_host[b] >= 0.0f && u_host[b] < 1.0f)) return fail(h, LLM_ERR_ARG, "u[%d] outside [0, 1)", b);
+  CUDA_TRY(h, cudaMemcpyAsync(h->page_table, table, (size_t)B * pages_per_row * 4, cudaMemcpyHostToDevice, h->stream));
+  TRY(begin(h, 0, B, tok_host, tok_dev, 1, 0, temp, k, p, u_host, u_dev, pos, h->page_table, pages_per_row));
+  TRY(run_step(h, B, mode));
+  if (host) {
+    if (logits) CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
+    if (ids) CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToHost, h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  } else {
+    if (logits && logits != h->logits)
+      CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToDevice, h->stream));
+    if (ids && ids != h->ids_buf) CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToDevice, h->stream));
+  }
+  return LLM_OK;
+}
+
+llm_status llm_decode_paged(llm_handle* h, const int32_t* tokens_host, int32_t B, const int32_t* positions_host,
+                            const int32_t* table_host, int32_t pages_per_row, float* logits_host) {
+  if (!h || !tokens_host || !positions_host || !table_host || !logits_host) return LLM_ERR_ARG;
+  return paged_impl(h, tokens_host, nullptr, B, positions_host, table_host, pages_per_row, MODE_HEAD, 0.0f, 1, 1.0f,
+                    nullptr, nullptr, nullptr, logits_host, true);
+}
+
+llm_status llm_decode_paged_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, const int32_t* positions_host,
+                                const int32_t* table_host, int32_t pages_per_row, float* logits_dev) {
+  if (!h || !tokens_dev || !positions_host || !table_host || !logits_dev) return LLM_ERR_ARG;
+  return paged_impl(h, nullptr, tokens_dev, B, positions_host, table_host, pages_per_row, MODE_HEAD, 0.0f, 1, 1.0f,
+                    nullptr, nullptr, nullptr, logits_dev, false);
+}
+
+llm_status llm_step_paged(llm_handle* h, const int32_t* tokens_host, int32_t B, const int32_t* positions_host,
+                          const int32_t* table_host, int32_t pages_per_row, float temp, int32_t k, float p,
+                          const float* u_host, int32_t* ids_host, float* logits_host) {
+  if (!h || !tokens_host || !positions_host || !table_host || !ids_host) return LLM_ERR_ARG;
+  return paged_impl(h, tokens_host, nullptr, B, positions_host, table_host, pages_per_row,
+                    temp > 0.0f ? MODE_TOPP : MODE_GREEDY, temp, k, p, u_host, nullptr, ids_host, logits_host, true);
+}
+
+llm_status llm_step_paged_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, const int32_t* positions_host,
+                              const int32_t* table_host, int32_t pages_per_row, float temp, int32_t k, float p,
+                              const float* u_dev, int32_t* ids_dev, float* logits_dev) {
+  if (!h || !tokens_dev || !positions_host || !table_host || !ids_dev) return LLM_ERR_ARG;
+  return paged_impl(h, nullptr, tokens_dev, B, positions_host, table_host, pages_per_row,
+                    temp > 0.0f ? MODE_TOPP : MODE_GREEDY, temp, k, p, nullptr, u_dev, ids_dev, logits_dev, false);
 }
 
 // n decode steps, each feeding its draws to the next as tokens, as CUDA graphs of kGenChunk

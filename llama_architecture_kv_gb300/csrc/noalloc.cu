@@ -46,6 +46,7 @@ __global__ void noalloc_params_kernel(StepState* st, float temp, int32_t k, floa
   st->temp = temp;
   st->k = k;
   st->p = p;
+  st->table = nullptr;
 }
 
 // the scratch address on the current device (looked up once per device)
