@@ -145,6 +145,22 @@ def traffic_from_profile(kernel_file, profile_name):
     return None
 
 
+def max_over_ranks(x, device):
+    """The largest of every rank's x: the job takes as long as its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, B, K, elapsed):
+    """Tokens per second of the whole job: every replica's B rows x K steps over the slowest time."""
+    return world * B * K / elapsed
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -325,11 +341,9 @@ def run_ours(args):
     ms = e0.elapsed_time(e1)
     elapsed = ms / 1e3
     if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+        elapsed = max_over_ranks(elapsed, dev)
         torch.distributed.barrier()
-    value = world * B * K / elapsed
+    value = whole_job_value(world, B, K, elapsed)
     clk = clocks.summary()
 
     # end to end through the public host API: tokens in from pinned host memory, ids out

@@ -1,0 +1,69 @@
+"""The multi-replica path of bench.py on CPU: two ranks over gloo (world size 2).
+
+One process per GPU runs an independent replica; the job's time is the slowest rank's (a
+max-reduction, the only collective) and its throughput counts every rank's tokens.  The
+reference arm runs on rank 0 alone; other ranks return at once.
+"""
+import contextlib
+import io
+import multiprocessing as mp
+import os
+import socket
+
+import pytest
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        elapsed = 1.5 + rank  # rank 1 is the slow one
+        slowest = bench.max_over_ranks(elapsed, "cpu")
+        value = bench.whole_job_value(world, 4, 10, slowest)
+        dist.barrier()
+        q.put((rank, slowest, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_replicas_take_the_slowest_time_and_count_all_tokens():
+    pytest.importorskip("torch")
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, slowest, value in out:
+        assert slowest == 2.5
+        assert value == 2 * 4 * 10 / 2.5
+
+
+def test_single_process_needs_no_collective():
+    import bench
+    assert bench.max_over_ranks(3.25, "cpu") == 3.25
+    assert bench.whole_job_value(1, 32, 100, 2.0) == 1600.0
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference"])
+        bench.run_reference(bench.parse())
+    assert buf.getvalue() == ""  # no work and no line on a non-zero rank
