@@ -67,3 +67,14 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
         monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference"])
         bench.run_reference(bench.parse())
     assert buf.getvalue() == ""  # no work and no line on a non-zero rank
+
+
+def test_step_roofline_fields():
+    import bench
+    # 15.28 GB per step at batch 1: 444.3 tok/s at the measured 6788 GB/s, 523.6 at 8 TB/s
+    r = bench.step_roofline(15.28e9, 1, 6788.3, 352.7, 100, 100 * 15.28e9 / 5.389e12)
+    assert abs(r["roofline_tok_s"] - 6788.3e9 / 15.28e9) < 1e-9
+    assert abs(r["frac_of_roofline"] - 352.7 / (6788.3e9 / 15.28e9)) < 1e-12
+    assert abs(r["roofline_tok_s_nominal_8tbs"] - 8000e9 / 15.28e9) < 1e-9
+    assert abs(r["frac_of_nominal_8tbs"] - 352.7 * 15.28e9 / 8000e9) < 1e-12
+    assert abs(r["hbm_gbs_achieved"] - 5389.0) < 1e-6
