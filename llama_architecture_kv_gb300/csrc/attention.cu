@@ -3,11 +3,15 @@
 // Computes, for every batch row b and query head h = j*g + i (group j reads key/value head j:
 // bend-ml-llama "Grouped-query attention", gqa_head), the output
 //   o_h = sum_{p=0..t} softmax_p(scale * q_h . K_j[p]) V_j[p],  scale = 1/sqrt(hd),
-// over exactly the cache positions 0..t, t = pos (bend-ml-llama law causal; Llama 3.1 8B card,
-// attention.linnet decode: seen[s] = s <= pos).
+// over exactly the cache positions 0..t, t = the row's position (bend-ml-llama law causal;
+// Llama 3.1 8B card, attention.linnet decode: seen[s] = s <= pos).
 //
 // Layout: the cache of one layer is [max_batch][kv][cap][hd] (attention.linnet cache_k), so the
-// positions of one (row, key/value head) are contiguous.  Grid: (splits, kv, B); a CTA takes a
+// positions of one (row, key/value head) are contiguous; in a paged step a row's positions are
+// found 64 at a time through its page table (cache_slot), and no chunk crosses a page.
+// Two kernels: attn_mma_kernel (bf16 caches, head size 64 or 128; warp-level tensor-core MMAs,
+// described further down) and attn_decode_kernel (everything else), described here.
+// attn_decode_kernel grid: (splits, kv, B); a CTA takes a
 // contiguous slice of positions of one (row, kv head) and its warps take 32-position chunks of
 // it in turn.  Each warp streams its own chunks through a private ring of shared-memory buffers
 // (a TMA tensor copy of the keys with the 128-byte swizzle, a bulk copy of the values; one

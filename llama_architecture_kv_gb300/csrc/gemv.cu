@@ -6,20 +6,22 @@
 // rmsnorm: g * (x * (1 / sqrt(mean(x^2) + eps)))), computed in the prologue of every CTA.
 // Epilogues fuse what follows each projection in the layer (bend-ml-llama "A layer", block):
 //   EPI_QKV    rows come in RoPE pairs (element i and i + half of one head): rotate q and k
-//              (rot_lo = lo*cos - hi*sin, rot_hi = hi*cos + lo*sin), store the rotated q, and
-//              write the rotated k and the plain v into the KV cache at position pos
-//              (KV.push), rounding to the cache element type;
+//              (rot_lo = lo*cos - hi*sin, rot_hi = hi*cos + lo*sin) at the row's position,
+//              store the rotated q, and write the rotated k and the plain v into the KV cache
+//              there (KV.push; through the row's page table in a paged step), rounding to the
+//              cache element type;
 //   EPI_RESID  x1 = x + W_o attn, y = x1 + W_down m;
 //   EPI_SWIGLU rows come in (gate, up) pairs: m = silu(gate) * up, silu(v) = v / (1 + exp(-v));
 //   EPI_STORE  logits = W_head nf.
 //
 // Design: the decode step is bound by HBM bandwidth (each weight byte is read once per step),
-// so the kernel is a streaming engine.  Each CTA owns a contiguous, balanced range of rows
-// (whole work units, so RoPE and SwiGLU pairs stay in one CTA) and reads them with 16-byte
-// non-allocating loads in groups of 8 per thread, two groups in flight (double buffered).
-// The threads of a row split its columns;
-// the (normalized) input lives in shared memory as f32.  Partial dot products are reduced
-// with warp shuffles and a fixed-order sum across warps, so results are deterministic.
+// so both kernels here are streaming engines.  gemv_kernel (any batch, bf16 or f32 weights):
+// each CTA owns a contiguous, balanced range of rows (whole work units, so RoPE and SwiGLU pairs
+// stay in one CTA) and reads them with 16-byte non-allocating loads in groups of 8 per thread,
+// two groups in flight (double buffered); the threads of a row split its columns; the
+// (normalized) input lives in shared memory as f32; partial dot products are reduced with warp
+// shuffles and a fixed-order sum across warps, so results are deterministic.  gemv_tma_kernel
+// (batch 1, bf16) streams the rows through per-warp rings of bulk copies instead (see below).
 #include "gemv.cuh"
 #include "tc.cuh"
 
