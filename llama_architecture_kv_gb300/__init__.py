@@ -44,6 +44,46 @@ class LlmError(RuntimeError):
         self.status = status
 
 
+# argument and result types of every entry point (ctypes)
+_i32, _u64, _f32, _vp = ctypes.c_int32, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
+_pcfg = ctypes.POINTER(LlmConfig)
+SIGNATURES = {
+    "llm_weight_count": ([_pcfg], _u64),
+    "llm_create": ([_pcfg, _vp, _u64, _i32, _vp, ctypes.POINTER(_vp)], _i32),
+    "llm_destroy": ([_vp], _i32),
+    "llm_reset": ([_vp], _i32),
+    "llm_prefill": ([_vp, _vp, _i32, _i32, _i32, _vp], _i32),
+    "llm_decode": ([_vp, _vp, _i32, _i32, _vp], _i32),
+    "llm_sample": ([_vp, _vp, _i32, _f32, _i32, _f32, _vp, _vp], _i32),
+    "llm_step": ([_vp, _vp, _i32, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
+    "llm_prefill_dev": ([_vp, _vp, _i32, _i32, _i32, _vp], _i32),
+    "llm_decode_dev": ([_vp, _vp, _i32, _i32, _vp], _i32),
+    "llm_sample_dev": ([_vp, _vp, _i32, _f32, _i32, _f32, _vp, _vp], _i32),
+    "llm_step_dev": ([_vp, _vp, _i32, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
+    "llm_decode_rows": ([_vp, _vp, _i32, _vp, _vp], _i32),
+    "llm_decode_rows_dev": ([_vp, _vp, _i32, _vp, _vp], _i32),
+    "llm_step_rows": ([_vp, _vp, _i32, _vp, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
+    "llm_step_rows_dev": ([_vp, _vp, _i32, _vp, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
+    "llm_generate": ([_vp, _vp, _i32, _i32, _i32, _f32, _i32, _f32, _vp, _vp], _i32),
+    "llm_generate_dev": ([_vp, _vp, _i32, _i32, _i32, _f32, _i32, _f32, _vp, _vp], _i32),
+    "llm_decode_paged": ([_vp, _vp, _i32, _vp, _vp, _i32, _vp], _i32),
+    "llm_decode_paged_dev": ([_vp, _vp, _i32, _vp, _vp, _i32, _vp], _i32),
+    "llm_step_paged": ([_vp, _vp, _i32, _vp, _vp, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
+    "llm_step_paged_dev": ([_vp, _vp, _i32, _vp, _vp, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
+    "llm_synchronize": ([_vp], _i32),
+    "llm_stream": ([_vp], _vp),
+    "llm_logits_buffer": ([_vp], _vp),
+    "llm_filled": ([_vp, _i32], _i32),
+    "llm_last_error": ([_vp], ctypes.c_char_p),
+    "llm_status_string": ([_i32], ctypes.c_char_p),
+    "llm_kv_import": ([_vp, _i32, _i32, _i32, _i32, _vp, _vp], _i32),
+    "llm_kv_export": ([_vp, _i32, _i32, _i32, _i32, _vp, _vp], _i32),
+    "llm_debug_trace": ([_vp, _i32, ctypes.c_char_p, _vp], _i32),
+    "llm_profile_kernel": ([_vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_f32)], _i32),
+    "llm_sample_noalloc": ([_vp, _i32, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
+    "llm_step_kernels": ([_vp, _i32, _f32, ctypes.POINTER(_i32)], _i32),
+    }
+
 _lib = None
 
 
@@ -55,45 +95,7 @@ def lib():
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                                "`python -m llama_architecture_kv_gb300.build`")
         L = ctypes.CDLL(LIB_PATH)
-        i32, u64, f32, vp = ctypes.c_int32, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
-        pcfg = ctypes.POINTER(LlmConfig)
-        sigs = {
-            "llm_weight_count": ([pcfg], u64),
-            "llm_create": ([pcfg, vp, u64, i32, vp, ctypes.POINTER(vp)], i32),
-            "llm_destroy": ([vp], i32),
-            "llm_reset": ([vp], i32),
-            "llm_prefill": ([vp, vp, i32, i32, i32, vp], i32),
-            "llm_decode": ([vp, vp, i32, i32, vp], i32),
-            "llm_sample": ([vp, vp, i32, f32, i32, f32, vp, vp], i32),
-            "llm_step": ([vp, vp, i32, i32, f32, i32, f32, vp, vp, vp], i32),
-            "llm_prefill_dev": ([vp, vp, i32, i32, i32, vp], i32),
-            "llm_decode_dev": ([vp, vp, i32, i32, vp], i32),
-            "llm_sample_dev": ([vp, vp, i32, f32, i32, f32, vp, vp], i32),
-            "llm_step_dev": ([vp, vp, i32, i32, f32, i32, f32, vp, vp, vp], i32),
-            "llm_decode_rows": ([vp, vp, i32, vp, vp], i32),
-            "llm_decode_rows_dev": ([vp, vp, i32, vp, vp], i32),
-            "llm_step_rows": ([vp, vp, i32, vp, f32, i32, f32, vp, vp, vp], i32),
-            "llm_step_rows_dev": ([vp, vp, i32, vp, f32, i32, f32, vp, vp, vp], i32),
-            "llm_generate": ([vp, vp, i32, i32, i32, f32, i32, f32, vp, vp], i32),
-            "llm_generate_dev": ([vp, vp, i32, i32, i32, f32, i32, f32, vp, vp], i32),
-            "llm_decode_paged": ([vp, vp, i32, vp, vp, i32, vp], i32),
-            "llm_decode_paged_dev": ([vp, vp, i32, vp, vp, i32, vp], i32),
-            "llm_step_paged": ([vp, vp, i32, vp, vp, i32, f32, i32, f32, vp, vp, vp], i32),
-            "llm_step_paged_dev": ([vp, vp, i32, vp, vp, i32, f32, i32, f32, vp, vp, vp], i32),
-            "llm_synchronize": ([vp], i32),
-            "llm_stream": ([vp], vp),
-            "llm_logits_buffer": ([vp], vp),
-            "llm_filled": ([vp, i32], i32),
-            "llm_last_error": ([vp], ctypes.c_char_p),
-            "llm_status_string": ([i32], ctypes.c_char_p),
-            "llm_kv_import": ([vp, i32, i32, i32, i32, vp, vp], i32),
-            "llm_kv_export": ([vp, i32, i32, i32, i32, vp, vp], i32),
-            "llm_debug_trace": ([vp, i32, ctypes.c_char_p, vp], i32),
-            "llm_profile_kernel": ([vp, i32, i32, i32, i32, ctypes.POINTER(f32)], i32),
-            "llm_sample_noalloc": ([vp, i32, i32, f32, i32, f32, vp, vp, vp], i32),
-            "llm_step_kernels": ([vp, i32, f32, ctypes.POINTER(i32)], i32),
-        }
-        for name, (args, res) in sigs.items():
+        for name, (args, res) in SIGNATURES.items():
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = res

@@ -76,3 +76,49 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(pkg, "_lib", None)
     with pytest.raises(RuntimeError):
         pkg.lib()
+
+
+def _prototypes():
+    """(name, parameter count) of every function include/llm.h declares."""
+    src = open(os.path.join(ROOT, "include", "llm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    out = {}
+    for m in re.finditer(r"\b(llm_[a-z_]+)\s*\(([^;{)]*)\)\s*;", src):
+        params = [p for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        out[m.group(1)] = len(params)
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    # a ctypes signature with the wrong number of arguments would pass garbage through the ABI
+    protos = _prototypes()
+    assert set(protos) == set(pkg.EXPORTS)
+    for name, (argtypes, _) in pkg.SIGNATURES.items():
+        assert len(argtypes) == protos[name], name
+
+
+def test_header_is_plain_c(tmp_path):
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text('#include "llm.h"\nint main(void) { return llm_status_string(LLM_OK) == 0; }\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_entries_refuse_a_null_handle(lib):
+    # every entry that takes a handle checks it (and its buffers) before any device work
+    protos = _prototypes()
+    skip = {"llm_create", "llm_weight_count", "llm_status_string", "llm_last_error", "llm_stream",
+            "llm_logits_buffer", "llm_filled", "llm_sample_noalloc"}
+    for name in sorted(protos):
+        if name in skip:
+            continue
+        argtypes, _ = pkg.SIGNATURES[name]
+        args = [None if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer) else 0
+                for t in argtypes]
+        assert getattr(lib, name)(*args) == pkg.LLM_ERR_ARG, name
