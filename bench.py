@@ -288,7 +288,7 @@ def run_ours(args):
         w = dataclasses.replace(w, prompt=args.prompt)
     s, B, P = w.shape, w.batch, w.prompt
     K, W = args.steps, args.warmup
-    cap = max(w.cap, P + W + K + 1)
+    cap = max(w.cap, P + max(W + K, 9) + 1)  # (9: the generation warm-up)
     stream = torch.cuda.Stream()
 
     t0 = time.perf_counter()
@@ -329,12 +329,16 @@ def run_ours(args):
         else:
             pkg.llm_step_rows_dev(h, tk, B, rowpos + i, temp, k_, p_, u, ids)
 
-    gen_ids = torch.empty((max(W, K), B), dtype=torch.int32, device=dev) if args.generate else None
+    # generation warm-up: 9 steps capture both generation graphs (8 steps, then a single step)
+    GW = 9
+    gen_ids = torch.empty((max(GW, K), B), dtype=torch.int32, device=dev) if args.generate else None
+    u_gw = (torch.from_numpy(synth.uniforms(w.seed_uniform, B * (W + K), B * GW).reshape(GW, B)).to(dev)
+            if args.generate else None)
     with torch.cuda.stream(stream):
         for i in range(W):  # warm-up: rewind to the prompt end every time
             step_dev(tok[0], 0, u_dev[i], tok[1])
-        if args.generate:  # captures the generation graphs
-            pkg.llm_generate_dev(h, tok[0], B, pos0, W, temp, k_, p_, u_dev[:W], gen_ids[:W])
+        if args.generate:
+            pkg.llm_generate_dev(h, tok[0], B, pos0, GW, temp, k_, p_, u_gw, gen_ids[:GW])
         pkg.llm_synchronize(h)
         if world > 1:
             torch.distributed.barrier()
