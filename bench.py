@@ -129,16 +129,44 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def kernel_function_text(src, name):
+    """The definition of function `name` in source text src: from its name through the closing
+    brace of its body (None if src does not define it)."""
+    for m in re.finditer(r"\b%s\s*\(" % re.escape(name), src):
+        i, depth = m.end(), 1
+        while depth and i < len(src):
+            depth += {"(": 1, ")": -1}.get(src[i], 0)
+            i += 1
+        while i < len(src) and src[i] in " \t\n":
+            i += 1
+        if i < len(src) and src[i] == "{":
+            depth = 0
+            for k in range(i, len(src)):
+                depth += {"{": 1, "}": -1}.get(src[k], 0)
+                if depth == 0:
+                    return src[m.start():k + 1]
+    return None
+
+
 def traffic_from_profile(kernel_file, profile_name):
-    """dram bytes per launch from the committed ncu summary, if taken on the current source."""
+    """dram bytes per launch from the committed ncu summary, if taken on the current source: the
+    profiled kernel's own definition (kernel_function / kernel_function_sha256_16) when the
+    summary names it, else the whole file (kernel_source_sha256_16)."""
     path = os.path.join(ROOT, "profiles", profile_name)
     src = os.path.join(ROOT, "llama_architecture_kv_gb300", "csrc", kernel_file)
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+        code = open(src, "rb").read()
         m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-        if m_sha and m_tr and m_sha.group(1) == sha:
+        m_fn = re.search(r"kernel_function:\s*(\w+)", text)
+        m_fsha = re.search(r"kernel_function_sha256_16:\s*([0-9a-f]+)", text)
+        if m_fn and m_fsha:
+            body = kernel_function_text(code.decode(), m_fn.group(1))
+            ok = body is not None and hashlib.sha256(body.encode()).hexdigest()[:16] == m_fsha.group(1)
+        else:
+            m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+            ok = m_sha is not None and m_sha.group(1) == hashlib.sha256(code).hexdigest()[:16]
+        if ok and m_tr:
             return float(m_tr.group(1))
     except OSError:
         pass

@@ -78,3 +78,12 @@ def test_step_roofline_fields():
     assert abs(r["roofline_tok_s_nominal_8tbs"] - 8000e9 / 15.28e9) < 1e-9
     assert abs(r["frac_of_nominal_8tbs"] - 352.7 * 15.28e9 / 8000e9) < 1e-12
     assert abs(r["hbm_gbs_achieved"] - 5389.0) < 1e-6
+
+
+def test_kernel_function_text_finds_the_definition():
+    import bench
+    src = ("void k(int a);\n__global__ void __launch_bounds__(256, 1) k(const A a, int n) {\n"
+           "  if (n) { f((n)); }\n}\nvoid other() {}\n")
+    body = bench.kernel_function_text(src, "k")
+    assert body.startswith("k(const A a, int n) {") and body.endswith("}") and "other" not in body
+    assert bench.kernel_function_text(src, "missing") is None
