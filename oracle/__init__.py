@@ -57,6 +57,7 @@ def lib():
             "or_reset": ([vp], None),
             "or_forward": ([vp, i32, i32, i32, vp], i32),
             "or_prefill": ([vp, i32, vp, i32, i32, vp], i32),
+            "or_prefill_packed": ([vp, vp, vp, vp, vp, i32, vp, i32, vp], i32),
             "or_embed": ([vp, i32], i32),
             "or_layer": ([vp, i32, i32, i32], i32),
             "or_head": ([vp, vp], None),
@@ -254,6 +255,21 @@ class Model:
                              out.ctypes.data if logits else None)
         if r:
             raise ValueError(f"or_prefill: {r}")
+        return out
+
+    def prefill_packed(self, toks, rows, positions, segments, last):
+        """Prompts packed end to end: token p is position positions[p] of prompt segments[p] in
+        cache row rows[p]; each attends to its own prompt's tokens up to itself.  Returns the
+        logits after token last[m], [len(last)][V]."""
+        arrs = [np.ascontiguousarray(a, dtype=np.int32).reshape(-1) for a in (toks, rows, positions, segments, last)]
+        toks, rows, positions, segments, last = arrs
+        P = toks.size
+        assert rows.size == P and positions.size == P and segments.size == P
+        out = np.empty((last.size, self.cfg.vocab), np.float32)
+        r = lib().or_prefill_packed(self.h, toks.ctypes.data, rows.ctypes.data, positions.ctypes.data,
+                                    segments.ctypes.data, P, last.ctypes.data, last.size, out.ctypes.data)
+        if r:
+            raise ValueError(f"or_prefill_packed: {r}")
         return out
 
     def attend(self, layer, b, q, t):

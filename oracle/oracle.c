@@ -16,7 +16,8 @@
  *        "Sampling" (topk, weight, total, kept, stops, pick, sample).
  *   [P3] "Llama 3.1 8B Instruct" model card: README "Entries" and "Validation";
  *        rope.linnet (tables: llama3 rescaling); attention.linnet (forward, decode,
- *        prefill: the cache layout [Batch, KvHeads, MaxSeq, hd] and the seen-mask).
+ *        prefill: the cache layout [Batch, KvHeads, MaxSeq, hd] and the seen-mask);
+ *        lib.linnet (prefill_packed: prompts packed end to end, each seeing only itself).
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared oracle.c -lm
  * (-ffp-contract=off: no multiply-add contraction, every product and sum rounded on its
@@ -33,6 +34,8 @@
  *  - The cache of bf16-weight models stores keys and values rounded to bf16 (round to
  *    nearest even) on write, as P3's cache of element type T = bf16; the f32 model keeps
  *    an f32 cache (as P1 does).
+ *  - prefill_packed's attention reads the pass's keys and values as the cache holds them
+ *    (rounded to bf16 for bf16-weight models), as a decode step reads its own key and value.
  *  - F32.exp inside the sampler: exp_s below (Cody-Waite reduction by ln 2 split in two,
  *    degree-8 Taylor polynomial in Horner form with fused multiply-adds, scaling by 2^n),
  *    so that sampled ids can be reproduced bit for bit.  Softmax and silu use libm expf.
@@ -633,6 +636,130 @@ int32_t or_prefill(or_model* M, int32_t b, const int32_t* toks, int32_t S, int32
     int32_t r = or_forward(M, b, toks[i], pos + i, i == S - 1 ? logits : 0);
     if (r) return r;
   }
+  return 0;
+}
+
+/*
+ * [P3] prefill_packed (lib.linnet "prefill_packed", its layer's prefill_packed): the tokens of
+ * several prompts packed end to end, P in all.  Token p is position positions[p] of prompt
+ * segments[p] and belongs to cache row rows[p].  Layer by layer, every token's rotated key
+ * and its value go to its row at its position; then token i attends to the tokens j of its own
+ * prompt (segments[j] == segments[i]) with positions[j] <= positions[i], in pack order, and to
+ * nothing else: not to what its row's cache held before the pass.  The keys and values are
+ * read back as the cache holds them (rounded to bf16 for bf16-weight models), as a decode step
+ * reads its own.  logits [nlast][V] (may be NULL): after token last[m].  Two tokens may not
+ * share a (row, position) slot.
+ */
+int32_t or_prefill_packed(or_model* M, const int32_t* toks, const int32_t* rows, const int32_t* positions,
+                          const int32_t* segments, int32_t P, const int32_t* last, int32_t nlast, float* logits) {
+  const or_cfg* c = &M->c;
+  if (P <= 0 || nlast < 0) return OR_ERR_ARG;
+  for (int32_t p = 0; p < P; ++p) {
+    if (toks[p] < 0 || toks[p] >= c->vocab) return OR_ERR_TOKEN_RANGE;
+    if (rows[p] < 0 || rows[p] >= c->batch) return OR_ERR_ARG;
+    if (positions[p] < 0 || positions[p] >= c->cap) return OR_ERR_POS_RANGE;
+    for (int32_t q = 0; q < p; ++q)
+      if (rows[q] == rows[p] && positions[q] == positions[p]) return OR_ERR_ARG;
+  }
+  for (int32_t m = 0; m < nlast; ++m)
+    if (last[m] < 0 || last[m] >= P) return OR_ERR_ARG;
+  const int32_t d = M->d, hd = M->hd, half = c->half, kvw = M->kvw, f = M->f, g = c->g;
+  const float scale = 1.0f / sqrtf((float)hd);
+  float* X = (float*)malloc(sizeof(float) * (size_t)P * (size_t)d);    /* residual streams */
+  float* QR = (float*)malloc(sizeof(float) * (size_t)P * (size_t)d);   /* rotated queries */
+  float* ATT = (float*)malloc(sizeof(float) * (size_t)P * (size_t)d);  /* attention outputs */
+  float* sc = (float*)malloc(sizeof(float) * (size_t)P);
+  float* wt = (float*)malloc(sizeof(float) * (size_t)P);
+  int32_t* own = (int32_t*)malloc(sizeof(int32_t) * (size_t)P);
+  float* gn = (float*)malloc(sizeof(float) * (size_t)d);   /* ln1 gains of the layer */
+  float* gn2 = (float*)malloc(sizeof(float) * (size_t)d);  /* ln2 gains */
+  float cs[256], sn[256];
+  for (int32_t p = 0; p < P; ++p)
+    for (int32_t i = 0; i < d; ++i) X[(size_t)p * d + i] = W(M, (uint64_t)toks[p] * (uint64_t)d + (uint64_t)i);
+  for (int32_t l = 0; l < M->L; ++l) {
+    /* every token: norm, projections, rotation, and its key and value into the cache */
+    gains(M, toff(M, l, T_LN1), d, gn);
+    for (int32_t p = 0; p < P; ++p) {
+      for (int32_t i = 0; i < half; ++i) {
+        float a = (float)positions[p] * M->inv[i];
+        cs[i] = (float)cos((double)a);
+        sn[i] = (float)sin((double)a);
+      }
+      or_rmsnorm(X + (size_t)p * d, gn, d, c->eps, M->n1);
+      matvec(M, toff(M, l, T_Q), d, d, M->n1, M->q);
+      matvec(M, toff(M, l, T_K), kvw, d, M->n1, M->k);
+      matvec(M, toff(M, l, T_V), kvw, d, M->n1, M->v);
+      for (int32_t h = 0; h < M->H; ++h)
+        or_rope_head(M->q + (size_t)h * hd, half, cs, sn, QR + (size_t)p * d + (size_t)h * hd);
+      for (int32_t j = 0; j < c->kv; ++j) or_rope_head(M->k + (size_t)j * hd, half, cs, sn, M->kr + (size_t)j * hd);
+      for (int32_t j = 0; j < c->kv; ++j)
+        for (int32_t e = 0; e < hd; ++e) {
+          uint64_t ci = cidx(M, l, rows[p], j, positions[p]) + (uint64_t)e;
+          cput(M, M->kc, ci, M->kr[j * hd + e]);
+          cput(M, M->vc, ci, M->v[j * hd + e]);
+        }
+    }
+    /* every token attends to its own prompt's tokens up to its position, in pack order */
+    for (int32_t i = 0; i < P; ++i) {
+      int32_t n = 0;
+      for (int32_t p = 0; p < P; ++p)
+        if (segments[p] == segments[i] && positions[p] <= positions[i]) own[n++] = p;
+      for (int32_t j = 0; j < c->kv; ++j)
+        for (int32_t ih = 0; ih < g; ++ih) {
+          const int32_t h = j * g + ih;
+          const float* qh = QR + (size_t)i * d + (size_t)h * hd;
+          for (int32_t a = 0; a < n; ++a) {
+            const uint64_t kb = cidx(M, l, rows[own[a]], j, positions[own[a]]);
+            float acc = 0.0f;
+            for (int32_t e = 0; e < hd; ++e) acc = acc + qh[e] * cget(M, M->kc, kb + (uint64_t)e);
+            sc[a] = scale * acc;
+          }
+          float mx = sc[0];
+          for (int32_t a = 1; a < n; ++a) mx = fmaxf(mx, sc[a]);
+          float z = 0.0f;
+          for (int32_t a = 0; a < n; ++a) {
+            wt[a] = expf(sc[a] - mx);
+            z = z + wt[a];
+          }
+          for (int32_t a = 0; a < n; ++a) wt[a] = wt[a] / z;
+          float* o = ATT + (size_t)i * d + (size_t)h * hd;
+          for (int32_t e = 0; e < hd; ++e) {
+            float acc = 0.0f;
+            for (int32_t a = 0; a < n; ++a) {
+              const uint64_t vb = cidx(M, l, rows[own[a]], j, positions[own[a]]);
+              acc = acc + wt[a] * cget(M, M->vc, vb + (uint64_t)e);
+            }
+            o[e] = acc;
+          }
+        }
+    }
+    /* every token: o_proj and the residual, the norm, SwiGLU, down and the residual */
+    gains(M, toff(M, l, T_LN2), d, gn2);
+    for (int32_t p = 0; p < P; ++p) {
+      float* x = X + (size_t)p * d;
+      matvec(M, toff(M, l, T_O), d, d, ATT + (size_t)p * d, M->a);
+      for (int32_t i = 0; i < d; ++i) M->x1[i] = x[i] + M->a[i];
+      or_rmsnorm(M->x1, gn2, d, c->eps, M->n2);
+      matvec(M, toff(M, l, T_GATE), f, d, M->n2, M->gg);
+      matvec(M, toff(M, l, T_UP), f, d, M->n2, M->uu);
+      for (int32_t i = 0; i < f; ++i) M->uu[i] = silu(M->gg[i]) * M->uu[i];
+      matvec(M, toff(M, l, T_DOWN), d, f, M->uu, M->m);
+      for (int32_t i = 0; i < d; ++i) x[i] = M->x1[i] + M->m[i];
+    }
+  }
+  if (logits)
+    for (int32_t m = 0; m < nlast; ++m) {
+      memcpy(M->x, X + (size_t)last[m] * d, sizeof(float) * (size_t)d);
+      or_head(M, logits + (size_t)m * (size_t)M->V);
+    }
+  free(X);
+  free(QR);
+  free(ATT);
+  free(sc);
+  free(wt);
+  free(own);
+  free(gn);
+  free(gn2);
   return 0;
 }
 

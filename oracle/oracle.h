@@ -39,6 +39,8 @@ int32_t or_embed(or_model* m, int32_t tok);
 int32_t or_layer(or_model* m, int32_t l, int32_t b, int32_t t);
 void or_head(or_model* m, float* logits);
 int32_t or_prefill(or_model* m, int32_t b, const int32_t* toks, int32_t S, int32_t pos, float* logits);
+int32_t or_prefill_packed(or_model* m, const int32_t* toks, const int32_t* rows, const int32_t* positions,
+                          const int32_t* segments, int32_t P, const int32_t* last, int32_t nlast, float* logits);
 int32_t or_forward_full(const or_cfg* c, const void* weights, uint64_t nbytes, const int32_t* toks,
                         int32_t S, float* logits);
 int32_t or_attend(or_model* m, int32_t layer, int32_t b, const float* q, int32_t t, float* out);

@@ -692,3 +692,93 @@ def test_rotation_is_identity_at_position_zero_in_the_model():
     a = (a + np.pi) % (2 * np.pi) - np.pi
     want = 1.0 / np.power(np.float64(s.theta), np.arange(h) * 2.0 / s.hd)
     np.testing.assert_allclose(a, want, atol=1e-5)
+
+
+# ---------------------------------------------------------------------------------------
+# packed prefill (Llama 3.1 8B Instruct card, "Entries": prefill_packed; lib.linnet)
+# ---------------------------------------------------------------------------------------
+
+PACK_SHAPES = [shrink(TINY, kv=2, g=2, layers=2), shrink(SMOL135M, layers=1, ffn=64, vocab=96)]
+
+
+@pytest.mark.parametrize("shape", PACK_SHAPES, ids=["f32", "bf16"])
+def test_packed_single_prompt_is_prefill(shape):
+    # one prompt at positions 0..S-1: token t attends to positions 0..t of its row, exactly as
+    # S decode steps do, in the same order -- bit for bit, logits and cache
+    S = 7
+    toks = synth.tokens(901, 0, S, shape.vocab)
+    a, blob = _model(shape, cap=16, batch=2, seed=902)
+    b, _ = _model(shape, cap=16, batch=2, blob=blob)
+    la = a.prefill_packed(toks, np.ones(S), np.arange(S), np.zeros(S), [S - 1])[0]
+    lb = b.prefill(1, toks, 0)
+    assert np.array_equal(la.view(np.uint32), lb.view(np.uint32))
+    for layer in range(shape.layers):
+        ka, va = a.kv_read(layer, 1, 0, S)
+        kb, vb = b.kv_read(layer, 1, 0, S)
+        assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    a.close()
+    b.close()
+
+
+@pytest.mark.parametrize("shape", PACK_SHAPES, ids=["f32", "bf16"])
+def test_packed_prompts_do_not_see_each_other(shape):
+    # two prompts packed end to end, then interleaved: each gives what it gives alone
+    t0 = synth.tokens(903, 0, 5, shape.vocab)
+    t1 = synth.tokens(904, 0, 3, shape.vocab)
+    alone = []
+    for r, t in ((0, t0), (1, t1)):
+        m, blob = _model(shape, cap=8, batch=2, seed=905)
+        alone.append(m.prefill(r, t, 0))
+        m.close()
+    toks = np.concatenate([t0, t1])
+    rows = np.array([0] * 5 + [1] * 3)
+    pos = np.array(list(range(5)) + list(range(3)))
+    seg = np.array([0] * 5 + [1] * 3)
+    m, blob = _model(shape, cap=8, batch=2, seed=905)
+    end_to_end = m.prefill_packed(toks, rows, pos, seg, [4, 7])
+    m.close()
+    order = [0, 5, 1, 6, 2, 7, 3, 4]  # alternate the prompts' tokens, each prompt still in order
+    m, blob = _model(shape, cap=8, batch=2, seed=905)
+    inter = m.prefill_packed(toks[order], rows[order], pos[order], seg[order], [order.index(4), order.index(7)])
+    m.close()
+    for k in range(2):
+        assert np.array_equal(end_to_end[k].view(np.uint32), alone[k].view(np.uint32))
+        assert np.array_equal(inter[k].view(np.uint32), alone[k].view(np.uint32))
+
+
+def test_packed_prompt_sees_only_itself_not_its_rows_older_cache():
+    # a prompt at positions 5..9 of a row whose cache already holds positions 0..4: the pass
+    # ignores them (a decode-style prefill at position 5 would not), and attention being
+    # relative, the result is the same prompt's at positions 0..4 up to RoPE rounding
+    shape = PACK_SHAPES[0]
+    toks = synth.tokens(906, 0, 5, shape.vocab)
+    seg = np.zeros(5)
+    m, blob = _model(shape, cap=16, batch=1, seed=907)
+    m.prefill(0, synth.tokens(908, 0, 5, shape.vocab), 0, logits=False)
+    a = m.prefill_packed(toks, np.zeros(5), np.arange(5, 10), seg, [4])[0]
+    m.prefill(0, synth.tokens(909, 0, 5, shape.vocab), 0, logits=False)  # other older content
+    b = m.prefill_packed(toks, np.zeros(5), np.arange(5, 10), seg, [4])[0]
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    m.prefill(0, synth.tokens(908, 0, 5, shape.vocab), 0, logits=False)
+    c = m.prefill(0, toks, 5)  # decode-style: reads positions 0..4 as well
+    assert not np.array_equal(a.view(np.uint32), c.view(np.uint32))
+    m.close()
+    z, _ = _model(shape, cap=16, batch=1, blob=blob)
+    at0 = z.prefill_packed(toks, np.zeros(5), np.arange(5), seg, [4])[0]
+    z.close()
+    assert float(np.max(np.abs(a - at0))) <= 1e-4 * float(at0.max() - at0.min())
+
+
+def test_packed_rejects_shared_slots_and_bad_indices():
+    shape = PACK_SHAPES[0]
+    m, _ = _model(shape, cap=8, batch=2, seed=910)
+    toks = np.array([1, 2, 3])
+    with pytest.raises(ValueError):  # two tokens in one (row, position) slot
+        m.prefill_packed(toks, [0, 0, 1], [0, 0, 0], [0, 1, 2], [0])
+    with pytest.raises(ValueError):  # last names no token
+        m.prefill_packed(toks, [0, 0, 0], [0, 1, 2], [0, 0, 0], [3])
+    with pytest.raises(ValueError):  # row outside the cache
+        m.prefill_packed(toks, [0, 0, 2], [0, 1, 2], [0, 0, 0], [2])
+    with pytest.raises(ValueError):  # position outside the cache
+        m.prefill_packed(toks, [0, 0, 0], [0, 1, 8], [0, 0, 0], [2])
+    m.close()
