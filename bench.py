@@ -173,7 +173,7 @@ def traffic_from_profile(kernel_file, profile_name):
     return None
 
 
-NOMINAL_HBM_GBS = 8000.0  # the "8 TB/s" the target names beside the measured copy rate
+NOMINAL_HBM_GBS = 8000.0  # nominal HBM3e bandwidth of the part, reported beside the measured copy rate
 
 
 def step_roofline(step_bytes, B, peak_gbs, per_gpu_tok_s, K, elapsed):

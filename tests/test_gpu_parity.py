@@ -1,6 +1,6 @@
 """Parity of the GPU library with the oracle, through the C ABI (needs a GPU).
 
-Tolerances (fixed by the target): token ids and every integer decision bit-exact; the f32
+Tolerances: token ids and every integer decision bit-exact; the f32
 model's logits within 1e-4 of the oracle's logit range; bf16-weight models within an absolute
 3e-2 with greedy argmax agreement on at least 99% of decode steps.  Decoding is teacher-forced:
 the oracle replays the token stream the GPU produced, so one near-tie cannot make the two runs
