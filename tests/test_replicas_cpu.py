@@ -87,3 +87,21 @@ def test_kernel_function_text_finds_the_definition():
     body = bench.kernel_function_text(src, "k")
     assert body.startswith("k(const A a, int n) {") and body.endswith("}") and "other" not in body
     assert bench.kernel_function_text(src, "missing") is None
+
+
+def test_profile_summaries_are_self_describing():
+    # every committed ncu summary names the command that made it (committed files only) and,
+    # where the bench reads traffic from it, the kernel it measured and the bytes per launch
+    import glob
+    import os
+    import re
+    import bench
+    files = sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "*.md")))
+    assert files
+    for p in files:
+        text = open(p).read()
+        assert "```" in text and ("ncu " in text), p
+        assert "_work" not in text and "gpurun" not in text, p
+        if "traffic_bytes_per_launch" in text:
+            assert re.search(r"traffic_bytes_per_launch:\s*\d+", text), p
+            assert re.search(r"kernel_function:\s*\w+", text) and re.search(r"kernel_function_sha256_16:\s*[0-9a-f]{16}", text), p
