@@ -75,6 +75,7 @@ def lib():
             "or_inv_freq": ([pc, vp], None),
             "or_rope_cs": ([pc, i32, vp, vp], None),
             "or_exp_s": ([f32], f32),
+            "or_f32_to_bf16": ([f32], ctypes.c_uint16),
             "or_argmax": ([vp, i32], i32),
             "or_topk": ([vp, i32, i32, vp], i32),
             "or_sample": ([vp, i32, f32, i32, f32, f32], i32),
@@ -157,6 +158,11 @@ def rope_cs(cfg: Cfg, t: int):
 
 def exp_s(x: float) -> float:
     return float(lib().or_exp_s(x))
+
+
+def f32_to_bf16(x: float) -> int:
+    """The bf16 bits the oracle stores for an f32 key or value (round to nearest even)."""
+    return int(lib().or_f32_to_bf16(x))
 
 
 def argmax(x) -> int:

@@ -71,6 +71,9 @@ static inline uint16_t f32_to_bf16(float f) {
   return (uint16_t)(u >> 16);
 }
 
+/* the bf16 cache rounding above, exported so that it can be checked on its own */
+uint16_t or_f32_to_bf16(float f) { return f32_to_bf16(f); }
+
 /* [P1] squares, pair_sums, tree_sum: adjacent pairs added, the odd tail carried, until one
  * value is left; 0 for an empty list. */
 float or_tree_sum(const float* xs, int32_t n) {

@@ -57,6 +57,7 @@ void or_rope_head(const float* x, int32_t half, const float* cs, const float* sn
 void or_inv_freq(const or_cfg* c, float* inv);
 void or_rope_cs(const or_cfg* c, int32_t t, float* cs, float* sn);
 float or_exp_s(float x);
+uint16_t or_f32_to_bf16(float f);
 int32_t or_argmax(const float* xs, int32_t n);
 int32_t or_topk(const float* xs, int32_t n, int32_t k, int32_t* ids);
 int32_t or_sample(const float* xs, int32_t n, float temp, int32_t k, float p, float u);

@@ -782,3 +782,110 @@ def test_packed_rejects_shared_slots_and_bad_indices():
     with pytest.raises(ValueError):  # position outside the cache
         m.prefill_packed(toks, [0, 0, 0], [0, 1, 8], [0, 0, 0], [2])
     m.close()
+
+
+# ---- bf16 cache rounding (Llama 3.1 8B Instruct card, attention.linnet decode: a cache of
+# element type T = bf16; the f32 value of a key or value is rounded to the nearest bf16, ties to
+# the even significand, as IEEE 754 round-to-nearest-even fixes) ----
+
+def _bits(x: float) -> int:
+    return int(np.array([x], np.float32).view(np.uint32)[0])
+
+
+def _f32(bits: int) -> float:
+    return float(np.array([bits], np.uint32).view(np.float32)[0])
+
+
+def _rne_bf16_exact(bits: int) -> int:
+    """Nearest bf16 to the f32 value with these bits, by exact comparison of the two
+    neighbouring bf16 values (distances in exact rationals); ties go to the even one."""
+    from fractions import Fraction
+    x = _f32(bits)
+    if math.isnan(x):
+        return None
+    if math.isinf(x):
+        return bits >> 16
+    lo = bits >> 16                       # truncation: the neighbour toward zero
+    hi = lo + 1                           # the neighbour away from zero (may be an infinity)
+    xv = Fraction(x)
+    lv = Fraction(_f32(lo << 16))
+    hx = _f32(hi << 16)
+    if math.isinf(hx):
+        # above the largest finite bf16 the next value up is 2^128 for rounding purposes
+        hv = Fraction(2) ** 128 * (1 if x > 0 else -1)
+    else:
+        hv = Fraction(hx)
+    dl, dh = abs(xv - lv), abs(xv - hv)
+    if dl < dh:
+        return lo
+    if dh < dl:
+        return hi
+    return lo if (lo & 1) == 0 else hi
+
+
+@pytest.mark.parametrize("bits, want", [
+    (0x3F808000, 0x3F80),  # 1 + 2^-8: tie, the even neighbour is 1
+    (0x3F818000, 0x3F82),  # 1 + 3*2^-8: tie, the even neighbour is 1 + 2^-6
+    (0x3F808001, 0x3F81),  # just above a tie
+    (0x3F807FFF, 0x3F80),  # just below a tie
+    (0x3F817FFF, 0x3F81),
+    (0xBF808000, 0xBF80),  # negative ties
+    (0xBF818000, 0xBF82),
+    (0xBF808001, 0xBF81),
+    (0x7F7FFFFF, 0x7F80),  # the largest finite f32 rounds to +infinity
+    (0x7F7F8000, 0x7F80),  # tie between the largest finite bf16 and infinity: even is infinity
+    (0x7F7F7FFF, 0x7F7F),
+    (0xFF7FFFFF, 0xFF80),
+    (0x7F800000, 0x7F80),  # infinities stay
+    (0xFF800000, 0xFF80),
+    (0x00000000, 0x0000),  # signed zeros stay
+    (0x80000000, 0x8000),
+    (0x00000001, 0x0000),  # subnormals round like any other value
+    (0x00008000, 0x0000),
+    (0x00018000, 0x0002),
+    (0x00008001, 0x0001),
+    (0x807F8000, 0x8080),  # largest negative subnormal tie rounds up to the smallest normal
+])
+def test_bf16_cache_rounding_fixed_cases(bits, want):
+    assert oracle.f32_to_bf16(_f32(bits)) == want
+
+
+@pytest.mark.parametrize("bits", [0x7FC00000, 0xFFC00000, 0x7F800001, 0x7F810000, 0xFFFFFFFF])
+def test_bf16_cache_rounding_keeps_nan(bits):
+    got = oracle.f32_to_bf16(_f32(bits))
+    assert (got & 0x7F80) == 0x7F80 and (got & 0x7F) != 0, hex(got)
+    assert (got >> 15) == (bits >> 31)
+
+
+def test_bf16_cache_rounding_matches_exact_nearest_even():
+    rng = np.random.default_rng(21)
+    # random bit patterns, plus values a few ulps around every tie of a range of exponents
+    pats = [int(b) for b in rng.integers(0, 2 ** 32, 20000, dtype=np.uint64)]
+    for e in range(0, 255, 7):
+        for m in rng.integers(0, 2 ** 7, 8):
+            tie = (e << 23) | (int(m) << 16) | 0x8000
+            pats += [tie + dd for dd in (-2, -1, 0, 1, 2)] + [(tie | 0x80000000) + dd for dd in (-1, 0, 1)]
+    n = 0
+    for b in pats:
+        want = _rne_bf16_exact(b & 0xFFFFFFFF)
+        if want is None:
+            continue
+        assert oracle.f32_to_bf16(_f32(b & 0xFFFFFFFF)) == want, hex(b)
+        n += 1
+    assert n > 20000
+
+
+def test_cache_holds_the_rounded_rotated_keys():
+    # the bf16 cache of a forward step holds exactly the rounding of the rotated keys and of the
+    # values the layer computed (kr and v of the trace)
+    s = shrink(SMOL135M, layers=1, vocab=64, ffn=64)
+    blob = synth.model_blob(s, 31)
+    M = oracle.Model(oracle.cfg_of(s, 1, 8), blob, trace=True)
+    M.forward(0, 11, 3)
+    k, v = M.kv_read(0, 0, 3, 1)
+    kr, vv = M.trace(0, "kr"), M.trace(0, "v")
+    want_k = np.array([oracle.f32_to_bf16(float(x)) for x in kr], np.uint16).reshape(s.kv, 1, s.hd)
+    want_v = np.array([oracle.f32_to_bf16(float(x)) for x in vv], np.uint16).reshape(s.kv, 1, s.hd)
+    np.testing.assert_array_equal(k, want_k)
+    np.testing.assert_array_equal(v, want_v)
+    M.close()
