@@ -285,6 +285,17 @@ llm_status llm_profile_kernel(llm_handle* h, int32_t which, int32_t B, int32_t p
                               float* ms_per_launch);
 
 /*
+ * Test hook for the device-timeout report (needle-core v2 model.rs: forward returns an error
+ * result instead of failing the process).  Launches, on the handle's stream, one small kernel
+ * that waits on a shared-memory barrier nothing arrives on, with the same bounded wait the
+ * kernels' copy rings use and a limit of limit_cycles SM cycles (1..1e9, else LLM_ERR_ARG).  The
+ * wait runs out and the kernel records LLM_ERR_DEVICE_TIMEOUT in the handle's status word, which
+ * the next llm_synchronize reports once (and clears, with the attention's merge counters).
+ * Nothing faults or hangs; the handle stays usable.
+ */
+llm_status llm_check_wait_timeout(llm_handle* h, int64_t limit_cycles);
+
+/*
  * How many kernels one llm_step / llm_step_dev of B rows launches at temperature temp (greedy
  * when temp == 0): the step prologue plus the kernels of the step's CUDA graph, which this call
  * captures if it does not exist yet (no kernel runs).  LLM_ERR_BATCH for B outside
@@ -304,8 +315,12 @@ llm_status llm_step_kernels(llm_handle* h, int32_t B, float temp, int32_t* kerne
  * loads it until the process exits: B * (V rounded up to 32) must not exceed
  * LLM_SAMPLE_NOALLOC_MAX_ELEMS, else LLM_ERR_ARG (as for B < 1, V < 1, NULL pointers or the
  * argument ranges of llm_sample).  Calls share that array, so calls that overlap on the GPU race.
- * The first call on a device (with it current) looks up the array's device address; make it
- * before any stream capture on that device.  Calls no allocator.
+ * The array is created lazily, with the library's CUDA module that holds it: the first call on a
+ * device (with it current) -- or llm_create on that device, which does the same set-up -- loads
+ * that module, which reserves the array's memory, and looks up its device address.  Make that
+ * first call (or llm_create) where allocating is allowed and before any stream capture on the
+ * device.  Later calls allocate nothing; after cudaDeviceReset (a new context) the next call
+ * looks the address up again and so counts as a first call.
  */
 #define LLM_SAMPLE_NOALLOC_MAX_ELEMS 262144
 llm_status llm_sample_noalloc(const float* logits_dev, int32_t B, int32_t V, float temp, int32_t k,

@@ -24,7 +24,7 @@ EXPORTS = ("llm_weight_count", "llm_create", "llm_destroy", "llm_reset", "llm_pr
            "llm_debug_trace", "llm_profile_kernel", "llm_sample_noalloc",
            "llm_step_kernels", "llm_decode_rows", "llm_decode_rows_dev", "llm_step_rows",
            "llm_step_rows_dev", "llm_generate", "llm_generate_dev", "llm_decode_paged",
-           "llm_decode_paged_dev", "llm_step_paged", "llm_step_paged_dev")
+           "llm_decode_paged_dev", "llm_step_paged", "llm_step_paged_dev", "llm_check_wait_timeout")
 
 
 class LlmConfig(ctypes.Structure):
@@ -45,7 +45,7 @@ class LlmError(RuntimeError):
 
 
 # argument and result types of every entry point (ctypes)
-_i32, _u64, _f32, _vp = ctypes.c_int32, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
+_i32, _i64, _u64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
 _pcfg = ctypes.POINTER(LlmConfig)
 SIGNATURES = {
     "llm_weight_count": ([_pcfg], _u64),
@@ -82,6 +82,7 @@ SIGNATURES = {
     "llm_profile_kernel": ([_vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_f32)], _i32),
     "llm_sample_noalloc": ([_vp, _i32, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
     "llm_step_kernels": ([_vp, _i32, _f32, ctypes.POINTER(_i32)], _i32),
+    "llm_check_wait_timeout": ([_vp, _i64], _i32),
     }
 
 _lib = None
@@ -281,6 +282,10 @@ def llm_step_kernels(h, B, temp) -> int:
     n = ctypes.c_int32()
     _check(h, lib().llm_step_kernels(h, B, temp, ctypes.byref(n)))
     return int(n.value)
+
+
+def llm_check_wait_timeout(h, limit_cycles):
+    _check(h, lib().llm_check_wait_timeout(h, limit_cycles))
 
 
 SAMPLE_NOALLOC_MAX_ELEMS = 262144

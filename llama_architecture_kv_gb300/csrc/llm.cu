@@ -23,6 +23,7 @@
 #include "gemv.cuh"
 #include "llm.h"
 #include "sampler.cuh"
+#include "tc.cuh"
 
 using namespace llm;
 
@@ -129,6 +130,21 @@ __global__ void gen_end_kernel(const GenState* gen, const int32_t* ids_buf, int 
 }
 
 __global__ void gen_set_kernel(GenState* gen, const GenState v) { *gen = v; }
+
+// a bounded wait that runs out: an mbarrier that nothing arrives on, waited on with the same
+// bounded wait as the kernels' copy rings; on timeout the status word records it (needle-core
+// v2 model.rs: a failed step is an error result, not a crash)
+__global__ void wait_timeout_kernel(int32_t* status, uint64_t limit_cycles) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(b, 0, limit_cycles));
+  if (!ok && threadIdx.x == 0) atomicCAS(status, 0, kErrDeviceTimeout);
+}
 
 template <int WT>
 __global__ void embed_kernel(const void* emb, const int32_t* tok, float* x, int d, int x_stride) {
@@ -241,6 +257,7 @@ struct llm_handle {
   float *xa = nullptr, *xb = nullptr, *q = nullptr, *attn = nullptr, *m = nullptr, *logits = nullptr;
   float* part = nullptr;
   uint32_t* ticket = nullptr;
+  int ticket_count = 0;
   int part_ns = 0;
   CUtensorMap kmap, vmap;  // the key and value caches as [layers * max_batch * kv * max_seq][hd]
   StepState* st = nullptr;
@@ -886,6 +903,8 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     h->tc_min = tc_min;
   }
   if ((ce = attn_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("attention kernel attributes", ce);
+  // the allocation-free sampler's array is reserved here, where allocating is allowed
+  if ((ce = noalloc_prepare()) != cudaSuccess) return cuda_bail("allocation-free sampler set-up", ce);
   // weights: a device copy of the blob when it is on the host, then repacked
   const char* blob = (const char*)weights;
   char* staging = nullptr;
@@ -929,6 +948,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     attn_cluster_merge(h->wt, h->hd, c.group, ns, b * c.kv_heads, c.max_seq);  // device queries before any capture
   }
   h->part_ns = maxns;
+  h->ticket_count = (int)(B * c.kv_heads);
   const int slots = attn_part_slots(h->wt, h->hd, maxns);
   if ((st = dalloc(h, &h->part, B * h->H * slots * (h->hd + 2) * 4)) ||
       (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, step_state_bytes(c.max_batch))) ||
@@ -1006,8 +1026,19 @@ llm_status llm_synchronize(llm_handle* h) {
   CUDA_TRY(h, cudaMemcpy(&s, h->status, 4, cudaMemcpyDeviceToHost));
   if (s != 0) {
     CUDA_TRY(h, cudaMemset(h->status, 0, 4));
+    // a kernel that gave up may have left the attention's merge tickets short of their count
+    if (s == LLM_ERR_DEVICE_TIMEOUT)
+      CUDA_TRY(h, cudaMemset(h->ticket, 0, (size_t)h->ticket_count * 4));
     return fail(h, s, "device reported: %s", llm_status_string(s));
   }
+  return LLM_OK;
+}
+
+llm_status llm_check_wait_timeout(llm_handle* h, int64_t limit_cycles) {
+  if (!h) return LLM_ERR_ARG;
+  if (limit_cycles < 1 || limit_cycles > 1000000000) return fail(h, LLM_ERR_ARG, "limit %lld outside 1..1e9 cycles", (long long)limit_cycles);
+  wait_timeout_kernel<<<1, 32, 0, h->stream>>>(h->status, (uint64_t)limit_cycles);
+  CUDA_TRY(h, cudaGetLastError());
   return LLM_OK;
 }
 

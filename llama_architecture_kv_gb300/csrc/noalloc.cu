@@ -17,9 +17,18 @@
 // threads) race on it and their results are undefined.
 //
 // Host code may not use the array's name as a device pointer (on the host it names a stand-in,
-// not device memory).  The first call on each device, with that device current, looks the real
-// address up with cudaGetSymbolAddress and records it; later calls reuse it.  Make that first
-// call before any stream capture on the device.
+// not device memory).  The set-up (scratch_for_current_device) looks the real address up with
+// cudaGetSymbolAddress, with the device current, and records it per device together with the
+// device's current context; a later call reuses it while that context is still current, and
+// looks it up again after the context changed (cudaDeviceReset, another driver context).
+//
+// The array belongs to this file's CUDA module.  The runtime loads modules lazily, so the
+// module -- and with it the array's device memory -- is created by the set-up, not at library
+// load: that first set-up on a device does reserve memory.  llm_create runs it for its device;
+// a caller without a handle makes one call on each device from a context that may allocate and
+// before any stream capture there.  Calls after that allocate nothing.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "llm.h"
@@ -39,6 +48,24 @@ static __device__ __align__(256) unsigned char g_sample_scratch[kScratchBytes];
 
 std::mutex g_setup_mu;
 unsigned char* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};  // the context each recorded address belongs to
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+bool g_ctx_queried = false;
+
+// the calling thread's current driver context, or null where the driver entry is unavailable
+CUcontext current_context() {
+  if (!g_ctx_queried) {
+    g_ctx_queried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && fn)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  }
+  CUcontext c = nullptr;
+  if (g_ctx_current && g_ctx_current(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
 
 __global__ void noalloc_params_kernel(StepState* st, float temp, int32_t k, float p) {
   st->pos = 0;
@@ -49,21 +76,39 @@ __global__ void noalloc_params_kernel(StepState* st, float temp, int32_t k, floa
   st->table = nullptr;
 }
 
-// the scratch address on the current device (looked up once per device)
+// the scratch address on the current device (looked up again when the device's context changed)
 llm_status scratch_for_current_device(unsigned char** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LLM_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (!g_scratch_ptr[dev]) {
+    // (the first runtime call on the device makes its primary context current)
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_sample_scratch) != cudaSuccess || !p) return LLM_ERR_CUDA;
     g_scratch_ptr[dev] = static_cast<unsigned char*>(p);
+    g_scratch_ctx[dev] = current_context();
+  } else {
+    CUcontext c = current_context();
+    if (c != g_scratch_ctx[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_sample_scratch) != cudaSuccess || !p) return LLM_ERR_CUDA;
+      g_scratch_ptr[dev] = static_cast<unsigned char*>(p);
+      g_scratch_ctx[dev] = c;
+    }
   }
   *out = g_scratch_ptr[dev];
   return LLM_OK;
 }
 
 }  // namespace
+
+namespace llm {
+// the set-up of the allocation-free sampler's array on the current device (llm_create runs it)
+cudaError_t noalloc_prepare() {
+  unsigned char* base = nullptr;
+  return scratch_for_current_device(&base) == LLM_OK ? cudaSuccess : cudaErrorInvalidSymbol;
+}
+}  // namespace llm
 
 extern "C" llm_status llm_sample_noalloc(const float* logits_dev, int32_t B, int32_t V, float temp,
                                          int32_t k, float p, const float* u_dev, int32_t* ids_dev,

@@ -24,5 +24,7 @@ constexpr size_t kSampleHistPerRow = 16 * kSortMaxSlicesPerRow;  // uint32 entri
 int sample_slices(int V);
 // greedy: one argmax kernel; otherwise the sort chain and the draw (temp, k, p from *step)
 cudaError_t launch_sample(const SampleArgs& a, int B, bool greedy, cudaStream_t s, bool pdl);
+// loads the allocation-free sampler's fixed array on the current device and records its address
+cudaError_t noalloc_prepare();
 
 }  // namespace llm

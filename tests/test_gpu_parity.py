@@ -250,6 +250,25 @@ def test_device_token_check_reports_on_synchronize():
     g.close()
 
 
+def test_bounded_wait_timeout_is_reported_once_and_the_handle_stays_usable():
+    # a wait on a barrier that nothing arrives on runs out after a few thousand cycles; the
+    # status reaches llm_synchronize once, then the handle steps normally (bit-identical logits)
+    w = WORKLOADS["tiny_f32"]
+    blob, g = make(w.shape, w.seed_weights, 1, 8)
+    toks = synth.tokens(w.seed_tokens, 0, 3, w.shape.vocab)
+    before = g.decode(toks[:1], 0)
+    pkg.llm_check_wait_timeout(g.h, 5000)
+    with pytest.raises(pkg.LlmError) as e:
+        g.synchronize()
+    assert e.value.status == pkg.LLM_ERR_DEVICE_TIMEOUT
+    g.synchronize()  # reported once, then cleared
+    np.testing.assert_array_equal(g.decode(toks[:1], 0), before)
+    with pytest.raises(pkg.LlmError) as e:
+        pkg.llm_check_wait_timeout(g.h, 0)
+    assert e.value.status == pkg.LLM_ERR_ARG
+    g.close()
+
+
 def test_device_pointer_variants_match_host_variants():
     torch = pytest.importorskip("torch")
     w = WORKLOADS["tiny_f32"]
