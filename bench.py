@@ -59,6 +59,10 @@ def parse():
                     help="rows at their own positions (decode_rows): row b at P - b * (P // 2B)")
     ap.add_argument("--kernels", action="store_true",
                     help="print each kernel's isolated launch time (CUDA events) and exit")
+    ap.add_argument("--max-tokens", type=int, default=0,
+                    help="prompt tokens per prefill pass (0: the library default)")
+    ap.add_argument("--b32-steps", type=int, default=64,
+                    help="default workload: also time this many batch-32 steps (0: skip)")
     return ap.parse_args()
 
 
@@ -299,6 +303,112 @@ def kernel_table(pkg, h, w, B, pos):
                       "kernels": rows, "sum_isolated_us_per_step": per_step}), flush=True)
 
 
+def host_cpu():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo) and its logical core count."""
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not name:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu model")):
+                    name = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return name or "unknown", os.cpu_count()
+
+
+def step_bytes_of(pkg, cfg, s, B, mean_pos):
+    """Algorithmic bytes of one decode step: every weight but the embedding table (the tied head
+    reads that table in full), plus the keys and values of positions 0..t of every row."""
+    es = 2 if s.bf16 else 4
+    wbytes = (pkg.llm_weight_count(cfg) - s.vocab * s.d) * es
+    if s.tied:
+        wbytes += s.vocab * s.d * es
+    kv_bytes = B * 2 * s.layers * s.kv * s.hd * es * (mean_pos + 1)
+    return wbytes, wbytes + kv_bytes
+
+
+def fill_cache(model, w, torch, stream, gpu_index):
+    """The workload's cache: its prompt through llm_prefill (timed: a first call captures the pass
+    graphs, the second is timed with CUDA events), or synthetic keys and values."""
+    s, B, P = w.shape, w.batch, w.prompt
+    if not P:
+        for layer in range(s.layers):
+            for b in range(B):
+                k, v = synth.kv_values(w.seed_kv, layer, b, B, s.kv, w.fill, s.hd, bf16=s.bf16)
+                model.kv_import(layer, b, 0, k, v)
+        return None
+    prompt = synth.tokens(w.seed_tokens, 0, B * P, s.vocab).reshape(B, P)
+    model.prefill(prompt, 0, logits=False)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index) as clocks:
+        e0.record(stream)
+        t0 = time.perf_counter()
+        model.prefill(prompt, 0, logits=True)
+        wall = time.perf_counter() - t0
+        e1.record(stream)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"tokens": B * P, "batch": B, "prompt": P, "ms": ms, "tok_s": B * P / (ms / 1e3),
+            "wall_ms": wall * 1e3, "max_tokens": int(model.cfg.max_tokens) or 512,
+            "what": "llm_prefill of the whole prompt (passes of prompt tokens; logits of the last)",
+            "clocks": clocks.summary()}
+
+
+def time_steps(pkg, torch, h, w, B, pos0, K, W, dev, stream, local, world, first, rowpos=None, generate=False):
+    """W warm-up steps rewinding to pos0, then K timed steps of llm_step_dev (or one
+    llm_generate_dev call) bracketed by CUDA events on the handle's stream, clocks sampled."""
+    s = w.shape
+    tok = [torch.from_numpy(first).to(dev), torch.empty(B, dtype=torch.int32, device=dev)]
+    u_all = synth.uniforms(w.seed_uniform, 0, B * (W + K)).reshape(W + K, B)
+    u_dev = torch.from_numpy(u_all).to(dev)
+    temp, k_, p_ = w.temp, (w.top_k or s.vocab), w.top_p
+
+    def step_dev(tk, i, u, ids):
+        if rowpos is None:
+            pkg.llm_step_dev(h, tk, B, pos0 + i, temp, k_, p_, u, ids)
+        else:
+            pkg.llm_step_rows_dev(h, tk, B, rowpos + i, temp, k_, p_, u, ids)
+
+    # generation warm-up: 9 steps capture both generation graphs (8 steps, then a single step)
+    GW = 9
+    gen_ids = torch.empty((max(GW, K), B), dtype=torch.int32, device=dev) if generate else None
+    u_gw = (torch.from_numpy(synth.uniforms(w.seed_uniform, B * (W + K), B * GW).reshape(GW, B)).to(dev)
+            if generate else None)
+    with torch.cuda.stream(stream):
+        for i in range(W):  # warm-up: rewind to the prompt end every time
+            step_dev(tok[0], 0, u_dev[i], tok[1])
+        if generate:
+            pkg.llm_generate_dev(h, tok[0], B, pos0, GW, temp, k_, p_, u_gw, gen_ids[:GW])
+        pkg.llm_synchronize(h)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clocks:
+            e0.record(stream)
+            if generate:
+                pkg.llm_generate_dev(h, tok[0], B, pos0, K, temp, k_, p_, u_dev[W:W + K], gen_ids[:K])
+            else:
+                for i in range(K):
+                    step_dev(tok[i % 2], i, u_dev[W + i], tok[(i + 1) % 2])
+            e1.record(stream)
+            e1.synchronize()
+        pkg.llm_synchronize(h)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return ms, clocks.summary(), u_all
+
+
 def run_ours(args):
     import torch
 
@@ -323,20 +433,15 @@ def run_ours(args):
     blob = synth.model_blob(s, w.seed_weights)
     log(f"[bench] weights generated: {blob.nbytes / 1e9:.2f} GB in {time.perf_counter() - t0:.1f} s")
     t0 = time.perf_counter()
-    model = pkg.Model(s, blob, max_batch=B, max_seq=cap, stream=stream.cuda_stream)
+    model = pkg.Model(s, blob, max_batch=B, max_seq=cap, stream=stream.cuda_stream, max_tokens=args.max_tokens)
     h = model.h
     log(f"[bench] model created in {time.perf_counter() - t0:.1f} s")
     t0 = time.perf_counter()
-    if P:
-        prompt = synth.tokens(w.seed_tokens, 0, B * P, s.vocab).reshape(B, P)
-        model.prefill(prompt, 0, logits=False)
-    else:
-        for layer in range(s.layers):
-            for b in range(B):
-                k, v = synth.kv_values(w.seed_kv, layer, b, B, s.kv, w.fill, s.hd, bf16=s.bf16)
-                model.kv_import(layer, b, 0, k, v)
+    with torch.cuda.stream(stream):
+        prefill = fill_cache(model, w, torch, stream, local)
     pos0 = P if P else w.fill
-    log(f"[bench] cache filled to {pos0} positions in {time.perf_counter() - t0:.1f} s")
+    log(f"[bench] cache filled to {pos0} positions in {time.perf_counter() - t0:.1f} s"
+        + (f" (timed prefill {prefill['ms']:.1f} ms, {prefill['tok_s']:.0f} tok/s)" if prefill else ""))
 
     if args.kernels:
         kernel_table(pkg, h, w, B, pos0)
@@ -344,52 +449,16 @@ def run_ours(args):
         return
     dev = torch.device("cuda", local)
     first = synth.tokens(w.seed_tokens, B * P, B, s.vocab)
-    tok = [torch.from_numpy(first).to(dev), torch.empty(B, dtype=torch.int32, device=dev)]
-    u_all = synth.uniforms(w.seed_uniform, 0, B * (W + K)).reshape(W + K, B)
-    u_dev = torch.from_numpy(u_all).to(dev)
     temp, k_, p_ = w.temp, (w.top_k or s.vocab), w.top_p
     # rows at their own positions: spread over the upper half of the cache
     rowpos = (pos0 - np.arange(B, dtype=np.int32) * (pos0 // (2 * B))).astype(np.int32) if args.rows else None
-
-    def step_dev(tk, i, u, ids):
-        if rowpos is None:
-            pkg.llm_step_dev(h, tk, B, pos0 + i, temp, k_, p_, u, ids)
-        else:
-            pkg.llm_step_rows_dev(h, tk, B, rowpos + i, temp, k_, p_, u, ids)
-
-    # generation warm-up: 9 steps capture both generation graphs (8 steps, then a single step)
-    GW = 9
-    gen_ids = torch.empty((max(GW, K), B), dtype=torch.int32, device=dev) if args.generate else None
-    u_gw = (torch.from_numpy(synth.uniforms(w.seed_uniform, B * (W + K), B * GW).reshape(GW, B)).to(dev)
-            if args.generate else None)
-    with torch.cuda.stream(stream):
-        for i in range(W):  # warm-up: rewind to the prompt end every time
-            step_dev(tok[0], 0, u_dev[i], tok[1])
-        if args.generate:
-            pkg.llm_generate_dev(h, tok[0], B, pos0, GW, temp, k_, p_, u_gw, gen_ids[:GW])
-        pkg.llm_synchronize(h)
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with ClockSampler(local) as clocks:
-            e0.record(stream)
-            if args.generate:
-                pkg.llm_generate_dev(h, tok[0], B, pos0, K, temp, k_, p_, u_dev[W:W + K], gen_ids[:K])
-            else:
-                for i in range(K):
-                    step_dev(tok[i % 2], i, u_dev[W + i], tok[(i + 1) % 2])
-            e1.record(stream)
-            e1.synchronize()
-        pkg.llm_synchronize(h)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms, clk, u_all = time_steps(pkg, torch, h, w, B, pos0, K, W, dev, stream, local, world, first, rowpos,
+                                args.generate)
     elapsed = ms / 1e3
     if world > 1:
         elapsed = max_over_ranks(elapsed, dev)
         torch.distributed.barrier()
     value = whole_job_value(world, B, K, elapsed)
-    clk = clocks.summary()
 
     # end to end through the public host API: tokens in from pinned host memory, ids out
     tok_h = torch.from_numpy(first.copy()).pin_memory()
@@ -433,15 +502,12 @@ def run_ours(args):
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": peak_kind, "traffic": traffic, "ms_per_launch": kms,
                 "algorithmic_bytes_per_launch": bytes_gu}
-    # whole-step byte roofline: weights (all but the embedding table) + the KV read
-    es = 2 if s.bf16 else 4
-    wbytes = (pkg.llm_weight_count(model.cfg) - s.vocab * s.d) * es  # all but the embedding table
-    if s.tied:
-        wbytes += s.vocab * s.d * es  # the tied LM head is that table, read in full every step
     mean_pos = (float(np.mean(rowpos)) if rowpos is not None else pos0) + (K - 1) / 2
-    kv_bytes = B * 2 * s.layers * s.kv * s.hd * es * (mean_pos + 1)
-    step_bytes = wbytes + kv_bytes
+    wbytes, step_bytes = step_bytes_of(pkg, model.cfg, s, B, mean_pos)
     step_roof = step_roofline(step_bytes, B, peak, value / world, K, elapsed)
+    launches = (K * (pkg.llm_step_kernels(h, B, temp) + 1) + K // 8 + K % 8 if args.generate
+                else K * pkg.llm_step_kernels(h, B, temp))
+    model.close()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -454,10 +520,37 @@ def run_ours(args):
             m.forward(0, int(first[0]), pos0 + (i % 2), logits=True)
             ts.append(time.perf_counter() - t1)
         m.close()
+        cpu_name, nproc = host_cpu()
         cpu = {"value": 1.0 / float(np.mean(ts)), "unit": "tok/s", "cores": 1, "kind": "oracle",
+               "cpu_model": cpu_name, "nproc": nproc,
                "sample": f"{n} full decode steps of row 0 at position {pos0} over a synthetic "
-                         f"{pos0}-position cache, single-threaded f32 C"}
+                         f"{pos0}-position cache, single-threaded f32 C on one of {nproc} cores ({cpu_name})"}
         log(f"[bench] cpu baseline in {time.perf_counter() - t0:.1f} s")
+
+    # the batch-32 half of the metric, in the same run (same weights, its own handle)
+    b32 = None
+    if (w.name == "llama8b_b1" and args.b32_steps > 0 and world == 1 and not args.rows and not args.generate
+            and args.layers <= 0 and args.prompt < 0):
+        w32 = WORKLOADS["llama8b_b32"]
+        K32, W32 = args.b32_steps, 3
+        cap32 = max(w32.cap, w32.prompt + W32 + K32 + 1)
+        m32 = pkg.Model(s, blob, max_batch=w32.batch, max_seq=cap32, stream=stream.cuda_stream,
+                        max_tokens=args.max_tokens)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            pf32 = fill_cache(m32, w32, torch, stream, local)
+        log(f"[bench] batch 32: cache filled in {time.perf_counter() - t0:.1f} s")
+        first32 = synth.tokens(w32.seed_tokens, w32.batch * w32.prompt, w32.batch, s.vocab)
+        ms32, clk32, _ = time_steps(pkg, torch, m32.h, w32, w32.batch, w32.prompt, K32, W32, dev, stream, local,
+                                    world, first32)
+        v32 = w32.batch * K32 / (ms32 / 1e3)
+        _, sb32 = step_bytes_of(pkg, m32.cfg, s, w32.batch, w32.prompt + (K32 - 1) / 2)
+        b32 = {"workload": w32.name, "batch": w32.batch, "value": v32, "unit": "tok/s", "steps": K32,
+               "warmup": W32, "ms_per_step": ms32 / K32,
+               "step_roofline": step_roofline(sb32, w32.batch, peak, v32, K32, ms32 / 1e3),
+               "clocks": clk32, "prefill": pf32,
+               "gpu_launches": K32 * pkg.llm_step_kernels(m32.h, w32.batch, 0.0)}
+        m32.close()
 
     line = {
         "metric": "decode tok/s", "value": value, "unit": "tok/s", "n_gpus": world, "steps": K,
@@ -472,15 +565,13 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (weights %.1f GB per step)" % (wbytes / 1e9),
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
-        "clocks": clk,
+        "clocks": clk, "prefill": prefill, "batch32": b32,
         # a generation step replaces the prologue by its own and ends with one copy of its draws;
         # each graph launch (8 steps, then single steps) is preceded by one state update
-        "gpu_launches": (K * (pkg.llm_step_kernels(h, B, temp) + 1) + K // 8 + K % 8 if args.generate
-                         else K * pkg.llm_step_kernels(h, B, temp)),
+        "gpu_launches": launches,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    model.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 

@@ -78,6 +78,9 @@ typedef struct llm_config {
   int32_t tc_min_batch; /* bf16 only: steps of at least this many rows run the projections on the
                            tensor cores (TMA-fed tcgen05 GEMM), fewer rows on the weight-streaming
                            GEMV; 0: the library default (16); above max_batch: never */
+  int32_t max_tokens;   /* prompt tokens one prefill pass processes together (llm_prefill with
+                           S > 1, llm_prefill_packed): activations and attention scratch are sized
+                           for max(max_batch, max_tokens) rows; 0: the library default (512) */
 } llm_config;
 
 typedef struct llm_handle llm_handle;
@@ -110,8 +113,12 @@ llm_status llm_reset(llm_handle* h);
 /*
  * Prefill (P3 "prefill<S>(tokens, pos)"; P1 forward_pre for every position but the last):
  * rows 0..B-1 take tokens[b*S + i] at positions pos+i, i < S; their keys and values are written
- * to the cache.  logits_host [B][V] (may be NULL: no final norm / head) receives the logits after
- * the last token.  Requires 1 <= B <= max_batch (else LLM_ERR_BATCH), S >= 1 (else LLM_ERR_ARG),
+ * to the cache, and token i of row b attends to positions 0..pos+i of its row.  logits_host
+ * [B][V] (may be NULL: no final norm / head) receives the logits after the last token.  The
+ * B*S tokens run as passes of whole positions, at most max(B, max_tokens) tokens each: a pass is
+ * one step whose rows are its tokens (projections on the tensor cores once a pass has
+ * tc_min_batch tokens), and only the last tokens go through the final norm and the LM head.
+ * Requires 1 <= B <= max_batch (else LLM_ERR_BATCH), S >= 1 (else LLM_ERR_ARG),
  * 0 <= pos <= filled length of every row b < B and pos + S <= max_seq (else LLM_ERR_POS_RANGE),
  * tokens in [0, vocab) (else LLM_ERR_TOKEN_RANGE).  On success the filled length of rows
  * b < B becomes pos + S (positions after it are dead and never read).
@@ -185,6 +192,25 @@ llm_status llm_step_rows(llm_handle* h, const int32_t* tokens_host, int32_t B,
 llm_status llm_step_rows_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B,
                              const int32_t* positions_host, float temp, int32_t k, float p,
                              const float* u_dev, int32_t* ids_dev, float* logits_dev);
+
+/*
+ * Packed prefill (Llama 3.1 8B Instruct card, "Entries": prefill_packed(tokens, rows, positions,
+ * segments, last)): P tokens of several prompts packed end to end; token p is position
+ * positions_host[p] of prompt segments_host[p] (any int32 id) in cache row rows_host[p].  Every
+ * token's key and value are written at its row and position, and each token attends to its own
+ * prompt's tokens up to its position and to nothing else (not to its row's older cache).
+ * logits_host [nlast][V] (may be NULL) receives the logits after token last_host[m].  Checks:
+ * P >= 1 and nlast >= 0 (LLM_ERR_ARG); rows in
+ * [0, max_batch) (LLM_ERR_BATCH); positions in [0, max_seq) (LLM_ERR_POS_RANGE); tokens in
+ * [0, vocab) (LLM_ERR_TOKEN_RANGE); each prompt in one row at consecutive positions, each once,
+ * prompts of a row not overlapping, no two tokens in one (row, position), last[m] in [0, P)
+ * (LLM_ERR_ARG).  The tokens run in position order as passes of at most max(max_batch,
+ * max_tokens) tokens, like llm_prefill's; on success each prompt's row is filled at least to its
+ * last position + 1.  All arrays are host memory; the call returns when done.
+ */
+llm_status llm_prefill_packed(llm_handle* h, const int32_t* tokens_host, const int32_t* rows_host,
+                              const int32_t* positions_host, const int32_t* segments_host, int32_t P,
+                              const int32_t* last_host, int32_t nlast, float* logits_host);
 
 /*
  * Paged caches (Llama 3.1 8B Instruct card, "Entries": decode_paged(tokens, positions, table)):

@@ -24,7 +24,8 @@ EXPORTS = ("llm_weight_count", "llm_create", "llm_destroy", "llm_reset", "llm_pr
            "llm_debug_trace", "llm_profile_kernel", "llm_sample_noalloc",
            "llm_step_kernels", "llm_decode_rows", "llm_decode_rows_dev", "llm_step_rows",
            "llm_step_rows_dev", "llm_generate", "llm_generate_dev", "llm_decode_paged",
-           "llm_decode_paged_dev", "llm_step_paged", "llm_step_paged_dev", "llm_check_wait_timeout")
+           "llm_decode_paged_dev", "llm_step_paged", "llm_step_paged_dev", "llm_check_wait_timeout",
+           "llm_prefill_packed")
 
 
 class LlmConfig(ctypes.Structure):
@@ -35,7 +36,8 @@ class LlmConfig(ctypes.Structure):
                 ("rope_low_freq", ctypes.c_float), ("rope_high_freq", ctypes.c_float),
                 ("rope_orig_max_pos", ctypes.c_float), ("max_batch", ctypes.c_int32),
                 ("max_seq", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("debug_trace", ctypes.c_int32), ("tc_min_batch", ctypes.c_int32)]
+                ("debug_trace", ctypes.c_int32), ("tc_min_batch", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32)]
 
 
 class LlmError(RuntimeError):
@@ -70,6 +72,7 @@ SIGNATURES = {
     "llm_decode_paged_dev": ([_vp, _vp, _i32, _vp, _vp, _i32, _vp], _i32),
     "llm_step_paged": ([_vp, _vp, _i32, _vp, _vp, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
     "llm_step_paged_dev": ([_vp, _vp, _i32, _vp, _vp, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
+    "llm_prefill_packed": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp], _i32),
     "llm_synchronize": ([_vp], _i32),
     "llm_stream": ([_vp], _vp),
     "llm_logits_buffer": ([_vp], _vp),
@@ -104,14 +107,14 @@ def lib():
     return _lib
 
 
-def config(shape, max_batch, max_seq, debug_trace=False, tc_min_batch=0) -> LlmConfig:
+def config(shape, max_batch, max_seq, debug_trace=False, tc_min_batch=0, max_tokens=0) -> LlmConfig:
     """An llm_config from a shape description (fields kv, g, half, ffn, layers, vocab, eps,
     theta, tied, llama3, factor, low_freq, high_freq, orig_max, bf16)."""
     return LlmConfig(shape.kv, shape.g, shape.half, shape.ffn, shape.layers, shape.vocab,
                      shape.eps, shape.theta, int(shape.tied), int(shape.llama3), shape.factor,
                      shape.low_freq, shape.high_freq, shape.orig_max, max_batch, max_seq,
                      LLM_DTYPE_BF16 if shape.bf16 else LLM_DTYPE_F32, int(debug_trace),
-                     int(tc_min_batch))
+                     int(tc_min_batch), int(max_tokens))
 
 
 def _ptr(a):
@@ -239,6 +242,11 @@ def llm_step_paged_dev(h, tokens, B, positions, table, pages_per_row, temp, k, p
                                        p, _ptr(u), _ptr(ids), _ptr(logits)))
 
 
+def llm_prefill_packed(h, tokens, rows, positions, segments, P, last, nlast, logits):
+    _check(h, lib().llm_prefill_packed(h, _ptr(tokens), _ptr(rows), _ptr(positions), _ptr(segments), P,
+                                       _ptr(last), nlast, _ptr(logits)))
+
+
 def llm_synchronize(h):
     _check(h, lib().llm_synchronize(h))
 
@@ -305,9 +313,9 @@ class Model:
     """One handle: host-memory entry points with numpy arrays."""
 
     def __init__(self, shape, weights, max_batch, max_seq, stream=None, debug_trace=False,
-                 weights_on_device=False, tc_min_batch=0):
+                 weights_on_device=False, tc_min_batch=0, max_tokens=0):
         self.shape = shape
-        self.cfg = config(shape, max_batch, max_seq, debug_trace, tc_min_batch)
+        self.cfg = config(shape, max_batch, max_seq, debug_trace, tc_min_batch, max_tokens)
         self.h = llm_create(self.cfg, weights, weights_on_device, stream)
         self.V = shape.vocab
         self.cache_dtype = np.uint16 if shape.bf16 else np.float32
@@ -386,6 +394,16 @@ class Model:
         u = None if u is None else np.ascontiguousarray(u, np.float32)
         llm_step_paged(self.h, tokens, B, positions, table, table.shape[1], temp, k, p, u, ids, out)
         return (ids, out) if logits else ids
+
+    def prefill_packed(self, tokens, rows, positions, segments, last, logits=True):
+        """Prompts packed end to end; logits [len(last)][V] after the tokens last names."""
+        arrs = [np.ascontiguousarray(a, np.int32).reshape(-1) for a in (tokens, rows, positions, segments, last)]
+        tokens, rows, positions, segments, last = arrs
+        P = tokens.size
+        assert rows.size == P and positions.size == P and segments.size == P
+        out = np.empty((last.size, self.V), np.float32) if logits else None
+        llm_prefill_packed(self.h, tokens, rows, positions, segments, P, last, last.size, out)
+        return out
 
     def sample(self, logits, temp, k, p, u):
         logits = np.ascontiguousarray(logits, np.float32)

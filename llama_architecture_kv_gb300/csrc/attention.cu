@@ -313,16 +313,20 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   float* fac = mypart + g * (HD + 2);                    // [g][kAttnMaxCluster]
   const uint32_t bars = (smem_u32(fac + g * kAttnMaxCluster) + 7u) & ~7u;
 
-  // positions 0..t of row b in contiguous slices of at least kMinChunk (multiples of 32)
+  // positions ts..t of row b (ts = 0 but in packed passes) in contiguous slices of at least
+  // kMinChunk (multiples of 32), starting from ts rounded down to 32 so that chunks stay aligned
+  // (and inside pages); positions below ts are masked
   const int t = row_pos(a.step, b);
-  const int npos = t + 1;
+  const int ts = row_start(a.step, b), tw = row_wfirst(a.step, b);
+  const int pbase = ts & ~(kChunk - 1);
+  const int npos = t + 1 - pbase;
   int chunk = (npos + a.ns - 1) / a.ns;
   chunk = (chunk + 31) & ~31;
   if (chunk < kMinChunk) chunk = kMinChunk;
   const int nact = (npos + chunk - 1) / chunk;
   if (!a.cluster && split >= nact) return;  // (a cluster's CTAs all take part in its barriers)
-  const int p0 = split * chunk;
-  const int p1 = min(npos, p0 + chunk);
+  const int p0 = pbase + split * chunk;
+  const int p1 = min(t + 1, p0 + chunk);
   const int nch = p0 < p1 ? (p1 - p0 + kChunk - 1) / kChunk : 0;
   const int cnt = nch > warp ? (nch - warp + NW - 1) / NW : 0;  // chunks of this warp
 
@@ -350,13 +354,14 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
       tma_load_2d(dst + (uint32_t)(bx * kChunk * S::BOXB), &kmap, bar, bx * (S::BOXB / S::ES), krow);
     bulk_load(dst + (uint32_t)(kChunk * ROWB), vsrc, (uint32_t)(nv * ROWB), bar);
   };
-  // chunks below position t do not depend on the previous kernel
+  // chunks below the first position this step writes in the row do not depend on the previous
+  // kernel
   const int npre = cnt < NR ? cnt : NR;
   int issued = 0;
   if (lane == 0) {
     while (issued < npre) {
       const int pb = p0 + (warp + issued * NW) * kChunk;
-      if (pb + min(kChunk, p1 - pb) > t) break;  // holds position t
+      if (pb + min(kChunk, p1 - pb) > tw) break;  // holds a position written by this step
       issue(issued++);
     }
   }
@@ -392,7 +397,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
     const int nv = min(kChunk, p1 - pb);
     const unsigned char* kreg = base + (size_t)(warp * NR + slot) * BUF;
     const unsigned char* vreg = kreg + kChunk * ROWB;
-    const bool valid = lane < nv;
+    const bool valid = lane < nv && pb + lane >= ts;
     // scores: lane = position
     float acc[GM][2];
 #pragma unroll
@@ -427,7 +432,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
     for (int h = 0; h < GM; ++h) {
       if (h < g) {
         const float s = valid ? (acc[h][0] + acc[h][1]) * a.scale : -INFINITY;
-        const float mnew = fmaxf(m[h], warp_max(s));  // finite: lane 0 holds a position
+        const float mnew = fmaxf(m[h], warp_max(s));  // finite: every chunk holds a position of the range
         const float corr = m[h] == -INFINITY ? 0.f : expf(m[h] - mnew);
         const float w = valid ? expf(s - mnew) : 0.f;
         l[h] = fmaf(l[h], corr, w);
@@ -442,7 +447,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
     if (lane < S::VL) {
       const unsigned char* vp = vreg + lane * DPL * S::ES;
 #pragma unroll 2
-      for (int pp = 0; pp < nv; ++pp) {
+      for (int pp = ts > pb ? ts - pb : 0; pp < nv; ++pp) {  // (rows below ts may not be finite)
         float wv[GM];
 #pragma unroll
         for (int h4 = 0; h4 < GM; h4 += 4) {
@@ -621,17 +626,25 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   const long long c1 = clus ? cbj * nchk + (long long)nchk * (crank + 1) / a.ns : T * (c + 1) / G;
   auto owner = [&](long long it) { return (int)(((it + 1) * G + T - 1) / T - 1); };
   // the segment starting at chunk st of the sequence: (row b, kv head j), chunks [k0, k1), of
-  // which [k0, kv1) hold positions 0..tb of row b
-  auto seg = [&](long long st, int& b, int& j, int& k0, int& k1, int& kv1, int& tb, long long& next) {
+  // which [kv0, kv1) hold positions of row b's range ts..tb (tw: the first position this step
+  // writes in the row)
+  struct Seg {
+    int b, j, k0, k1, kv0, kv1, tb, ts, tw;
+  };
+  auto seg = [&](long long st, Seg& sg, long long& next) {
     const long long bj = st / nchk;
-    k0 = (int)(st - bj * nchk);
+    sg.k0 = (int)(st - bj * nchk);
     const long long end = c1 < (bj + 1) * nchk ? c1 : (bj + 1) * nchk;
-    k1 = k0 + (int)(end - st);
-    j = (int)(bj % a.kv);
-    b = (int)(bj / a.kv);
-    tb = row_pos(a.step, b);
-    const int nb = (tb + 1 + CH - 1) / CH;
-    kv1 = k1 < nb ? k1 : (k0 > nb ? k0 : nb);
+    sg.k1 = sg.k0 + (int)(end - st);
+    sg.j = (int)(bj % a.kv);
+    sg.b = (int)(bj / a.kv);
+    sg.tb = row_pos(a.step, sg.b);
+    sg.ts = row_start(a.step, sg.b);
+    sg.tw = row_wfirst(a.step, sg.b);
+    const int nb = (sg.tb + 1 + CH - 1) / CH, cs = sg.ts / CH;
+    sg.kv0 = sg.k0 > cs ? sg.k0 : cs;
+    sg.kv1 = sg.k1 < nb ? sg.k1 : nb;
+    if (sg.kv1 < sg.kv0) sg.kv1 = sg.kv0;
     next = end;
   };
 
@@ -644,23 +657,24 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
 
   // the issuing side of this warp (lane 0): cursor over (segment, chunk) pairs
   long long ist = c0, inext = c0;
-  int iq = warp, issued = 0, ib = 0, ij = 0, ik0 = 0, ik1 = 0, ikv1 = 0, itb = 0;
-  if (ist < c1) seg(ist, ib, ij, ik0, ik1, ikv1, itb, inext);
+  int iq = warp, issued = 0;
+  Seg is = {};
+  if (ist < c1) seg(ist, is, inext);
   auto settle = [&]() {  // move the cursor to a pair that exists (or past the run)
-    while (ist < c1 && iq >= ikv1 - ik0) {
+    while (ist < c1 && iq >= is.kv1 - is.kv0) {
       ist = inext;
       iq = warp;
-      if (ist < c1) seg(ist, ib, ij, ik0, ik1, ikv1, itb, inext);
+      if (ist < c1) seg(ist, is, inext);
     }
   };
   settle();
   auto issue = [&]() {
     const int slot = issued % NR;
-    const int pb = (ik0 + iq) * CH;
+    const int pb = (is.kv0 + iq) * CH;
     // the cache row and position holding position pb (a chunk never crosses a page)
     int r, pp;
-    cache_slot(a.step, a.cap, ib, pb, r, pp);
-    const int krow = a.krow0 + (r * a.kv + ij) * a.cap + pp;
+    cache_slot(a.step, a.cap, is.b, pb, r, pp);
+    const int krow = a.krow0 + (r * a.kv + is.j) * a.cap + pp;
     const uint32_t bar = bars + 8u * (warp * NR + slot);
     const uint32_t dst = s_base + (uint32_t)((warp * NR + slot) * BUF);
     fence_proxy_async_smem();
@@ -677,8 +691,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   if (lane == 0) {
     tma_prefetch_map(&kmap);
     tma_prefetch_map(&vmap);
-    // chunks below the row's position do not depend on the previous kernel
-    while (issued < NR && ist < c1 && (ik0 + iq) * CH + min(CH, itb + 1 - (ik0 + iq) * CH) <= itb) issue();
+    // chunks below the first position this step writes in the row do not depend on the
+    // previous kernel
+    while (issued < NR && ist < c1 && (is.kv0 + iq) * CH + min(CH, is.tb + 1 - (is.kv0 + iq) * CH) <= is.tw) issue();
   }
   grid_dep_wait();
   grid_dep_launch();
@@ -703,10 +718,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     }
   };
   if (c0 < c1) {
-    int b, j, k0, k1, kv1, tb;
+    Seg s0;
     long long nx;
-    seg(c0, b, j, k0, k1, kv1, tb, nx);
-    load_q(b, j);
+    seg(c0, s0, nx);
+    load_q(s0.b, s0.j);
   }
   __syncthreads();
 
@@ -757,9 +772,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   int lu = 0;
   long long next = c0;
   for (long long st = c0; st < c1; st = next, ++lu) {
-    int b, j, k0, k1, kv1, tb;
-    seg(st, b, j, k0, k1, kv1, tb, next);
-    const int p0 = k0 * CH, p1 = min(tb + 1, kv1 * CH), nch = kv1 - k0;  // nch may be 0
+    Seg sg;
+    seg(st, sg, next);
+    const int b = sg.b, j = sg.j, k0 = sg.k0, ts = sg.ts;
+    const int p0 = sg.kv0 * CH, p1 = min(sg.tb + 1, sg.kv1 * CH), nch = sg.kv1 - sg.kv0;  // nch may be 0
     // this segment's queries as B fragments (k = dimensions, n = heads), hi and lo, kept in
     // registers: x4 loads give (b0, b1) of two consecutive k-steps
     uint32_t qfh[NG][KS][2], qfl[NG][KS][2];
@@ -794,12 +810,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
       const int nv = min(CH, p1 - pb);
       const uint32_t kreg = s_base + (uint32_t)((warp * NR + slot) * BUF);
       const uint32_t vreg = kreg + (uint32_t)(CH * ROWB);
-      if (nv < CH) {
-        // rows past the last position hold other data (possibly not finite): zero the values
+      const int r0 = ts > pb ? ts - pb : 0;  // rows below the range's start (first chunk only)
+      if (nv < CH || r0 > 0) {
+        // rows outside the range hold other data (possibly not finite): zero the values
         unsigned char* vz = base + (size_t)(warp * NR + slot) * BUF + CH * ROWB;
-        for (int i = lane; i < (CH - nv) * (ROWB / 16); i += 32) {
-          const int r = nv + i / (ROWB / 16), cc = i - (i / (ROWB / 16)) * (ROWB / 16);
-          *reinterpret_cast<uint4*>(vz + swz_off(r, cc)) = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = lane; i < CH * (ROWB / 16); i += 32) {
+          const int r = i / (ROWB / 16), cc = i - r * (ROWB / 16);
+          if (r >= nv || r < r0) *reinterpret_cast<uint4*>(vz + swz_off(r, cc)) = make_uint4(0u, 0u, 0u, 0u);
         }
         __syncwarp();
       }
@@ -827,7 +844,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int pos = gid + 8 * (i >> 1), hh = n * 8 + 2 * tig + (i & 1);
-          p[n][i] = (pos < nv && hh < g) ? (sh[n][i] + sl[n][i]) * a.scale : -INFINITY;
+          p[n][i] = (pos < nv && pos >= r0 && hh < g) ? (sh[n][i] + sl[n][i]) * a.scale : -INFINITY;
         }
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
@@ -934,10 +951,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
       mypart[idx] = r;
     }
     if (next < c1) {  // (every warp is past this segment's chunks: the query buffer is free)
-      int b2, j2, k02, k12, kv12, tb2;
+      Seg s2;
       long long nx2;
-      seg(next, b2, j2, k02, k12, kv12, tb2, nx2);
-      load_q(b2, j2);
+      seg(next, s2, nx2);
+      load_q(s2.b, s2.j);
     }
     __syncthreads();
     if (clus) {

@@ -97,8 +97,10 @@ LLM_D float warp_max(float v) {
 }
 
 // ---- step parameters written by the step prologue --------------------------------------
-// The state is followed in memory by the position of every row ([max_batch] int32): rows may
-// sit at different positions (a decode of rows at their own positions); pos is their maximum.
+// The state is followed in memory by the position of every row ([B] int32): rows may sit at
+// different positions (a decode of rows at their own positions); pos is their maximum.  A prefill
+// pass (its rows are prompt tokens, "entries") adds each entry's attention start, the first
+// position the pass writes in the entry's cache row, and that cache row ([B] each) after them.
 struct StepState {
   int32_t pos;     // the largest position of this step's rows
   int32_t B;       // rows in this step
@@ -107,18 +109,31 @@ struct StepState {
   float p;         // sampling: top-p
   int32_t table_stride;  // paged steps: entries per row of table
   const int32_t* table;  // paged steps: [B][table_stride] pool pages of each row's positions, or null
+  int32_t ranges;        // 1: the rows' attention ranges follow their positions (prefill passes)
+  int32_t pad;
+  const int32_t* rowmap; // prefill passes: [B] cache row of each entry (no table), or null
 };
 // position of row b in this step
 LLM_D int32_t row_pos(const StepState* s, int b) { return reinterpret_cast<const int32_t*>(s + 1)[b]; }
+// Row b attends to positions row_start .. row_pos (0 .. row_pos unless ranges are given); this
+// step writes its row's positions from row_wfirst on (row_pos itself unless ranges are given),
+// so only cache positions below it may be read before the previous kernel finishes.
+LLM_D int32_t row_start(const StepState* s, int b) {
+  return s->ranges ? reinterpret_cast<const int32_t*>(s + 1)[s->B + b] : 0;
+}
+LLM_D int32_t row_wfirst(const StepState* s, int b) {
+  return s->ranges ? reinterpret_cast<const int32_t*>(s + 1)[2 * s->B + b] : row_pos(s, b);
+}
 
 // Paged caches (Llama 3.1 8B Instruct card, "Entries": decode_paged): the cache of a layer is a
 // pool of pages of kPage positions; page q is positions [(q % (cap / kPage)) * kPage, + kPage) of
 // cache row q / (cap / kPage).  Position pos of row b lies in page table[b][pos / kPage]; without
-// a table it lies in row b itself.  (r, pp): the cache row and position that hold it.
+// a table it lies in row b itself, or, in a prefill pass, in the entry's cache row rowmap[b].
+// (r, pp): the cache row and position that hold it.
 constexpr int kPage = 64;
 LLM_D void cache_slot(const StepState* s, int cap, int b, int pos, int& r, int& pp) {
   if (!s->table) {
-    r = b;
+    r = s->rowmap ? s->rowmap[b] : b;
     pp = pos;
     return;
   }
@@ -127,7 +142,7 @@ LLM_D void cache_slot(const StepState* s, int cap, int b, int pos, int& r, int& 
   r = page / per_row;
   pp = (page - r * per_row) * kPage + (pos & (kPage - 1));
 }
-LLM_HD size_t step_state_bytes(int max_batch) { return sizeof(StepState) + (size_t)max_batch * 4; }
+LLM_HD size_t step_state_bytes(int max_rows) { return sizeof(StepState) + (size_t)max_rows * 4 * 4; }
 
 // device error codes (same values as llm.h)
 

@@ -87,11 +87,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     flags[0] = 1;
     atomicCAS(a.status, 0, kErrDeviceTimeout);
   };
-  // unit u = (t * MT + m) * S + s: activation tile t, weight tile m, split s
+  // unit u = (m * T + t) * S + s: weight tile m, activation tile t, split s.  The activation
+  // tiles of one weight tile are neighbours, so the CTAs that run them at the same time share
+  // the weight tile through L2 (a pass of many prompt tokens reads its weights from HBM once).
+  const int T = a.Ntot / NP;
   auto unit = [&](int u, int& t, int& m, int& kb0, int& kb1) {
     const int s = u % S, tm = u / S;
-    m = tm % MT;
-    t = tm / MT;
+    t = tm % T;
+    m = tm / T;
     kb0 = KB * s / S;
     kb1 = KB * (s + 1) / S;
   };

@@ -33,6 +33,8 @@ constexpr int kInline = 64;  // rows whose token / draw travel inside the prolog
 
 constexpr int kGenChunk = 8;  // steps per generation graph
 
+constexpr int kDefaultTokens = 512;  // prompt tokens per prefill pass unless the config says
+
 // where the steps of one generation graph launch read and write (set before each launch)
 struct GenState {
   int32_t pos;          // position of the graph's first step
@@ -53,15 +55,16 @@ struct BeginArgs {
   const int32_t* pos_dev;
   const int32_t* table;    // paged step: [B][table_stride] pages, or null
   int32_t table_stride;
+  const int32_t* ranges;   // prefill pass: [3][B] attention starts, first written positions, cache rows
   float temp;
   int32_t k;
   float p;
   int32_t vocab;
-  const int32_t* tok_dev;  // [B] with stride tok_stride, or NULL: tok_inline
-  int32_t tok_stride, tok_col;
+  const int32_t* tok_dev;  // token of row b at (b / tok_np) * tok_stride + b % tok_np + tok_col,
+  int32_t tok_stride, tok_col, tok_np;  // or NULL: tok_inline
   const float* u_dev;      // or NULL: u_inline
-  int32_t* tok_buf;        // [max_batch]
-  float* u_buf;            // [max_batch]
+  int32_t* tok_buf;        // [NT]
+  float* u_buf;            // [NT]
   int32_t* status;
   int32_t tok_inline[kInline];
   float u_inline[kInline];
@@ -79,24 +82,31 @@ __global__ void step_begin_kernel(const BeginArgs a) {
     a.st->p = a.p;
     a.st->table = a.table;
     a.st->table_stride = a.table_stride;
+    a.st->ranges = a.ranges ? 1 : 0;
+    a.st->rowmap = a.ranges ? reinterpret_cast<int32_t*>(a.st + 1) + 3 * a.B : nullptr;
   }
   __syncthreads();
   int32_t* rowpos = reinterpret_cast<int32_t*>(a.st + 1);
   for (int b = t; b < a.B; b += blockDim.x) {
     const int32_t pb = !a.own_pos ? a.pos : a.pos_dev ? a.pos_dev[b] : a.pos_inline[b];  // validated by the host
     rowpos[b] = pb;
+    if (a.ranges) {
+      rowpos[a.B + b] = a.ranges[b];
+      rowpos[2 * a.B + b] = a.ranges[a.B + b];
+      rowpos[3 * a.B + b] = a.ranges[2 * a.B + b];
+    }
     atomicMax(&s_max, pb);
   }
   __syncthreads();
   if (t == 0) a.st->pos = s_max;
   for (int b = t; b < a.B; b += blockDim.x) {
-    int tok = a.tok_dev ? a.tok_dev[(size_t)b * a.tok_stride + a.tok_col] : a.tok_inline[b];
+    int tok = a.tok_dev ? a.tok_dev[(size_t)(b / a.tok_np) * a.tok_stride + b % a.tok_np + a.tok_col] : a.tok_inline[b];
     if (tok < 0 || tok >= a.vocab) {
       atomicCAS(a.status, 0, kErrTokenRange);
       tok = 0;
     }
     a.tok_buf[b] = tok;
-    a.u_buf[b] = a.u_dev ? a.u_dev[b] : a.u_inline[b];
+    a.u_buf[b] = a.u_dev ? a.u_dev[b] : b < kInline ? a.u_inline[b] : 0.0f;
   }
 }
 
@@ -113,6 +123,8 @@ __global__ void gen_begin_kernel(StepState* st, const GenState* gen, int32_t* to
     st->p = g.p;
     st->table = nullptr;
     st->table_stride = 0;
+    st->ranges = 0;
+    st->rowmap = nullptr;
   }
   int32_t* rowpos = reinterpret_cast<int32_t*>(st + 1);
   for (int b = t; b < g.B; b += blockDim.x) {
@@ -242,6 +254,7 @@ enum { MODE_NOHEAD = 0, MODE_HEAD = 1, MODE_GREEDY = 2, MODE_TOPP = 3 };
 struct llm_handle {
   llm_config cfg;
   int hd, H, d, kvw, f, V, L, wt, es;
+  int NT;  // rows of the activation and attention buffers: max(max_batch, max_tokens)
   int dev, num_sms, smem_optin;
   cudaStream_t stream = nullptr, cap_stream = nullptr;
   bool own_stream = false;
@@ -261,9 +274,12 @@ struct llm_handle {
   int part_ns = 0;
   CUtensorMap kmap, vmap;  // the key and value caches as [layers * max_batch * kv * max_seq][hd]
   StepState* st = nullptr;
-  int32_t* pos_buf = nullptr;  // [max_batch] positions of a decode of rows at their own positions
+  int32_t* pos_buf = nullptr;  // [NT] positions of the rows of a step (or the entries of a pass) at their own positions
   GenState* gen = nullptr;     // generation: the state of the graph launch in flight
   int32_t* page_table = nullptr;  // paged steps: [max_batch][max_seq / kPage] (max_seq % kPage == 0)
+  int32_t* range_buf = nullptr;   // prefill passes: [3][NT] attention starts, first written positions, cache rows
+  float* xh = nullptr;            // [max_batch][d] final residual rows gathered for the LM head
+  int32_t* head_map = nullptr;    // [max_batch] the entries those rows come from
   float* u_gen = nullptr;      // [kGenChunk][max_batch] draws of one host-memory generation launch
   int32_t* ids_gen = nullptr;  // [kGenChunk][max_batch] its drawn tokens
   int32_t* status = nullptr;
@@ -321,6 +337,7 @@ const char* check_config(const llm_config* c) {
   if (c->kv_heads <= 0 || c->group <= 0 || c->half <= 0 || c->ffn <= 0 || c->layers <= 0 || c->vocab <= 0)
     return "kv_heads, group, half, ffn, layers and vocab must be positive";
   if (c->max_batch <= 0 || c->max_seq <= 0) return "max_batch and max_seq must be positive";
+  if (c->max_tokens < 0 || c->max_tokens > 65535) return "max_tokens must be in 0..65535";
   if (c->dtype != LLM_DTYPE_F32 && c->dtype != LLM_DTYPE_BF16) return "dtype must be LLM_DTYPE_F32 or LLM_DTYPE_BF16";
   if (!(c->eps >= 0.0f) || !(c->theta > 0.0f)) return "eps must be >= 0 and theta > 0";
   if (c->rope_llama3 && !(c->rope_factor > 0.0f && c->rope_low_freq > 0.0f && c->rope_high_freq > c->rope_low_freq &&
@@ -717,10 +734,11 @@ llm_status run_step(llm_handle* h, int B, int mode) {
 // the step prologue; rows at their own positions when pos_host is given (copied to pos_buf)
 llm_status begin(llm_handle* h, int pos, int B, const int32_t* tok_host, const int32_t* tok_dev, int tok_stride,
                  int tok_col, float temp, int k, float p, const float* u_host, const float* u_dev,
-                 const int32_t* pos_host = nullptr, const int32_t* table_dev = nullptr, int table_stride = 0) {
+                 const int32_t* pos_host = nullptr, const int32_t* table_dev = nullptr, int table_stride = 0,
+                 const int32_t* ranges_dev = nullptr, int tok_np = 1) {
   BeginArgs a = {};
   a.st = h->st; a.pos = pos; a.B = B; a.temp = temp; a.k = k; a.p = p; a.vocab = h->V;
-  a.table = table_dev; a.table_stride = table_stride;
+  a.table = table_dev; a.table_stride = table_stride; a.ranges = ranges_dev;
   if (pos_host) {
     a.own_pos = 1;
     if (B <= kInline) {
@@ -731,18 +749,20 @@ llm_status begin(llm_handle* h, int pos, int B, const int32_t* tok_host, const i
     }
   }
   a.tok_buf = h->tok_buf; a.u_buf = h->u_buf; a.status = h->status;
-  a.tok_stride = tok_stride; a.tok_col = tok_col;
+  a.tok_stride = tok_stride; a.tok_col = tok_col; a.tok_np = tok_np;
+  auto tok_of = [&](int b) { return tok_host[(size_t)(b / tok_np) * tok_stride + b % tok_np + tok_col]; };
   if (tok_dev) {
     a.tok_dev = tok_dev;
   } else if (B <= kInline) {
-    for (int b = 0; b < B; ++b) a.tok_inline[b] = tok_host[(size_t)b * tok_stride + tok_col];
+    for (int b = 0; b < B; ++b) a.tok_inline[b] = tok_of(b);
   } else {
     std::vector<int32_t> col(B);
-    for (int b = 0; b < B; ++b) col[b] = tok_host[(size_t)b * tok_stride + tok_col];
+    for (int b = 0; b < B; ++b) col[b] = tok_of(b);
     CUDA_TRY(h, cudaMemcpyAsync(h->tok_buf, col.data(), (size_t)B * 4, cudaMemcpyHostToDevice, h->stream));
     a.tok_dev = h->tok_buf;
     a.tok_stride = 1;
     a.tok_col = 0;
+    a.tok_np = 1;
   }
   if (u_dev) {
     a.u_dev = u_dev;
@@ -871,6 +891,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   h->wt = c.dtype == LLM_DTYPE_BF16 ? 1 : 0;
   h->es = (int)es;
   h->filled.assign(c.max_batch, 0);
+  h->NT = std::max(c.max_batch, c.max_tokens > 0 ? c.max_tokens : kDefaultTokens);
   llm_status st = LLM_OK;
   auto bail = [&](llm_status s) {
     cudaError_t ce = cudaGetLastError();
@@ -898,7 +919,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   // tensor-core path: bf16 weights, rows a whole number of 16-byte chunks (checked above)
   const int tc_min = c.tc_min_batch > 0 ? c.tc_min_batch : kTcDefaultMinBatch;
   // (debug_trace handles keep every step on the GEMV: the traced buffers are written in order there)
-  if (h->wt && !c.debug_trace && tc_min <= c.max_batch && tc_available()) {
+  if (h->wt && !c.debug_trace && tc_min <= h->NT && tc_available()) {
     if ((ce = tc_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("tensor-core kernel attributes", ce);
     h->tc_min = tc_min;
   }
@@ -937,25 +958,28 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
       (st = dalloc(h, &h->rope_sin, (size_t)c.max_seq * c.half * 4)))
     return bail(st);
   const size_t B = c.max_batch;
-  if ((st = dalloc(h, &h->xa, B * h->d * 4)) || (st = dalloc(h, &h->xb, B * h->d * 4)) ||
-      (st = dalloc(h, &h->q, B * h->d * 4)) || (st = dalloc(h, &h->attn, B * h->d * 4)) ||
-      (st = dalloc(h, &h->m, B * h->f * 4)) || (st = dalloc(h, &h->logits, B * h->V * 4)))
+  const size_t NT = h->NT;  // rows of a step or of a prefill pass
+  if ((st = dalloc(h, &h->xa, NT * h->d * 4)) || (st = dalloc(h, &h->xb, NT * h->d * 4)) ||
+      (st = dalloc(h, &h->q, NT * h->d * 4)) || (st = dalloc(h, &h->attn, NT * h->d * 4)) ||
+      (st = dalloc(h, &h->m, NT * h->f * 4)) || (st = dalloc(h, &h->logits, B * h->V * 4)) ||
+      (st = dalloc(h, &h->xh, B * h->d * 4)) || (st = dalloc(h, &h->head_map, B * 4)))
     return bail(st);
   int maxns = 1;
-  for (int b = 1; b <= c.max_batch; ++b) {
+  for (int b = 1; b <= h->NT; ++b) {
     const int ns = attn_splits(b, c.kv_heads, c.max_seq, h->num_sms);
     maxns = std::max(maxns, ns);
     attn_cluster_merge(h->wt, h->hd, c.group, ns, b * c.kv_heads, c.max_seq);  // device queries before any capture
   }
   h->part_ns = maxns;
-  h->ticket_count = (int)(B * c.kv_heads);
+  h->ticket_count = (int)(NT * c.kv_heads);
   const int slots = attn_part_slots(h->wt, h->hd, maxns);
-  if ((st = dalloc(h, &h->part, B * h->H * slots * (h->hd + 2) * 4)) ||
-      (st = dalloc(h, &h->ticket, B * c.kv_heads * 4)) || (st = dalloc(h, &h->st, step_state_bytes(c.max_batch))) ||
-      (st = dalloc(h, &h->pos_buf, B * 4)) || (st = dalloc(h, &h->gen, sizeof(GenState))) ||
+  if ((st = dalloc(h, &h->part, NT * h->H * slots * (h->hd + 2) * 4)) ||
+      (st = dalloc(h, &h->ticket, NT * c.kv_heads * 4)) || (st = dalloc(h, &h->st, step_state_bytes((int)NT))) ||
+      (st = dalloc(h, &h->pos_buf, NT * 4)) || (st = dalloc(h, &h->gen, sizeof(GenState))) ||
       (st = dalloc(h, &h->u_gen, (size_t)kGenChunk * B * 4)) || (st = dalloc(h, &h->ids_gen, (size_t)kGenChunk * B * 4)) ||
       (c.max_seq % kPage == 0 && (st = dalloc(h, &h->page_table, B * (size_t)(c.max_seq / kPage) * 4))) ||
-      (st = dalloc(h, &h->status, 16)) || (st = dalloc(h, &h->tok_buf, B * 4)) || (st = dalloc(h, &h->u_buf, B * 4)) ||
+      (st = dalloc(h, &h->range_buf, 3 * NT * 4)) ||
+      (st = dalloc(h, &h->status, 16)) || (st = dalloc(h, &h->tok_buf, NT * 4)) || (st = dalloc(h, &h->u_buf, NT * 4)) ||
       (st = dalloc(h, &h->ids_buf, B * 4)))
     return bail(st);
   h->V_pad = (h->V + 31) & ~31;
@@ -963,17 +987,17 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
       (st = dalloc(h, &h->s_pre, B * h->V_pad * 4)) || (st = dalloc(h, &h->s_hist, B * kSampleHistPerRow * 4)))
     return bail(st);
   if (h->tc_min) {
-    // split activations for up to max_batch rows; split sums of the largest projection
+    // split activations for up to NT rows; split sums of the largest projection
     const int64_t qkv_rows = (int64_t)(h->H + 2 * c.kv_heads) * h->hd;
     size_t part = 0;
-    for (int b = h->tc_min; b <= c.max_batch; ++b) {
+    for (int b = h->tc_min; b <= h->NT; ++b) {
       const int64_t shapes[4][2] = {{qkv_rows, h->d}, {h->d, h->d}, {2 * (int64_t)h->f, h->d}, {h->d, h->f}};
       for (auto& sh : shapes) {
         const TcPlan p = plan_tc((int)sh[0], (int)sh[1], b, h->num_sms);
         part = std::max(part, (size_t)p.S * b * (size_t)sh[0]);
       }
     }
-    const size_t xs_elems = (size_t)2 * tc_ntot(c.max_batch) * std::max(h->d, h->f);
+    const size_t xs_elems = (size_t)2 * tc_ntot(h->NT) * std::max(h->d, h->f);
     if ((st = dalloc(h, &h->tc_xs, xs_elems * 2)) || (st = dalloc(h, &h->tc_part, part * 4))) return bail(st);
     if (cudaMemsetAsync(h->tc_xs, 0, xs_elems * 2, h->stream) != cudaSuccess ||
         cudaMemsetAsync(h->tc_part, 0, part * 4, h->stream) != cudaSuccess)
@@ -993,7 +1017,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     if (!ok || !tc_make_map(&h->tmap_head, h->head, h->d, h->V, kTcK, (uint32_t)head_rows)) h->tc_min = 0;
   }
   if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * 5 * B * std::max(h->d, h->f) * 4))) return bail(st);
-  if (cudaMemsetAsync(h->ticket, 0, B * c.kv_heads * 4, h->stream) != cudaSuccess ||
+  if (cudaMemsetAsync(h->ticket, 0, NT * c.kv_heads * 4, h->stream) != cudaSuccess ||
       cudaMemsetAsync(h->status, 0, 16, h->stream) != cudaSuccess ||
       cudaMemsetAsync(h->kc, 0, cache_bytes, h->stream) != cudaSuccess ||
       cudaMemsetAsync(h->vc, 0, cache_bytes, h->stream) != cudaSuccess)
@@ -1042,24 +1066,127 @@ llm_status llm_check_wait_timeout(llm_handle* h, int64_t limit_cycles) {
   return LLM_OK;
 }
 
+// ---- prefill passes ----
+//
+// A pass is one step whose rows are prompt tokens ("entries"): entry e is token tokens[e] at
+// position positions[e] of cache row rowmap[e], attending to positions start[e] .. positions[e]
+// of that row.  The step prologue puts positions, starts, the first position the pass writes in
+// each entry's row (wfirst: attention copies below it may start before the Q/K/V kernel ends) and
+// the rows into the step state; the projections see n = entries rows (on the tensor cores once n
+// reaches tc_min_batch) and the Q/K/V kernel writes every entry's key and value before the
+// attention reads them.  No pass runs the LM head: the entries whose logits are wanted are
+// gathered afterwards (pass_logits).
+
+// gather rows of the final residual stream: dst[i] = src[map[i]] (width floats)
+__global__ void gather_rows_f32_kernel(float* dst, const float* src, const int32_t* map, int width) {
+  const float* s = src + (size_t)map[blockIdx.x] * width;
+  float* o = dst + (size_t)blockIdx.x * width;
+  for (int i = threadIdx.x; i < width; i += blockDim.x) o[i] = s[i];
+}
+
+// final norm + LM head over rows 0..m-1 of xh into the logits buffer
+static llm_status head_rows(llm_handle* h, int m) {
+  if (h->tc_min > 0 && m >= h->tc_min) {
+    PrepIn in;
+    in.x = h->xh; in.x_stride = h->d; in.gain = h->lnf;
+    TRY(launch_prep(h, in, h->d, m, false));
+    return launch_gemm(h, h->tmap_head, h->V, h->d, m, h->logits, false, true);
+  }
+  const GemvPlan p = plan_gemv(h->V, h->d, 1, h->wt, m, h->num_sms, 2);
+  GemvArgs a = {};
+  a.step = h->st; a.B = m; a.eps = h->cfg.eps; a.W = h->head; a.rows = h->V; a.cols = h->d; a.rg = 1;
+  a.x = h->xh; a.x_stride = h->d; a.gain = h->lnf;
+  a.lpr = p.lpr; a.seg_ch = p.seg_ch; a.nseg = p.nseg; a.rows_cap = p.rows_cap; a.ws = p.ws;
+  a.out = h->logits; a.out_stride = h->V;
+  a.status = h->status;
+  CUDA_TRY(h, launch_gemv(a, p, h->wt, EPI_STORE, true, h->stream, false));
+  return LLM_OK;
+}
+
+// logits after entries ents[i] of the pass of n entries just run, into dst rows dst_row[i]
+// ([.][V], host or device memory)
+static llm_status pass_logits(llm_handle* h, int n, const std::vector<int32_t>& ents, const std::vector<int>& dst_row,
+                              float* dst, bool host) {
+  if (ents.empty()) return LLM_OK;
+  if (h->tc_min > 0 && n >= h->tc_min) {
+    // the residual stream after the last layer: its down projection's split sums + x1
+    PrepIn in;
+    in.src_rows = h->d; in.src_K = h->f; in.resid = h->xb; in.xout = h->xa;
+    TRY(launch_prep(h, in, h->d, n, false));
+  }
+  const int mb = h->cfg.max_batch;
+  for (size_t c0 = 0; c0 < ents.size(); c0 += mb) {
+    const int m = (int)std::min<size_t>(mb, ents.size() - c0);
+    CUDA_TRY(h, cudaMemcpyAsync(h->head_map, ents.data() + c0, (size_t)m * 4, cudaMemcpyHostToDevice, h->stream));
+    gather_rows_f32_kernel<<<m, 256, 0, h->stream>>>(h->xh, h->xa, h->head_map, h->d);
+    CUDA_TRY(h, cudaGetLastError());
+    TRY(head_rows(h, m));
+    for (int i = 0; i < m; ++i)
+      CUDA_TRY(h, cudaMemcpyAsync(dst + (size_t)dst_row[c0 + i] * h->V, h->logits + (size_t)i * h->V, (size_t)h->V * 4,
+                                  host ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice, h->stream));
+  }
+  return LLM_OK;
+}
+
+// one pass of n entries; ranges [3][n]: attention starts, first written positions, cache rows;
+// tokens as for begin (host array, or device array read at (e / tok_np) * tok_stride + e % tok_np
+// + tok_col)
+static llm_status run_pass(llm_handle* h, int n, const int32_t* tok_host, const int32_t* tok_dev, int tok_stride,
+                           int tok_col, int tok_np, const int32_t* pos_host, const int32_t* ranges_host) {
+  CUDA_TRY(h, cudaMemcpyAsync(h->range_buf, ranges_host, (size_t)3 * n * 4, cudaMemcpyHostToDevice, h->stream));
+  TRY(begin(h, 0, n, tok_host, tok_dev, tok_stride, tok_col, 0.0f, 1, 1.0f, nullptr, nullptr, pos_host, nullptr, 0,
+            h->range_buf, tok_np));
+  return run_step(h, n, MODE_NOHEAD);
+}
+
 static llm_status prefill_impl(llm_handle* h, const int32_t* tok_host, const int32_t* tok_dev, int32_t B, int32_t S,
                                int32_t pos, float* logits, bool logits_on_host) {
   TRY(check_rows(h, B, pos, S));
   if (tok_host) TRY(check_tokens(h, tok_host, (size_t)B * S));
-  for (int i = 0; i < S; ++i) {
-    TRY(begin(h, pos + i, B, tok_host, tok_dev, S, i, 0.0f, 1, 1.0f, nullptr, nullptr));
-    TRY(run_step(h, B, (i == S - 1 && logits) ? MODE_HEAD : MODE_NOHEAD));
-  }
-  if (logits) {
-    if (logits_on_host) {
-      CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
-      CUDA_TRY(h, cudaStreamSynchronize(h->stream));
-    } else if (logits != h->logits) {
-      CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToDevice, h->stream));
+  if (S == 1 || h->cfg.debug_trace) {
+    // single positions (a decode), or a traced handle: one step of all B rows per position
+    for (int i = 0; i < S; ++i) {
+      TRY(begin(h, pos + i, B, tok_host, tok_dev, S, i, 0.0f, 1, 1.0f, nullptr, nullptr));
+      TRY(run_step(h, B, (i == S - 1 && logits) ? MODE_HEAD : MODE_NOHEAD));
     }
-  } else if (logits_on_host) {
-    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+    if (logits) {
+      if (logits_on_host) {
+        CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
+      } else if (logits != h->logits) {
+        CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToDevice, h->stream));
+      }
+    }
+  } else {
+    // passes of np whole positions of all B rows; entry e = b * cnt + i: row b, position
+    // pos + p0 + i, token tokens[b * S + p0 + i]
+    const int np = std::max(1, h->NT / B);
+    std::vector<int32_t> epos, ranges, ents;
+    std::vector<int> dst;
+    for (int p0 = 0; p0 < S; p0 += np) {
+      const int cnt = std::min(np, S - p0), n = B * cnt;
+      epos.resize(n);
+      ranges.resize(3 * (size_t)n);
+      for (int b = 0; b < B; ++b)
+        for (int i = 0; i < cnt; ++i) {
+          const int e = b * cnt + i;
+          epos[e] = pos + p0 + i;
+          ranges[e] = 0;               // the whole cache of the row up to the position
+          ranges[n + e] = pos + p0;    // this pass writes the row from pos + p0 on
+          ranges[2 * n + e] = b;
+        }
+      TRY(run_pass(h, n, tok_host, tok_dev, S, p0, cnt, epos.data(), ranges.data()));
+      if (p0 + cnt == S && logits) {
+        ents.clear();
+        dst.clear();
+        for (int b = 0; b < B; ++b) {
+          ents.push_back(b * cnt + cnt - 1);
+          dst.push_back(b);
+        }
+        TRY(pass_logits(h, n, ents, dst, logits, logits_on_host));
+      }
+    }
   }
+  if (logits_on_host) CUDA_TRY(h, cudaStreamSynchronize(h->stream));
   set_filled(h, B, pos + S);
   return LLM_OK;
 }
@@ -1182,6 +1309,103 @@ llm_status llm_step_paged_dev(llm_handle* h, const int32_t* tokens_dev, int32_t 
   if (!h || !tokens_dev || !positions_host || !table_host || !ids_dev) return LLM_ERR_ARG;
   return paged_impl(h, nullptr, tokens_dev, B, positions_host, table_host, pages_per_row,
                     temp > 0.0f ? MODE_TOPP : MODE_GREEDY, temp, k, p, nullptr, u_dev, ids_dev, logits_dev, false);
+}
+
+// Prompts packed end to end (Llama 3.1 8B Instruct card, "Entries": prefill_packed): token p is
+// position positions[p] of prompt segments[p], in cache row rows[p]; each token attends to its
+// own prompt's tokens up to itself.  The tokens run as the entries of prefill passes of at most
+// NT entries, in position order: entry e reads and writes cache row rows[e], attends to positions
+// start .. its position (start: its prompt's first position), and reads nothing its pass writes
+// before the Q/K/V kernel has finished.
+static llm_status packed_impl(llm_handle* h, const int32_t* toks, const int32_t* rows, const int32_t* positions,
+                              const int32_t* segments, int32_t P, const int32_t* last, int32_t nlast, float* logits) {
+  if (P < 1 || nlast < 0) return fail(h, LLM_ERR_ARG, "tokens %d < 1 or last count %d < 0", P, nlast);
+  if (h->cfg.debug_trace) return fail(h, LLM_ERR_ARG, "debug_trace handles run without graphs");
+  TRY(check_tokens(h, toks, (size_t)P));
+  for (int i = 0; i < P; ++i) {
+    if (rows[i] < 0 || rows[i] >= h->cfg.max_batch)
+      return fail(h, LLM_ERR_BATCH, "token %d: row %d outside 0..%d", i, rows[i], h->cfg.max_batch - 1);
+    if (positions[i] < 0 || positions[i] >= h->cfg.max_seq)
+      return fail(h, LLM_ERR_POS_RANGE, "token %d: position %d outside the cache of %d", i, positions[i], h->cfg.max_seq);
+  }
+  for (int m = 0; m < nlast; ++m)
+    if (last[m] < 0 || last[m] >= P) return fail(h, LLM_ERR_ARG, "last[%d] = %d names no token", m, last[m]);
+  // each prompt: one row, consecutive positions first..first+n-1, each once; prompts of one row
+  // do not overlap
+  struct Span { int row, lo, hi, n; };
+  std::map<int32_t, Span> span;
+  for (int i = 0; i < P; ++i) {
+    auto it = span.find(segments[i]);
+    if (it == span.end()) {
+      span[segments[i]] = Span{rows[i], positions[i], positions[i], 1};
+    } else {
+      Span& sp = it->second;
+      if (sp.row != rows[i]) return fail(h, LLM_ERR_ARG, "prompt %d spans rows %d and %d", segments[i], sp.row, rows[i]);
+      sp.lo = std::min(sp.lo, positions[i]);
+      sp.hi = std::max(sp.hi, positions[i]);
+      ++sp.n;
+    }
+  }
+  {
+    std::map<std::pair<int, int>, int> slot;  // (row, position) -> token
+    for (int i = 0; i < P; ++i)
+      if (!slot.emplace(std::make_pair(rows[i], positions[i]), i).second)
+        return fail(h, LLM_ERR_ARG, "tokens %d and %d share row %d position %d", slot[{rows[i], positions[i]}], i,
+                    rows[i], positions[i]);
+    for (auto& kv : span)
+      if (kv.second.hi - kv.second.lo + 1 != kv.second.n)
+        return fail(h, LLM_ERR_ARG, "prompt %d does not fill positions %d..%d", kv.first, kv.second.lo, kv.second.hi);
+    for (auto& a : span)
+      for (auto& b : span)
+        if (a.first < b.first && a.second.row == b.second.row && a.second.lo <= b.second.hi && b.second.lo <= a.second.hi)
+          return fail(h, LLM_ERR_ARG, "prompts %d and %d overlap in row %d", a.first, b.first, a.second.row);
+  }
+  // position order, then passes of at most NT entries
+  std::vector<int> order(P);
+  for (int i = 0; i < P; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return positions[x] < positions[y]; });
+  std::vector<std::vector<int>> last_of(P);  // token -> the indices m of last naming it
+  for (int m = 0; m < nlast; ++m) last_of[last[m]].push_back(m);
+  const int cap_e = h->NT;
+  std::vector<int32_t> etok, epos, eranges, ents;
+  std::vector<int> dst;
+  for (int p0 = 0; p0 < P; p0 += cap_e) {
+    const int n = std::min(cap_e, P - p0);
+    etok.assign(n, 0);
+    epos.assign(n, 0);
+    eranges.assign(3 * (size_t)n, 0);
+    ents.clear();
+    dst.clear();
+    std::map<int, int> wfirst;  // row -> first position this pass writes in it
+    for (int e = 0; e < n; ++e) {
+      const int i = order[p0 + e];
+      etok[e] = toks[i];
+      epos[e] = positions[i];
+      eranges[e] = span[segments[i]].lo;
+      eranges[2 * (size_t)n + e] = rows[i];
+      auto w = wfirst.find(rows[i]);
+      if (w == wfirst.end() || positions[i] < w->second) wfirst[rows[i]] = positions[i];
+      for (int m : last_of[i]) {
+        ents.push_back(e);
+        dst.push_back(m);
+      }
+    }
+    for (int e = 0; e < n; ++e) eranges[n + e] = wfirst[rows[order[p0 + e]]];
+    TRY(run_pass(h, n, etok.data(), nullptr, 1, 0, 1, epos.data(), eranges.data()));
+    if (logits) TRY(pass_logits(h, n, ents, dst, logits, true));
+    // (the host vectors are refilled for the next pass: its copies read them first)
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  }
+  for (auto& kv : span) h->filled[kv.second.row] = std::max(h->filled[kv.second.row], kv.second.hi + 1);
+  return LLM_OK;
+}
+
+llm_status llm_prefill_packed(llm_handle* h, const int32_t* tokens_host, const int32_t* rows_host,
+                              const int32_t* positions_host, const int32_t* segments_host, int32_t P,
+                              const int32_t* last_host, int32_t nlast, float* logits_host) {
+  if (!h || !tokens_host || !rows_host || !positions_host || !segments_host || (nlast > 0 && !last_host))
+    return LLM_ERR_ARG;
+  return packed_impl(h, tokens_host, rows_host, positions_host, segments_host, P, last_host, nlast, logits_host);
 }
 
 // n decode steps, each feeding its draws to the next as tokens, as CUDA graphs of kGenChunk

@@ -74,6 +74,8 @@ __global__ void noalloc_params_kernel(StepState* st, float temp, int32_t k, floa
   st->k = k;
   st->p = p;
   st->table = nullptr;
+  st->ranges = 0;
+  st->rowmap = nullptr;
 }
 
 // the scratch address on the current device (looked up again when the device's context changed)
