@@ -37,7 +37,7 @@ class LlmConfig(ctypes.Structure):
                 ("rope_orig_max_pos", ctypes.c_float), ("max_batch", ctypes.c_int32),
                 ("max_seq", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("debug_trace", ctypes.c_int32), ("tc_min_batch", ctypes.c_int32),
-                ("max_tokens", ctypes.c_int32)]
+                ("max_tokens", ctypes.c_int32), ("step_kernel", ctypes.c_int32)]
 
 
 class LlmError(RuntimeError):
@@ -107,14 +107,15 @@ def lib():
     return _lib
 
 
-def config(shape, max_batch, max_seq, debug_trace=False, tc_min_batch=0, max_tokens=0) -> LlmConfig:
+def config(shape, max_batch, max_seq, debug_trace=False, tc_min_batch=0, max_tokens=0,
+           step_kernel=0) -> LlmConfig:
     """An llm_config from a shape description (fields kv, g, half, ffn, layers, vocab, eps,
     theta, tied, llama3, factor, low_freq, high_freq, orig_max, bf16)."""
     return LlmConfig(shape.kv, shape.g, shape.half, shape.ffn, shape.layers, shape.vocab,
                      shape.eps, shape.theta, int(shape.tied), int(shape.llama3), shape.factor,
                      shape.low_freq, shape.high_freq, shape.orig_max, max_batch, max_seq,
                      LLM_DTYPE_BF16 if shape.bf16 else LLM_DTYPE_F32, int(debug_trace),
-                     int(tc_min_batch), int(max_tokens))
+                     int(tc_min_batch), int(max_tokens), int(step_kernel))
 
 
 def _ptr(a):
@@ -313,9 +314,9 @@ class Model:
     """One handle: host-memory entry points with numpy arrays."""
 
     def __init__(self, shape, weights, max_batch, max_seq, stream=None, debug_trace=False,
-                 weights_on_device=False, tc_min_batch=0, max_tokens=0):
+                 weights_on_device=False, tc_min_batch=0, max_tokens=0, step_kernel=0):
         self.shape = shape
-        self.cfg = config(shape, max_batch, max_seq, debug_trace, tc_min_batch, max_tokens)
+        self.cfg = config(shape, max_batch, max_seq, debug_trace, tc_min_batch, max_tokens, step_kernel)
         self.h = llm_create(self.cfg, weights, weights_on_device, stream)
         self.V = shape.vocab
         self.cache_dtype = np.uint16 if shape.bf16 else np.float32

@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libllm.so")
-SOURCES = ["llm.cu", "gemv.cu", "gemm.cu", "attention.cu", "sampler.cu", "noalloc.cu"]
+SOURCES = ["llm.cu", "gemv.cu", "gemm.cu", "attention.cu", "sampler.cu", "noalloc.cu", "mega.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

@@ -20,6 +20,7 @@
 #include "attention.cuh"
 #include "common.cuh"
 #include "gemm.cuh"
+#include "mega.cuh"
 #include "gemv.cuh"
 #include "llm.h"
 #include "sampler.cuh"
@@ -56,6 +57,7 @@ struct BeginArgs {
   const int32_t* table;    // paged step: [B][table_stride] pages, or null
   int32_t table_stride;
   const int32_t* ranges;   // prefill pass: [3][B] attention starts, first written positions, cache rows
+  uint32_t* mega_bar;      // the persistent step kernel's barrier counter, reset here (or null)
   float temp;
   int32_t k;
   float p;
@@ -84,6 +86,7 @@ __global__ void step_begin_kernel(const BeginArgs a) {
     a.st->table_stride = a.table_stride;
     a.st->ranges = a.ranges ? 1 : 0;
     a.st->rowmap = a.ranges ? reinterpret_cast<int32_t*>(a.st + 1) + 3 * a.B : nullptr;
+    if (a.mega_bar) *a.mega_bar = 0u;
   }
   __syncthreads();
   int32_t* rowpos = reinterpret_cast<int32_t*>(a.st + 1);
@@ -112,10 +115,12 @@ __global__ void step_begin_kernel(const BeginArgs a) {
 
 // step i of a generation graph: the prologue of a step at position gen.pos + i whose tokens are
 // the previous step's draws (gen.prev for i == 0) and whose draws are gen.u[i]
-__global__ void gen_begin_kernel(StepState* st, const GenState* gen, int32_t* tok_buf, float* u_buf, int i) {
+__global__ void gen_begin_kernel(StepState* st, const GenState* gen, int32_t* tok_buf, float* u_buf, int i,
+                                 uint32_t* mega_bar) {
   const GenState g = *gen;
   const int t = threadIdx.x;
   if (t == 0) {
+    if (mega_bar) *mega_bar = 0u;
     st->pos = g.pos + i;
     st->B = g.B;
     st->temp = g.temp;
@@ -280,6 +285,14 @@ struct llm_handle {
   int32_t* range_buf = nullptr;   // prefill passes: [3][NT] attention starts, first written positions, cache rows
   float* xh = nullptr;            // [max_batch][d] final residual rows gathered for the LM head
   int32_t* head_map = nullptr;    // [max_batch] the entries those rows come from
+  // batch-1 steps in one persistent kernel (bf16, supported shapes)
+  bool mega = false;
+  MegaLayer* mega_layers = nullptr;  // [L], device
+  float* mega_part = nullptr;        // attention partials [H][kMegaMaxSplits][hd + 2]
+  uint32_t* mega_ticket = nullptr;   // [kv + 1]
+  uint32_t* mega_bar = nullptr;      // grid barrier counter (reset by each step's prologue)
+  float* mega_cv = nullptr;          // [num_sms] argmax candidates
+  int32_t* mega_ci = nullptr;
   float* u_gen = nullptr;      // [kGenChunk][max_batch] draws of one host-memory generation launch
   int32_t* ids_gen = nullptr;  // [kGenChunk][max_batch] its drawn tokens
   int32_t* status = nullptr;
@@ -664,6 +677,20 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
 llm_status launch_layer_kernels(llm_handle* h, int B, int mode, bool pdl, bool trace) {
   const llm_config& c = h->cfg;
   TRY(launch_one(h, K_EMBED, 0, B, false));
+  if (h->mega && B == 1 && !trace) {
+    // every layer, the head and a greedy draw in one persistent kernel; a top-k top-p draw after
+    MegaArgs a = {};
+    a.layers = h->mega_layers; a.L = h->L; a.d = h->d; a.f = h->f; a.V = h->V; a.H = h->H; a.kv = c.kv_heads;
+    a.g = c.group; a.hd = h->hd; a.cap = c.max_seq; a.max_batch = c.max_batch; a.eps = c.eps;
+    a.scale = 1.0f / sqrtf((float)h->hd); a.lnf = h->lnf; a.head = h->head; a.kc = h->kc; a.vc = h->vc;
+    a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin; a.step = h->st; a.x = h->xa; a.x1 = h->xb; a.q = h->q;
+    a.attn = h->attn; a.m = h->m; a.logits = h->logits; a.apart = h->mega_part; a.ticket = h->mega_ticket;
+    a.bar = h->mega_bar; a.cand_v = h->mega_cv; a.cand_i = h->mega_ci; a.ids = h->ids_buf; a.status = h->status;
+    a.head_mode = mode == MODE_NOHEAD ? 0 : mode == MODE_GREEDY ? 2 : 1;
+    CUDA_TRY(h, launch_mega(a, h->num_sms, h->stream));
+    if (mode == MODE_TOPP) TRY(launch_one(h, K_SAMPLE, 0, B, false));
+    return LLM_OK;
+  }
   const size_t maxw = (size_t)std::max(h->d, h->f);
   for (int l = 0; l < h->L; ++l) {
     for (int k = K_QKV; k <= K_DOWN; ++k) TRY(launch_one(h, k, l, B, pdl));
@@ -698,7 +725,7 @@ llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t,
       s = launch_layer_kernels(h, B, mode, true, false);
     } else {
       for (int i = 0; i < gen && s == LLM_OK; ++i) {
-        gen_begin_kernel<<<1, 128, 0, h->stream>>>(h->st, h->gen, h->tok_buf, h->u_buf, i);
+        gen_begin_kernel<<<1, 128, 0, h->stream>>>(h->st, h->gen, h->tok_buf, h->u_buf, i, h->mega_bar);
         s = launch_layer_kernels(h, B, mode, true, false);
         if (s == LLM_OK) gen_end_kernel<<<1, 128, 0, h->stream>>>(h->gen, h->ids_buf, i);
       }
@@ -738,7 +765,7 @@ llm_status begin(llm_handle* h, int pos, int B, const int32_t* tok_host, const i
                  const int32_t* ranges_dev = nullptr, int tok_np = 1) {
   BeginArgs a = {};
   a.st = h->st; a.pos = pos; a.B = B; a.temp = temp; a.k = k; a.p = p; a.vocab = h->V;
-  a.table = table_dev; a.table_stride = table_stride; a.ranges = ranges_dev;
+  a.table = table_dev; a.table_stride = table_stride; a.ranges = ranges_dev; a.mega_bar = h->mega_bar;
   if (pos_host) {
     a.own_pos = 1;
     if (B <= kInline) {
@@ -1017,6 +1044,30 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     if (!ok || !tc_make_map(&h->tmap_head, h->head, h->d, h->V, kTcK, (uint32_t)head_rows)) h->tc_min = 0;
   }
   if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * 5 * B * std::max(h->d, h->f) * 4))) return bail(st);
+  {
+    // batch-1 steps as one persistent kernel where the shape allows it and every CTA can be resident
+    int coop = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->dev);
+    if (coop && !c.debug_trace && c.step_kernel == 0 && h->num_sms >= c.kv_heads &&
+        mega_supported(h->wt, h->hd, c.group, h->d, h->f) &&
+        mega_smem(h->d, h->f) + 1024 <= (size_t)h->smem_optin && mega_prepare(h->smem_optin) == cudaSuccess) {
+      if ((st = dalloc(h, &h->mega_layers, sizeof(MegaLayer) * (size_t)h->L)) ||
+          (st = dalloc(h, &h->mega_part, (size_t)h->H * kMegaMaxSplits * (h->hd + 2) * 4)) ||
+          (st = dalloc(h, &h->mega_ticket, ((size_t)c.kv_heads + 1) * 4)) || (st = dalloc(h, &h->mega_bar, 4)) ||
+          (st = dalloc(h, &h->mega_cv, (size_t)h->num_sms * 4)) || (st = dalloc(h, &h->mega_ci, (size_t)h->num_sms * 4)))
+        return bail(st);
+      std::vector<MegaLayer> ml(h->L);
+      for (int l = 0; l < h->L; ++l)
+        ml[l] = MegaLayer{h->lw[l].qkv, h->lw[l].ln1, h->lw[l].o, h->lw[l].ln2, h->lw[l].gu, h->lw[l].down};
+      if (cudaMemcpy(h->mega_layers, ml.data(), sizeof(MegaLayer) * (size_t)h->L, cudaMemcpyHostToDevice) != cudaSuccess ||
+          cudaMemsetAsync(h->mega_ticket, 0, ((size_t)c.kv_heads + 1) * 4, h->stream) != cudaSuccess ||
+          cudaMemsetAsync(h->mega_bar, 0, 4, h->stream) != cudaSuccess)
+        return cuda_bail("persistent step kernel setup", cudaGetLastError());
+      h->mega = true;
+    } else {
+      cudaGetLastError();
+    }
+  }
   if (cudaMemsetAsync(h->ticket, 0, NT * c.kv_heads * 4, h->stream) != cudaSuccess ||
       cudaMemsetAsync(h->status, 0, 16, h->stream) != cudaSuccess ||
       cudaMemsetAsync(h->kc, 0, cache_bytes, h->stream) != cudaSuccess ||

@@ -375,11 +375,34 @@ static uint64_t toff(const or_model* M, int32_t l, int32_t t) {
   return o;
 }
 
-/* y = W x for W [rows][cols] at element offset off (see the matvec reading above) */
+/* y = W x for W [rows][cols] at element offset off (see the matvec reading above): every y[r]
+ * is one f32 accumulator summed over c = 0..cols-1 in order.  Eight rows are summed side by side
+ * (eight independent accumulators, each in its own order: no result changes), so the processor
+ * is not idle while one row's additions wait on each other. */
 static void matvec(const or_model* M, uint64_t off, int32_t rows, int32_t cols, const float* x,
                    float* y) {
-  for (int32_t r = 0; r < rows; ++r) {
-    uint64_t base = off + (uint64_t)r * (uint64_t)cols;
+  int32_t r = 0;
+  if (M->c.bf16) {
+    const uint16_t* w = (const uint16_t*)M->w + off;
+    for (; r + 8 <= rows; r += 8) {
+      const uint16_t* w0 = w + (uint64_t)r * (uint64_t)cols;
+      float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+      for (int32_t cc = 0; cc < cols; ++cc) {
+        const float xv = x[cc];
+        a[0] = a[0] + bf16_to_f32(w0[cc]) * xv;
+        a[1] = a[1] + bf16_to_f32(w0[cols + cc]) * xv;
+        a[2] = a[2] + bf16_to_f32(w0[2 * (uint64_t)cols + cc]) * xv;
+        a[3] = a[3] + bf16_to_f32(w0[3 * (uint64_t)cols + cc]) * xv;
+        a[4] = a[4] + bf16_to_f32(w0[4 * (uint64_t)cols + cc]) * xv;
+        a[5] = a[5] + bf16_to_f32(w0[5 * (uint64_t)cols + cc]) * xv;
+        a[6] = a[6] + bf16_to_f32(w0[6 * (uint64_t)cols + cc]) * xv;
+        a[7] = a[7] + bf16_to_f32(w0[7 * (uint64_t)cols + cc]) * xv;
+      }
+      for (int32_t k = 0; k < 8; ++k) y[r + k] = a[k];
+    }
+  }
+  for (; r < rows; ++r) {
+    const uint64_t base = off + (uint64_t)r * (uint64_t)cols;
     float acc = 0.0f;
     for (int32_t cc = 0; cc < cols; ++cc) acc = acc + W(M, base + (uint64_t)cc) * x[cc];
     y[r] = acc;

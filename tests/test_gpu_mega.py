@@ -1,0 +1,64 @@
+"""Batch-1 steps as one persistent kernel (all layers, the head and the greedy draw), against the
+oracle and against the per-operation kernels of the same handle configuration."""
+import numpy as np
+import pytest
+
+import llama_architecture_kv_gb300 as pkg
+import oracle
+import synth
+from synth import WORKLOADS, shrink
+
+pytestmark = pytest.mark.gpu
+
+BF16_ABS = 3e-2
+
+CASES = [
+    ("llama_like_hd128_g4", shrink(WORKLOADS["llama8b_b1"].shape, layers=2, kv=2, ffn=512, vocab=1000)),
+    ("smol135_like_hd64_g3", shrink(WORKLOADS["smollm2_135m"].shape, layers=2, ffn=256, vocab=700)),
+    ("smol17_like_hd64_g1", shrink(WORKLOADS["smollm2_1_7b_b16"].shape, layers=2, kv=4, ffn=712, vocab=2500)),
+]
+
+
+@pytest.mark.parametrize("name,shape", CASES, ids=[c[0] for c in CASES])
+def test_step_kernel_matches_oracle(name, shape):
+    P, steps, cap = 40, 6, 64
+    blob = synth.model_blob(shape, 701)
+    g = pkg.Model(shape, blob, max_batch=1, max_seq=cap)
+    assert pkg.llm_step_kernels(g.h, 1, 0.0) == 3  # prologue, embedding, the persistent kernel
+    toks = synth.tokens(702, 0, P, shape.vocab)
+    ref = oracle.Model(oracle.cfg_of(shape, 1, cap), blob)
+    lg = g.prefill(toks[None], 0)[0]
+    lo = ref.prefill(0, toks, 0)
+    assert float(np.max(np.abs(lg - lo))) <= BF16_ABS
+    cur = int(np.argmax(lg))
+    agree = []
+    for s in range(steps):
+        ids, lg = g.step(np.array([cur], np.int32), P + s, logits=True)
+        lo = ref.forward(0, cur, P + s)
+        assert float(np.max(np.abs(lg[0] - lo))) <= BF16_ABS, (name, s)
+        assert int(ids[0]) == oracle.argmax(lg[0])  # the kernel's own argmax of its logits
+        agree.append(int(ids[0]) == oracle.argmax(lo))
+        cur = int(ids[0])
+    assert np.mean(agree) >= 0.99 or len(agree) - sum(agree) <= 1
+    ref.close()
+    g.close()
+
+
+@pytest.mark.parametrize("name,shape", CASES, ids=[c[0] for c in CASES])
+def test_step_kernel_agrees_with_per_operation_kernels(name, shape):
+    P, cap = 37, 64
+    blob = synth.model_blob(shape, 703)
+    toks = synth.tokens(704, 0, P + 1, shape.vocab)
+    outs = []
+    for sk in (0, -1):
+        g = pkg.Model(shape, blob, max_batch=1, max_seq=cap, step_kernel=sk)
+        g.prefill(toks[None, :P], 0, logits=False)
+        ids, lg = g.step(toks[P:P + 1], P, logits=True)
+        u = synth.uniforms(705, 0, 1)
+        sid = g.step(toks[P:P + 1], P, 0.8, 50, 0.9, u)
+        assert int(sid[0]) == oracle.sample(lg[0], 0.8, 50, 0.9, float(u[0]))
+        outs.append(lg[0])
+        g.close()
+    # the projections are the same sums in the same order; attention differs (f32 on CUDA cores
+    # here, bf16 hi + lo tensor-core MMAs there), so the logits agree to a few ulps of their range
+    assert float(np.max(np.abs(outs[0] - outs[1]))) <= 2e-3
