@@ -1280,4 +1280,323 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   return cudaLaunchKernelEx(&cfg, fn, kmap, a);
 }
 
+// ---------------------------------------------------------------------------------------
+// Causal attention of a prefill pass (Llama 3.1 8B Instruct card, attention.linnet prefill<S>:
+// token i of a prompt at position pos + i sees the positions s <= pos + i; bend-ml-llama law
+// causal).  The entries of a pass come in tiles: up to 64 / g consecutive prompt tokens of one
+// cache row, at consecutive positions, with one attention start (0, or the prompt's first
+// position for packed prompts).  A unit is (tile, kv head j): its columns are the (token, head)
+// pairs t * g + h, and the keys and values of positions start .. the tile's last position are
+// streamed once for all of them -- instead of once per token as a decode step would.
+//
+// One CTA per SM walks the units (the host sorts them longest first, CTA c takes c, c + G, ...).
+// A producer warp streams 16-position chunks of the unit's keys and values through a ring of
+// shared-memory stages (TMA tensor copies, 128-byte swizzle; full / empty mbarriers), running on
+// into the next unit; eight consumer warps each own 8 of the tile's 64 columns and read every
+// chunk: scores S^T = K Q^T (rows = the chunk's 16 positions, columns = the warp's 8 (token,
+// head) pairs; the queries as bf16 hi + lo B fragments), an online softmax per column with the
+// causal mask start <= s <= that token's position, and O^T += V^T P^T (the weights as hi + lo B
+// fragments).  A warp owns its columns' whole key range, so it writes o / l straight to the
+// output; nothing is merged across CTAs.  Every wait is bounded; after one runs out the CTA
+// records kErrDeviceTimeout and its warps stop waiting (they still pass the same barriers).
+// ---------------------------------------------------------------------------------------
+
+constexpr int kPfWarps = 8;              // consumer warps, 8 columns each
+constexpr int kPfCols = kPfWarps * 8;    // (token, head) columns of a tile
+constexpr int kPfStages = 8;             // ring stages (16 positions of keys and values each)
+
+template <int HD>
+struct PfShape {
+  static constexpr int ROWB = HD * 2;
+  static constexpr int NBOX = ROWB / 128;
+  static constexpr int STAGE = 2 * kMmaChunk * ROWB;  // keys, then values
+  static constexpr int QP = HD + 8;                    // padded query row (elements)
+  static constexpr int KS = HD / 16;
+  static constexpr int DT = HD / 16;
+};
+
+template <int HD>
+LLM_HD size_t attn_prefill_smem() {
+  using P = PfShape<HD>;
+  return 1024 + (size_t)kPfStages * P::STAGE + 2 * (size_t)kPfCols * P::QP * 2 + 2 * kPfStages * 8;
+}
+
+int attn_prefill_tile_tokens(int g) { return kPfCols / g; }
+
+template <int HD>
+__global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const AttnPrefillArgs a) {
+  using P = PfShape<HD>;
+  constexpr int ROWB = P::ROWB, STAGE = P::STAGE, QP = P::QP, KS = P::KS, DT = P::DT;
+  constexpr int CH = kMmaChunk;
+  extern __shared__ unsigned char praw[];
+  const uint32_t s_raw = smem_u32(praw);
+  unsigned char* base = praw + (((s_raw + 1023u) & ~1023u) - s_raw);
+  const uint32_t s_base = smem_u32(base);
+  uint16_t* qbase = reinterpret_cast<uint16_t*>(base + (size_t)kPfStages * STAGE);  // [hi, lo][64][QP]
+  const uint32_t FULL0 = smem_u32(qbase + 2 * kPfCols * QP);
+  const uint32_t EMPTY0 = FULL0 + 8u * kPfStages;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, mr = lane & 7;
+  const int g = a.g;
+  const int nunits = a.tiles[0];
+  const int4* tiles = reinterpret_cast<const int4*>(a.tiles + 4);
+  const int2* units = reinterpret_cast<const int2*>(a.tiles + 4 + 4 * a.max_tiles);
+
+  if (tid == 0) {
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(FULL0 + 8u * s, 1);
+      mbar_init(EMPTY0 + 8u * s, kPfWarps);
+    }
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // the queries and the cache positions of this pass are written by the Q/K/V kernel
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // unit u: tile (first entry e0, tokens nq, cache row, attention start), kv head j, positions
+  // P0 .. P0 + nq - 1, chunks [k0, k1) covering positions start .. P0 + nq - 1
+  struct Unit {
+    int e0, nq, row, start, j, P0, k0, k1;
+  };
+  auto unit = [&](int u) {
+    Unit U;
+    const int2 uj = units[u];
+    const int4 t = tiles[uj.x];
+    U.e0 = t.x; U.nq = t.y; U.row = t.z; U.start = t.w; U.j = uj.y;
+    U.P0 = row_pos(a.step, U.e0);
+    U.k0 = U.start / CH;
+    U.k1 = (U.P0 + U.nq - 1) / CH + 1;
+    return U;
+  };
+  auto fail = [&]() {
+    if (!s_abort) {
+      s_abort = 1;
+      atomicCAS(a.status, 0, kErrDeviceTimeout);
+    }
+  };
+
+  if (warp == kPfWarps) {
+    // ---- producer ----
+    if (lane == 0) {
+      tma_prefetch_map(&kmap);
+      tma_prefetch_map(&vmap);
+      int it = 0;
+      for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+        const Unit U = unit(u);
+        for (int k = U.k0; k < U.k1; ++k, ++it) {
+          const int s = it % kPfStages;
+          if (it >= kPfStages && !s_abort &&
+              !mbar_wait(EMPTY0 + 8u * s, (uint32_t)(it / kPfStages - 1) & 1u, kAttnWaitCycles))
+            fail();
+          if (s_abort) break;
+          const int krow = a.krow0 + (U.row * a.kv + U.j) * a.cap + k * CH;
+          const uint32_t dst = s_base + (uint32_t)(s * STAGE);
+          fence_proxy_async_smem();
+          mbar_expect_tx(FULL0 + 8u * s, (uint32_t)STAGE);
+#pragma unroll
+          for (int bx = 0; bx < P::NBOX; ++bx) {
+            tma_load_2d(dst + (uint32_t)(bx * CH * 128), &kmap, FULL0 + 8u * s, bx * 64, krow);
+            tma_load_2d(dst + (uint32_t)(CH * ROWB + bx * CH * 128), &vmap, FULL0 + 8u * s, bx * 64, krow);
+          }
+        }
+        if (s_abort) break;
+      }
+      // no copy may still be writing shared memory when the CTA exits
+      for (int i = it > kPfStages ? it - kPfStages : 0; i < it; ++i)
+        mbar_wait(FULL0 + 8u * (i % kPfStages), (uint32_t)(i / kPfStages) & 1u, kAttnWaitCycles);
+    }
+    return;
+  }
+
+  // ---- consumers: warp w owns columns 8w .. 8w + 7 ----
+  int it = 0;
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+    const Unit U = unit(u);
+    named_sync(1, kPfWarps * 32);  // the previous unit's readers of the queries are done
+    {
+      // the tile's queries as bf16 hi + lo, columns t * g + h, padding columns zero
+      uint16_t* qh = qbase;
+      uint16_t* ql = qh + kPfCols * QP;
+      for (int i = tid; i < kPfCols * HD / 2; i += kPfWarps * 32) {
+        const int col = (2 * i) / HD, e = (2 * i) - col * HD;
+        const int t = col / g, h = col - t * g;
+        float x0 = 0.f, x1 = 0.f;
+        if (t < U.nq) {
+          const float2 v = *reinterpret_cast<const float2*>(a.q + (size_t)(U.e0 + t) * a.q_stride +
+                                                            (size_t)(U.j * g + h) * HD + e);
+          x0 = v.x;
+          x1 = v.y;
+        }
+        uint32_t hi, lo;
+        split_bf16x2(x0, x1, hi, lo);
+        *reinterpret_cast<uint32_t*>(qh + col * QP + e) = hi;
+        *reinterpret_cast<uint32_t*>(ql + col * QP + e) = lo;
+      }
+    }
+    named_sync(1, kPfWarps * 32);
+    uint32_t qfh[KS][2], qfl[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ks += 2) {
+      const uint32_t off = (uint32_t)(((warp * 8 + mr) * QP + ks * 16 + mi * 8) * 2);
+      uint32_t r[4];
+      ldsm_x4(smem_u32(qbase) + off, r);
+      qfh[ks][0] = r[0]; qfh[ks][1] = r[1]; qfh[ks + 1][0] = r[2]; qfh[ks + 1][1] = r[3];
+      ldsm_x4(smem_u32(qbase + kPfCols * QP) + off, r);
+      qfl[ks][0] = r[0]; qfl[ks][1] = r[1]; qfl[ks + 1][0] = r[2]; qfl[ks + 1][1] = r[3];
+    }
+    // this lane's two columns: token, its position (the last key it sees), whether it exists
+    int pc[2];
+    bool cv[2];
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      const int col = warp * 8 + 2 * tig + hc, t = col / g;
+      cv[hc] = t < U.nq;
+      pc[hc] = U.P0 + t;
+    }
+    const int plast = U.P0 + U.nq - 1;
+    float o[DT][4];
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    for (int k = U.k0; k < U.k1; ++k, ++it) {
+      const int s = it % kPfStages;
+      if (!s_abort) {
+        const bool w = __all_sync(0xffffffffu, mbar_wait(FULL0 + 8u * s, (uint32_t)(it / kPfStages) & 1u, kAttnWaitCycles));
+        if (!w && lane == 0) fail();
+        __syncwarp();
+      }
+      const int kb = k * CH;
+      const uint32_t kreg = s_base + (uint32_t)(s * STAGE);
+      const uint32_t vreg = kreg + (uint32_t)(CH * ROWB);
+      // scores: rows = positions kb + 0..15, columns = this warp's 8
+      float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t ka[4];
+        ldsm_x4(kreg + swz_off((mi & 1) * 8 + mr, 2 * ks + (mi >> 1)), ka);
+        mma_bf16_16816(sh, ka, qfh[ks][0], qfh[ks][1]);
+        mma_bf16_16816(sl, ka, qfl[ks][0], qfl[ks][1]);
+      }
+      float p[4], corr[2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int pos = kb + gid + 8 * (i >> 1), hc = i & 1;
+        p[i] = (cv[hc] && pos >= U.start && pos <= pc[hc]) ? (sh[i] + sl[i]) * a.scale : -INFINITY;
+      }
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float mx = fmaxf(p[hc], p[2 + hc]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(mrow[hc], mx);  // -inf while the column has seen no position
+        corr[hc] = mrow[hc] == -INFINITY ? 0.f : expf(mrow[hc] - mnew);
+        mrow[hc] = mnew;
+        const float w0 = p[hc] == -INFINITY ? 0.f : expf(p[hc] - mnew);
+        const float w1 = p[2 + hc] == -INFINITY ? 0.f : expf(p[2 + hc] - mnew);
+        p[hc] = w0;
+        p[2 + hc] = w1;
+        lrow[hc] = fmaf(lrow[hc], corr[hc], w0 + w1);
+      }
+      if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          o[dt][0] *= corr[0];
+          o[dt][1] *= corr[1];
+          o[dt][2] *= corr[0];
+          o[dt][3] *= corr[1];
+        }
+      }
+      // the weights as B fragments (k = positions, n = columns), gathered from the score
+      // fragments: lane (gid = column, tig = t) takes positions 2t, 2t + 1 (and + 8)
+      uint32_t pfh[2], pfl[2];
+      {
+        const int sa = 8 * tig + (gid >> 1), sb = sa + 4;
+        const bool odd = gid & 1;
+        const float a0 = __shfl_sync(0xffffffffu, p[0], sa), a1 = __shfl_sync(0xffffffffu, p[1], sa);
+        const float a2 = __shfl_sync(0xffffffffu, p[2], sa), a3 = __shfl_sync(0xffffffffu, p[3], sa);
+        const float b0 = __shfl_sync(0xffffffffu, p[0], sb), b1 = __shfl_sync(0xffffffffu, p[1], sb);
+        const float b2 = __shfl_sync(0xffffffffu, p[2], sb), b3 = __shfl_sync(0xffffffffu, p[3], sb);
+        split_bf16x2(odd ? a1 : a0, odd ? b1 : b0, pfh[0], pfl[0]);
+        split_bf16x2(odd ? a3 : a2, odd ? b3 : b2, pfh[1], pfl[1]);
+      }
+      // positions outside start .. plast hold other data (possibly not finite): their value
+      // elements are zeroed in the A fragments (keys 2 tig, 2 tig + 1 in a0 / a1, + 8 in a2 / a3)
+      const bool edge = kb < U.start || kb + CH - 1 > plast;
+      uint32_t km0 = 0xffffffffu, km1 = 0xffffffffu;
+      if (edge) {
+        const int p0 = kb + 2 * tig, p8 = p0 + 8;
+        km0 = (p0 >= U.start && p0 <= plast ? 0x0000ffffu : 0u) | (p0 + 1 >= U.start && p0 + 1 <= plast ? 0xffff0000u : 0u);
+        km1 = (p8 >= U.start && p8 <= plast ? 0x0000ffffu : 0u) | (p8 + 1 >= U.start && p8 + 1 <= plast ? 0xffff0000u : 0u);
+      }
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) {
+        uint32_t va[4];
+        ldsm_x4_t(vreg + swz_off((mi >> 1) * 8 + mr, 2 * dt + (mi & 1)), va);
+        va[0] &= km0;
+        va[1] &= km0;
+        va[2] &= km1;
+        va[3] &= km1;
+        mma_bf16_16816(o[dt], va, pfh[0], pfh[1]);
+        mma_bf16_16816(o[dt], va, pfl[0], pfl[1]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(EMPTY0 + 8u * s);
+    }
+    // the unit's end: o / l of each of this lane's columns
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      float l = lrow[hc];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      if (!cv[hc]) continue;
+      const int col = warp * 8 + 2 * tig + hc, t = col / g, h = col - t * g;
+      float* ob = a.out + (size_t)(U.e0 + t) * a.out_stride + (size_t)(U.j * g + h) * HD;
+      const float rl = 1.0f / l;
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) {
+        ob[dt * 16 + gid] = o[dt][hc] * rl;
+        ob[dt * 16 + gid + 8] = o[dt][2 + hc] * rl;
+      }
+    }
+  }
+}
+
+bool attn_prefill_supported(int kt, int hd, int g) { return kt == 1 && (hd == 64 || hd == 128) && g >= 1 && g <= 8; }
+
+cudaError_t attn_prefill_prepare(int max_smem_optin) {
+  for (auto fn : {attn_prefill_kernel<64>, attn_prefill_kernel<128>}) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_attn_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnPrefillArgs& a, int grid,
+                                cudaStream_t s, bool pdl) {
+  if (!attn_prefill_supported(1, a.hd, a.g)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3((kPfWarps + 1) * 32);
+  cfg.dynamicSmemBytes = a.hd == 64 ? attn_prefill_smem<64>() : attn_prefill_smem<128>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.hd == 64) return cudaLaunchKernelEx(&cfg, attn_prefill_kernel<64>, kmap, vmap, a);
+  return cudaLaunchKernelEx(&cfg, attn_prefill_kernel<128>, kmap, vmap, a);
+}
+
 }  // namespace llm

@@ -43,4 +43,28 @@ bool attn_cluster_merge(int kt, int hd, int g, int ns, int clusters, int cap);
 cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a, int kt, cudaStream_t s,
                         bool pdl);
 
+// Causal attention of a prefill pass over tiles of consecutive prompt tokens (bf16 caches, head
+// size 64 or 128, at most 8 query heads per kv head).  tiles: int32 [4 + 4 * max_tiles + 2 *
+// max_tiles * kv] = {units, tiles, 0, 0}, then per tile {first entry, tokens, cache row,
+// attention start}, then per unit {tile, kv head}, units longest first.  A tile holds at most
+// attn_prefill_tile_tokens(g) tokens of one cache row at consecutive positions.
+struct AttnPrefillArgs {
+  const float* q;        // rotated queries of the pass's entries [n][q_stride]
+  int32_t q_stride;
+  float* out;            // [n][out_stride]
+  int32_t out_stride;
+  const int32_t* tiles;  // device memory, layout above
+  int32_t max_tiles;
+  int32_t krow0;         // row of this layer's position 0 of (cache row 0, kv head 0) in the maps
+  int32_t kv, g, hd, cap;
+  float scale;
+  const StepState* step; // entry positions (row_pos)
+  int32_t* status;
+};
+bool attn_prefill_supported(int kt, int hd, int g);
+int attn_prefill_tile_tokens(int g);
+cudaError_t attn_prefill_prepare(int max_smem_optin);
+cudaError_t launch_attn_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnPrefillArgs& a, int grid,
+                                cudaStream_t s, bool pdl);
+
 }  // namespace llm

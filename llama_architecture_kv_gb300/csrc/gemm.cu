@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t s_raw = smem_u32(tc_smem);
   const uint32_t s_base = (s_raw + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 bytes
   uint8_t* g_base = tc_smem + (s_base - s_raw);
-  const int NP = a.NP, KB = a.KB, S = a.S, MT = a.MT, NT = a.n_tile;
+  const int NP = a.NP, KB = a.KB, S = a.S, NT = a.n_tile;
   const uint32_t kTcW = (uint32_t)NT * 128u;   // weight tile: NT rows x 128 bytes
   const uint32_t kTcStage = kTcA + kTcW;
   float* xchg = reinterpret_cast<float*>(g_base + kTcStages * kTcStage);  // [64][kXchgPitch]

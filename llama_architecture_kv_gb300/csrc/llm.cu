@@ -247,8 +247,9 @@ struct TcMaps {
 
 struct GraphKey {
   int B, mode, gen;  // gen: steps of a generation graph (0: one step after a host prologue)
+  int pass;          // 1: a prefill pass (its rows are prompt tokens with attention ranges)
   bool operator<(const GraphKey& o) const {
-    return B != o.B ? B < o.B : mode != o.mode ? mode < o.mode : gen < o.gen;
+    return B != o.B ? B < o.B : mode != o.mode ? mode < o.mode : gen != o.gen ? gen < o.gen : pass < o.pass;
   }
 };
 
@@ -283,10 +284,13 @@ struct llm_handle {
   GenState* gen = nullptr;     // generation: the state of the graph launch in flight
   int32_t* page_table = nullptr;  // paged steps: [max_batch][max_seq / kPage] (max_seq % kPage == 0)
   int32_t* range_buf = nullptr;   // prefill passes: [3][NT] attention starts, first written positions, cache rows
+  int32_t* tile_buf = nullptr;    // prefill passes: the causal attention's tiles and units (attention.cuh)
+  bool pf_attn = false;           // prefill passes run the tiled causal attention (bf16, head 64 / 128)
   float* xh = nullptr;            // [max_batch][d] final residual rows gathered for the LM head
   int32_t* head_map = nullptr;    // [max_batch] the entries those rows come from
   // batch-1 steps in one persistent kernel (bf16, supported shapes)
   bool mega = false;
+  bool capturing_pass = false;  // the graph being captured is a prefill pass (never the persistent kernel)
   MegaLayer* mega_layers = nullptr;  // [L], device
   float* mega_part = nullptr;        // attention partials [H][kMegaMaxSplits][hd + 2]
   uint32_t* mega_ticket = nullptr;   // [kv + 1]
@@ -629,6 +633,15 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin;
     a.status = h->status;
     CUDA_TRY(h, launch_gemv(a, p, wt, EPI_QKV, true, h->stream, pdl));
+  } else if (which == K_ATTN && h->capturing_pass && h->pf_attn) {
+    // a prefill pass: tiles of consecutive prompt tokens share each key/value stream
+    AttnPrefillArgs pa = {};
+    pa.q = h->q; pa.q_stride = h->d; pa.out = h->attn; pa.out_stride = h->d;
+    pa.tiles = h->tile_buf; pa.max_tiles = h->NT;
+    pa.krow0 = (int32_t)((size_t)l * c.max_batch * c.kv_heads * c.max_seq);
+    pa.kv = c.kv_heads; pa.g = c.group; pa.hd = h->hd; pa.cap = c.max_seq; pa.scale = 1.0f / sqrtf((float)h->hd);
+    pa.step = h->st; pa.status = h->status;
+    CUDA_TRY(h, launch_attn_prefill(h->kmap, h->vmap, pa, h->num_sms, h->stream, pdl));
   } else if (which == K_ATTN) {
     const int ns = attn_splits(B, c.kv_heads, c.max_seq, h->num_sms);
     if (ns > h->part_ns) return fail(h, LLM_ERR_ARG, "internal: attention splits %d > %d", ns, h->part_ns);
@@ -677,7 +690,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
 llm_status launch_layer_kernels(llm_handle* h, int B, int mode, bool pdl, bool trace) {
   const llm_config& c = h->cfg;
   TRY(launch_one(h, K_EMBED, 0, B, false));
-  if (h->mega && B == 1 && !trace) {
+  if (h->mega && B == 1 && !trace && !h->capturing_pass) {
     // every layer, the head and a greedy draw in one persistent kernel; a top-k top-p draw after
     MegaArgs a = {};
     a.layers = h->mega_layers; a.L = h->L; a.d = h->d; a.f = h->f; a.V = h->V; a.H = h->H; a.kv = c.kv_heads;
@@ -712,8 +725,9 @@ llm_status launch_layer_kernels(llm_handle* h, int B, int mode, bool pdl, bool t
 
 // the step graph of (B, mode), captured on first use; with gen > 0, a generation graph of gen
 // steps, each its own prologue (gen_begin_kernel), the step's kernels and gen_end_kernel
-llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t, int>** out, int gen = 0) {
-  GraphKey key{B, mode, gen};
+llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t, int>** out, int gen = 0,
+                      bool pass = false) {
+  GraphKey key{B, mode, gen, pass ? 1 : 0};
   auto it = h->graphs.find(key);
   if (it == h->graphs.end()) {
     // capture on a private stream, then replay on the handle's stream
@@ -721,6 +735,7 @@ llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t,
     h->stream = h->cap_stream;
     CUDA_TRY(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
     llm_status s = LLM_OK;
+    h->capturing_pass = pass;
     if (gen == 0) {
       s = launch_layer_kernels(h, B, mode, true, false);
     } else {
@@ -730,6 +745,7 @@ llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t,
         if (s == LLM_OK) gen_end_kernel<<<1, 128, 0, h->stream>>>(h->gen, h->ids_buf, i);
       }
     }
+    h->capturing_pass = false;
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(h->stream, &graph);
     h->stream = saved;
@@ -750,10 +766,10 @@ llm_status step_graph(llm_handle* h, int B, int mode, std::pair<cudaGraphExec_t,
   return LLM_OK;
 }
 
-llm_status run_step(llm_handle* h, int B, int mode) {
+llm_status run_step(llm_handle* h, int B, int mode, bool pass = false) {
   if (h->cfg.debug_trace) return launch_layer_kernels(h, B, mode, false, true);
   std::pair<cudaGraphExec_t, int>* g = nullptr;
-  TRY(step_graph(h, B, mode, &g));
+  TRY(step_graph(h, B, mode, &g, 0, pass));
   CUDA_TRY(h, cudaGraphLaunch(g->first, h->stream));
   return LLM_OK;
 }
@@ -951,6 +967,9 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     h->tc_min = tc_min;
   }
   if ((ce = attn_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("attention kernel attributes", ce);
+  h->pf_attn = attn_prefill_supported(h->wt, 2 * c.half, c.group);
+  if (h->pf_attn && (ce = attn_prefill_prepare(h->smem_optin)) != cudaSuccess)
+    return cuda_bail("prefill attention kernel attributes", ce);
   // the allocation-free sampler's array is reserved here, where allocating is allowed
   if ((ce = noalloc_prepare()) != cudaSuccess) return cuda_bail("allocation-free sampler set-up", ce);
   // weights: a device copy of the blob when it is on the host, then repacked
@@ -1006,6 +1025,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
       (st = dalloc(h, &h->u_gen, (size_t)kGenChunk * B * 4)) || (st = dalloc(h, &h->ids_gen, (size_t)kGenChunk * B * 4)) ||
       (c.max_seq % kPage == 0 && (st = dalloc(h, &h->page_table, B * (size_t)(c.max_seq / kPage) * 4))) ||
       (st = dalloc(h, &h->range_buf, 3 * NT * 4)) ||
+      (st = dalloc(h, &h->tile_buf, (4 + 4 * NT + 2 * NT * (size_t)c.kv_heads) * 4)) ||
       (st = dalloc(h, &h->status, 16)) || (st = dalloc(h, &h->tok_buf, NT * 4)) || (st = dalloc(h, &h->u_buf, NT * 4)) ||
       (st = dalloc(h, &h->ids_buf, B * 4)))
     return bail(st);
@@ -1102,8 +1122,10 @@ llm_status llm_synchronize(llm_handle* h) {
   if (s != 0) {
     CUDA_TRY(h, cudaMemset(h->status, 0, 4));
     // a kernel that gave up may have left the attention's merge tickets short of their count
-    if (s == LLM_ERR_DEVICE_TIMEOUT)
+    if (s == LLM_ERR_DEVICE_TIMEOUT) {
       CUDA_TRY(h, cudaMemset(h->ticket, 0, (size_t)h->ticket_count * 4));
+      if (h->mega_ticket) CUDA_TRY(h, cudaMemset(h->mega_ticket, 0, ((size_t)h->cfg.kv_heads + 1) * 4));
+    }
     return fail(h, s, "device reported: %s", llm_status_string(s));
   }
   return LLM_OK;
@@ -1185,9 +1207,47 @@ static llm_status pass_logits(llm_handle* h, int n, const std::vector<int32_t>& 
 static llm_status run_pass(llm_handle* h, int n, const int32_t* tok_host, const int32_t* tok_dev, int tok_stride,
                            int tok_col, int tok_np, const int32_t* pos_host, const int32_t* ranges_host) {
   CUDA_TRY(h, cudaMemcpyAsync(h->range_buf, ranges_host, (size_t)3 * n * 4, cudaMemcpyHostToDevice, h->stream));
+  if (h->pf_attn) {
+    // tiles: runs of at most qt entries of one cache row with one attention start at consecutive
+    // positions; units (tile, kv head), longest key range first
+    const int qt = attn_prefill_tile_tokens(h->cfg.group), kv = h->cfg.kv_heads, NT = h->NT;
+    const int32_t* start = ranges_host;
+    const int32_t* row = ranges_host + 2 * (size_t)n;
+    std::vector<int32_t> tb(4 + 4 * (size_t)NT + 2 * (size_t)NT * kv, 0);
+    int nt = 0;
+    for (int e = 0; e < n; ++e) {
+      int32_t* t = &tb[4 + 4 * (size_t)(nt - 1 >= 0 ? nt - 1 : 0)];
+      if (nt > 0 && row[e] == t[2] && start[e] == t[3] && pos_host[e] == pos_host[e - 1] + 1 && t[1] < qt &&
+          t[0] + t[1] == e) {
+        ++t[1];
+      } else {
+        int32_t* nt_ = &tb[4 + 4 * (size_t)nt++];
+        nt_[0] = e; nt_[1] = 1; nt_[2] = row[e]; nt_[3] = start[e];
+      }
+    }
+    std::vector<int> order(nt);
+    for (int i = 0; i < nt; ++i) order[i] = i;
+    auto work = [&](int i) {
+      const int32_t* t = &tb[4 + 4 * (size_t)i];
+      return pos_host[t[0]] + t[1] - t[3];
+    };
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return work(x) > work(y); });
+    int32_t* units = &tb[4 + 4 * (size_t)NT];
+    int nu = 0;
+    for (int i : order)
+      for (int j = 0; j < kv; ++j) {
+        units[2 * nu] = i;
+        units[2 * nu + 1] = j;
+        ++nu;
+      }
+    tb[0] = nu;
+    tb[1] = nt;
+    CUDA_TRY(h, cudaMemcpyAsync(h->tile_buf, tb.data(), (4 + 4 * (size_t)NT + 2 * (size_t)nu) * 4,
+                                cudaMemcpyHostToDevice, h->stream));
+  }
   TRY(begin(h, 0, n, tok_host, tok_dev, tok_stride, tok_col, 0.0f, 1, 1.0f, nullptr, nullptr, pos_host, nullptr, 0,
             h->range_buf, tok_np));
-  return run_step(h, n, MODE_NOHEAD);
+  return run_step(h, n, MODE_NOHEAD, true);
 }
 
 static llm_status prefill_impl(llm_handle* h, const int32_t* tok_host, const int32_t* tok_dev, int32_t B, int32_t S,
@@ -1422,6 +1482,12 @@ static llm_status packed_impl(llm_handle* h, const int32_t* toks, const int32_t*
   std::vector<int> dst;
   for (int p0 = 0; p0 < P; p0 += cap_e) {
     const int n = std::min(cap_e, P - p0);
+    // inside a pass, the entries of one row in position order (runs of one prompt form the
+    // attention's tiles)
+    std::vector<int> pe(order.begin() + p0, order.begin() + p0 + n);
+    std::stable_sort(pe.begin(), pe.end(), [&](int x, int y) {
+      return rows[x] != rows[y] ? rows[x] < rows[y] : positions[x] < positions[y];
+    });
     etok.assign(n, 0);
     epos.assign(n, 0);
     eranges.assign(3 * (size_t)n, 0);
@@ -1429,7 +1495,7 @@ static llm_status packed_impl(llm_handle* h, const int32_t* toks, const int32_t*
     dst.clear();
     std::map<int, int> wfirst;  // row -> first position this pass writes in it
     for (int e = 0; e < n; ++e) {
-      const int i = order[p0 + e];
+      const int i = pe[e];
       etok[e] = toks[i];
       epos[e] = positions[i];
       eranges[e] = span[segments[i]].lo;
@@ -1441,7 +1507,7 @@ static llm_status packed_impl(llm_handle* h, const int32_t* toks, const int32_t*
         dst.push_back(m);
       }
     }
-    for (int e = 0; e < n; ++e) eranges[n + e] = wfirst[rows[order[p0 + e]]];
+    for (int e = 0; e < n; ++e) eranges[n + e] = wfirst[rows[pe[e]]];
     TRY(run_pass(h, n, etok.data(), nullptr, 1, 0, 1, epos.data(), eranges.data()));
     if (logits) TRY(pass_logits(h, n, ents, dst, logits, true));
     // (the host vectors are refilled for the next pass: its copies read them first)

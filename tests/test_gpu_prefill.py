@@ -43,7 +43,8 @@ def _check(lg, lo, f32):
 def _cache_close(gk, ok, f32, first_layer, what):
     """Cache rows against the oracle's.  bf16 caches: layer 0's keys and values come from the
     exact embeddings, so the two sides round the same f32 sums and differ only where the sum
-    lies within rounding of a bf16 tie (at most one unit in the last place); later layers read
+    lies within rounding of a bf16 tie (one unit in the last place, or the f32 sum's absolute
+    error for values near zero); later layers read
     attention over those cached values, so their inputs (and roundings) drift a little more.
     (The tensor cores accumulate the f32 sums in their own order and rounding, so a few per cent
     of the roundings differ by one unit even in layer 0.)"""
@@ -53,7 +54,9 @@ def _cache_close(gk, ok, f32, first_layer, what):
     fa, fb = synth.bf16_to_f32(gk), synth.bf16_to_f32(ok)
     same = float(np.mean(gk == ok))
     if first_layer:
-        assert np.all(np.abs(fa - fb) <= 2 ** -7 * np.abs(fb) + 1e-30), what
+        # one unit in the last place of the value, or a small absolute error of the f32 sum
+        # (values near zero)
+        assert np.all(np.abs(fa - fb) <= 2 ** -7 * np.abs(fb) + 1e-4 * np.max(np.abs(fb))), what
         assert same > 0.9, (what, same)
     else:
         assert np.max(np.abs(fa - fb)) <= 2 ** -6 * np.max(np.abs(fb)), (what, float(np.max(np.abs(fa - fb))))
