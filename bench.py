@@ -63,6 +63,8 @@ def parse():
                     help="prompt tokens per prefill pass (0: the library default)")
     ap.add_argument("--b32-steps", type=int, default=64,
                     help="default workload: also time this many batch-32 steps (0: skip)")
+    ap.add_argument("--step-kernel", type=int, default=0, choices=[0, 1],
+                    help="batch 1: 1 runs each step as one persistent kernel")
     return ap.parse_args()
 
 
@@ -351,12 +353,14 @@ def fill_cache(model, w, torch, stream, gpu_index):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_index) as clocks:
+        torch.cuda.nvtx.range_push(f"prefill_b{B}")  # (a profiler can select the timed region)
         e0.record(stream)
         t0 = time.perf_counter()
         model.prefill(prompt, 0, logits=True)
         wall = time.perf_counter() - t0
         e1.record(stream)
         e1.synchronize()
+        torch.cuda.nvtx.range_pop()
     ms = e0.elapsed_time(e1)
     return {"tokens": B * P, "batch": B, "prompt": P, "ms": ms, "tok_s": B * P / (ms / 1e3),
             "wall_ms": wall * 1e3, "max_tokens": int(model.cfg.max_tokens) or 512,
@@ -395,6 +399,7 @@ def time_steps(pkg, torch, h, w, B, pos0, K, W, dev, stream, local, world, first
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(local) as clocks:
+            torch.cuda.nvtx.range_push(f"decode_b{B}")  # (a profiler can select the timed region)
             e0.record(stream)
             if generate:
                 pkg.llm_generate_dev(h, tok[0], B, pos0, K, temp, k_, p_, u_dev[W:W + K], gen_ids[:K])
@@ -403,6 +408,7 @@ def time_steps(pkg, torch, h, w, B, pos0, K, W, dev, stream, local, world, first
                     step_dev(tok[i % 2], i, u_dev[W + i], tok[(i + 1) % 2])
             e1.record(stream)
             e1.synchronize()
+            torch.cuda.nvtx.range_pop()
         pkg.llm_synchronize(h)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
@@ -433,7 +439,8 @@ def run_ours(args):
     blob = synth.model_blob(s, w.seed_weights)
     log(f"[bench] weights generated: {blob.nbytes / 1e9:.2f} GB in {time.perf_counter() - t0:.1f} s")
     t0 = time.perf_counter()
-    model = pkg.Model(s, blob, max_batch=B, max_seq=cap, stream=stream.cuda_stream, max_tokens=args.max_tokens)
+    model = pkg.Model(s, blob, max_batch=B, max_seq=cap, stream=stream.cuda_stream, max_tokens=args.max_tokens,
+                      step_kernel=args.step_kernel)
     h = model.h
     log(f"[bench] model created in {time.perf_counter() - t0:.1f} s")
     t0 = time.perf_counter()

@@ -82,8 +82,9 @@ typedef struct llm_config {
                            S > 1, llm_prefill_packed): activations and attention scratch are sized
                            for max(max_batch, max_tokens) rows; 0: the library default (512) */
   int32_t step_kernel;  /* batch-1 steps with bf16 weights (head size 64 or 128, at most 8 query
-                           heads per kv head): 0 run all layers and the head as one persistent
-                           kernel where the device allows it; -1 one kernel per operation */
+                           heads per kv head): 1 run all layers and the head as one persistent
+                           kernel where the device allows it; 0 one kernel per operation (the
+                           default: faster at the 8B shape so far) */
 } llm_config;
 
 typedef struct llm_handle llm_handle;

@@ -1068,7 +1068,7 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     // batch-1 steps as one persistent kernel where the shape allows it and every CTA can be resident
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->dev);
-    if (coop && !c.debug_trace && c.step_kernel == 0 && h->num_sms >= c.kv_heads &&
+    if (coop && !c.debug_trace && c.step_kernel == 1 && h->num_sms >= c.kv_heads &&
         mega_supported(h->wt, h->hd, c.group, h->d, h->f) &&
         mega_smem(h->d, h->f) + 1024 <= (size_t)h->smem_optin && mega_prepare(h->smem_optin) == cudaSuccess) {
       if ((st = dalloc(h, &h->mega_layers, sizeof(MegaLayer) * (size_t)h->L)) ||

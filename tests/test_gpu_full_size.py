@@ -117,3 +117,124 @@ def test_smollm2_135m_full_workload_teacher_forced():
     assert np.mean(agree) >= 0.99
     g.close()
     ref.close()
+
+
+# ---------------------------------------------------------------------------------------
+# The workloads as the benchmark runs them (llm_prefill of the synthetic prompts, then decode
+# steps through llm_step), against oracle results stored under tests/golden/ (written offline by
+# tests/golden/make_fullsize.py, which runs only the oracle and the input generators: an 8B
+# prompt of 2048 positions is hours of single-core oracle work).  Checked rows are teacher-forced
+# with the oracle's own tokens; at every step the GPU logits at the stored indices and at the
+# oracle's 16 largest are within 3e-2 of the oracle's, the GPU draw equals the oracle sampler's on
+# the GPU logits, and the GPU argmax agrees with the oracle's on at least 99% of the checks.
+# ---------------------------------------------------------------------------------------
+
+import json  # noqa: E402
+import os  # noqa: E402
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(job):
+    path = os.path.join(GOLDEN, f"fullsize_{job}.json")
+    if not os.path.exists(path):
+        pytest.skip(f"stored oracle results {os.path.basename(path)} not written yet")
+    with open(path) as f:
+        return json.load(f)
+
+
+def _against(lg, rec, idx, what):
+    """lg: one row's GPU logits; rec: the stored oracle digest of the same step."""
+    err = float(np.max(np.abs(lg[idx] - np.asarray(rec["vals"], np.float32))))
+    top = np.asarray(rec["top_ids"])
+    err = max(err, float(np.max(np.abs(lg[top] - np.asarray(rec["top_vals"], np.float32)))))
+    assert err <= BF16_ABS, (what, err)
+    return int(np.argmax(lg)) == int(rec["argmax"])
+
+
+def _replay(w, B, P, golds, g, steps_key="steps", nsteps=None):
+    """Prefill the workload's prompts on the GPU, then teacher-forced decode steps; golds maps a
+    row to its stored oracle results."""
+    s = w.shape
+    temp, k, p = w.temp, (w.top_k or s.vocab), w.top_p
+    agree = []
+    if P:
+        prompt = synth.tokens(w.seed_tokens, 0, B * P, s.vocab).reshape(B, P)
+        lg = g.prefill(prompt, 0)
+        for b, gd in golds.items():
+            agree.append(_against(lg[b], gd["prefill"], np.asarray(gd["idx"]), ("prefill", b)))
+    t0 = max(P, w.fill)
+    toks = synth.tokens(w.seed_tokens, B * P, B, s.vocab)
+    n = nsteps or min(len(gd[steps_key]) for gd in golds.values())
+    for i in range(n):
+        for b, gd in golds.items():
+            assert int(toks[b]) == gd[steps_key][i]["tok"]
+        u = synth.uniforms(w.seed_uniform, i * B, B) if temp > 0 else None
+        ids, lg = g.step(toks, t0 + i, temp, k, p, u, logits=True)
+        toks = ids.copy()
+        for b, gd in golds.items():
+            rec = gd[steps_key][i]
+            agree.append(_against(lg[b], rec, np.asarray(gd["idx"]), (i, b)))
+            if temp > 0:
+                assert int(ids[b]) == oracle.sample(lg[b], temp, k, p, float(u[b]))
+                toks[b] = rec["id"]      # the oracle's draw feeds the next step
+            else:
+                assert int(ids[b]) == oracle.argmax(lg[b])
+                toks[b] = rec["argmax"]
+    assert np.mean(agree) >= 0.99, agree
+    return len(agree)
+
+
+def test_llama8b_b1_prefill_2048_and_16_greedy_steps_against_stored_oracle():
+    gd = _golden("llama8b_row0")
+    w = WORKLOADS["llama8b_b1"]
+    blob = synth.model_blob(w.shape, w.seed_weights)
+    g = pkg.Model(w.shape, blob, max_batch=1, max_seq=w.cap)
+    _replay(w, 1, w.prompt, {0: gd}, g)
+    g.close()
+
+
+def test_llama8b_b32_prefill_and_greedy_steps_rows_0_and_31_against_stored_oracle():
+    g0, g31 = _golden("llama8b_row0"), _golden("llama8b_row31")
+    w = WORKLOADS["llama8b_b32"]
+    blob = synth.model_blob(w.shape, w.seed_weights)
+    g = pkg.Model(w.shape, blob, max_batch=w.batch, max_seq=w.cap)
+    # row 0's batch-32 steps are stored under steps_llama8b_b32 of the row-0 file
+    gold0 = dict(g0, steps=g0["steps_llama8b_b32"])
+    _replay(w, w.batch, w.prompt, {0: gold0, 31: g31}, g)
+    g.close()
+
+
+def test_smollm2_1_7b_b16_prefill_and_sampled_steps_rows_0_7_15_against_stored_oracle():
+    golds = {b: _golden(f"smollm2_1_7b_row{b}") for b in (0, 7, 15)}
+    w = WORKLOADS["smollm2_1_7b_b16"]
+    blob = synth.model_blob(w.shape, w.seed_weights)
+    g = pkg.Model(w.shape, blob, max_batch=w.batch, max_seq=w.cap)
+    _replay(w, w.batch, w.prompt, golds, g)
+    g.close()
+
+
+def _long(name, rows, jobs):
+    golds = {b: _golden(j) for b, j in zip(rows, jobs)}
+    w = WORKLOADS[name]
+    s = w.shape
+    blob = synth.model_blob(s, w.seed_weights)
+    g = pkg.Model(s, blob, max_batch=w.batch, max_seq=w.cap)
+    z = np.zeros((s.kv, 1, s.hd), np.uint16)
+    for layer in range(s.layers):
+        for b in range(w.batch):
+            if b in golds:
+                k, v = synth.kv_values(w.seed_kv, layer, b, w.batch, s.kv, w.fill, s.hd, bf16=s.bf16)
+                g.kv_import(layer, b, 0, k, v)
+            elif layer == 0:
+                g.kv_import(0, b, w.fill - 1, z, z)
+    _replay(w, w.batch, 0, golds, g)
+    g.close()
+
+
+def test_llama8b_long_b1_sampled_steps_at_131072_against_stored_oracle():
+    _long("llama8b_long_b1", [0], ["llama8b_long_b1_row0"])
+
+
+def test_llama8b_long_b8_sampled_steps_at_32768_rows_0_and_7_against_stored_oracle():
+    _long("llama8b_long_b8", [0, 7], ["llama8b_long_b8_row0", "llama8b_long_b8_row7"])

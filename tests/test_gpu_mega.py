@@ -23,7 +23,7 @@ CASES = [
 def test_step_kernel_matches_oracle(name, shape):
     P, steps, cap = 40, 6, 64
     blob = synth.model_blob(shape, 701)
-    g = pkg.Model(shape, blob, max_batch=1, max_seq=cap)
+    g = pkg.Model(shape, blob, max_batch=1, max_seq=cap, step_kernel=1)
     assert pkg.llm_step_kernels(g.h, 1, 0.0) == 3  # prologue, embedding, the persistent kernel
     toks = synth.tokens(702, 0, P, shape.vocab)
     ref = oracle.Model(oracle.cfg_of(shape, 1, cap), blob)
@@ -50,7 +50,7 @@ def test_step_kernel_agrees_with_per_operation_kernels(name, shape):
     blob = synth.model_blob(shape, 703)
     toks = synth.tokens(704, 0, P + 1, shape.vocab)
     outs = []
-    for sk in (0, -1):
+    for sk in (1, 0):
         g = pkg.Model(shape, blob, max_batch=1, max_seq=cap, step_kernel=sk)
         g.prefill(toks[None, :P], 0, logits=False)
         ids, lg = g.step(toks[P:P + 1], P, logits=True)
