@@ -512,8 +512,8 @@ def run_ours(args):
     mean_pos = (float(np.mean(rowpos)) if rowpos is not None else pos0) + (K - 1) / 2
     wbytes, step_bytes = step_bytes_of(pkg, model.cfg, s, B, mean_pos)
     step_roof = step_roofline(step_bytes, B, peak, value / world, K, elapsed)
-    launches = (K * (pkg.llm_step_kernels(h, B, temp) + 1) + K // 8 + K % 8 if args.generate
-                else K * pkg.llm_step_kernels(h, B, temp))
+    launches = (K * (pkg.llm_step_kernels(h, B, temp, k_) + 1) + K // 8 + K % 8 if args.generate
+                else K * pkg.llm_step_kernels(h, B, temp, k_))
     model.close()
 
     cpu = None

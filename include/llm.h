@@ -296,10 +296,14 @@ llm_status llm_kv_export(llm_handle* h, int32_t layer, int32_t row, int32_t pos0
                          void* k_host, void* v_host);
 
 /*
- * Intermediates of the last decode step, kept only when created with debug_trace = 1
- * (the step then runs kernel by kernel, not as a graph).  name: "q" (rotated queries [B][d]),
- * "attn" (attention output [B][d]), "x1" (after o_proj + residual [B][d]), "m" (SwiGLU
- * [B][f]), "y" (layer output [B][d]).  dst_host receives [B][width] f32.
+ * Intermediates of the last decode step of layer `layer`, kept only when created with
+ * debug_trace = 1 (the step then runs kernel by kernel on the weight-streaming path, not as a
+ * graph).  Names after P1 "A layer" (Act): "n1" (attention_norm output [d]), "q" [d], "k" [kvw],
+ * "v" [kvw] (projections before RoPE, heads in order), "qr" [d] and "kr" [kvw] (after RoPE; "kr"
+ * in f32, before the cache's rounding), "attn" (attention output [d]), "a" (o_proj output
+ * [d]), "x1" (x + a [d]), "n2" (ffn_norm output [d]), "swiglu" (silu(gate) * up [f]), "m" (down
+ * projection output [d]), "y" (layer output x1 + m [d]).  dst_host receives [max_batch][width]
+ * f32 (rows past the step's B are stale).  LLM_ERR_ARG for an unknown name or layer.
  */
 llm_status llm_debug_trace(llm_handle* h, int32_t layer, const char* name, float* dst_host);
 
@@ -326,12 +330,14 @@ llm_status llm_profile_kernel(llm_handle* h, int32_t which, int32_t B, int32_t p
 llm_status llm_check_wait_timeout(llm_handle* h, int64_t limit_cycles);
 
 /*
- * How many kernels one llm_step / llm_step_dev of B rows launches at temperature temp (greedy
- * when temp == 0): the step prologue plus the kernels of the step's CUDA graph, which this call
- * captures if it does not exist yet (no kernel runs).  LLM_ERR_BATCH for B outside
- * 1..max_batch; LLM_ERR_ARG for handles created with debug_trace (they run without a graph).
+ * How many kernels one llm_step / llm_step_dev of B rows launches at temperature temp and top-k
+ * k (greedy when temp == 0; a draw with min(k, vocab) <= 1024 candidates is one selection
+ * kernel, a larger one the sort of the whole row): the step prologue plus the kernels of the
+ * step's CUDA graph, which this call captures if it does not exist yet (no kernel runs).
+ * LLM_ERR_BATCH for B outside 1..max_batch; LLM_ERR_ARG for handles created with debug_trace
+ * (they run without a graph).
  */
-llm_status llm_step_kernels(llm_handle* h, int32_t B, float temp, int32_t* kernels);
+llm_status llm_step_kernels(llm_handle* h, int32_t B, float temp, int32_t k, int32_t* kernels);
 
 /*
  * Sampling without a handle and without allocating: the same draw as llm_sample_dev (greedy

@@ -84,7 +84,7 @@ SIGNATURES = {
     "llm_debug_trace": ([_vp, _i32, ctypes.c_char_p, _vp], _i32),
     "llm_profile_kernel": ([_vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_f32)], _i32),
     "llm_sample_noalloc": ([_vp, _i32, _i32, _f32, _i32, _f32, _vp, _vp, _vp], _i32),
-    "llm_step_kernels": ([_vp, _i32, _f32, ctypes.POINTER(_i32)], _i32),
+    "llm_step_kernels": ([_vp, _i32, _f32, _i32, ctypes.POINTER(_i32)], _i32),
     "llm_check_wait_timeout": ([_vp, _i64], _i32),
     }
 
@@ -287,9 +287,9 @@ def llm_profile_kernel(h, which, B, pos, reps) -> float:
     return float(ms.value)
 
 
-def llm_step_kernels(h, B, temp) -> int:
+def llm_step_kernels(h, B, temp, k=1 << 30) -> int:
     n = ctypes.c_int32()
-    _check(h, lib().llm_step_kernels(h, B, temp, ctypes.byref(n)))
+    _check(h, lib().llm_step_kernels(h, B, temp, k, ctypes.byref(n)))
     return int(n.value)
 
 
@@ -434,7 +434,10 @@ class Model:
         return k, v
 
     def trace(self, layer, name):
-        w = self.shape.ffn if name == "m" else self.shape.d
+        """One intermediate of the last traced step: [max_batch][width] (include/llm.h lists the
+        names)."""
+        w = {"swiglu": self.shape.ffn, "k": self.shape.kvw, "v": self.shape.kvw,
+             "kr": self.shape.kvw}.get(name, self.shape.d)
         out = np.empty((self.cfg.max_batch, w), np.float32)
         llm_debug_trace(self.h, layer, name, out)
         return out

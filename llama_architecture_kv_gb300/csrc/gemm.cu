@@ -27,6 +27,7 @@
 // drain (bounded again), frees its tensor memory and returns.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gemm.cuh"
@@ -491,12 +492,15 @@ TcPlan plan_tc(int rows, int K, int B, int num_sms, bool whole) {
     p.n_tile = eff((long long)m128 * p.ntiles) > eff((long long)m256 * p.ntiles) + 1e-9 ? 128 : 256;
     p.S = 1;
   } else {
-    // splits: the most even fill of the SMs (units / (waves * SMs)), at least 4 K blocks a split
+    // splits: the most even fill of the SMs (units / (waves * SMs)), at least 4 K blocks a split.
+    // Split sums cost S * B * rows * 4 bytes written and read again: never more than a quarter
+    // of the weight bytes (many activation rows, as in a prefill pass, have tiles enough).
     p.n_tile = kTcN;
     const int base = p.ntiles * ((rows + kTcN - 1) / kTcN);
     double best = -1.0;
     p.S = 1;
-    for (int S = 1; S <= kMaxSplits && S <= p.KB; ++S) {
+    const int smax = std::max(1, std::min(kMaxSplits, K / (8 * B)));
+    for (int S = 1; S <= smax && S <= p.KB; ++S) {
       if (S > 1 && p.KB / S < 4) break;
       const double e = eff((long long)base * S);
       if (e > best + 1e-9) {

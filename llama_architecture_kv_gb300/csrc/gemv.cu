@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
           }
         }
         *reinterpret_cast<float4*>(xs + b * seg_cols + c) = v;
+        if (a.tr_in && blockIdx.x == 0 && b < nb)
+          *reinterpret_cast<float4*>(a.tr_in + (size_t)(b0 + b) * a.tr_stride + c0 + c) = v;
       }
       __syncthreads();
       const char* Wseg = Wb + (size_t)seg * a.seg_ch * 16;
@@ -282,6 +284,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
         const int head = R / a.hd, e = (R - head * a.hd) >> 1;
         const float x0 = acc[(2 * p) * BT + b], x1 = acc[(2 * p + 1) * BT + b];
         const size_t row = (size_t)(b0 + b);
+        if (a.tr_pre) {
+          a.tr_pre[row * a.tr_stride + (size_t)head * a.hd + e] = x0;
+          a.tr_pre[row * a.tr_stride + (size_t)head * a.hd + e + half] = x1;
+        }
         if (head < a.H + a.kv) {
           const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];
           const float lo = __fadd_rn(__fmul_rn(x0, c), __fmul_rn(-x1, s));
@@ -291,6 +297,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
             q[e] = lo;
             q[e + half] = hi;
           } else {
+            if (a.tr_rot) {
+              a.tr_rot[row * a.tr_stride + (size_t)(head - a.H) * a.hd + e] = lo;
+              a.tr_rot[row * a.tr_stride + (size_t)(head - a.H) * a.hd + e + half] = hi;
+            }
             int r, pp;
             cache_slot(a.step, a.cap, (int)row, pos, r, pp);
             const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H)) * a.cap + pp) * a.hd;
@@ -318,6 +328,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
         const int b = i / nrows, r = i - b * nrows;
         const float rv = a.resid[(size_t)(b0 + b) * a.resid_stride + r0 + r];
         a.out[(size_t)(b0 + b) * a.out_stride + r0 + r] = __fadd_rn(rv, acc[r * BT + b]);
+        if (a.tr_pre) a.tr_pre[(size_t)(b0 + b) * a.tr_stride + r0 + r] = acc[r * BT + b];
       }
     } else {
       for (int i = tid; i < nrows * nb; i += kGemvThreads) {
@@ -672,7 +683,7 @@ cudaError_t gemv_prepare(int max_smem_optin) {
 
 cudaError_t launch_gemv(const GemvArgs& a, const GemvPlan& p, int wt, int epi, bool norm,
                         cudaStream_t s, bool pdl) {
-  if (p.tma_ns > 0 && a.B == 1) {
+  if (p.tma_ns > 0 && a.B == 1 && !a.tr_in && !a.tr_pre) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.tma_grid);
     cfg.blockDim = dim3(kTmaWarps * 32);

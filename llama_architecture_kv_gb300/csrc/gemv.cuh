@@ -39,6 +39,11 @@ struct GemvArgs {
   const float* rope_cos;  // [cap][hd/2]
   const float* rope_sin;
   int32_t* status;      // device error flag (a bounded wait that ran out)
+  // intermediates for a traced step (null otherwise; set, the launch runs gemv_kernel):
+  float* tr_in;         // the (normalized) input [B][cols], written by CTA 0
+  float* tr_pre;        // EPI_QKV: q|k|v before RoPE [B][rows] in head order; EPI_RESID: W x [B][rows]
+  float* tr_rot;        // EPI_QKV: the rotated keys in f32 [B][kv * hd]
+  int32_t tr_stride;    // floats between two rows of a trace
 };
 
 struct GemvPlan {

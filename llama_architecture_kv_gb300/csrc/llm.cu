@@ -254,8 +254,14 @@ struct GraphKey {
 };
 
 
+// the intermediates of a traced step, per layer (bend-ml-llama "A layer", Act: n1, q, k, v, qr,
+// kr, attn, a, n2, m, y; plus x1 = x + a and the SwiGLU activations)
+enum { TR_N1 = 0, TR_QKV, TR_QR, TR_KR, TR_ATTN, TR_A, TR_X1, TR_N2, TR_SWIGLU, TR_M, TR_Y, kTraceSlots };
+
 // what follows the layers: nothing, the LM head, or the head and a greedy / top-k top-p draw
-enum { MODE_NOHEAD = 0, MODE_HEAD = 1, MODE_GREEDY = 2, MODE_TOPP = 3 };
+// (MODE_TOPK: top-k of at most sample_select_max() candidates, by a radix select; MODE_TOPP: a
+// sort of the whole row)
+enum { MODE_NOHEAD = 0, MODE_HEAD = 1, MODE_GREEDY = 2, MODE_TOPP = 3, MODE_TOPK = 4 };
 
 struct llm_handle {
   llm_config cfg;
@@ -308,7 +314,9 @@ struct llm_handle {
   float* s_pre = nullptr;
   uint32_t* s_hist = nullptr;
   int V_pad = 0;
-  float* trace = nullptr;  // [L][5][max_batch][max(d, f)]
+  float* trace = nullptr;  // [L][kTraceSlots][max_batch][trace_w]: a traced handle's intermediates
+  size_t trace_w = 0;      // max(d + 2 kvw, f)
+  bool tracing = false;    // the kernels being launched write the trace
   // tensor-core projections (bf16, steps of at least tc_min rows)
   int tc_min = 0;          // 0: the tensor-core path is off for this handle
   std::vector<TcMaps> tmaps;
@@ -469,8 +477,10 @@ llm_status load_weights(llm_handle* h, const char* blob /* device */) {
 
 // ---- the decode step ----
 
-// K_SAMPLE is the temperature / top-k / top-p chain, K_GREEDY the argmax
-enum { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GATEUP = 3, K_DOWN = 4, K_HEAD = 5, K_SAMPLE = 6, K_EMBED = 7, K_GREEDY = 8 };
+// K_SAMPLE is the temperature / top-k / top-p chain, K_SELECT the same draw for a small top-k,
+// K_GREEDY the argmax
+enum { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GATEUP = 3, K_DOWN = 4, K_HEAD = 5, K_SAMPLE = 6, K_EMBED = 7, K_GREEDY = 8,
+       K_SELECT = 9 };
 
 SampleArgs sample_args(const llm_handle* h) {
   SampleArgs s = {};
@@ -533,6 +543,12 @@ llm_status launch_gemm(llm_handle* h, const CUtensorMap& tw, int rows, int K, in
   return LLM_OK;
 }
 
+// trace slot `slot` of layer l ([max_batch][trace_w]), or null when the step is not traced
+float* tr_slot(llm_handle* h, int l, int slot) {
+  if (!h->tracing) return nullptr;
+  return h->trace + ((size_t)l * kTraceSlots + slot) * h->cfg.max_batch * h->trace_w;
+}
+
 // launch one kernel of the decode step (layer l where it applies); on the tensor-core path a
 // projection is two kernels (activation split, then the GEMM)
 llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
@@ -573,8 +589,8 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     CUDA_TRY(h, launch_gemv(hd, p_h, wt, EPI_STORE, true, h->stream, pdl));
     return LLM_OK;
   }
-  if (which == K_SAMPLE || which == K_GREEDY) {
-    CUDA_TRY(h, launch_sample(sample_args(h), B, which == K_GREEDY, h->stream, pdl));
+  if (which == K_SAMPLE || which == K_GREEDY || which == K_SELECT) {
+    CUDA_TRY(h, launch_sample(sample_args(h), B, which == K_GREEDY, h->stream, pdl, which == K_SELECT));
     return LLM_OK;
   }
   const LayerW& w = h->lw[l];
@@ -632,6 +648,8 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     a.H = h->H; a.kv = c.kv_heads; a.hd = h->hd; a.cap = c.max_seq;
     a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin;
     a.status = h->status;
+    a.tr_in = tr_slot(h, l, TR_N1); a.tr_pre = tr_slot(h, l, TR_QKV); a.tr_rot = tr_slot(h, l, TR_KR);
+    a.tr_stride = (int32_t)h->trace_w;
     CUDA_TRY(h, launch_gemv(a, p, wt, EPI_QKV, true, h->stream, pdl));
   } else if (which == K_ATTN && h->capturing_pass && h->pf_attn) {
     // a prefill pass: tiles of consecutive prompt tokens share each key/value stream
@@ -650,6 +668,13 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     at.krow0 = (int32_t)((size_t)l * c.max_batch * c.kv_heads * c.max_seq); at.status = h->status;
     at.part = h->part; at.ticket = h->ticket; at.B = B; at.kv = c.kv_heads; at.g = c.group; at.hd = h->hd;
     at.cap = c.max_seq; at.ns = ns; at.scale = 1.0f / sqrtf((float)h->hd); at.step = h->st;
+    // the tensor-core kernel merging in clusters (a small batch) is latency-bound: it brings the
+    // o_proj weights of this layer into L2 for the next kernel
+    if (attn_uses_mma(wt, h->hd) && attn_cluster_merge(wt, h->hd, c.group, ns, B * c.kv_heads, c.max_seq) &&
+        !tc) {
+      at.l2pf = (const char*)w.o;
+      at.l2pf_bytes = (uint64_t)h->d * h->d * h->es;
+    }
     CUDA_TRY(h, launch_attn(h->kmap, h->vmap, at, wt, h->stream, pdl));
   } else if (which == K_O) {
     // o_proj + residual: x1 (xb) = x (xa) + W_o attn
@@ -660,6 +685,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     o.lpr = p.lpr; o.seg_ch = p.seg_ch; o.nseg = p.nseg; o.rows_cap = p.rows_cap; o.ws = p.ws;
     o.out = h->xb; o.out_stride = h->d; o.resid = h->xa; o.resid_stride = h->d;
     o.status = h->status;
+    o.tr_pre = tr_slot(h, l, TR_A); o.tr_stride = (int32_t)h->trace_w;
     CUDA_TRY(h, launch_gemv(o, p, wt, EPI_RESID, false, h->stream, pdl));
   } else if (which == K_GATEUP) {
     // RMSNorm + gate/up + SwiGLU: m = silu(W_g n2) * (W_u n2)
@@ -670,6 +696,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     g.lpr = p.lpr; g.seg_ch = p.seg_ch; g.nseg = p.nseg; g.rows_cap = p.rows_cap; g.ws = p.ws;
     g.out = h->m; g.out_stride = h->f;
     g.status = h->status;
+    g.tr_in = tr_slot(h, l, TR_N2); g.tr_stride = (int32_t)h->trace_w;
     CUDA_TRY(h, launch_gemv(g, p, wt, EPI_SWIGLU, true, h->stream, pdl));
   } else if (which == K_DOWN) {
     // down + residual: y (xa) = x1 (xb) + W_down m
@@ -680,6 +707,7 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     dn.lpr = p.lpr; dn.seg_ch = p.seg_ch; dn.nseg = p.nseg; dn.rows_cap = p.rows_cap; dn.ws = p.ws;
     dn.out = h->xa; dn.out_stride = h->d; dn.resid = h->xb; dn.resid_stride = h->d;
     dn.status = h->status;
+    dn.tr_pre = tr_slot(h, l, TR_M); dn.tr_stride = (int32_t)h->trace_w;
     CUDA_TRY(h, launch_gemv(dn, p, wt, EPI_RESID, false, h->stream, pdl));
   } else {
     return fail(h, LLM_ERR_ARG, "unknown kernel %d", which);
@@ -702,24 +730,34 @@ llm_status launch_layer_kernels(llm_handle* h, int B, int mode, bool pdl, bool t
     a.head_mode = mode == MODE_NOHEAD ? 0 : mode == MODE_GREEDY ? 2 : 1;
     CUDA_TRY(h, launch_mega(a, h->num_sms, h->stream));
     if (mode == MODE_TOPP) TRY(launch_one(h, K_SAMPLE, 0, B, false));
+    if (mode == MODE_TOPK) TRY(launch_one(h, K_SELECT, 0, B, false));
     return LLM_OK;
   }
-  const size_t maxw = (size_t)std::max(h->d, h->f);
+  const size_t tw = h->trace_w;
+  h->tracing = trace;
   for (int l = 0; l < h->L; ++l) {
-    for (int k = K_QKV; k <= K_DOWN; ++k) TRY(launch_one(h, k, l, B, pdl));
+    for (int k = K_QKV; k <= K_DOWN; ++k) {
+      llm_status s_ = launch_one(h, k, l, B, pdl);
+      if (s_ != LLM_OK) {
+        h->tracing = false;
+        return s_;
+      }
+    }
     if (trace) {
-      float* t = h->trace + (size_t)l * 5 * c.max_batch * maxw;
-      const size_t row = (size_t)c.max_batch * maxw;
-      CUDA_TRY(h, cudaMemcpy2DAsync(t + 0 * row, maxw * 4, h->q, (size_t)h->d * 4, (size_t)h->d * 4, B, cudaMemcpyDeviceToDevice, h->stream));
-      CUDA_TRY(h, cudaMemcpy2DAsync(t + 1 * row, maxw * 4, h->attn, (size_t)h->d * 4, (size_t)h->d * 4, B, cudaMemcpyDeviceToDevice, h->stream));
-      CUDA_TRY(h, cudaMemcpy2DAsync(t + 2 * row, maxw * 4, h->xb, (size_t)h->d * 4, (size_t)h->d * 4, B, cudaMemcpyDeviceToDevice, h->stream));
-      CUDA_TRY(h, cudaMemcpy2DAsync(t + 3 * row, maxw * 4, h->m, (size_t)h->f * 4, (size_t)h->f * 4, B, cudaMemcpyDeviceToDevice, h->stream));
-      CUDA_TRY(h, cudaMemcpy2DAsync(t + 4 * row, maxw * 4, h->xa, (size_t)h->d * 4, (size_t)h->d * 4, B, cudaMemcpyDeviceToDevice, h->stream));
+      // the buffers that hold an intermediate whole after the layer (the GEMVs wrote the rest)
+      const struct { int slot; const float* src; int width; } cp[] = {
+          {TR_QR, h->q, h->d}, {TR_ATTN, h->attn, h->d}, {TR_X1, h->xb, h->d}, {TR_SWIGLU, h->m, h->f},
+          {TR_Y, h->xa, h->d}};
+      for (const auto& x : cp)
+        CUDA_TRY(h, cudaMemcpy2DAsync(tr_slot(h, l, x.slot), tw * 4, x.src, (size_t)x.width * 4, (size_t)x.width * 4, B,
+                                      cudaMemcpyDeviceToDevice, h->stream));
     }
   }
+  h->tracing = false;
   if (mode >= MODE_HEAD) TRY(launch_one(h, K_HEAD, 0, B, pdl));
   if (mode == MODE_GREEDY) TRY(launch_one(h, K_GREEDY, 0, B, pdl));
   if (mode == MODE_TOPP) TRY(launch_one(h, K_SAMPLE, 0, B, pdl));
+  if (mode == MODE_TOPK) TRY(launch_one(h, K_SELECT, 0, B, pdl));
   return LLM_OK;
 }
 
@@ -844,6 +882,12 @@ llm_status check_sample_args(llm_handle* h, float temp, int k, float p) {
     if (!(p > 0.0f && p <= 1.0f)) return fail(h, LLM_ERR_ARG, "top-p must be in (0, 1]");
   }
   return LLM_OK;
+}
+
+// the mode of a step that draws with (temp, k): greedy, a small top-k, or the full sort
+int draw_mode(const llm_handle* h, float temp, int k) {
+  if (!(temp > 0.0f)) return MODE_GREEDY;
+  return std::min(k, h->V) <= sample_select_max() ? MODE_TOPK : MODE_TOPP;
 }
 
 void set_filled(llm_handle* h, int B, int v) {
@@ -1063,7 +1107,8 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
     const int head_rows = plan_tc(h->V, h->d, 1, h->num_sms, true).n_tile;
     if (!ok || !tc_make_map(&h->tmap_head, h->head, h->d, h->V, kTcK, (uint32_t)head_rows)) h->tc_min = 0;
   }
-  if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * 5 * B * std::max(h->d, h->f) * 4))) return bail(st);
+  h->trace_w = (size_t)std::max(h->d + 2 * h->kvw, h->f);
+  if (c.debug_trace && (st = dalloc(h, &h->trace, (size_t)h->L * kTraceSlots * B * h->trace_w * 4))) return bail(st);
   {
     // batch-1 steps as one persistent kernel where the shape allows it and every CTA can be resident
     int coop = 0;
@@ -1411,7 +1456,7 @@ llm_status llm_step_paged(llm_handle* h, const int32_t* tokens_host, int32_t B, 
                           const float* u_host, int32_t* ids_host, float* logits_host) {
   if (!h || !tokens_host || !positions_host || !table_host || !ids_host) return LLM_ERR_ARG;
   return paged_impl(h, tokens_host, nullptr, B, positions_host, table_host, pages_per_row,
-                    temp > 0.0f ? MODE_TOPP : MODE_GREEDY, temp, k, p, u_host, nullptr, ids_host, logits_host, true);
+                    draw_mode(h, temp, k), temp, k, p, u_host, nullptr, ids_host, logits_host, true);
 }
 
 llm_status llm_step_paged_dev(llm_handle* h, const int32_t* tokens_dev, int32_t B, const int32_t* positions_host,
@@ -1419,7 +1464,7 @@ llm_status llm_step_paged_dev(llm_handle* h, const int32_t* tokens_dev, int32_t 
                               const float* u_dev, int32_t* ids_dev, float* logits_dev) {
   if (!h || !tokens_dev || !positions_host || !table_host || !ids_dev) return LLM_ERR_ARG;
   return paged_impl(h, nullptr, tokens_dev, B, positions_host, table_host, pages_per_row,
-                    temp > 0.0f ? MODE_TOPP : MODE_GREEDY, temp, k, p, nullptr, u_dev, ids_dev, logits_dev, false);
+                    draw_mode(h, temp, k), temp, k, p, nullptr, u_dev, ids_dev, logits_dev, false);
 }
 
 // Prompts packed end to end (Llama 3.1 8B Instruct card, "Entries": prefill_packed): token p is
@@ -1540,7 +1585,7 @@ static llm_status generate_impl(llm_handle* h, const int32_t* tok_host, const in
   if (u_host && sampled)
     for (size_t i = 0; i < (size_t)n * B; ++i)
       if (!(u_host[i] >= 0.0f && u_host[i] < 1.0f)) return fail(h, LLM_ERR_ARG, "u[%zu] outside [0, 1)", i);
-  const int mode = sampled ? MODE_TOPP : MODE_GREEDY;
+  const int mode = draw_mode(h, temp, k);
   const int32_t* prev = tok_dev;
   if (tok_host) {
     CUDA_TRY(h, cudaMemcpyAsync(h->tok_buf, tok_host, (size_t)B * 4, cudaMemcpyHostToDevice, h->stream));
@@ -1605,7 +1650,7 @@ static llm_status sample_impl(llm_handle* h, const float* logits, bool logits_on
   // the prologue also carries temp, k, p and u; its tokens are unused here
   std::vector<int32_t> toks(B, 0);
   TRY(begin(h, 0, B, toks.data(), nullptr, 1, 0, temp, k, p, u_on_host ? u : nullptr, u_on_host ? nullptr : u));
-  CUDA_TRY(h, launch_sample(sample_args(h), B, !(temp > 0.0f), h->stream, false));
+  CUDA_TRY(h, launch_sample(sample_args(h), B, !(temp > 0.0f), h->stream, false, draw_mode(h, temp, k) == MODE_TOPK));
   if (ids_on_host) {
     CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToHost, h->stream));
     CUDA_TRY(h, cudaStreamSynchronize(h->stream));
@@ -1639,7 +1684,7 @@ static llm_status step_impl(llm_handle* h, const int32_t* tok_host, const int32_
     for (int b = 0; b < B; ++b)
       if (!(u_host[b] >= 0.0f && u_host[b] < 1.0f)) return fail(h, LLM_ERR_ARG, "u[%d] outside [0, 1)", b);
   TRY(begin(h, pos, B, tok_host, tok_dev, 1, 0, temp, k, p, u_host, u_dev, pos_rows));
-  TRY(run_step(h, B, temp > 0.0f ? MODE_TOPP : MODE_GREEDY));
+  TRY(run_step(h, B, draw_mode(h, temp, k)));
   if (host) {
     if (logits) CUDA_TRY(h, cudaMemcpyAsync(logits, h->logits, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, h->stream));
     CUDA_TRY(h, cudaMemcpyAsync(ids, h->ids_buf, (size_t)B * 4, cudaMemcpyDeviceToHost, h->stream));
@@ -1720,12 +1765,12 @@ llm_status llm_kv_export(llm_handle* h, int32_t layer, int32_t row, int32_t pos0
   return kv_copy(h, layer, row, pos0, n, k_host, v_host, false);
 }
 
-llm_status llm_step_kernels(llm_handle* h, int32_t B, float temp, int32_t* kernels) {
+llm_status llm_step_kernels(llm_handle* h, int32_t B, float temp, int32_t k, int32_t* kernels) {
   if (!h || !kernels) return LLM_ERR_ARG;
   if (B < 1 || B > h->cfg.max_batch) return fail(h, LLM_ERR_BATCH, "batch %d outside 1..%d", B, h->cfg.max_batch);
   if (h->cfg.debug_trace) return fail(h, LLM_ERR_ARG, "debug_trace handles run without a step graph");
   std::pair<cudaGraphExec_t, int>* g = nullptr;
-  TRY(step_graph(h, B, temp > 0.0f ? MODE_TOPP : MODE_GREEDY, &g));
+  TRY(step_graph(h, B, draw_mode(h, temp, k), &g));
   *kernels = 1 + g->second;  // the step prologue, then the graph
   return LLM_OK;
 }
@@ -1757,14 +1802,21 @@ llm_status llm_debug_trace(llm_handle* h, int32_t layer, const char* name, float
   if (!h || !name || !dst_host) return LLM_ERR_ARG;
   if (!h->cfg.debug_trace) return fail(h, LLM_ERR_ARG, "the handle was created without debug_trace");
   if (layer < 0 || layer >= h->L) return fail(h, LLM_ERR_ARG, "layer %d outside 0..%d", layer, h->L - 1);
-  static const char* names[5] = {"q", "attn", "x1", "m", "y"};
+  // name -> (slot, first element, width)
+  const int d = h->d, kvw = h->kvw;
+  const struct { const char* name; int slot, off, width; } names[] = {
+      {"n1", TR_N1, 0, d},     {"q", TR_QKV, 0, d},       {"k", TR_QKV, d, kvw},   {"v", TR_QKV, d + kvw, kvw},
+      {"qr", TR_QR, 0, d},     {"kr", TR_KR, 0, kvw},     {"attn", TR_ATTN, 0, d}, {"a", TR_A, 0, d},
+      {"x1", TR_X1, 0, d},     {"n2", TR_N2, 0, d},       {"swiglu", TR_SWIGLU, 0, h->f},
+      {"m", TR_M, 0, d},       {"y", TR_Y, 0, d}};
   int which = -1;
-  for (int i = 0; i < 5; ++i)
-    if (!strcmp(name, names[i])) which = i;
+  for (int i = 0; i < (int)(sizeof names / sizeof names[0]); ++i)
+    if (!strcmp(name, names[i].name)) which = i;
   if (which < 0) return fail(h, LLM_ERR_ARG, "unknown trace name %s", name);
-  const size_t maxw = (size_t)std::max(h->d, h->f);
-  const size_t width = which == 3 ? (size_t)h->f : (size_t)h->d;
-  const float* src = h->trace + ((size_t)layer * 5 + which) * h->cfg.max_batch * maxw;
+  const size_t maxw = h->trace_w;
+  const size_t width = (size_t)names[which].width;
+  const float* src = h->trace + ((size_t)layer * kTraceSlots + names[which].slot) * h->cfg.max_batch * maxw +
+                     names[which].off;
   CUDA_TRY(h, cudaStreamSynchronize(h->stream));
   CUDA_TRY(h, cudaMemcpy2D(dst_host, width * 4, src, maxw * 4, width * 4, h->cfg.max_batch, cudaMemcpyDeviceToHost));
   return LLM_OK;

@@ -254,30 +254,25 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(const Sample
   }
 }
 
-// weights of the top min(k, V) candidates, their in-order running sum, the kept count and the draw
+// weights of the top k candidates, their in-order running sum, the kept count and the draw.
+// cand[j] is the j-th candidate's id (largest logit first, ties by lower id); pre is [k] scratch
+// in global memory.  Every thread of the CTA calls this; thread 0 writes ids[b].
 constexpr int kFinalThreads = 1024;
 constexpr int kRunChunk = 8192;
 
-__global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const SampleArgs a) {
-  grid_dep_wait();
-  grid_dep_launch();
-  const int b = blockIdx.x, tid = threadIdx.x;
-  const int V = a.V;
+LLM_D void draw_from_candidates(const SampleArgs& a, int b, const int32_t* cand, int k, float* pre, float* chunk) {
+  const int tid = threadIdx.x, nt = blockDim.x;
   const float* lg = a.logits + (size_t)b * a.logits_stride;
-  const int32_t* is = a.idx + (size_t)b * 2 * a.V_pad;  // after 8 passes the sorted row is in buffer 0
-  float* pre = a.pre + (size_t)b * a.V_pad;
-  __shared__ float chunk[kRunChunk];
   const float temp = a.step->temp;
-  const int k = min(a.step->k, V);
-  const float top = lg[is[0]];
+  const float top = lg[cand[0]];
   const float ttop = __fdiv_rn(top, temp);
-  for (int j = tid; j < k; j += kFinalThreads) pre[j] = exp_s(__fsub_rn(__fdiv_rn(lg[is[j]], temp), ttop));
+  for (int j = tid; j < k; j += nt) pre[j] = exp_s(__fsub_rn(__fdiv_rn(lg[cand[j]], temp), ttop));
   __syncthreads();
   // the running sum is sequential by definition: one thread adds, in order, chunk by chunk
   float run = 0.0f;
   for (int c0 = 0; c0 < k; c0 += kRunChunk) {
     const int n = min(kRunChunk, k - c0);
-    for (int j = tid; j < n; j += kFinalThreads) chunk[j] = pre[c0 + j];
+    for (int j = tid; j < n; j += nt) chunk[j] = pre[c0 + j];
     __syncthreads();
     if (tid == 0) {
       int j = 0;
@@ -297,7 +292,7 @@ __global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const Sampl
       }
     }
     __syncthreads();
-    for (int j = tid; j < n; j += kFinalThreads) pre[c0 + j] = chunk[j];
+    for (int j = tid; j < n; j += nt) pre[c0 + j] = chunk[j];
     __syncthreads();
   }
   if (tid == 0) {
@@ -320,8 +315,143 @@ __global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const Sampl
       if (target < pre[mid]) hi = mid;
       else lo = mid + 1;
     }
-    a.ids[b] = is[lo];
+    a.ids[b] = cand[lo];
   }
+}
+
+__global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const SampleArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x;
+  __shared__ float chunk[kRunChunk];
+  const int32_t* is = a.idx + (size_t)b * 2 * a.V_pad;  // after 8 passes the sorted row is in buffer 0
+  draw_from_candidates(a, b, is, min(a.step->k, a.V), a.pre + (size_t)b * a.V_pad, chunk);
+}
+
+// ---------------------------------------------------------------------------------------
+// top-k for k <= kSelectMax: the k candidates by a radix select, not a sort of the whole row
+// ---------------------------------------------------------------------------------------
+// One CTA per row.  The k-th smallest order key T (the k-th largest logit) is found most
+// significant byte first: four passes, each a 256-bin histogram of the keys that share the
+// prefix found so far.  The candidates are then every id whose key is below T and the first
+// k - (their number) ids whose key equals T, taken in ascending id order (threads own contiguous
+// id ranges and a block scan orders them), and a bitonic sort of (key, id) pairs puts them in
+// the sorted order of the full sort's first k: the same candidates in the same order, so the
+// draw is bit for bit the same.
+
+constexpr int kSelectMax = 1024;
+constexpr int kSelectThreads = 1024;
+
+__global__ void __launch_bounds__(kSelectThreads) sample_topk_kernel(const SampleArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = a.V;
+  const int k = min(min(a.step->k, V), kSelectMax);  // (the host sends larger k to the sort)
+  const float* lg = a.logits + (size_t)b * a.logits_stride;
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t s_prefix, s_rank, s_lt;
+  __shared__ uint32_t wsum[kSelectThreads / 32];
+  __shared__ unsigned long long cand[kSelectMax];
+  __shared__ int32_t cand_id[kSelectMax];
+  __shared__ float chunk[kSelectMax];
+
+  // ---- radix select: T = the key of rank k - 1 (0-based) in ascending key order ----
+  uint32_t prefix = 0u, rank = (uint32_t)(k - 1);
+  for (int pass = 0; pass < 4; ++pass) {
+    const int sh = 24 - 8 * pass;
+    const uint32_t mask = pass == 0 ? 0u : 0xffffffffu << (sh + 8);
+    if (tid < 256) hist[tid] = 0u;
+    __syncthreads();
+    for (int i = tid; i < V; i += kSelectThreads) {
+      const uint32_t key = desc_key(lg[i]);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t r = rank, d = 0;
+      while (hist[d] <= r) r -= hist[d++];
+      s_prefix = prefix | (d << sh);
+      s_rank = r;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    rank = s_rank;
+  }
+  const uint32_t T = prefix;
+  const uint32_t need_eq = rank + 1;  // ties at T to take (the k - count below T lowest ids)
+
+  // ---- candidates, in ascending id order within each class ----
+  const int per = (V + kSelectThreads - 1) / kSelectThreads;
+  const int i0 = tid * per, i1 = min(V, i0 + per);
+  uint32_t nlt = 0u, neq = 0u;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = desc_key(lg[i]);
+    nlt += key < T;
+    neq += key == T;
+  }
+  // exclusive block scans of nlt and neq (packed: below-T count in the high half)
+  auto scan = [&](uint32_t v) {
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t w = lane < kSelectThreads / 32 ? wsum[lane] : 0u;
+      uint32_t wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += x;
+      }
+      if (lane < kSelectThreads / 32) wsum[lane] = wi - w;
+    }
+    __syncthreads();
+    const uint32_t r = wsum[warp] + incl - v;
+    __syncthreads();
+    return r;
+  };
+  uint32_t olt = scan(nlt);
+  uint32_t oeq = scan(neq);
+  if (tid == kSelectThreads - 1) s_lt = olt + nlt;
+  __syncthreads();
+  const uint32_t total_lt = s_lt;  // = k - need_eq
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = desc_key(lg[i]);
+    if (key < T) {
+      cand[olt++] = ((unsigned long long)key << 32) | (uint32_t)i;
+    } else if (key == T) {
+      if (oeq < need_eq) cand[total_lt + oeq] = ((unsigned long long)key << 32) | (uint32_t)i;
+      ++oeq;
+    }
+  }
+  // pad to a power of two and sort ascending (key, then id)
+  int n2 = 1;
+  while (n2 < k) n2 <<= 1;
+  for (int j = k + tid; j < n2; j += kSelectThreads) cand[j] = ~0ull;
+  __syncthreads();
+  for (int size = 2; size <= n2; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int j = tid; j < n2; j += kSelectThreads) {
+        const int p = j ^ stride;
+        if (p > j) {
+          const bool up = (j & size) == 0;
+          const unsigned long long x = cand[j], y = cand[p];
+          if ((x > y) == up) {
+            cand[j] = y;
+            cand[p] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  for (int j = tid; j < k; j += kSelectThreads) cand_id[j] = (int32_t)(cand[j] & 0xffffffffull);
+  __syncthreads();
+  draw_from_candidates(a, b, cand_id, k, a.pre + (size_t)b * a.V_pad, chunk);
 }
 
 static cudaError_t launch(void (*fn)(const SampleArgs), dim3 grid, int threads, const SampleArgs& a,
@@ -355,8 +485,11 @@ static cudaError_t launch2(void (*fn)(const SampleArgs, Arg), dim3 grid, int thr
 
 int sample_slices(int V) { return (V + sort_slice(V) - 1) / sort_slice(V); }
 
-cudaError_t launch_sample(const SampleArgs& a, int B, bool greedy, cudaStream_t s, bool pdl) {
+int sample_select_max() { return kSelectMax; }
+
+cudaError_t launch_sample(const SampleArgs& a, int B, bool greedy, cudaStream_t s, bool pdl, bool select) {
   if (greedy) return launch(sample_kernel, dim3(B), kSampThreads, a, s, pdl);
+  if (select) return launch(sample_topk_kernel, dim3(B), kSelectThreads, a, s, pdl);
   const int NB = sample_slices(a.V);
   cudaError_t e = launch(sort_init_kernel, dim3(NB, B), kSortThreads, a, s, pdl);
   for (int pass = 0; pass < 8 && e == cudaSuccess; ++pass) {

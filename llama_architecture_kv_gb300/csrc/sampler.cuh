@@ -22,8 +22,10 @@ constexpr int kSortMaxSlicesPerRow = 64;
 constexpr size_t kSampleHistPerRow = 16 * kSortMaxSlicesPerRow;  // uint32 entries a row needs at most
 
 int sample_slices(int V);
-// greedy: one argmax kernel; otherwise the sort chain and the draw (temp, k, p from *step)
-cudaError_t launch_sample(const SampleArgs& a, int B, bool greedy, cudaStream_t s, bool pdl);
+// greedy: one argmax kernel; select (top-k with k <= sample_select_max()): one radix-select
+// kernel per row; otherwise the sort chain and the draw (temp, k, p from *step)
+cudaError_t launch_sample(const SampleArgs& a, int B, bool greedy, cudaStream_t s, bool pdl, bool select = false);
+int sample_select_max();
 // loads the allocation-free sampler's fixed array on the current device and records its address
 cudaError_t noalloc_prepare();
 

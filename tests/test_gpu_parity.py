@@ -189,14 +189,16 @@ def test_sampler_ids_bit_exact(V):
     s = shrink(TINY, vocab=V)
     blob, g = make(s, 3, 8, 4)
     rng = np.random.default_rng(V)
-    for trial in range(12):
+    # k <= 1024 candidates: the radix-select kernel; more: the sort of the whole row
+    ks = [1, 2, 50, 1000, 1024, 1025, V, V + 10]
+    for trial in range(24):
         B = int(rng.integers(1, 9))
         if trial % 4 == 0:
             logits = rng.integers(-3, 4, (B, V)).astype(np.float32)  # many ties
         else:
             logits = (rng.standard_normal((B, V)) * rng.choice([0.5, 2, 8])).astype(np.float32)
-        temp = float(rng.choice([0.0, 0.3, 0.7, 0.8, 1.5]))
-        k = int(rng.choice([1, 2, 50, V, V + 10]))
+        temp = float(rng.choice([0.0, 0.3, 0.7, 0.8, 1.5])) if trial >= len(ks) else 0.8
+        k = int(ks[trial]) if trial < len(ks) else int(rng.choice(ks))
         p = float(rng.choice([1e-3, 0.5, 0.9, 0.95, 1.0]))
         u = synth.uniforms(4000 + trial, 0, B)
         ids = g.sample(logits, temp, k, p, u)
@@ -375,6 +377,7 @@ def test_step_kernel_counts():
     # the head: split + GEMM, and a sum of its K splits when it has more than one
     assert pkg.llm_step_kernels(g.h, 16, 0.0) - greedy_gemv in (5 * L + 1, 5 * L + 2)
     assert pkg.llm_step_kernels(g.h, 4, 0.8) == greedy_gemv + 25  # 8 passes x 3 sort kernels + init + draw
+    assert pkg.llm_step_kernels(g.h, 4, 0.8, 50) == greedy_gemv  # top-50: one selection kernel
     with pytest.raises(pkg.LlmError):
         pkg.llm_step_kernels(g.h, 21, 0.0)
     g.close()
@@ -434,4 +437,36 @@ def test_causality_bf16_cache(name, shape):
             g.kv_import(layer, b, t + 1, junk, junk)
     b_ = g.decode(toks[:, t], t)
     assert np.array_equal(a.view(np.uint32), b_.view(np.uint32))
+    g.close()
+
+
+# ---------------------------------------------------------------------------------------
+# the divergence ladder: every intermediate of a layer against the oracle's trace
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_debug_trace_every_intermediate_matches_oracle(B):
+    # one bf16 step of the 8B head shape: n1, q, k, v, qr, kr, attn, a, x1, n2, m, y of both
+    # layers against the oracle's trace of the same step (bend-ml-llama "A layer", Act), each
+    # within a few f32 roundings of its scale
+    s = shrink(WORKLOADS["llama8b_b1"].shape, layers=2, kv=2, ffn=512, vocab=700)
+    blob = synth.model_blob(s, 141)
+    P = 9
+    toks = synth.tokens(142, 0, B * (P + 1), s.vocab).reshape(B, P + 1)
+    g = pkg.Model(s, blob, max_batch=B, max_seq=16, debug_trace=True)
+    g.prefill(toks[:, :P], 0, logits=False)
+    g.decode(toks[:, P], P)
+    for b in range(B):
+        ref = oracle.Model(oracle.cfg_of(s, 1, 16), blob, trace=True)
+        ref.prefill(0, toks[b, :P], 0, logits=False)
+        ref.forward(0, int(toks[b, P]), P)
+        for layer in range(s.layers):
+            for name in ("n1", "q", "k", "v", "qr", "kr", "attn", "a", "x1", "n2", "m", "y"):
+                got = g.trace(layer, name)[b]
+                want = ref.trace(layer, name)
+                assert got.shape == want.shape, (name, got.shape, want.shape)
+                scale = float(np.max(np.abs(want))) + 1e-30
+                err = float(np.max(np.abs(got - want)))
+                assert err <= 2e-3 * scale, (layer, name, b, err, scale)
+        ref.close()
     g.close()
