@@ -695,16 +695,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     // previous kernel
     while (issued < NR && ist < c1 && (is.kv0 + iq) * CH + min(CH, is.tb + 1 - (is.kv0 + iq) * CH) <= is.tw) issue();
   }
-  if (a.l2pf && tid == 32) {
-    // a latency-bound launch leaves HBM idle: pull this CTA's share of the next kernel's weights
-    // into L2 meanwhile (pieces of at most 64 KB)
-    const uint64_t n16 = a.l2pf_bytes >> 4;
-    const uint64_t b0 = (n16 * (uint64_t)c / G) << 4, b1 = (n16 * (uint64_t)(c + 1) / G) << 4;
-    for (uint64_t o = b0; o < b1; o += 65536) {
-      const uint64_t n = b1 - o < 65536 ? b1 - o : 65536;
-      prefetch_l2(a.l2pf + o, (uint32_t)n);
-    }
-  }
   grid_dep_wait();
   grid_dep_launch();
   if (lane == 0)

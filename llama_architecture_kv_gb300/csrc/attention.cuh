@@ -20,8 +20,6 @@ struct AttnArgs {
   const StepState* step;
   int32_t* status;     // device error flag
   int32_t cluster;     // set by launch_attn: the splits form one thread-block cluster
-  const char* l2pf;    // or null: bytes the next kernel reads (its weights), brought into L2 by
-  uint64_t l2pf_bytes; //   this kernel's CTAs while it waits on its own latency (16-byte multiple)
 };
 
 constexpr int kAttnMaxCluster = 16;  // most splits merged inside one thread-block cluster

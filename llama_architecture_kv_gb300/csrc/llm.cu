@@ -668,13 +668,6 @@ llm_status launch_one(llm_handle* h, int which, int l, int B, bool pdl) {
     at.krow0 = (int32_t)((size_t)l * c.max_batch * c.kv_heads * c.max_seq); at.status = h->status;
     at.part = h->part; at.ticket = h->ticket; at.B = B; at.kv = c.kv_heads; at.g = c.group; at.hd = h->hd;
     at.cap = c.max_seq; at.ns = ns; at.scale = 1.0f / sqrtf((float)h->hd); at.step = h->st;
-    // the tensor-core kernel merging in clusters (a small batch) is latency-bound: it brings the
-    // o_proj weights of this layer into L2 for the next kernel
-    if (attn_uses_mma(wt, h->hd) && attn_cluster_merge(wt, h->hd, c.group, ns, B * c.kv_heads, c.max_seq) &&
-        !tc) {
-      at.l2pf = (const char*)w.o;
-      at.l2pf_bytes = (uint64_t)h->d * h->d * h->es;
-    }
     CUDA_TRY(h, launch_attn(h->kmap, h->vmap, at, wt, h->stream, pdl));
   } else if (which == K_O) {
     // o_proj + residual: x1 (xb) = x (xa) + W_o attn
