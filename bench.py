@@ -65,6 +65,8 @@ def parse():
                     help="default workload: also time this many batch-32 steps (0: skip)")
     ap.add_argument("--step-kernel", type=int, default=0, choices=[0, 1],
                     help="batch 1: 1 runs each step as one persistent kernel")
+    ap.add_argument("--tc-min-batch", type=int, default=0,
+                    help="rows from which a step runs its projections on the tensor cores (0: library default)")
     return ap.parse_args()
 
 
@@ -440,7 +442,7 @@ def run_ours(args):
     log(f"[bench] weights generated: {blob.nbytes / 1e9:.2f} GB in {time.perf_counter() - t0:.1f} s")
     t0 = time.perf_counter()
     model = pkg.Model(s, blob, max_batch=B, max_seq=cap, stream=stream.cuda_stream, max_tokens=args.max_tokens,
-                      step_kernel=args.step_kernel)
+                      step_kernel=args.step_kernel, tc_min_batch=args.tc_min_batch)
     h = model.h
     log(f"[bench] model created in {time.perf_counter() - t0:.1f} s")
     t0 = time.perf_counter()
@@ -497,7 +499,7 @@ def run_ours(args):
     bytes_gu = 2 * s.ffn * s.d * (2 if s.bf16 else 4)  # algorithmic: the gate and up weights
     achieved = bytes_gu / (kms / 1e3) / 1e9
     peak, peak_kind = peaks()
-    tc = s.bf16 and B >= 16  # the handle's default tensor-core threshold
+    tc = s.bf16 and B >= (args.tc_min_batch or 2)  # the handle's tensor-core threshold
     if tc:
         kname = "tc_gemm_kernel (gate/up, timed with its tc_prep_kernel: x1 = x + o_proj, norm, bf16 split)"
         traffic = traffic_from_profile("gemm.cu", "tc_gemm_gate_up_llama8b_b32.md") if w.name == "llama8b_b32" else None

@@ -517,8 +517,13 @@ TcPlan plan_tc(int rows, int K, int B, int num_sms, bool whole) {
   return p;
 }
 
+__global__ void tc_prep_rows_kernel(const TcPrepArgs a);
+constexpr int kPrepRowMaxKDecl = 16384;
+
 cudaError_t tc_prepare(int max_smem_optin) {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_prep_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepRowMaxKDecl * 4);
   return e;
 }
 
@@ -536,8 +541,88 @@ static cudaLaunchConfig_t cfg_of(dim3 grid, int threads, size_t smem, cudaStream
   return cfg;
 }
 
+// The same reader for many rows (a prefill pass): one CTA of kPrepRowThreads per row keeps the
+// whole row in shared memory, so the sum of squares needs no cluster; the rows themselves fill
+// the GPU.
+constexpr int kPrepRowThreads = 256;
+constexpr int kPrepRowMaxK = kPrepRowMaxKDecl;  // floats of a row in shared memory (64 KB)
+constexpr int kPrepRowsFrom = 128;   // rows from which the per-row kernel is used
+
+__global__ void __launch_bounds__(kPrepRowThreads) tc_prep_rows_kernel(const TcPrepArgs a) {
+  extern __shared__ float4 rowv[];  // [K / 4]
+  __shared__ float red[kPrepRowThreads / 32];
+  __shared__ float s_inv;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k4 = a.K >> 2;
+  const size_t split = (size_t)a.B * a.part_rows;
+  float ss = 0.f;
+  for (int i = tid; i < k4; i += kPrepRowThreads) {
+    float4 v;
+    if (!a.part) {
+      v = *reinterpret_cast<const float4*>(a.x_in + (size_t)b * a.x_stride + 4 * i);
+    } else if (a.swiglu) {
+      const float* p = a.part + (size_t)b * a.part_rows + 8 * i;
+      const float4 s0 = sum_splits4(p, split, a.S), s1 = sum_splits4(p + 4, split, a.S);
+      v = make_float4(silu_mul(s0.x, s0.y), silu_mul(s0.z, s0.w), silu_mul(s1.x, s1.y), silu_mul(s1.z, s1.w));
+    } else {
+      v = sum_splits4(a.part + (size_t)b * a.part_rows + 4 * i, split, a.S);
+      if (a.resid) {
+        const float4 rr = *reinterpret_cast<const float4*>(a.resid + (size_t)b * a.resid_stride + 4 * i);
+        v.x = __fadd_rn(rr.x, v.x); v.y = __fadd_rn(rr.y, v.y); v.z = __fadd_rn(rr.z, v.z); v.w = __fadd_rn(rr.w, v.w);
+      }
+    }
+    if (a.xout) *reinterpret_cast<float4*>(a.xout + (size_t)b * a.xout_stride + 4 * i) = v;
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+    rowv[i] = v;
+  }
+  float inv = 1.0f;
+  if (a.gain) {
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < kPrepRowThreads / 32; ++w) t += red[w];
+      s_inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)a.K), a.eps)));
+    }
+  }
+  __syncthreads();
+  if (a.gain) inv = s_inv;
+  uint16_t* hi = a.xs + (size_t)b * a.K;
+  uint16_t* lo = a.xs + ((size_t)a.Ntot + b) * a.K;
+  for (int i = tid; i < k4; i += kPrepRowThreads) {
+    float4 v = rowv[i];
+    if (a.gain) {
+      const float4 g = *reinterpret_cast<const float4*>(a.gain + 4 * i);
+      v.x = __fmul_rn(g.x, __fmul_rn(inv, v.x));
+      v.y = __fmul_rn(g.y, __fmul_rn(inv, v.y));
+      v.z = __fmul_rn(g.z, __fmul_rn(inv, v.z));
+      v.w = __fmul_rn(g.w, __fmul_rn(inv, v.w));
+    }
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    uint16_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      h[e] = f32_to_bf16(f[e]);
+      l[e] = f32_to_bf16(__fsub_rn(f[e], bf16_to_f32(h[e])));
+    }
+    reinterpret_cast<uint2*>(hi)[i] = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+    reinterpret_cast<uint2*>(lo)[i] = make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
+  }
+}
+
 cudaError_t launch_tc_prep(const TcPrepArgs& a, cudaStream_t s, bool pdl) {
   if (a.K > kPrepCluster * kPrepThreads * kPrepMaxV * 4 || (a.K & 3) || a.S > kMaxSplits) return cudaErrorInvalidValue;
+  if (a.B >= kPrepRowsFrom && a.K <= kPrepRowMaxK) {
+    cudaLaunchAttribute attr1[1];
+    const cudaLaunchConfig_t cfg = cfg_of(dim3(a.B), kPrepRowThreads, (size_t)a.K * 4, s, pdl, attr1);
+    return cudaLaunchKernelEx(&cfg, tc_prep_rows_kernel, a);
+  }
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cfg_of(dim3(kPrepCluster, a.B), kPrepThreads, 0, s, pdl, attr);
   if (a.gain) {

@@ -10,7 +10,7 @@ constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 read the
 constexpr int kTcN = 256;         // weight rows per tile (the MMA's N)
 constexpr int kTcK = 64;          // K elements per stage (one 128-byte swizzle row)
 constexpr int kTcRows = 64;       // activation rows per tile (hi in MMA rows 0..63, lo in 64..127)
-constexpr int kTcDefaultMinBatch = 16;  // rows from which a step uses the tensor cores
+constexpr int kTcDefaultMinBatch = 2;   // rows from which a step uses the tensor cores
 
 // out[s][j][r] = sum over K block range s of W[r][c] * x'[j][c]: raw split sums, f32
 struct TcArgs {
