@@ -1283,7 +1283,7 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
 // ---------------------------------------------------------------------------------------
 // Causal attention of a prefill pass (Llama 3.1 8B Instruct card, attention.linnet prefill<S>:
 // token i of a prompt at position pos + i sees the positions s <= pos + i; bend-ml-llama law
-// causal).  The entries of a pass come in tiles: up to 64 / g consecutive prompt tokens of one
+// causal).  The entries of a pass come in tiles: up to 128 / g consecutive prompt tokens of one
 // cache row, at consecutive positions, with one attention start (0, or the prompt's first
 // position for packed prompts).  A unit is (tile, kv head j): its columns are the (token, head)
 // pairs t * g + h, and the keys and values of positions start .. the tile's last position are
@@ -1292,17 +1292,19 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
 // One CTA per SM walks the units (the host sorts them longest first, CTA c takes c, c + G, ...).
 // A producer warp streams 16-position chunks of the unit's keys and values through a ring of
 // shared-memory stages (TMA tensor copies, 128-byte swizzle; full / empty mbarriers), running on
-// into the next unit; eight consumer warps each own 8 of the tile's 64 columns and read every
-// chunk: scores S^T = K Q^T (rows = the chunk's 16 positions, columns = the warp's 8 (token,
-// head) pairs; the queries as bf16 hi + lo B fragments), an online softmax per column with the
+// into the next unit; eight consumer warps each own 16 of the tile's 128 columns (two 8-column
+// MMA tiles, so every key fragment feeds two MMAs) and read every chunk: scores S^T = K Q^T
+// (rows = the chunk's 16 positions, columns = the warp's (token, head) pairs; the queries as
+// bf16 hi + lo B fragments), an online softmax per column with the
 // causal mask start <= s <= that token's position, and O^T += V^T P^T (the weights as hi + lo B
 // fragments).  A warp owns its columns' whole key range, so it writes o / l straight to the
 // output; nothing is merged across CTAs.  Every wait is bounded; after one runs out the CTA
 // records kErrDeviceTimeout and its warps stop waiting (they still pass the same barriers).
 // ---------------------------------------------------------------------------------------
 
-constexpr int kPfWarps = 8;              // consumer warps, 8 columns each
-constexpr int kPfCols = kPfWarps * 8;    // (token, head) columns of a tile
+constexpr int kPfWarps = 8;              // consumer warps
+constexpr int kPfNT = 2;                 // 8-column MMA tiles per warp
+constexpr int kPfCols = kPfWarps * 8 * kPfNT;  // (token, head) columns of a tile
 constexpr int kPfStages = 8;             // ring stages (16 positions of keys and values each)
 
 template <int HD>
@@ -1324,7 +1326,7 @@ LLM_HD size_t attn_prefill_smem() {
 int attn_prefill_tile_tokens(int g) { return kPfCols / g; }
 
 template <int HD>
-__global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
+__global__ void __maxnreg__(224)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const AttnPrefillArgs a) {
   using P = PfShape<HD>;
@@ -1414,7 +1416,8 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
     return;
   }
 
-  // ---- consumers: warp w owns columns 8w .. 8w + 7 ----
+  // ---- consumers: warp w owns columns 16w .. 16w + 15 (MMA tiles n = 0, 1) ----
+  constexpr int NT = kPfNT;
   int it = 0;
   for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
     const Unit U = unit(u);
@@ -1440,30 +1443,38 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
       }
     }
     named_sync(1, kPfWarps * 32);
-    uint32_t qfh[KS][2], qfl[KS][2];
+    uint32_t qfh[NT][KS][2], qfl[NT][KS][2];
 #pragma unroll
-    for (int ks = 0; ks < KS; ks += 2) {
-      const uint32_t off = (uint32_t)(((warp * 8 + mr) * QP + ks * 16 + mi * 8) * 2);
-      uint32_t r[4];
-      ldsm_x4(smem_u32(qbase) + off, r);
-      qfh[ks][0] = r[0]; qfh[ks][1] = r[1]; qfh[ks + 1][0] = r[2]; qfh[ks + 1][1] = r[3];
-      ldsm_x4(smem_u32(qbase + kPfCols * QP) + off, r);
-      qfl[ks][0] = r[0]; qfl[ks][1] = r[1]; qfl[ks + 1][0] = r[2]; qfl[ks + 1][1] = r[3];
-    }
-    // this lane's two columns: token, its position (the last key it sees), whether it exists
-    int pc[2];
-    bool cv[2];
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      const int col = warp * 8 + 2 * tig + hc, t = col / g;
-      cv[hc] = t < U.nq;
-      pc[hc] = U.P0 + t;
-    }
+      for (int ks = 0; ks < KS; ks += 2) {
+        const uint32_t off = (uint32_t)((((warp * NT + n) * 8 + mr) * QP + ks * 16 + mi * 8) * 2);
+        uint32_t r[4];
+        ldsm_x4(smem_u32(qbase) + off, r);
+        qfh[n][ks][0] = r[0]; qfh[n][ks][1] = r[1]; qfh[n][ks + 1][0] = r[2]; qfh[n][ks + 1][1] = r[3];
+        ldsm_x4(smem_u32(qbase + kPfCols * QP) + off, r);
+        qfl[n][ks][0] = r[0]; qfl[n][ks][1] = r[1]; qfl[n][ks + 1][0] = r[2]; qfl[n][ks + 1][1] = r[3];
+      }
+    // this lane's columns (n, hc): token, its position (the last key it sees), whether it exists
+    int pc[NT][2];
+    bool cv[NT][2];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        const int col = (warp * NT + n) * 8 + 2 * tig + hc, t = col / g;
+        cv[n][hc] = t < U.nq;
+        pc[n][hc] = U.P0 + t;
+      }
     const int plast = U.P0 + U.nq - 1;
-    float o[DT][4];
+    float o[NT][DT][4];
 #pragma unroll
-    for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) o[n][dt][0] = o[n][dt][1] = o[n][dt][2] = o[n][dt][3] = 0.f;
+    float mrow[NT][2], lrow[NT][2];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) mrow[n][0] = mrow[n][1] = -INFINITY, lrow[n][0] = lrow[n][1] = 0.f;
     for (int k = U.k0; k < U.k1; ++k, ++it) {
       const int s = it % kPfStages;
       if (!s_abort) {
@@ -1474,57 +1485,78 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
       const int kb = k * CH;
       const uint32_t kreg = s_base + (uint32_t)(s * STAGE);
       const uint32_t vreg = kreg + (uint32_t)(CH * ROWB);
-      // scores: rows = positions kb + 0..15, columns = this warp's 8
-      float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+      // scores: rows = positions kb + 0..15, columns = this warp's 16; even / odd k-steps in
+      // separate accumulators (shorter dependency chains)
+      float sh[NT][2][4], sl[NT][2][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int par = 0; par < 2; ++par)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sh[n][par][i] = sl[n][par][i] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t ka[4];
         ldsm_x4(kreg + swz_off((mi & 1) * 8 + mr, 2 * ks + (mi >> 1)), ka);
-        mma_bf16_16816(sh, ka, qfh[ks][0], qfh[ks][1]);
-        mma_bf16_16816(sl, ka, qfl[ks][0], qfl[ks][1]);
-      }
-      float p[4], corr[2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int pos = kb + gid + 8 * (i >> 1), hc = i & 1;
-        p[i] = (cv[hc] && pos >= U.start && pos <= pc[hc]) ? (sh[i] + sl[i]) * a.scale : -INFINITY;
-      }
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        float mx = fmaxf(p[hc], p[2 + hc]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mnew = fmaxf(mrow[hc], mx);  // -inf while the column has seen no position
-        corr[hc] = mrow[hc] == -INFINITY ? 0.f : expf(mrow[hc] - mnew);
-        mrow[hc] = mnew;
-        const float w0 = p[hc] == -INFINITY ? 0.f : expf(p[hc] - mnew);
-        const float w1 = p[2 + hc] == -INFINITY ? 0.f : expf(p[2 + hc] - mnew);
-        p[hc] = w0;
-        p[2 + hc] = w1;
-        lrow[hc] = fmaf(lrow[hc], corr[hc], w0 + w1);
-      }
-      if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
-#pragma unroll
-        for (int dt = 0; dt < DT; ++dt) {
-          o[dt][0] *= corr[0];
-          o[dt][1] *= corr[1];
-          o[dt][2] *= corr[0];
-          o[dt][3] *= corr[1];
+        for (int n = 0; n < NT; ++n) {
+          mma_bf16_16816(sh[n][ks & 1], ka, qfh[n][ks][0], qfh[n][ks][1]);
+          mma_bf16_16816(sl[n][ks & 1], ka, qfl[n][ks][0], qfl[n][ks][1]);
         }
       }
+      float p[NT][4];
+      bool same = true;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int pos = kb + gid + 8 * (i >> 1), hc = i & 1;
+          const float sc = (sh[n][0][i] + sh[n][1][i]) + (sl[n][0][i] + sl[n][1][i]);
+          p[n][i] = (cv[n][hc] && pos >= U.start && pos <= pc[n][hc]) ? sc * a.scale : -INFINITY;
+        }
+        float corr[2];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          float mx = fmaxf(p[n][hc], p[n][2 + hc]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(mrow[n][hc], mx);  // -inf while the column has seen no position
+          corr[hc] = mrow[n][hc] == -INFINITY ? 0.f : expf(mrow[n][hc] - mnew);
+          mrow[n][hc] = mnew;
+          const float w0 = p[n][hc] == -INFINITY ? 0.f : expf(p[n][hc] - mnew);
+          const float w1 = p[n][2 + hc] == -INFINITY ? 0.f : expf(p[n][2 + hc] - mnew);
+          p[n][hc] = w0;
+          p[n][2 + hc] = w1;
+          lrow[n][hc] = fmaf(lrow[n][hc], corr[hc], w0 + w1);
+        }
+        if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
+          same = false;
+#pragma unroll
+          for (int dt = 0; dt < DT; ++dt) {
+            o[n][dt][0] *= corr[0];
+            o[n][dt][1] *= corr[1];
+            o[n][dt][2] *= corr[0];
+            o[n][dt][3] *= corr[1];
+          }
+        }
+      }
+      (void)same;
       // the weights as B fragments (k = positions, n = columns), gathered from the score
       // fragments: lane (gid = column, tig = t) takes positions 2t, 2t + 1 (and + 8)
-      uint32_t pfh[2], pfl[2];
+      uint32_t pfh[NT][2], pfl[NT][2];
       {
         const int sa = 8 * tig + (gid >> 1), sb = sa + 4;
         const bool odd = gid & 1;
-        const float a0 = __shfl_sync(0xffffffffu, p[0], sa), a1 = __shfl_sync(0xffffffffu, p[1], sa);
-        const float a2 = __shfl_sync(0xffffffffu, p[2], sa), a3 = __shfl_sync(0xffffffffu, p[3], sa);
-        const float b0 = __shfl_sync(0xffffffffu, p[0], sb), b1 = __shfl_sync(0xffffffffu, p[1], sb);
-        const float b2 = __shfl_sync(0xffffffffu, p[2], sb), b3 = __shfl_sync(0xffffffffu, p[3], sb);
-        split_bf16x2(odd ? a1 : a0, odd ? b1 : b0, pfh[0], pfl[0]);
-        split_bf16x2(odd ? a3 : a2, odd ? b3 : b2, pfh[1], pfl[1]);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const float a0 = __shfl_sync(0xffffffffu, p[n][0], sa), a1 = __shfl_sync(0xffffffffu, p[n][1], sa);
+          const float a2 = __shfl_sync(0xffffffffu, p[n][2], sa), a3 = __shfl_sync(0xffffffffu, p[n][3], sa);
+          const float b0 = __shfl_sync(0xffffffffu, p[n][0], sb), b1 = __shfl_sync(0xffffffffu, p[n][1], sb);
+          const float b2 = __shfl_sync(0xffffffffu, p[n][2], sb), b3 = __shfl_sync(0xffffffffu, p[n][3], sb);
+          split_bf16x2(odd ? a1 : a0, odd ? b1 : b0, pfh[n][0], pfl[n][0]);
+          split_bf16x2(odd ? a3 : a2, odd ? b3 : b2, pfh[n][1], pfl[n][1]);
+        }
       }
       // positions outside start .. plast hold other data (possibly not finite): their value
       // elements are zeroed in the A fragments (keys 2 tig, 2 tig + 1 in a0 / a1, + 8 in a2 / a3)
@@ -1543,29 +1575,34 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
         va[1] &= km0;
         va[2] &= km1;
         va[3] &= km1;
-        mma_bf16_16816(o[dt], va, pfh[0], pfh[1]);
-        mma_bf16_16816(o[dt], va, pfl[0], pfl[1]);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          mma_bf16_16816(o[n][dt], va, pfh[n][0], pfh[n][1]);
+          mma_bf16_16816(o[n][dt], va, pfl[n][0], pfl[n][1]);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(EMPTY0 + 8u * s);
     }
     // the unit's end: o / l of each of this lane's columns
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      float l = lrow[hc];
-      l += __shfl_xor_sync(0xffffffffu, l, 4);
-      l += __shfl_xor_sync(0xffffffffu, l, 8);
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      if (!cv[hc]) continue;
-      const int col = warp * 8 + 2 * tig + hc, t = col / g, h = col - t * g;
-      float* ob = a.out + (size_t)(U.e0 + t) * a.out_stride + (size_t)(U.j * g + h) * HD;
-      const float rl = 1.0f / l;
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int dt = 0; dt < DT; ++dt) {
-        ob[dt * 16 + gid] = o[dt][hc] * rl;
-        ob[dt * 16 + gid + 8] = o[dt][2 + hc] * rl;
+      for (int hc = 0; hc < 2; ++hc) {
+        float l = lrow[n][hc];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (!cv[n][hc]) continue;
+        const int col = (warp * NT + n) * 8 + 2 * tig + hc, t = col / g, h = col - t * g;
+        float* ob = a.out + (size_t)(U.e0 + t) * a.out_stride + (size_t)(U.j * g + h) * HD;
+        const float rl = 1.0f / l;
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          ob[dt * 16 + gid] = o[n][dt][hc] * rl;
+          ob[dt * 16 + gid + 8] = o[n][dt][2 + hc] * rl;
+        }
       }
-    }
   }
 }
 
