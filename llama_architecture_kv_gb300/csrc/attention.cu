@@ -1283,7 +1283,7 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
 // ---------------------------------------------------------------------------------------
 // Causal attention of a prefill pass (Llama 3.1 8B Instruct card, attention.linnet prefill<S>:
 // token i of a prompt at position pos + i sees the positions s <= pos + i; bend-ml-llama law
-// causal).  The entries of a pass come in tiles: up to 128 / g consecutive prompt tokens of one
+// causal).  The entries of a pass come in tiles: up to 64 / g consecutive prompt tokens of one
 // cache row, at consecutive positions, with one attention start (0, or the prompt's first
 // position for packed prompts).  A unit is (tile, kv head j): its columns are the (token, head)
 // pairs t * g + h, and the keys and values of positions start .. the tile's last position are
@@ -1292,10 +1292,10 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
 // One CTA per SM walks the units (the host sorts them longest first, CTA c takes c, c + G, ...).
 // A producer warp streams 16-position chunks of the unit's keys and values through a ring of
 // shared-memory stages (TMA tensor copies, 128-byte swizzle; full / empty mbarriers), running on
-// into the next unit; eight consumer warps each own 16 of the tile's 128 columns (two 8-column
-// MMA tiles, so every key fragment feeds two MMAs) and read every chunk: scores S^T = K Q^T
-// (rows = the chunk's 16 positions, columns = the warp's (token, head) pairs; the queries as
-// bf16 hi + lo B fragments), an online softmax per column with the
+// into the next unit; eight consumer warps each own kPfNT 8-column MMA tiles of the tile's
+// columns and read every chunk: scores S^T = K Q^T (rows = the chunk's 16 positions, columns =
+// the warp's (token, head) pairs; the queries as bf16 hi + lo B fragments), an online softmax
+// per column with the
 // causal mask start <= s <= that token's position, and O^T += V^T P^T (the weights as hi + lo B
 // fragments).  A warp owns its columns' whole key range, so it writes o / l straight to the
 // output; nothing is merged across CTAs.  Every wait is bounded; after one runs out the CTA
@@ -1303,7 +1303,7 @@ cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
 // ---------------------------------------------------------------------------------------
 
 constexpr int kPfWarps = 8;              // consumer warps
-constexpr int kPfNT = 2;                 // 8-column MMA tiles per warp
+constexpr int kPfNT = 1;                 // 8-column MMA tiles per warp (two measured slower: fewer, longer units)
 constexpr int kPfCols = kPfWarps * 8 * kPfNT;  // (token, head) columns of a tile
 constexpr int kPfStages = 8;             // ring stages (16 positions of keys and values each)
 
@@ -1326,7 +1326,7 @@ LLM_HD size_t attn_prefill_smem() {
 int attn_prefill_tile_tokens(int g) { return kPfCols / g; }
 
 template <int HD>
-__global__ void __maxnreg__(224)
+__global__ void __launch_bounds__((kPfWarps + 1) * 32, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const AttnPrefillArgs a) {
   using P = PfShape<HD>;
@@ -1416,7 +1416,7 @@ __global__ void __maxnreg__(224)
     return;
   }
 
-  // ---- consumers: warp w owns columns 16w .. 16w + 15 (MMA tiles n = 0, 1) ----
+  // ---- consumers: warp w owns columns 8 kPfNT w .. 8 kPfNT (w + 1) - 1 (MMA tiles n) ----
   constexpr int NT = kPfNT;
   int it = 0;
   for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
@@ -1485,7 +1485,7 @@ __global__ void __maxnreg__(224)
       const int kb = k * CH;
       const uint32_t kreg = s_base + (uint32_t)(s * STAGE);
       const uint32_t vreg = kreg + (uint32_t)(CH * ROWB);
-      // scores: rows = positions kb + 0..15, columns = this warp's 16; even / odd k-steps in
+      // scores: rows = positions kb + 0..15, columns = this warp's; even / odd k-steps in
       // separate accumulators (shorter dependency chains)
       float sh[NT][2][4], sl[NT][2][4];
 #pragma unroll

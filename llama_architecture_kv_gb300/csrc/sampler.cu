@@ -275,18 +275,31 @@ LLM_D void draw_from_candidates(const SampleArgs& a, int b, const int32_t* cand,
     for (int j = tid; j < n; j += nt) chunk[j] = pre[c0 + j];
     __syncthreads();
     if (tid == 0) {
-      int j = 0;
-      for (; j + 8 <= n; j += 8) {
-        float w[8];
+      // 16 values at a time in registers, the next 16 loaded while these are added, so the
+      // dependent additions are the only latency left
+      float4* c4 = reinterpret_cast<float4*>(chunk);
+      const int n32 = n & ~15;
+      float4 cur[4], nxt[4];
+      if (n32 > 0)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) w[q] = chunk[j + q];
+        for (int q = 0; q < 4; ++q) cur[q] = c4[q];
+      for (int j = 0; j < n32; j += 16) {
+        if (j + 16 < n32)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          run = __fadd_rn(run, w[q]);
-          chunk[j + q] = run;
+          for (int q = 0; q < 4; ++q) nxt[q] = c4[(j >> 2) + 4 + q];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          run = __fadd_rn(run, cur[q].x); cur[q].x = run;
+          run = __fadd_rn(run, cur[q].y); cur[q].y = run;
+          run = __fadd_rn(run, cur[q].z); cur[q].z = run;
+          run = __fadd_rn(run, cur[q].w); cur[q].w = run;
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) c4[(j >> 2) + q] = cur[q];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
       }
-      for (; j < n; ++j) {
+      for (int j = n32; j < n; ++j) {
         run = __fadd_rn(run, chunk[j]);
         chunk[j] = run;
       }
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const Sampl
   grid_dep_wait();
   grid_dep_launch();
   const int b = blockIdx.x;
-  __shared__ float chunk[kRunChunk];
+  __shared__ __align__(16) float chunk[kRunChunk];
   const int32_t* is = a.idx + (size_t)b * 2 * a.V_pad;  // after 8 passes the sorted row is in buffer 0
   draw_from_candidates(a, b, is, min(a.step->k, a.V), a.pre + (size_t)b * a.V_pad, chunk);
 }
@@ -354,7 +367,7 @@ __global__ void __launch_bounds__(kSelectThreads) sample_topk_kernel(const Sampl
   __shared__ uint32_t wsum[kSelectThreads / 32];
   __shared__ unsigned long long cand[kSelectMax];
   __shared__ int32_t cand_id[kSelectMax];
-  __shared__ float chunk[kSelectMax];
+  __shared__ __align__(16) float chunk[kSelectMax];
 
   // ---- radix select: T = the key of rank k - 1 (0-based) in ascending key order ----
   uint32_t prefix = 0u, rank = (uint32_t)(k - 1);
