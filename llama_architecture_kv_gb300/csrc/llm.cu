@@ -485,7 +485,7 @@ enum { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GATEUP = 3, K_DOWN = 4, K_HEAD = 5, K_S
 SampleArgs sample_args(const llm_handle* h) {
   SampleArgs s = {};
   s.logits = h->logits; s.logits_stride = h->V; s.V = h->V; s.V_pad = h->V_pad;
-  s.keys = h->s_keys; s.idx = h->s_idx; s.pre = h->s_pre; s.hist = h->s_hist;
+  s.keys = h->s_keys; s.idx = h->s_idx; s.pre = h->s_pre; s.hist = h->s_hist; s.hist_per_row = kSampleHistPerRow;
   s.u = h->u_buf; s.ids = h->ids_buf; s.step = h->st;
   return s;
 }

@@ -23,7 +23,6 @@
 namespace llm {
 
 constexpr int kSampThreads = 1024;
-constexpr int kDigits = 16;
 constexpr int kSortMaxSlices = kSortMaxSlicesPerRow;
 
 LLM_D float exp_s(float x) {
@@ -126,7 +125,8 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const SampleArgs a
 // ---------------------------------------------------------------------------------------
 // temperature / top-k / top-p: a stable radix sort of each row, then the in-order sums
 // ---------------------------------------------------------------------------------------
-// Sort: least-significant-digit radix on the 32-bit order key, 4-bit digits, 8 passes; every
+// Sort: least-significant-digit radix on the 32-bit order key, 8-bit digits and 4 passes (4-bit
+// and 8 where the digit-count scratch is small, as in the fixed-array sampler); every
 // pass is count (per CTA slice) -> exclusive scan (per row, digit-major) -> stable scatter (each
 // CTA writes its slice in index order).  Stability keeps equal values in id order, so the sorted
 // row is exactly "largest value first, ties by lower id".
@@ -153,40 +153,43 @@ __global__ void __launch_bounds__(kSortThreads) sort_init_kernel(const SampleArg
   }
 }
 
+// DB-bit digits (4 or 8): 32 / DB passes of 2^DB bins
+template <int DB>
 __global__ void __launch_bounds__(kSortThreads) sort_count_kernel(const SampleArgs a, int pass) {
+  constexpr int ND = 1 << DB;
+  constexpr uint32_t MASK = ND - 1;
   grid_dep_wait();
   grid_dep_launch();
-  const int b = blockIdx.y, c = blockIdx.x, NB = gridDim.x, S = sort_slice(a.V), sh = 4 * pass;
+  const int b = blockIdx.y, c = blockIdx.x, NB = gridDim.x, S = sort_slice(a.V), sh = DB * pass;
   const int s0 = c * S, s1 = min(a.V, s0 + S);
   const uint32_t* ks = a.keys + (size_t)b * 2 * a.V_pad + (pass & 1) * a.V_pad;
-  __shared__ uint32_t cnt[kDigits];
-  if (threadIdx.x < kDigits) cnt[threadIdx.x] = 0u;
+  __shared__ uint32_t cnt[ND];
+  for (int i = threadIdx.x; i < ND; i += kSortThreads) cnt[i] = 0u;
   __syncthreads();
   const int lane = threadIdx.x & 31;
   for (int i0 = s0; i0 < s1; i0 += kSortThreads) {
     const int i = i0 + threadIdx.x;
-    const uint32_t d = i < s1 ? (ks[i] >> sh) & 15u : 16u;
+    const uint32_t d = i < s1 ? (ks[i] >> sh) & MASK : (uint32_t)ND;
     const uint32_t peers = __match_any_sync(0xffffffffu, d);
-    if (d < 16u && lane == __ffs(peers) - 1) atomicAdd(&cnt[d], (uint32_t)__popc(peers));
+    if (d < (uint32_t)ND && lane == __ffs(peers) - 1) atomicAdd(&cnt[d], (uint32_t)__popc(peers));
   }
   __syncthreads();
-  if (threadIdx.x < kDigits) a.hist[((size_t)b * kDigits + threadIdx.x) * NB + c] = cnt[threadIdx.x];
+  for (int i = threadIdx.x; i < ND; i += kSortThreads) a.hist[((size_t)b * ND + i) * NB + c] = cnt[i];
 }
 
+// exclusive scan of one row's ND * NB digit counts, digit-major (thread t scans a contiguous run)
+template <int DB>
 __global__ void __launch_bounds__(kSortThreads) sort_scan_kernel(const SampleArgs a, int NB) {
+  constexpr int ND = 1 << DB;
   grid_dep_wait();
   grid_dep_launch();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t* h = a.hist + (size_t)b * kDigits * NB;
-  const int n = kDigits * NB;                    // at most 16 * 64 = 1024 entries
+  uint32_t* h = a.hist + (size_t)b * ND * NB;
+  const int n = ND * NB;                         // at most 256 * 64 = 16384 entries
   const int per = (n + kSortThreads - 1) / kSortThreads;
-  uint32_t loc[4], sum = 0u;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int i = tid * per + e;
-    loc[e] = (e < per && i < n) ? h[i] : 0u;
-    sum += loc[e];
-  }
+  const int i0 = tid * per, i1 = min(n, i0 + per);
+  uint32_t sum = 0u;
+  for (int i = i0; i < i1; ++i) sum += h[i];
   uint32_t incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -199,20 +202,20 @@ __global__ void __launch_bounds__(kSortThreads) sort_scan_kernel(const SampleArg
   uint32_t before = 0u;
   for (int w = 0; w < warp; ++w) before += wt[w];
   uint32_t run = before + incl - sum;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int i = tid * per + e;
-    if (e < per && i < n) {
-      h[i] = run;
-      run += loc[e];
-    }
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t v = h[i];
+    h[i] = run;
+    run += v;
   }
 }
 
+template <int DB>
 __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(const SampleArgs a, int pass) {
+  constexpr int ND = 1 << DB;
+  constexpr uint32_t MASK = ND - 1;
   grid_dep_wait();
   grid_dep_launch();
-  const int b = blockIdx.y, c = blockIdx.x, NB = gridDim.x, S = sort_slice(a.V), sh = 4 * pass;
+  const int b = blockIdx.y, c = blockIdx.x, NB = gridDim.x, S = sort_slice(a.V), sh = DB * pass;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = kSortThreads / 32;
   const int s0 = c * S, s1 = min(a.V, s0 + S);
@@ -221,27 +224,27 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(const Sample
   uint32_t* kd = a.keys + rowk + ((pass + 1) & 1) * a.V_pad;
   const int32_t* is = a.idx + rowk + (pass & 1) * a.V_pad;
   int32_t* id = a.idx + rowk + ((pass + 1) & 1) * a.V_pad;
-  __shared__ uint32_t base[kDigits], tot[kDigits], wcnt[NW][kDigits], wpre[NW][kDigits];
-  if (tid < kDigits) base[tid] = a.hist[((size_t)b * kDigits + tid) * NB + c];
+  __shared__ uint32_t base[ND], tot[ND], wcnt[NW][ND], wpre[NW][ND];
+  for (int i = tid; i < ND; i += kSortThreads) base[i] = a.hist[((size_t)b * ND + i) * NB + c];
   for (int i0 = s0; i0 < s1; i0 += kSortThreads) {
-    if (tid < NW * kDigits) wcnt[tid / kDigits][tid % kDigits] = 0u;
+    for (int i = tid; i < NW * ND; i += kSortThreads) wcnt[i / ND][i % ND] = 0u;
     __syncthreads();
     const int i = i0 + tid;
     const bool valid = i < s1;
     const uint32_t key = valid ? ks[i] : 0u;
     const int32_t idv = valid ? is[i] : 0;
-    const uint32_t d = valid ? (key >> sh) & 15u : 16u;
+    const uint32_t d = valid ? (key >> sh) & MASK : (uint32_t)ND;
     const uint32_t peers = __match_any_sync(0xffffffffu, d);
     const uint32_t rank = __popc(peers & ((1u << lane) - 1u));
     if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] = __popc(peers);
     __syncthreads();
-    if (tid < kDigits) {
+    for (int dd = tid; dd < ND; dd += kSortThreads) {
       uint32_t r = 0u;
       for (int w = 0; w < NW; ++w) {
-        wpre[w][tid] = r;
-        r += wcnt[w][tid];
+        wpre[w][dd] = r;
+        r += wcnt[w][dd];
       }
-      tot[tid] = r;
+      tot[dd] = r;
     }
     __syncthreads();
     if (valid) {
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(const Sample
       id[dst] = idv;
     }
     __syncthreads();
-    if (tid < kDigits) base[tid] += tot[tid];
+    for (int dd = tid; dd < ND; dd += kSortThreads) base[dd] += tot[dd];
   }
 }
 
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const Sampl
   grid_dep_launch();
   const int b = blockIdx.x;
   __shared__ __align__(16) float chunk[kRunChunk];
-  const int32_t* is = a.idx + (size_t)b * 2 * a.V_pad;  // after 8 passes the sorted row is in buffer 0
+  const int32_t* is = a.idx + (size_t)b * 2 * a.V_pad;  // after an even number of passes the sorted row is in buffer 0
   draw_from_candidates(a, b, is, min(a.step->k, a.V), a.pre + (size_t)b * a.V_pad, chunk);
 }
 
@@ -505,10 +508,15 @@ cudaError_t launch_sample(const SampleArgs& a, int B, bool greedy, cudaStream_t 
   if (select) return launch(sample_topk_kernel, dim3(B), kSelectThreads, a, s, pdl);
   const int NB = sample_slices(a.V);
   cudaError_t e = launch(sort_init_kernel, dim3(NB, B), kSortThreads, a, s, pdl);
-  for (int pass = 0; pass < 8 && e == cudaSuccess; ++pass) {
-    e = launch2(sort_count_kernel, dim3(NB, B), kSortThreads, a, pass, s, true);
-    if (e == cudaSuccess) e = launch2(sort_scan_kernel, dim3(B), kSortThreads, a, NB, s, true);
-    if (e == cudaSuccess) e = launch2(sort_scatter_kernel, dim3(NB, B), kSortThreads, a, pass, s, true);
+  // 8-bit digits (four passes) where the caller's digit counts have room, else 4-bit (eight)
+  const bool wide = a.hist_per_row >= (size_t)256 * NB;
+  const int npass = wide ? 4 : 8;
+  for (int pass = 0; pass < npass && e == cudaSuccess; ++pass) {
+    e = launch2(wide ? sort_count_kernel<8> : sort_count_kernel<4>, dim3(NB, B), kSortThreads, a, pass, s, true);
+    if (e == cudaSuccess)
+      e = launch2(wide ? sort_scan_kernel<8> : sort_scan_kernel<4>, dim3(B), kSortThreads, a, NB, s, true);
+    if (e == cudaSuccess)
+      e = launch2(wide ? sort_scatter_kernel<8> : sort_scatter_kernel<4>, dim3(NB, B), kSortThreads, a, pass, s, true);
   }
   if (e == cudaSuccess) e = launch(sample_final_kernel, dim3(B), kFinalThreads, a, s, true);
   return e;

@@ -12,14 +12,15 @@ struct SampleArgs {
   uint32_t* keys;        // scratch [B][2][V_pad]
   int32_t* idx;          // scratch [B][2][V_pad]
   float* pre;            // scratch [B][V_pad]: weights, then their running sums
-  uint32_t* hist;        // scratch [B][16][sample_slices(V)]: digit counts, then offsets, per CTA slice
+  uint32_t* hist;        // scratch [B][digits][sample_slices(V)]: digit counts, then offsets, per CTA slice
+  size_t hist_per_row;   // uint32 entries of hist per row: 256 digits (8-bit) need 256 * slices
   const float* u;        // [B] uniform draws
   int32_t* ids;          // [B] drawn ids
   const StepState* step; // temp, k, p
 };
 
 constexpr int kSortMaxSlicesPerRow = 64;
-constexpr size_t kSampleHistPerRow = 16 * kSortMaxSlicesPerRow;  // uint32 entries a row needs at most
+constexpr size_t kSampleHistPerRow = 256 * kSortMaxSlicesPerRow;  // uint32 entries a row needs at most (8-bit digits)
 
 int sample_slices(int V);
 // greedy: one argmax kernel; select (top-k with k <= sample_select_max()): one radix-select

@@ -376,7 +376,7 @@ def test_step_kernel_counts():
     # tensor-core path, per layer: split activations + GEMM for each projection, the Q/K/V finish;
     # the head: split + GEMM, and a sum of its K splits when it has more than one
     assert pkg.llm_step_kernels(g.h, 16, 0.0) - greedy_gemv in (5 * L + 1, 5 * L + 2)
-    assert pkg.llm_step_kernels(g.h, 4, 0.8) == greedy_gemv + 25  # 8 passes x 3 sort kernels + init + draw
+    assert pkg.llm_step_kernels(g.h, 4, 0.8) == greedy_gemv + 13  # 4 passes x 3 sort kernels + init + draw
     assert pkg.llm_step_kernels(g.h, 4, 0.8, 50) == greedy_gemv  # top-50: one selection kernel
     with pytest.raises(pkg.LlmError):
         pkg.llm_step_kernels(g.h, 21, 0.0)
