@@ -630,6 +630,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   // writes in the row)
   struct Seg {
     int b, j, k0, k1, kv0, kv1, tb, ts, tw;
+    int kbase;  // key-map row of position 0 of (b, j) when the step has no page table, else -1
   };
   auto seg = [&](long long st, Seg& sg, long long& next) {
     const long long bj = st / nchk;
@@ -645,6 +646,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     sg.kv0 = sg.k0 > cs ? sg.k0 : cs;
     sg.kv1 = sg.k1 < nb ? sg.k1 : nb;
     if (sg.kv1 < sg.kv0) sg.kv1 = sg.kv0;
+    sg.kbase = -1;
+    if (!a.step->table) {
+      int r, pp;
+      cache_slot(a.step, a.cap, sg.b, 0, r, pp);
+      sg.kbase = a.krow0 + (r * a.kv + sg.j) * a.cap;
+    }
     next = end;
   };
 
@@ -668,13 +675,20 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     }
   };
   settle();
+  int islot = 0;  // issued % NR
   auto issue = [&]() {
-    const int slot = issued % NR;
+    const int slot = islot;
+    if (++islot == NR) islot = 0;
     const int pb = (is.kv0 + iq) * CH;
-    // the cache row and position holding position pb (a chunk never crosses a page)
-    int r, pp;
-    cache_slot(a.step, a.cap, is.b, pb, r, pp);
-    const int krow = a.krow0 + (r * a.kv + is.j) * a.cap + pp;
+    // the key-map row holding position pb (a chunk never crosses a page)
+    int krow;
+    if (is.kbase >= 0) {
+      krow = is.kbase + pb;
+    } else {
+      int r, pp;
+      cache_slot(a.step, a.cap, is.b, pb, r, pp);
+      krow = a.krow0 + (r * a.kv + is.j) * a.cap + pp;
+    }
     const uint32_t bar = bars + 8u * (warp * NR + slot);
     const uint32_t dst = s_base + (uint32_t)((warp * NR + slot) * BUF);
     fence_proxy_async_smem();
@@ -728,6 +742,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   const int mi = lane >> 3, mr = lane & 7;
   bool ok = true;
   int consumed = 0;
+  int cslot = 0;       // consumed % NR
+  uint32_t cpar = 0u;  // (consumed / NR) & 1
 
   // the splits of (row b, kv head j) merge in rank 0: every CTA stores its partial into rank 0's
   // shared memory (distributed shared memory), one cluster barrier publishes them, and rank 0
@@ -801,11 +817,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
 #pragma unroll
     for (int n = 0; n < NG; ++n) mrow[n][0] = mrow[n][1] = -INFINITY, lrow[n][0] = lrow[n][1] = 0.f;
     for (int ci = warp; ci < nch && ok; ci += NW) {
-      const int slot = consumed % NR;
+      const int slot = cslot;
       const uint32_t bar = bars + 8u * (warp * NR + slot);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar, (uint32_t)(consumed / NR) & 1u, kAttnWaitCycles));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar, cpar, kAttnWaitCycles));
       if (!ok) break;
       ++consumed;
+      if (++cslot == NR) cslot = 0, cpar ^= 1u;
       const int pb = p0 + ci * CH;
       const int nv = min(CH, p1 - pb);
       const uint32_t kreg = s_base + (uint32_t)((warp * NR + slot) * BUF);
