@@ -358,6 +358,7 @@ constexpr int kTmaWarps = 8;
 constexpr int kPiece = 4096;              // bytes of one row per step
 constexpr int kStepBytes = 2 * kPiece;    // both rows of a group
 constexpr int kTmaMaxSteps = 2;           // steps in flight per warp
+constexpr int kTmaXr = 4;                 // float4s of the input a thread keeps in registers
 constexpr uint64_t kTmaWaitCycles = 4000000000ull;  // SM cycles: about 2 s at 2 GHz
 static int g_smem_optin = 0;              // set by gemv_prepare
 
@@ -380,7 +381,6 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
   const uint32_t bars = ring_s + (uint32_t)(NW * ns * kStepBytes);
   float* part = reinterpret_cast<float*>(ring + (size_t)NW * ns * (kStepBytes + 8));  // [steps][2]
   __shared__ float red[NW];
-  __shared__ float s_inv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int groups = (a.rows + 1) >> 1;
@@ -414,43 +414,86 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
   };
   if (lane == 0)
     for (int t = 0; t < ns && t < total; ++t) issue(t);
+
+  // the (normalized) input, f32, in its two planes.  Up to kTmaXr float4s per thread stay in
+  // registers, so the input is read once (one round trip after the wait); the gains are constant
+  // and are read before the wait.  Thread i owns float4s i, i + NT, ... in both paths, so the sum
+  // of squares has the same order either way.
+  constexpr int NT = NW * 32;
+  const int c4 = cols >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(a.x);
+  const float4* gr4 = reinterpret_cast<const float4*>(a.gain);
+  const bool in_regs = c4 <= kTmaXr * NT;
+  float4 gv[kTmaXr];
+  if constexpr (NORM) {
+    if (in_regs) {
+#pragma unroll
+      for (int k = 0; k < kTmaXr; ++k)
+        if (tid + k * NT < c4) gv[k] = __ldg(gr4 + tid + k * NT);
+    }
+  }
   grid_dep_wait();
   grid_dep_launch();
 
-  // the (normalized) input, f32, in its two planes
-  const int c4 = cols >> 2;
-  const float4* xr = reinterpret_cast<const float4*>(a.x);
-  float inv = 1.f;
-  if constexpr (NORM) {
-    float ss = 0.f;
-    for (int i = tid; i < c4; i += NW * 32) {
-      const float4 v = __ldg(xr + i);
-      ss = fmaf(v.x, v.x, ss);
-      ss = fmaf(v.y, v.y, ss);
-      ss = fmaf(v.z, v.z, ss);
-      ss = fmaf(v.w, v.w, ss);
-    }
+  auto put = [&](int i, float4 v) { reinterpret_cast<float4*>((i & 1) ? xhi : xlo)[i >> 1] = v; };
+  auto scale = [](float4 v, float4 g, float inv) {
+    v.x = __fmul_rn(g.x, __fmul_rn(inv, v.x));
+    v.y = __fmul_rn(g.y, __fmul_rn(inv, v.y));
+    v.z = __fmul_rn(g.z, __fmul_rn(inv, v.z));
+    v.w = __fmul_rn(g.w, __fmul_rn(inv, v.w));
+    return v;
+  };
+  // 1 / rms from the warps' sums of squares (every thread adds them in the same order)
+  auto inv_rms = [&](float ss) {
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < NW; ++w) t += red[w];
-      s_inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)cols), a.eps)));
-    }
-    __syncthreads();
-    inv = s_inv;
-  }
-  for (int i = tid; i < c4; i += NW * 32) {
-    float4 v = __ldg(xr + i);
+    float t = 0.f;
+    for (int w = 0; w < NW; ++w) t += red[w];
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)cols), a.eps)));
+  };
+  if (in_regs) {
+    float4 xv[kTmaXr];
+#pragma unroll
+    for (int k = 0; k < kTmaXr; ++k)
+      if (tid + k * NT < c4) xv[k] = __ldg(xr + tid + k * NT);
     if constexpr (NORM) {
-      const float4 g = __ldg(reinterpret_cast<const float4*>(a.gain) + i);
-      v.x = __fmul_rn(g.x, __fmul_rn(inv, v.x));
-      v.y = __fmul_rn(g.y, __fmul_rn(inv, v.y));
-      v.z = __fmul_rn(g.z, __fmul_rn(inv, v.z));
-      v.w = __fmul_rn(g.w, __fmul_rn(inv, v.w));
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < kTmaXr; ++k)
+        if (tid + k * NT < c4) {
+          ss = fmaf(xv[k].x, xv[k].x, ss);
+          ss = fmaf(xv[k].y, xv[k].y, ss);
+          ss = fmaf(xv[k].z, xv[k].z, ss);
+          ss = fmaf(xv[k].w, xv[k].w, ss);
+        }
+      const float inv = inv_rms(ss);
+#pragma unroll
+      for (int k = 0; k < kTmaXr; ++k)
+        if (tid + k * NT < c4) xv[k] = scale(xv[k], gv[k], inv);
     }
-    reinterpret_cast<float4*>((i & 1) ? xhi : xlo)[i >> 1] = v;
+#pragma unroll
+    for (int k = 0; k < kTmaXr; ++k)
+      if (tid + k * NT < c4) put(tid + k * NT, xv[k]);
+  } else {
+    float inv = 1.f;
+    if constexpr (NORM) {
+      float ss = 0.f;
+      for (int i = tid; i < c4; i += NT) {
+        const float4 v = __ldg(xr + i);
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+      }
+      inv = inv_rms(ss);
+    }
+#pragma unroll 4
+    for (int i = tid; i < c4; i += NT) {
+      float4 v = __ldg(xr + i);
+      if constexpr (NORM) v = scale(v, __ldg(gr4 + i), inv);
+      put(i, v);
+    }
   }
   __syncthreads();
 
