@@ -702,6 +702,11 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
     iq += NW;
     settle();
   };
+  // the first segment, from the step state (written by the step prologue, long complete): before
+  // the wait, so that no dependent read of it lies on the path after the previous kernel
+  Seg s0 = {};
+  long long nx0 = c0;
+  if (c0 < c1) seg(c0, s0, nx0);
   if (lane == 0) {
     tma_prefetch_map(&kmap);
     tma_prefetch_map(&vmap);
@@ -731,12 +736,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
       *reinterpret_cast<uint32_t*>(ql + r * QP + e) = lo;
     }
   };
-  if (c0 < c1) {
-    Seg s0;
-    long long nx;
-    seg(c0, s0, nx);
-    load_q(s0.b, s0.j);
-  }
+  if (c0 < c1) load_q(s0.b, s0.j);
   __syncthreads();
 
   const int mi = lane >> 3, mr = lane & 7;
@@ -789,7 +789,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1)
   long long next = c0;
   for (long long st = c0; st < c1; st = next, ++lu) {
     Seg sg;
-    seg(st, sg, next);
+    if (st == c0) {
+      sg = s0;
+      next = nx0;
+    } else {
+      seg(st, sg, next);
+    }
     const int b = sg.b, j = sg.j, k0 = sg.k0, ts = sg.ts;
     const int p0 = sg.kv0 * CH, p1 = min(sg.tb + 1, sg.kv1 * CH), nch = sg.kv1 - sg.kv0;  // nch may be 0
     // this segment's queries as B fragments (k = dimensions, n = heads), hi and lo, kept in

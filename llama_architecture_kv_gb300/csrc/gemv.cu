@@ -432,6 +432,34 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
         if (tid + k * NT < c4) gv[k] = __ldg(gr4 + tid + k * NT);
     }
   }
+  // the epilogue's other inputs of group g: the residual rows (EPI_RESID), or the step's
+  // position, its RoPE factors and the cache slot (EPI_QKV).  For this thread's first group they
+  // are read before the wait: the RoPE tables are constant, the step state was written by the
+  // step prologue, and the residual two kernels back (o_proj: the previous layer's down; down:
+  // o_proj), all complete before this kernel can start; the residual is read through L2.
+  struct EpiIn {
+    float r0, r1, c, s;
+    int pos, r, pp;
+  };
+  auto epi_in = [&](int g, bool early) {
+    EpiIn in = {0.f, 0.f, 0.f, 0.f, 0, 0, 0};
+    if constexpr (EPI == EPI_RESID) {
+      in.r0 = early ? __ldcg(a.resid + 2 * g) : a.resid[2 * g];
+      if (2 * g + 1 < a.rows) in.r1 = early ? __ldcg(a.resid + 2 * g + 1) : a.resid[2 * g + 1];
+    } else if constexpr (EPI == EPI_QKV) {
+      const int R = 2 * g, half = a.hd >> 1;
+      const int head = R / a.hd, e = (R - head * a.hd) >> 1;
+      in.pos = row_pos(a.step, 0);
+      if (head < a.H + a.kv) {
+        in.c = __ldg(a.rope_cos + (size_t)in.pos * half + e);
+        in.s = __ldg(a.rope_sin + (size_t)in.pos * half + e);
+      }
+      if (head >= a.H) cache_slot(a.step, a.cap, 0, in.pos, in.r, in.pp);
+    }
+    return in;
+  };
+  EpiIn pre = {0.f, 0.f, 0.f, 0.f, 0, 0, 0};
+  if (tid < g1 - g0) pre = epi_in(g0 + tid, true);
   grid_dep_wait();
   grid_dep_launch();
 
@@ -561,36 +589,36 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
       v1 += part[2 * (i * ppr + pc) + 1];
     }
     const int g = g0 + i;
-    if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+    if constexpr (EPI == EPI_STORE) {
       const int r0 = 2 * g;
-      a.out[r0] = EPI == EPI_RESID ? __fadd_rn(a.resid[r0], v0) : v0;
-      if (r0 + 1 < a.rows) a.out[r0 + 1] = EPI == EPI_RESID ? __fadd_rn(a.resid[r0 + 1], v1) : v1;
+      a.out[r0] = v0;
+      if (r0 + 1 < a.rows) a.out[r0 + 1] = v1;
+    } else if constexpr (EPI == EPI_RESID) {
+      const EpiIn in = i == tid ? pre : epi_in(g, false);
+      const int r0 = 2 * g;
+      a.out[r0] = __fadd_rn(in.r0, v0);
+      if (r0 + 1 < a.rows) a.out[r0 + 1] = __fadd_rn(in.r1, v1);
     } else if constexpr (EPI == EPI_SWIGLU) {
       const float si = __fdiv_rn(v0, __fadd_rn(1.0f, expf(-v0)));
       a.out[g] = __fmul_rn(si, v1);
     } else {
-      const int R = 2 * g;
-      const int pos = row_pos(a.step, 0), half = a.hd >> 1;
+      const EpiIn in = i == tid ? pre : epi_in(g, false);
+      const int R = 2 * g, half = a.hd >> 1;
       const int head = R / a.hd, e = (R - head * a.hd) >> 1;
       if (head < a.H + a.kv) {
-        const float c = a.rope_cos[(size_t)pos * half + e], s = a.rope_sin[(size_t)pos * half + e];
-        const float lo = __fadd_rn(__fmul_rn(v0, c), __fmul_rn(-v1, s));
-        const float hi = __fadd_rn(__fmul_rn(v1, c), __fmul_rn(v0, s));
+        const float lo = __fadd_rn(__fmul_rn(v0, in.c), __fmul_rn(-v1, in.s));
+        const float hi = __fadd_rn(__fmul_rn(v1, in.c), __fmul_rn(v0, in.s));
         if (head < a.H) {
           float* qo = a.q_out + (size_t)head * a.hd;
           qo[e] = lo;
           qo[e + half] = hi;
         } else {
-          int r, pp;
-          cache_slot(a.step, a.cap, 0, pos, r, pp);
-          const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H)) * a.cap + pp) * a.hd;
+          const size_t ci = (((size_t)in.r * a.kv + (size_t)(head - a.H)) * a.cap + in.pp) * a.hd;
           store_elem<1>(a.kc, ci + e, lo);
           store_elem<1>(a.kc, ci + e + half, hi);
         }
       } else {
-        int r, pp;
-        cache_slot(a.step, a.cap, 0, pos, r, pp);
-        const size_t ci = (((size_t)r * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + pp) * a.hd;
+        const size_t ci = (((size_t)in.r * a.kv + (size_t)(head - a.H - a.kv)) * a.cap + in.pp) * a.hd;
         store_elem<1>(a.vc, ci + e, v0);
         store_elem<1>(a.vc, ci + e + half, v1);
       }
