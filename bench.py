@@ -232,10 +232,35 @@ def oracle_for(w, blob, cap):
     return m
 
 
+def blob_step_bytes(w, blob):
+    """The weight bytes a decode step reads, from the weight blob: every weight but the embedding
+    table (a tied head reads that table in full)."""
+    s = w.shape
+    es = 2 if s.bf16 else 4
+    return blob.nbytes - (0 if s.tied else s.vocab * s.d * es)
+
+
+def workload_config(w, args, world, wbytes):
+    """The `config` of a bench line (both arms): the workload as the GPU arm runs it."""
+    s, B, P = w.shape, w.batch, w.prompt
+    pos0 = P if P else w.fill
+    temp, k_, p_ = w.temp, (w.top_k or s.vocab), w.top_p
+    rows = getattr(args, "rows", False)
+    return {"workload": w.name, "batch": B, "prompt": P, "cache_positions": pos0,
+            "weights": "bf16" if s.bf16 else "f32", "kv_cache": "bf16" if s.bf16 else "f32",
+            "sampling": "greedy" if temp == 0 else f"temp {temp} top-k {k_} top-p {p_}",
+            "positions": ("own per row (decode_rows): row b at %d - %d b" % (pos0, pos0 // (2 * B))
+                          if rows else "shared"),
+            "loop": "llm_generate_dev (graphs of 8 chained steps)" if args.generate else "llm_step_dev per step",
+            "l2": "inputs larger than L2 (weights %.1f GB per step)" % (wbytes / 1e9),
+            "parallelism": f"replicas x{world}"}
+
+
 def time_oracle_layers(m, w, pos, nl, steps, warmup):
     """Per timed step: one token's embedding plus `nl` consecutive layers (rotating through the
     model), and the final norm + LM head on every (L / nl)-th step, so that L / nl steps do
-    exactly one token's work.  Returns seconds per token (the mean step time x L / nl)."""
+    exactly one token's work.  Returns (seconds per token = the mean step time x L / nl, the mean
+    step time, steps timed)."""
     L = w.shape.layers
     per_token = max(1, L // nl)
     times = []
@@ -249,7 +274,7 @@ def time_oracle_layers(m, w, pos, nl, steps, warmup):
             m.head()
         if i >= warmup:
             times.append(time.perf_counter() - t0)
-    return float(np.mean(times)) * per_token, len(times)
+    return float(np.mean(times)) * per_token, float(np.mean(times)), len(times)
 
 
 def run_reference(args):
@@ -262,7 +287,7 @@ def run_reference(args):
     m = oracle_for(w, blob, cap)
     nl = max(1, min(args.ref_layers, w.shape.layers))
     t0 = time.perf_counter()
-    sec_per_tok, n = time_oracle_layers(m, w, w.prompt, nl, args.steps, args.warmup)
+    sec_per_tok, sec_per_step, n = time_oracle_layers(m, w, w.prompt, nl, args.steps, args.warmup)
     wall = time.perf_counter() - t0
     value = w.batch / (sec_per_tok * w.batch)  # one row at a time: tokens per second of one row
     sample = (f"row 0 of batch {w.batch} at position {w.prompt} over a synthetic {w.prompt}-position "
@@ -271,9 +296,11 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": "decode tok/s", "value": value, "unit": "tok/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": sec_per_tok * 1e3, "higher_is_better": True, "scaling": "weak",
+        # ms_per_step: a timed step as it ran (the sample); ms_per_token: the scaled full token
+        "ms_per_step": sec_per_step * 1e3, "ms_per_token": sec_per_tok * 1e3,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "prompt": w.prompt},
+        "config": workload_config(w, args, world, blob_step_bytes(w, blob)),
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -569,14 +596,7 @@ def run_ours(args):
         "metric": "decode tok/s", "value": value, "unit": "tok/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "batch": B, "prompt": P, "cache_positions": pos0,
-                   "weights": "bf16" if s.bf16 else "f32", "kv_cache": "bf16" if s.bf16 else "f32",
-                   "sampling": "greedy" if temp == 0 else f"temp {temp} top-k {k_} top-p {p_}",
-                   "positions": ("own per row (decode_rows): row b at %d - %d b" % (pos0, pos0 // (2 * B))
-                                 if rowpos is not None else "shared"),
-                   "loop": "llm_generate_dev (graphs of 8 chained steps)" if args.generate else "llm_step_dev per step",
-                   "l2": "inputs larger than L2 (weights %.1f GB per step)" % (wbytes / 1e9),
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, args, world, wbytes),
         "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clk, "prefill": prefill, "batch32": b32,
         # a generation step replaces the prologue by its own and ends with one copy of its draws;
