@@ -347,6 +347,30 @@ def test_tensor_core_path_teacher_forced(name, shape, B):
     g.close()
 
 
+@pytest.mark.parametrize("ffn", [6000, 17000], ids=["mlp6000", "mlp17000"])
+def test_batch1_gemv_wide_mlp_teacher_forced(ffn):
+    # batch 1 on the bulk-copy GEMVs with a down projection input of 6000 floats (held in
+    # registers, every load in flight) and of 17000 (staged in a loop): against the oracle
+    shape = shrink(WORKLOADS["llama8b_b1"].shape, layers=2, kv=2, ffn=ffn, vocab=1000)
+    S, steps, cap = 4, 4, 12
+    blob = synth.model_blob(shape, 95)
+    g = pkg.Model(shape, blob, max_batch=1, max_seq=cap)
+    ref = oracle.Model(oracle.cfg_of(shape, 1, cap), blob)
+    prompt = synth.tokens(96, 0, S, shape.vocab)
+    agree = []
+    lg = g.prefill(prompt[None], 0)
+    check_bf16(lg[0], ref.prefill(0, prompt, 0), agree)
+    tok = np.array([np.argmax(lg[0])], np.int32)
+    for t in range(S, S + steps):
+        ids, lg = g.step(tok, t, logits=True)
+        check_bf16(lg[0], ref.forward(0, int(tok[0]), t), agree)
+        assert int(ids[0]) == oracle.argmax(lg[0])
+        tok = ids
+    assert np.mean(agree) >= ARGMAX_AGREE
+    ref.close()
+    g.close()
+
+
 def test_tensor_core_and_gemv_paths_agree():
     shape = TC_SHAPES[1][1]
     B, S, cap = 16, 6, 10
