@@ -78,7 +78,8 @@ typedef struct llm_config {
   int32_t tc_min_batch; /* bf16 only: steps of at least this many rows run the projections on the
                            tensor cores (TMA-fed tcgen05 GEMM), fewer rows on the weight-streaming
                            GEMV; 0: the library default (2: only batch-1 steps stream through the
-                           GEMV); above max(max_batch, max_tokens): never */
+                           GEMV); above max(max_batch, max_tokens): never.  Models whose hidden
+                           or MLP width exceeds 16384 keep every step on the GEMV */
   int32_t max_tokens;   /* prompt tokens one prefill pass processes together (llm_prefill with
                            S > 1, llm_prefill_packed): activations and attention scratch are sized
                            for max(max_batch, max_tokens) rows; 0: the library default (512) */

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 constexpr int kPrepThreads = 128;
 constexpr int kPrepCluster = 8;   // CTAs sharing one activation row (a thread-block cluster)
-constexpr int kPrepMaxV = 4;      // float4 of the row per thread (K <= 8 * 128 * 4 * 4 = 16384)
+constexpr int kPrepMaxV = 4;      // float4 of the row per thread (K <= 8 * 128 * 4 * 4 = kTcMaxK)
 constexpr int kMaxSplits = 16;  // K splits a reader adds (plan_tc stays within it)
 
 LLM_D float silu_mul(float g, float u) { return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u); }

@@ -11,6 +11,7 @@ constexpr int kTcN = 256;         // weight rows per tile (the MMA's N)
 constexpr int kTcK = 64;          // K elements per stage (one 128-byte swizzle row)
 constexpr int kTcRows = 64;       // activation rows per tile (hi in MMA rows 0..63, lo in 64..127)
 constexpr int kTcDefaultMinBatch = 2;   // rows from which a step uses the tensor cores
+constexpr int kTcMaxK = 16384;          // widest projection input the prep kernels stage (hidden, MLP)
 
 // out[s][j][r] = sum over K block range s of W[r][c] * x'[j][c]: raw split sums, f32
 struct TcArgs {

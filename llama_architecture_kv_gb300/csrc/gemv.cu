@@ -359,7 +359,6 @@ constexpr int kPiece = 4096;              // bytes of one row per step
 constexpr int kStepBytes = 2 * kPiece;    // both rows of a group
 constexpr int kTmaMaxSteps = 2;           // steps in flight per warp
 constexpr int kTmaXr = 4;                 // float4s of the input a thread keeps in registers
-constexpr int kTmaXrWide = 16;            // the same for an input without norm (a wider row)
 constexpr uint64_t kTmaWaitCycles = 4000000000ull;  // SM cycles: about 2 s at 2 GHz
 static int g_smem_optin = 0;              // set by gemv_prepare
 
@@ -481,23 +480,7 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) gemv_tma_kernel(const GemvA
     for (int w = 0; w < NW; ++w) t += red[w];
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)cols), a.eps)));
   };
-  // a plain input too long for kTmaXr (the down projection's): up to kTmaXrWide float4s per
-  // thread, every load in flight at once
-  bool wide = false;
-  if constexpr (!NORM) {
-    if (!in_regs && c4 <= kTmaXrWide * NT) {
-      wide = true;
-      float4 xw[kTmaXrWide];
-#pragma unroll
-      for (int k = 0; k < kTmaXrWide; ++k)
-        if (tid + k * NT < c4) xw[k] = __ldg(xr + tid + k * NT);
-#pragma unroll
-      for (int k = 0; k < kTmaXrWide; ++k)
-        if (tid + k * NT < c4) put(tid + k * NT, xw[k]);
-    }
-  }
-  if (wide) {
-  } else if (in_regs) {
+  if (in_regs) {
     float4 xv[kTmaXr];
 #pragma unroll
     for (int k = 0; k < kTmaXr; ++k)

@@ -998,8 +998,9 @@ llm_status llm_create(const llm_config* cfg, const void* weights, uint64_t nbyte
   if ((ce = gemv_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("gemv kernel attributes", ce);
   // tensor-core path: bf16 weights, rows a whole number of 16-byte chunks (checked above)
   const int tc_min = c.tc_min_batch > 0 ? c.tc_min_batch : kTcDefaultMinBatch;
-  // (debug_trace handles keep every step on the GEMV: the traced buffers are written in order there)
-  if (h->wt && !c.debug_trace && tc_min <= h->NT && tc_available()) {
+  // (debug_trace handles keep every step on the GEMV: the traced buffers are written in order there;
+  // so do models whose hidden or MLP width exceeds what the prep kernels stage per row)
+  if (h->wt && !c.debug_trace && tc_min <= h->NT && h->d <= kTcMaxK && h->f <= kTcMaxK && tc_available()) {
     if ((ce = tc_prepare(h->smem_optin)) != cudaSuccess) return cuda_bail("tensor-core kernel attributes", ce);
     h->tc_min = tc_min;
   }

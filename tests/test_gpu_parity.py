@@ -349,8 +349,9 @@ def test_tensor_core_path_teacher_forced(name, shape, B):
 
 @pytest.mark.parametrize("ffn", [6000, 17000], ids=["mlp6000", "mlp17000"])
 def test_batch1_gemv_wide_mlp_teacher_forced(ffn):
-    # batch 1 on the bulk-copy GEMVs with a down projection input of 6000 floats (held in
-    # registers, every load in flight) and of 17000 (staged in a loop): against the oracle
+    # batch 1 on the bulk-copy GEMVs with down projection inputs of 6000 and 17000 floats (wider
+    # than the inputs a thread holds in registers); 17000 also keeps the prefill passes on the
+    # GEMVs (wider than the tensor-core prep kernels stage): against the oracle
     shape = shrink(WORKLOADS["llama8b_b1"].shape, layers=2, kv=2, ffn=ffn, vocab=1000)
     S, steps, cap = 4, 4, 12
     blob = synth.model_blob(shape, 95)
