@@ -69,6 +69,30 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     assert buf.getvalue() == ""  # no work and no line on a non-zero rank
 
 
+def test_reference_line_has_the_gpu_arm_config_and_its_own_time(monkeypatch):
+    # the reference arm's line describes the GPU arm's workload (one function builds both
+    # configs), and its ms_per_step is a step as it ran, so steps x ms_per_step fits in its time
+    import json
+    import bench
+    import synth
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference", "--workload", "tiny_f32",
+                                         "--steps", "4", "--warmup", "1"])
+        args = bench.parse()
+        bench.run_reference(args)
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    w = bench.WORKLOADS["tiny_f32"]
+    blob = synth.model_blob(w.shape, w.seed_weights)
+    assert line["config"] == bench.workload_config(w, args, 1, bench.blob_step_bytes(w, blob))
+    assert line["impl"] == "reference" and line["steps"] == 4
+    assert line["steps"] * line["ms_per_step"] <= line["wall_s"] * 1e3
+    assert line["ms_per_token"] >= line["ms_per_step"]
+    assert abs(line["value"] - 1e3 / line["ms_per_token"]) < 1e-9 * line["value"]
+
+
 def test_step_roofline_fields():
     import bench
     # 15.28 GB per step at batch 1: 444.3 tok/s at the measured 6788 GB/s, 523.6 at 8 TB/s
