@@ -125,7 +125,7 @@ def test_profile_summaries_are_self_describing():
     for p in files:
         text = open(p).read()
         assert "```" in text and ("ncu " in text), p
-        assert "_work" not in text and "gpurun" not in text, p
+        assert "_work" not in text and "_out/" not in text, p
         if "traffic_bytes_per_launch" in text:
             assert re.search(r"traffic_bytes_per_launch:\s*\d+", text), p
             assert re.search(r"kernel_function:\s*\w+", text) and re.search(r"kernel_function_sha256_16:\s*[0-9a-f]{16}", text), p
