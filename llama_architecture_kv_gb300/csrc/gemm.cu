@@ -518,7 +518,7 @@ TcPlan plan_tc(int rows, int K, int B, int num_sms, bool whole) {
 }
 
 __global__ void tc_prep_rows_kernel(const TcPrepArgs a);
-constexpr int kPrepRowMaxKDecl = 16384;
+constexpr int kPrepRowMaxKDecl = kTcMaxK;
 
 cudaError_t tc_prepare(int max_smem_optin) {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin);
